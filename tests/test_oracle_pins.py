@@ -1,0 +1,523 @@
+"""Pins of the CPU oracle against things other than itself: closed forms, invariants,
+library routines, brute force and finite differences.  CPU only.
+
+Each test names what fixes the expected value.  A plausible slip in the oracle (a
+dropped term, a wrong sign or index, a transposed operand) fails at least one.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+import gs_inputs as gi
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# ----------------------------------------------------------------------------- helpers
+
+def _ulp_err(y32: np.ndarray, ref: np.ndarray) -> np.ndarray:
+    ulp = np.spacing(np.abs(ref).astype(np.float32)).astype(np.float64)
+    return np.abs(y32.astype(np.float64) - ref) / ulp
+
+
+def _cam(W=32, H=32, eye=(0.0, 0.0, 3.0)):
+    return gi.camera(eye, W, H)
+
+
+def _scene(means, log_scale, quats=None, logits=None, sh=None):
+    means = np.asarray(means, np.float64).reshape(-1, 3)
+    n = means.shape[0]
+    ls = np.broadcast_to(np.asarray(log_scale, np.float64), (n, 3)) if np.ndim(log_scale) < 2 else log_scale
+    if quats is None:
+        quats = np.tile([1.0, 0.0, 0.0, 0.0], (n, 1))
+    if logits is None:
+        logits = np.zeros(n)
+    if sh is None:
+        sh = np.zeros((n, 16, 3))
+    return gi.pack(means, np.array(ls), np.asarray(quats), np.asarray(logits), np.asarray(sh)), n
+
+
+# ----------------------------------------------------------------------------- layout
+
+def test_layout_matches_pages():
+    """59 parameters per Gaussian at SH degree 3 (16 per channel, 192 B), 708 B with
+    two Adam moments, 12-scalar / 48-B projected record: the pages' numbers."""
+    g = json.load(open(os.path.join(GOLDEN, "pages_layout.json")))
+    assert gi.N_PLANES == g["params_per_gaussian_sh3"]["value"] == oracle.N_PLANES
+    sh_planes = gi.N_PLANES - gi.PLANE_SH
+    assert sh_planes == 3 * g["sh_coeffs_per_channel_sh3"]["value"]
+    assert sh_planes * 4 == g["sh_bytes_sh3"]["value"]
+    # SH degree 2 would keep 9 coefficients per channel: 59 - 3 * (16 - 9) = 38
+    assert gi.N_PLANES - 3 * (16 - g["sh_coeffs_per_channel_sh2"]["value"]) == g["params_per_gaussian_sh2"]["value"]
+    assert gi.N_PLANES * 4 * 3 == g["bytes_per_gaussian_with_adam_sh3"]["value"]
+    assert g["record_scalars"]["value"] * 4 == g["record_bytes"]["value"] == 48
+    assert 3 * 4 == g["rgb_bytes"]["value"]
+
+
+# ----------------------------------------------------------------------------- exp
+
+def test_expf_within_two_ulp_of_fp64():
+    """The decision exponential stays within 2 ulp of the correctly rounded fp64 exp
+    across its whole domain (a wrong polynomial coefficient or reduction constant
+    breaks this)."""
+    x = np.concatenate([np.linspace(-87.0, 88.0, 400_001, dtype=np.float32),
+                        np.random.default_rng(0).uniform(-6.0, 0.0, 200_000).astype(np.float32)])
+    y = oracle.expf(x)
+    err = _ulp_err(y, np.exp(x.astype(np.float64)))
+    assert err.max() <= 2.0, err.max()
+    assert np.mean(err <= 0.5) > 0.9
+
+
+def test_expf_special_values():
+    x = np.array([0.0, -0.0, np.nan, 100.0, -100.0, 88.0, -87.0, 1.0], np.float32)
+    y = oracle.expf(x)
+    assert y[0] == 1.0 and y[1] == 1.0
+    assert np.isnan(y[2])
+    assert y[3] == np.inf and y[4] == 0.0
+    assert np.isfinite(y[5]) and y[6] > np.finfo(np.float32).tiny
+    assert abs(float(y[7]) - math.e) <= np.spacing(np.float32(math.e))
+
+
+# ----------------------------------------------------------------------------- SH
+
+def _random_dirs(n, seed=0):
+    d = np.random.default_rng(seed).normal(size=(n, 3))
+    return d / np.linalg.norm(d, axis=1, keepdims=True)
+
+
+def test_sh_addition_theorem():
+    """sum_m Y_lm(d)^2 = (2l+1)/(4 pi) for every unit d and each band l."""
+    Y = oracle.sh_basis(_random_dirs(1000))
+    for l in range(4):
+        s = (Y[:, l * l:(l + 1) * (l + 1)] ** 2).sum(axis=1)
+        np.testing.assert_allclose(s, (2 * l + 1) / (4 * math.pi), rtol=1e-12)
+
+
+def test_sh_orthonormal_by_quadrature():
+    """Gauss-Legendre in cos(theta) x uniform azimuth integrates products of degree
+    <= 6 exactly: the Gram matrix of the 16 basis functions is the identity."""
+    mu, w = np.polynomial.legendre.leggauss(8)
+    n_phi = 16
+    phi = 2 * math.pi * np.arange(n_phi) / n_phi
+    M, P = np.meshgrid(mu, phi, indexing="ij")
+    S = np.sqrt(1 - M ** 2)
+    dirs = np.stack([S * np.cos(P), S * np.sin(P), M], axis=-1).reshape(-1, 3)
+    wt = (w[:, None] * np.full(n_phi, 2 * math.pi / n_phi)[None, :]).reshape(-1)
+    Y = oracle.sh_basis(dirs)
+    G = (Y * wt[:, None]).T @ Y
+    np.testing.assert_allclose(G, np.eye(16), atol=1e-12)
+
+
+def test_sh_matches_scipy_complex_harmonics():
+    """Real SH with the Condon-Shortley phase from scipy's complex harmonics:
+    sqrt(2) Re Y_l^m (m > 0), sqrt(2) Im Y_l^|m| (m < 0), Y_l^0 (m = 0)."""
+    special = pytest.importorskip("scipy.special")
+    if not hasattr(special, "sph_harm_y"):
+        pytest.skip("scipy without sph_harm_y")
+    d = _random_dirs(500, seed=3)
+    theta = np.arccos(np.clip(d[:, 2], -1, 1))
+    phi = np.arctan2(d[:, 1], d[:, 0])
+    Y = oracle.sh_basis(d)
+    for l in range(4):
+        for m in range(-l, l + 1):
+            c = special.sph_harm_y(l, abs(m), theta, phi)
+            ref = c.real if m == 0 else (math.sqrt(2) * (c.real if m > 0 else c.imag))
+            np.testing.assert_allclose(Y[:, l * l + l + m], ref, atol=1e-12, err_msg=f"l={l} m={m}")
+    # explicit l = 1 sign convention: (-y, z, -x) sqrt(3 / 4 pi)
+    k1 = math.sqrt(3 / (4 * math.pi))
+    np.testing.assert_allclose(Y[:, 1:4], np.stack([-k1 * d[:, 1], k1 * d[:, 2], -k1 * d[:, 0]], 1), atol=1e-14)
+
+
+# ----------------------------------------------------------------------------- projection
+
+@pytest.mark.parametrize("prec", [64, 32])
+def test_projection_isotropic_on_axis_closed_form(prec):
+    """An isotropic Gaussian of scale s on the optical axis at depth z projects to
+    Sigma_2 = (f s / z)^2 I + 0.3 I, conic I / that, mean at the principal point,
+    radius ceil(3 sqrt(lambda)) with lambda = diag + sqrt(0.1) (the discriminant is
+    0 and takes the 0.1 floor), opacity sigmoid(logit)."""
+    W = H = 64
+    cam = _cam(W, H)
+    sig = np.array([0.05, 0.1, 0.2])
+    logits = np.array([0.3, -1.0, 2.0])
+    P, n = _scene(np.zeros((3, 3)), np.log(sig)[:, None].repeat(3, 1), logits=logits)
+    pr = oracle.project(P, n, cam, prec)
+    f = float(cam["fx"])
+    sig = np.exp(P[3, :n].astype(np.float64))      # the scale the fp32 planes hold
+    logits = P[10, :n].astype(np.float64)
+    s2 = (f * sig / 3.0) ** 2 + 0.3
+    tol = dict(rtol=1e-12) if prec == 64 else dict(rtol=2e-6)
+    np.testing.assert_allclose(pr["cov2d"][:, 0], s2, **tol)
+    np.testing.assert_allclose(pr["cov2d"][:, 2], s2, **tol)
+    np.testing.assert_allclose(pr["cov2d"][:, 1], 0.0, atol=1e-12 if prec == 64 else 1e-6)
+    np.testing.assert_allclose(pr["conic"][:, 0], 1 / s2, **tol)
+    np.testing.assert_allclose(pr["conic"][:, 2], 1 / s2, **tol)
+    np.testing.assert_allclose(pr["mean2d"], np.full((3, 2), W / 2), rtol=1e-7)
+    np.testing.assert_allclose(pr["depth"], 3.0, rtol=1e-7)
+    np.testing.assert_allclose(pr["opacity"], 1 / (1 + np.exp(-logits)), rtol=1e-12 if prec == 64 else 1e-6)
+    np.testing.assert_array_equal(pr["radius"], np.ceil(3 * np.sqrt(s2 + math.sqrt(0.1))).astype(int))
+
+
+def test_projection_ewa_matches_finite_difference_of_perspective():
+    """The 2D covariance minus the 0.3 low-pass equals sum_j d_j d_j^T where d_j is
+    the central difference of the exact pinhole map along the j-th scaled principal
+    axis (rotation from scipy): the EWA linearisation, fixed independently."""
+    Rot = pytest.importorskip("scipy.spatial.transform").Rotation
+    rng = np.random.default_rng(5)
+    n = 12
+    means = rng.uniform(-0.5, 0.5, (n, 3))
+    ls = rng.normal(-3.0, 0.4, (n, 3))
+    q = rng.normal(size=(n, 4))
+    q /= np.linalg.norm(q, axis=1, keepdims=True)
+    P, _ = _scene(means, ls, quats=q)
+    # the values the fp32 planes hold
+    means = P[0:3, :n].T.astype(np.float64)
+    ls = P[3:6, :n].T.astype(np.float64)
+    q = P[6:10, :n].T.astype(np.float64)
+    cam = gi.camera((2.0, -1.5, 1.8), 256, 192)
+    pr = oracle.project(P, n, cam, 64)
+    R = cam["R"].astype(np.float64)
+    t = cam["t"].astype(np.float64)
+    fx, fy, cx, cy = (float(cam[k]) for k in ("fx", "fy", "cx", "cy"))
+
+    def pinhole(x):
+        c = R @ x + t
+        return np.array([fx * c[0] / c[2] + cx, fy * c[1] / c[2] + cy])
+
+    for i in range(n):
+        # scipy quaternions are (x, y, z, w)
+        rot = Rot.from_quat([q[i, 1], q[i, 2], q[i, 3], q[i, 0]]).as_matrix()
+        L = rot @ np.diag(np.exp(ls[i]))
+        h = 1e-4
+        cov = np.zeros((2, 2))
+        for j in range(3):
+            d = (pinhole(means[i] + h * L[:, j]) - pinhole(means[i] - h * L[:, j])) / (2 * h)
+            cov += np.outer(d, d)
+        got = np.array([[pr["cov2d"][i, 0] - 0.3, pr["cov2d"][i, 1]], [pr["cov2d"][i, 1], pr["cov2d"][i, 2] - 0.3]])
+        np.testing.assert_allclose(got, cov, rtol=1e-6, atol=1e-8 * np.abs(cov).max())
+        np.testing.assert_allclose(pr["mean2d"][i], pinhole(means[i]), rtol=1e-12)
+
+
+def test_projection_invariant_under_joint_rotation():
+    """Rotating the scene and the camera together leaves mean2d, conic and depth
+    unchanged (catches a transposed camera rotation or quaternion product)."""
+    Rot = pytest.importorskip("scipy.spatial.transform").Rotation
+    rng = np.random.default_rng(7)
+    n = 64
+    means = rng.uniform(-0.6, 0.6, (n, 3))
+    ls = rng.normal(-3.0, 0.3, (n, 3))
+    q = rng.normal(size=(n, 4))
+    q /= np.linalg.norm(q, axis=1, keepdims=True)
+    cam = gi.camera((0.5, -2.5, 1.2), 200, 160)
+    Q = Rot.from_rotvec([0.3, -0.7, 0.4])
+    Qm = Q.as_matrix()
+    rq = (Q * Rot.from_quat(q[:, [1, 2, 3, 0]])).as_quat()[:, [3, 0, 1, 2]]
+    cam2 = dict(cam)
+    cam2["R"] = (cam["R"].astype(np.float64) @ Qm.T).astype(np.float32)
+    cam2["campos"] = (Qm @ cam["campos"].astype(np.float64)).astype(np.float32)
+    P1, _ = _scene(means, ls, quats=q)
+    P2, _ = _scene(means @ Qm.T, ls, quats=rq)
+    a = oracle.project(P1, n, cam, 64)
+    b = oracle.project(P2, n, cam2, 64)
+    for k, tol in (("mean2d", 1e-4), ("conic", 1e-5), ("depth", 1e-6)):
+        np.testing.assert_allclose(b[k], a[k], rtol=tol, atol=tol * 1e-2)
+
+
+def test_projection_fp32_tracks_fp64():
+    """The frozen fp32 sequence agrees with the fp64 instantiation to fp32 rounding;
+    integer outputs agree except where a value sits within rounding of a ceiling."""
+    cfg = gi.CONFIGS["tiny"]
+    P = gi.scene_for(cfg)
+    cam = gi.cameras_for(cfg)[0]
+    a = oracle.project(P, cfg.n, cam, 32)
+    b = oracle.project(P, cfg.n, cam, 64)
+    v = a["visible"] & b["visible"]
+    assert v.sum() > 0.95 * cfg.n
+    # mean2d = fx u + cx: absolute error scales with the image coordinates (~100 px)
+    np.testing.assert_allclose(a["mean2d"][v], b["mean2d"][v], rtol=2e-5, atol=128 * 4e-7)
+    for k in ("conic", "opacity", "rgb", "depth"):
+        np.testing.assert_allclose(a[k][v], b[k][v], rtol=2e-5, atol=1e-6)
+    assert np.mean(a["radius"][v] == b["radius"][v]) > 0.999
+
+
+# ----------------------------------------------------------------------------- binning
+
+def test_tile_lists_brute_force():
+    """Every tile's list equals, as a sequence, the Gaussians whose closed box
+    [m - r, m + r]^2 overlaps the tile's half-open pixel square, sorted by
+    (fp32 depth, index): interval overlap, not the floor arithmetic of the rect."""
+    cfg = gi.CONFIGS["tiny"]
+    P = gi.scene_for(cfg, n=600)
+    cam = gi.camera((0.0, 0.0, 3.0), 72, 56)   # ragged tiles on both axes
+    pr = oracle.project(P, 600, cam, 32)
+    tl = oracle.tile_lists(pr, 72, 56)
+    m, r, z = pr["mean2d"].astype(np.float64), pr["radius"].astype(np.float64), pr["depth"]
+    vis = pr["count"] > 0
+    order = np.lexsort((np.arange(600), z))
+    TX, TY = 5, 4
+    keys, ids, ranges = tl["keys"], tl["ids"], tl["ranges"]
+    for ty in range(TY):
+        for tx in range(TX):
+            hit = (vis & (m[:, 0] - r < 16 * (tx + 1)) & (m[:, 0] + r >= 16 * tx)
+                   & (m[:, 1] - r < 16 * (ty + 1)) & (m[:, 1] + r >= 16 * ty))
+            exp = [g for g in order if hit[g]]
+            t = ty * TX + tx
+            s, e = ranges[t]
+            assert list(ids[s:e]) == exp
+            assert np.all((keys[s:e] >> np.uint64(32)) == t)
+            zb = z[ids[s:e]].view(np.uint32)
+            assert np.all((keys[s:e] & np.uint64(0xFFFFFFFF)) == zb)
+    assert tl["K"] == int(pr["count"].astype(np.int64).sum())
+
+
+# ----------------------------------------------------------------------------- compositing
+
+def _on_pixel_scene(k, opacity, rgb, W=32, H=32, sigma=0.05):
+    """k coincident isotropic Gaussians centred on the centre of pixel (W/2, H/2)."""
+    cam = _cam(W, H)
+    f = float(cam["fx"])
+    # mean2d = f x / z + cx -> world x for a pixel-centre offset of 0.5 px
+    x = 0.5 * 3.0 / f
+    means = np.tile([x, -x, 0.0], (k, 1))           # camera y axis points down
+    logit = math.log(opacity / (1 - opacity))
+    sh = np.zeros((k, 16, 3))
+    sh[:, 0, :] = (np.asarray(rgb) - 0.5) / (0.5 / math.sqrt(math.pi))
+    P, n = _scene(means, math.log(sigma), logits=np.full(k, logit), sh=sh)
+    return P, n, cam
+
+
+@pytest.mark.parametrize("prec", [64, 32])
+def test_stacked_gaussians_transmittance_closed_form(prec):
+    """k identical coincident Gaussians at a pixel centre (power = 0, alpha = o):
+    T = (1 - o)^j after j entries; the pixel stops at the first j with
+    (1 - o)^j < 1e-4, and C = rgb (1 - (1 - o)^(j - 1))."""
+    o, k = 0.4, 40
+    rgb = np.array([0.9, 0.3, 0.6])
+    P, n, cam = _on_pixel_scene(k, o, rgb)
+    pr = oracle.project(P, n, cam, prec)
+    assert np.allclose(pr["mean2d"], 16.5, atol=1e-4)
+    rd = oracle.render(pr, 32, 32, prec=prec)
+    o = 1.0 / (1.0 + math.exp(-float(P[10, 0])))   # the opacity the fp32 logit holds
+    rgb = np.array([0.5 + float(P[11 + c, 0]) * 0.5 / math.sqrt(math.pi) for c in range(3)])
+    j_stop = next(j for j in range(1, k + 1) if (1 - o) ** j < 1e-4)
+    comp = j_stop - 1
+    tol = 1e-12 if prec == 64 else 2e-6
+    assert rd["n_contrib"][16, 16] == comp
+    np.testing.assert_allclose(rd["T_final"][16, 16], (1 - o) ** comp, rtol=tol * 10)
+    np.testing.assert_allclose(rd["image"][:, 16, 16], rgb * (1 - (1 - o) ** comp), rtol=tol * 10)
+
+
+def test_single_gaussian_alpha_falloff_closed_form():
+    """One isotropic on-axis Gaussian: each pixel's colour is rgb o exp(-|d|^2 / (2 s^2))
+    with s^2 = (f sigma / z)^2 + 0.3, zero where that is below 1/255, 0.99 cap."""
+    W = H = 48
+    cam = _cam(W, H)
+    sig, o = 0.08, 0.7
+    P, n = _scene(np.zeros((1, 3)), math.log(sig), logits=[math.log(o / (1 - o))],
+                  sh=np.tile(np.array([[[(1.0 - 0.5) * 2 * math.sqrt(math.pi)] * 3] + [[0.0] * 3] * 15]), (1, 1, 1)))
+    pr = oracle.project(P, n, cam, 64)
+    rd = oracle.render(pr, W, H, prec=64)
+    sig = math.exp(float(P[3, 0]))                  # values the fp32 planes hold
+    o = 1.0 / (1.0 + math.exp(-float(P[10, 0])))
+    rgb0 = 0.5 + float(P[11, 0]) * 0.5 / math.sqrt(math.pi)
+    s2 = (float(cam["fx"]) * sig / 3.0) ** 2 + 0.3
+    ys, xs = np.mgrid[0:H, 0:W] + 0.5
+    a = o * np.exp(-((xs - W / 2) ** 2 + (ys - H / 2) ** 2) / (2 * s2))
+    a = np.minimum(a, 0.99)
+    a[a < 1 / 255] = 0.0
+    r = int(pr["radius"][0])
+    inside = (np.floor((xs - 0.5) / 16) >= np.floor((W / 2 - r) / 16)) & (np.floor((xs - 0.5) / 16) <= np.floor((W / 2 + r) / 16))
+    inside &= (np.floor((ys - 0.5) / 16) >= np.floor((H / 2 - r) / 16)) & (np.floor((ys - 0.5) / 16) <= np.floor((H / 2 + r) / 16))
+    a[~inside] = 0.0
+    np.testing.assert_allclose(rd["image"][0], rgb0 * a, atol=1e-12)
+    np.testing.assert_allclose(rd["T_final"], 1 - a, atol=1e-12)
+
+
+def test_alpha_sum_and_colour_bounds():
+    """Accumulated alpha 1 - T lies in [0, 1 - 1e-4]; each channel is at most
+    max colour x (1 - T) with a black background."""
+    cfg = gi.CONFIGS["tiny"]
+    P = gi.scene_for(cfg)
+    cam = gi.cameras_for(cfg)[0]
+    pr = oracle.project(P, cfg.n, cam, 32)
+    rd = oracle.render(pr, 128, 128)
+    T = rd["T_final"].astype(np.float64)
+    assert T.max() <= 1.0 and T.min() >= 1e-4 * (1 - 1e-6)
+    cmax = pr["rgb"][pr["visible"]].max()
+    assert np.all(rd["image"] <= cmax * (1 - T)[None] * (1 + 1e-5) + 1e-6)
+    assert np.all(rd["image"] >= 0)
+
+
+def test_permutation_invariance_distinct_depths():
+    """Reordering the Gaussians in memory leaves the fp32 image, T and n_contrib
+    bit-identical when depths are distinct (order comes from depth, not index)."""
+    cfg = gi.CONFIGS["tiny"]
+    P = gi.scene_for(cfg, n=1500)
+    cam = gi.camera((0.0, 0.0, 3.0), 96, 80)
+    n = 1500
+    # drop (put behind the camera) all but one member of any group of equal fp32 depth
+    z0 = oracle.project(P, n, cam, 32)["depth"]
+    _, first = np.unique(z0, return_index=True)
+    dup = np.setdiff1d(np.arange(n), first)
+    P[0:3, dup] = np.array([[0.0], [0.0], [10.0]], np.float32)
+    perm = np.random.default_rng(1).permutation(n)
+    P2 = P.copy()
+    P2[:, :n] = P[:, :n][:, perm]
+    a = oracle.project(P, n, cam, 32)
+    b = oracle.project(P2, n, cam, 32)
+    assert len(np.unique(a["depth"][a["visible"]])) == a["visible"].sum()
+    ra, rb = oracle.render(a, 96, 80), oracle.render(b, 96, 80)
+    for k in ("image", "T_final", "n_contrib"):
+        np.testing.assert_array_equal(ra[k], rb[k])
+
+
+def test_equal_depth_order_invariance():
+    """Coincident Gaussians at equal depth with equal colours: swapping their order
+    leaves colour and transmittance unchanged (products commute)."""
+    rgb = np.array([0.2, 0.8, 0.5])
+    cam = _cam(32, 32)
+    means = np.zeros((3, 3))
+    logits = np.array([0.5, -0.3, 1.1])
+    sh = np.zeros((3, 16, 3))
+    sh[:, 0, :] = (rgb - 0.5) * 2 * math.sqrt(math.pi)
+    P1, n = _scene(means, math.log(0.07), logits=logits, sh=sh)
+    P2, _ = _scene(means, math.log(0.07), logits=logits[::-1].copy(), sh=sh)
+    r1 = oracle.render(oracle.project(P1, n, cam, 64), 32, 32, prec=64)
+    r2 = oracle.render(oracle.project(P2, n, cam, 64), 32, 32, prec=64)
+    np.testing.assert_allclose(r1["T_final"], r2["T_final"], atol=1e-14)
+    np.testing.assert_allclose(r1["image"], r2["image"], atol=1e-14)
+
+
+# ----------------------------------------------------------------------------- gradients
+
+def _fd_scene(n=6, seed=11, W=32, H=32):
+    rng = np.random.default_rng(seed)
+    means = np.column_stack([rng.uniform(-0.35, 0.35, n), rng.uniform(-0.35, 0.35, n), rng.uniform(-0.3, 0.3, n)])
+    ls = rng.normal(-2.2, 0.25, (n, 3))
+    q = rng.normal(size=(n, 4))
+    q /= np.linalg.norm(q, axis=1, keepdims=True)
+    logits = rng.normal(0.0, 0.8, n)
+    sh = np.zeros((n, 16, 3))
+    sh[:, 0, :] = rng.uniform(-1, 1, (n, 3))
+    sh[:, 1:, :] = rng.normal(0, 0.3, (n, 15, 3))
+    P, _ = _scene(means, ls, quats=q, logits=logits, sh=sh)
+    cam = gi.camera((0.4, -0.3, 2.9), W, H)
+    return P, n, cam
+
+
+def test_render_backward_matches_finite_differences():
+    """The suffix-sum backward equals central differences (fp64) of the L1 loss with
+    respect to each projected quantity (mean2d, conic, opacity, colour), with
+    tile rects held fixed and every residual sign far from zero."""
+    P, n, cam = _fd_scene()
+    pr = oracle.project(P, n, cam, 64)
+    base = oracle.render(pr, 32, 32, prec=64)
+    tgt = gi.offset_target(base["image"], seed=3)
+    rd = oracle.render(pr, 32, 32, target=tgt, prec=64)
+    g2 = rd["grad2d"]
+    assert np.abs(g2).max() > 0
+    cols = [0, 1, 2, 3, 4, 5, 6, 7, 8]
+    for i in range(n):
+        if not pr["visible"][i]:
+            continue
+        for q, col in enumerate(cols):
+            x0 = pr["proj16"][i, col]
+            h = 1e-6 * max(1.0, abs(x0))
+            vals = []
+            for sgn in (1, -1):
+                p2 = dict(pr)
+                p2["proj16"] = pr["proj16"].copy()
+                p2["proj16"][i, col] = x0 + sgn * h
+                r = oracle.render(p2, 32, 32, target=tgt, prec=64)
+                np.testing.assert_array_equal(r["n_contrib"], rd["n_contrib"])
+                vals.append(r["loss"])
+            fd = (vals[0] - vals[1]) / (2 * h)
+            assert abs(fd - g2[q, i]) <= 1e-6 * abs(fd) + 1e-10, (i, q, fd, g2[q, i])
+
+
+def test_project_backward_matches_finite_differences():
+    """The projection chain rule equals central differences (fp64) of a random
+    linear functional of the nine projected outputs with respect to all 59
+    parameters of each Gaussian (SH, quaternion normalisation, scales, mean)."""
+    P, n, cam = _fd_scene(n=4, seed=2)
+    w = np.random.default_rng(4).normal(size=(9, n))
+    pr = oracle.project(P, n, cam, 64)
+    assert pr["visible"].all()
+    an = oracle.project_bwd(P, n, cam, w, prec=64)
+
+    def func(Pm):
+        r = oracle.project(Pm, n, cam, 64)
+        return float((r["proj16"][:, :9].T * w).sum())
+
+    for i in range(n):
+        for pl in range(59):
+            x0 = float(P[pl, i])
+            h = 1e-3 * max(abs(x0), 0.05)
+            Pp, Pm_ = P.copy(), P.copy()
+            Pp[pl, i] = np.float32(x0 + h)
+            Pm_[pl, i] = np.float32(x0 - h)
+            he = (float(Pp[pl, i]) - float(Pm_[pl, i])) / 2
+            fd = (func(Pp) - func(Pm_)) / (2 * he)
+            assert abs(fd - an[pl, i]) <= 2e-5 * abs(fd) + 1e-7 * np.abs(an[:, i]).max() + 1e-9, (i, pl, fd, an[pl, i])
+
+
+def test_whole_step_gradient_matches_finite_differences():
+    """End to end: d loss / d params from render backward then projection backward
+    equals central differences of the whole fp64 forward (all 59 planes)."""
+    P, n, cam = _fd_scene(n=3, seed=9)
+    pr = oracle.project(P, n, cam, 64)
+    tgt = gi.offset_target(oracle.render(pr, 32, 32, prec=64)["image"], seed=5)
+    rd = oracle.render(pr, 32, 32, target=tgt, prec=64)
+    an = oracle.project_bwd(P, n, cam, rd["grad2d"], prec=64)
+
+    def loss(Pm):
+        return oracle.render(oracle.project(Pm, n, cam, 64), 32, 32, target=tgt, prec=64)["loss"]
+
+    checked = 0
+    for i in range(n):
+        for pl in range(59):
+            x0 = float(P[pl, i])
+            h = 1e-3 * max(abs(x0), 0.05)
+            Pp, Pm_ = P.copy(), P.copy()
+            Pp[pl, i] = np.float32(x0 + h)
+            Pm_[pl, i] = np.float32(x0 - h)
+            he = (float(Pp[pl, i]) - float(Pm_[pl, i])) / 2
+            fd = (loss(Pp) - loss(Pm_)) / (2 * he)
+            assert abs(fd - an[pl, i]) <= 2e-4 * abs(fd) + 2e-7 * np.abs(an).max(), (i, pl, fd, an[pl, i])
+            checked += 1
+    assert checked == 3 * 59
+
+
+# ----------------------------------------------------------------------------- Adam
+
+def test_adam_constant_gradient_closed_form():
+    """With a constant gradient g the bias-corrected moments are exactly g and g^2,
+    so after t steps p = p0 - t lr g / (|g| + eps)."""
+    rng = np.random.default_rng(0)
+    planes, stride = 59, 64
+    p0 = rng.normal(size=(planes, stride))
+    g = rng.normal(size=(planes, stride)) * 10.0 ** rng.integers(-6, 1, (planes, stride))
+    lr = gi.lr_planes()
+    p, m, v = p0, np.zeros_like(p0), np.zeros_like(p0)
+    T = 7
+    for t in range(1, T + 1):
+        p, m, v = oracle.adam(p, g, m, v, lr, 0.9, 0.999, 1e-15, t)
+    np.testing.assert_allclose(p, p0 - T * lr[:, None] * g / (np.abs(g) + 1e-15), rtol=1e-12, atol=1e-15)
+    np.testing.assert_allclose(m, g * (1 - 0.9 ** T), rtol=1e-12)
+    np.testing.assert_allclose(v, g * g * (1 - 0.999 ** T), rtol=1e-12)
+
+
+def test_adam_first_step_is_signed_lr():
+    """One step from zero moments moves each parameter by lr sign(g) (|g| >> eps),
+    whatever beta1 and beta2 are."""
+    rng = np.random.default_rng(1)
+    p0 = rng.normal(size=(59, 32))
+    g = rng.normal(size=(59, 32))
+    lr = gi.lr_planes()
+    for b1, b2 in ((0.9, 0.999), (0.0, 0.5)):
+        p, _, _ = oracle.adam(p0, g, np.zeros_like(p0), np.zeros_like(p0), lr, b1, b2, 1e-15, 1)
+        np.testing.assert_allclose(p, p0 - lr[:, None] * np.sign(g), rtol=1e-12)
