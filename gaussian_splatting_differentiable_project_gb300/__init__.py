@@ -1,0 +1,252 @@
+"""GB300 (sm_103a) 3D Gaussian Splatting training step.
+
+A thin ctypes binding over the C-ABI library ``libgs.so`` (declared in
+``include/gs.h``).  Every step of the path runs in the library's CUDA kernels;
+this module only marshals arguments: PyTorch tensors supply device memory and the
+current CUDA stream.  There is no CPU path: if the library is missing or no GPU is
+present, the calls raise.
+
+Entry points (same names as the C ABI, without the ``gs_`` prefix):
+``project``, ``bin_sort``, ``render_fwd``, ``render_bwd``, ``project_bwd``,
+``adam_step``, plus ``util_expf`` and ``bin_sort_workspace_bytes``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import numpy as np
+
+from . import _build
+
+N_PLANES = 59
+TILE = 16
+REC_FLOATS = 12
+N_GRAD2D = 9
+
+GS_OK = 0
+GS_ERR_INVALID_ARG = 1
+GS_ERR_CUDA = 2
+GS_ERR_CAPACITY = 4
+GS_ERR_TIMEOUT = 8
+GS_ERR_NONFINITE = 16
+
+_lock = threading.Lock()
+_lib = None
+
+
+class GsError(RuntimeError):
+    pass
+
+
+class GsCamera(ctypes.Structure):
+    _fields_ = [("R", ctypes.c_float * 9), ("t", ctypes.c_float * 3),
+                ("fx", ctypes.c_float), ("fy", ctypes.c_float),
+                ("cx", ctypes.c_float), ("cy", ctypes.c_float),
+                ("width", ctypes.c_int32), ("height", ctypes.c_int32),
+                ("campos", ctypes.c_float * 3), ("near_z", ctypes.c_float)]
+
+
+class GsDims(ctypes.Structure):
+    _fields_ = [("n", ctypes.c_int64), ("n_pad", ctypes.c_int64)]
+
+
+class GsProj(ctypes.Structure):
+    _fields_ = [("rec", ctypes.c_void_p), ("depth", ctypes.c_void_p), ("radius", ctypes.c_void_p),
+                ("rect", ctypes.c_void_p), ("count", ctypes.c_void_p)]
+
+
+class GsBins(ctypes.Structure):
+    _fields_ = [("keys", ctypes.c_void_p), ("ids", ctypes.c_void_p), ("rec", ctypes.c_void_p),
+                ("ranges", ctypes.c_void_p), ("n_isect", ctypes.c_void_p)]
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load(build_if_missing: bool = True):
+    """Load libgs.so (building it in-tree first if it is missing or stale)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if build_if_missing and not _build.up_to_date():
+            _build.build()
+        if not os.path.exists(_build.LIB):
+            raise GsError(f"CUDA library not built: {_build.LIB}")
+        lib = ctypes.CDLL(_build.LIB)
+        P = ctypes.c_void_p
+        st = ctypes.c_int
+        lib.gs_project.argtypes = [GsDims, P, ctypes.POINTER(GsCamera), GsProj, P, P]
+        lib.gs_project.restype = st
+        lib.gs_bin_sort_workspace_bytes.argtypes = [GsDims, ctypes.c_uint32, ctypes.c_int32, ctypes.c_int32]
+        lib.gs_bin_sort_workspace_bytes.restype = ctypes.c_size_t
+        lib.gs_bin_sort.argtypes = [GsDims, ctypes.POINTER(GsProj), ctypes.POINTER(GsCamera), ctypes.c_uint32,
+                                    GsBins, P, ctypes.c_size_t, P, P]
+        lib.gs_bin_sort.restype = st
+        lib.gs_render_fwd.argtypes = [ctypes.POINTER(GsCamera), ctypes.POINTER(GsBins), ctypes.c_uint32,
+                                      ctypes.POINTER(ctypes.c_float), P, P, P, P, P]
+        lib.gs_render_fwd.restype = st
+        lib.gs_render_bwd.argtypes = [GsDims, ctypes.POINTER(GsCamera), ctypes.POINTER(GsBins), ctypes.c_uint32,
+                                      ctypes.POINTER(ctypes.c_float), P, P, P, P, P, P, P, P]
+        lib.gs_render_bwd.restype = st
+        lib.gs_project_bwd.argtypes = [GsDims, P, ctypes.POINTER(GsCamera), ctypes.POINTER(GsProj), P, P, P, P]
+        lib.gs_project_bwd.restype = st
+        lib.gs_adam_step.argtypes = [GsDims, P, P, P, P, ctypes.POINTER(ctypes.c_float), ctypes.c_double,
+                                     ctypes.c_double, ctypes.c_double, ctypes.c_int64, P]
+        lib.gs_adam_step.restype = st
+        lib.gs_util_expf.argtypes = [P, P, ctypes.c_int64, P]
+        lib.gs_util_expf.restype = st
+        lib.gs_status_str.argtypes = [ctypes.c_uint32]
+        lib.gs_status_str.restype = ctypes.c_char_p
+        lib.gs_version.restype = ctypes.c_char_p
+        _lib = lib
+        return lib
+
+
+def status_str(code: int) -> str:
+    return load().gs_status_str(int(code)).decode()
+
+
+def _check(code: int, what: str) -> None:
+    if code != GS_OK:
+        raise GsError(f"{what}: {status_str(code)} ({code})")
+
+
+def _stream(stream=None):
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _p(t) -> ctypes.c_void_p:
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def camera(cam: dict) -> GsCamera:
+    c = GsCamera()
+    c.R[:] = [float(v) for v in np.asarray(cam["R"], np.float32).reshape(9)]
+    c.t[:] = [float(v) for v in np.asarray(cam["t"], np.float32).reshape(3)]
+    c.fx, c.fy, c.cx, c.cy = (float(np.float32(cam[k])) for k in ("fx", "fy", "cx", "cy"))
+    c.width, c.height = int(cam["width"]), int(cam["height"])
+    c.campos[:] = [float(v) for v in np.asarray(cam["campos"], np.float32).reshape(3)]
+    c.near_z = float(np.float32(cam.get("near_z", 0.01)))
+    return c
+
+
+def dims(n: int, n_pad: int) -> GsDims:
+    return GsDims(int(n), int(n_pad))
+
+
+def n_tiles(width: int, height: int) -> int:
+    return (-(-width // TILE)) * (-(-height // TILE))
+
+
+# ----------------------------------------------------------------------------- buffers
+
+class ProjBuffers:
+    """Device outputs of ``project`` for n_pad Gaussians."""
+
+    def __init__(self, n_pad: int, device="cuda"):
+        import torch
+        self.rec = torch.empty((n_pad, REC_FLOATS), dtype=torch.float32, device=device)
+        self.depth = torch.empty(n_pad, dtype=torch.float32, device=device)
+        self.radius = torch.empty(n_pad, dtype=torch.int32, device=device)
+        self.rect = torch.empty((n_pad, 2), dtype=torch.int32, device=device)
+        self.count = torch.empty(n_pad, dtype=torch.int32, device=device)
+
+    def c(self) -> GsProj:
+        return GsProj(self.rec.data_ptr(), self.depth.data_ptr(), self.radius.data_ptr(), self.rect.data_ptr(),
+                      self.count.data_ptr())
+
+
+class BinBuffers:
+    """Device outputs and scratch of ``bin_sort`` for ``capacity`` intersections."""
+
+    def __init__(self, n: int, capacity: int, width: int, height: int, device="cuda"):
+        import torch
+        self.capacity = int(capacity)
+        self.keys = torch.empty(capacity, dtype=torch.int64, device=device)
+        self.ids = torch.empty(capacity, dtype=torch.int32, device=device)
+        self.rec = torch.empty((capacity, REC_FLOATS), dtype=torch.float32, device=device)
+        self.ranges = torch.empty((n_tiles(width, height), 2), dtype=torch.int32, device=device)
+        self.n_isect = torch.zeros(2, dtype=torch.int32, device=device)
+        ws = bin_sort_workspace_bytes(n, capacity, width, height)
+        self.workspace = torch.empty(ws + 256, dtype=torch.uint8, device=device)
+        self.ws_bytes = ws
+
+    def ws_ptr(self) -> int:
+        p = self.workspace.data_ptr()
+        return (p + 255) & ~255
+
+    def c(self) -> GsBins:
+        return GsBins(self.keys.data_ptr(), self.ids.data_ptr(), self.rec.data_ptr(), self.ranges.data_ptr(),
+                      self.n_isect.data_ptr())
+
+
+# ----------------------------------------------------------------------------- entry points
+
+def project(n: int, params, cam: dict, proj: ProjBuffers, dev_status, stream=None) -> None:
+    cc = camera(cam)
+    _check(load().gs_project(dims(n, params.shape[1]), _p(params), ctypes.byref(cc), proj.c(), _p(dev_status),
+                             _stream(stream)), "gs_project")
+
+
+def bin_sort_workspace_bytes(n: int, capacity: int, width: int, height: int) -> int:
+    return int(load().gs_bin_sort_workspace_bytes(dims(n, max(256, n)), int(capacity), int(width), int(height)))
+
+
+def bin_sort(n: int, n_pad: int, proj: ProjBuffers, cam: dict, bins: BinBuffers, dev_status, stream=None) -> None:
+    cc = camera(cam)
+    pc = proj.c()
+    _check(load().gs_bin_sort(dims(n, n_pad), ctypes.byref(pc), ctypes.byref(cc), bins.capacity, bins.c(),
+                              ctypes.c_void_p(bins.ws_ptr()), bins.ws_bytes, _p(dev_status), _stream(stream)),
+           "gs_bin_sort")
+
+
+def _bg(bg):
+    return (ctypes.c_float * 3)(*[float(x) for x in bg])
+
+
+def render_fwd(cam: dict, bins: BinBuffers, bg, image, T_final, n_contrib, dev_status, stream=None) -> None:
+    cc = camera(cam)
+    bc = bins.c()
+    _check(load().gs_render_fwd(ctypes.byref(cc), ctypes.byref(bc), bins.capacity, _bg(bg), _p(image), _p(T_final),
+                                _p(n_contrib), _p(dev_status), _stream(stream)), "gs_render_fwd")
+
+
+def render_bwd(n: int, n_pad: int, cam: dict, bins: BinBuffers, bg, image, target, T_final, n_contrib, grad2d,
+               loss, dev_status, stream=None) -> None:
+    cc = camera(cam)
+    bc = bins.c()
+    _check(load().gs_render_bwd(dims(n, n_pad), ctypes.byref(cc), ctypes.byref(bc), bins.capacity, _bg(bg),
+                                _p(image), _p(target), _p(T_final), _p(n_contrib), _p(grad2d), _p(loss),
+                                _p(dev_status), _stream(stream)), "gs_render_bwd")
+
+
+def project_bwd(n: int, params, cam: dict, proj: ProjBuffers, grad2d, grads, dev_status, stream=None) -> None:
+    cc = camera(cam)
+    pc = proj.c()
+    _check(load().gs_project_bwd(dims(n, params.shape[1]), _p(params), ctypes.byref(cc), ctypes.byref(pc),
+                                 _p(grad2d), _p(grads), _p(dev_status), _stream(stream)), "gs_project_bwd")
+
+
+def adam_step(n: int, params, grads, m, v, lr_plane, beta1: float, beta2: float, eps: float, t: int,
+              stream=None) -> None:
+    """Adam step number ``t`` (>= 1); bias corrections are formed inside the call."""
+    lr = (ctypes.c_float * N_PLANES)(*[float(x) for x in lr_plane])
+    _check(load().gs_adam_step(dims(n, params.shape[1]), _p(params), _p(grads), _p(m), _p(v), lr, float(beta1),
+                               float(beta2), float(eps), int(t), _stream(stream)), "gs_adam_step")
+
+
+def util_expf(x, y, stream=None) -> None:
+    _check(load().gs_util_expf(_p(x), _p(y), x.numel(), _stream(stream)), "gs_util_expf")
+
+
+def version() -> str:
+    return load().gs_version().decode()
+
+
+from .trainer import Trainer  # noqa: E402  (re-export)

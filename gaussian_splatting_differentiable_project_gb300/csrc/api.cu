@@ -1,0 +1,33 @@
+// Small C-ABI utilities: status strings, version, and the library exponential
+// exposed for cross-checking.
+#include "api_util.h"
+#include "gs_common.cuh"
+
+namespace gs {
+
+__global__ void k_expf(const float* __restrict__ x, float* __restrict__ y, int64_t n) {
+  const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+  for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride) y[i] = gs_expf(x[i]);
+}
+
+}  // namespace gs
+
+extern "C" gs_status gs_util_expf(const float* x, float* y, int64_t n, cudaStream_t stream) {
+  using namespace gs;
+  if (n < 0 || (n > 0 && (!x || !y))) return GS_ERR_INVALID_ARG;
+  if (n == 0) return GS_OK;
+  k_expf<<<grid_for(n, 256, kSmCount * 16), 256, 0, stream>>>(x, y, n);
+  return launch_status();
+}
+
+extern "C" const char* gs_status_str(uint32_t status) {
+  if (status == 0) return "ok";
+  if (status & GS_ERR_INVALID_ARG) return "invalid argument";
+  if (status & GS_ERR_CUDA) return "CUDA launch failed";
+  if (status & GS_ERR_CAPACITY) return "tile intersections exceed capacity";
+  if (status & GS_ERR_TIMEOUT) return "bounded device wait gave up";
+  if (status & GS_ERR_NONFINITE) return "non-finite Gaussian parameters";
+  return "unknown status";
+}
+
+extern "C" const char* gs_version(void) { return "gs-gb300 0.1 sm_103a"; }

@@ -1,0 +1,65 @@
+// gs_project: one thread per Gaussian, coalesced reads of the 59 SoA parameter
+// planes (each warp reads 128 contiguous bytes per plane), SH read only for
+// Gaussians that survive culling, 48-byte record written per visible Gaussian.
+#include "api_util.h"
+#include "project_frozen.cuh"
+
+namespace gs {
+
+__global__ void __launch_bounds__(256)
+    k_project(const float* __restrict__ P, int64_t n, int64_t n_pad, CamDev cam, float4* __restrict__ rec,
+              float* __restrict__ depth, int32_t* __restrict__ radius, uint2* __restrict__ rect,
+              uint32_t* __restrict__ count, uint32_t* __restrict__ dev_status) {
+  const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+  for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n_pad; i += stride) {
+    Geo g;
+    g.visible = false;
+    g.nonfinite = false;
+    if (i < n) project_geo(P, n_pad, i, cam, g);
+    bool vis = g.visible;
+    bool nonfin = g.nonfinite;
+    float o = 0.0f, rgb[3] = {0.0f, 0.0f, 0.0f};
+    if (vis) {
+      o = opacity_of(ldp(P, n_pad, 10, i));
+      float d[3], len;
+      view_dir(g.mux, g.muy, g.muz, cam, d, &len);
+      float Y[16];
+      sh_basis(d[0], d[1], d[2], Y);
+      bool cl[3];
+      sh_colour(P, n_pad, i, Y, rgb, cl, &nonfin);
+      if (nonfin) vis = false;
+    }
+    if (nonfin) raise_status(dev_status, GS_ERR_NONFINITE);
+    if (vis) {
+      rec[3 * i + 0] = make_float4(g.mx, g.my, __fmul_rn(-0.5f, g.A), -g.B);
+      rec[3 * i + 1] = make_float4(__fmul_rn(-0.5f, g.C), o, rgb[0], rgb[1]);
+      rec[3 * i + 2] = make_float4(rgb[2], __uint_as_float(uint32_t(i)), 0.0f, 0.0f);
+      depth[i] = g.tz;
+      radius[i] = g.radius;
+      rect[i] = make_uint2(uint32_t(g.tx0) | (uint32_t(g.ty0) << 16), uint32_t(g.tx1) | (uint32_t(g.ty1) << 16));
+      count[i] = uint32_t(g.tx1 - g.tx0 + 1) * uint32_t(g.ty1 - g.ty0 + 1);
+    } else {
+      depth[i] = 0.0f;
+      radius[i] = 0;
+      rect[i] = make_uint2(0u, 0u);
+      count[i] = 0u;
+    }
+  }
+}
+
+}  // namespace gs
+
+extern "C" gs_status gs_project(gs_dims dims, const float* params, const gs_camera* cam, gs_proj proj,
+                                uint32_t* dev_status, cudaStream_t stream) {
+  using namespace gs;
+  if (!dims_ok(dims) || !camera_ok(cam) || !params || !dev_status) return GS_ERR_INVALID_ARG;
+  if (!proj.rec || !proj.depth || !proj.radius || !proj.rect || !proj.count) return GS_ERR_INVALID_ARG;
+  if (!aligned(params, 16) || !aligned(proj.rec, 16) || !aligned(proj.rect, 8)) return GS_ERR_INVALID_ARG;
+  if (dims.n == 0 && dims.n_pad == 0) return GS_OK;
+  const int threads = 256;
+  const int blocks = grid_for(dims.n_pad, threads, kSmCount * 64);
+  k_project<<<blocks, threads, 0, stream>>>(params, dims.n, dims.n_pad, cam_dev(*cam),
+                                            reinterpret_cast<float4*>(proj.rec), proj.depth, proj.radius,
+                                            reinterpret_cast<uint2*>(proj.rect), proj.count, dev_status);
+  return launch_status();
+}

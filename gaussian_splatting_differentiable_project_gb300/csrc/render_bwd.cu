@@ -1,0 +1,221 @@
+// gs_render_bwd: L1 loss gradient and the compositing backward.
+//
+// One CTA per tile, one thread per pixel, the tile's records staged in reverse
+// batches by cp.async.bulk (as in the forward).  Each pixel walks its composited
+// entries back to front, recovering the transmittance before each entry by
+// division by (1 - alpha) and carrying the normalised colour of everything
+// behind it.  Per entry each lane holds nine partials; a warp that has any
+// contribution reduces them with a shuffle reduce-scatter (14 shuffles instead
+// of 45 for nine butterflies) and nine lanes issue one global atomic each.
+#include "api_util.h"
+#include "raster_common.cuh"
+
+namespace gs {
+
+// Reduce-scatter of nine per-lane values over the warp.  On return lane l with
+// (l & 3) == 0 holds the warp sum of value l >> 2 (values 0..7) in *out8 and every
+// lane holds the warp sum of value 8 in *out9.
+__device__ __forceinline__ void warp_reduce9(const float v[9], float* out8, float* out9) {
+  const int lane = threadIdx.x & 31;
+  const bool b16 = lane & 16, b8 = lane & 8, b4 = lane & 4;
+  float w[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float send = b16 ? v[k] : v[k + 4];
+    const float keep = b16 ? v[k + 4] : v[k];
+    w[k] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+  }
+  float x[2];
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const float send = b8 ? w[k] : w[k + 2];
+    const float keep = b8 ? w[k + 2] : w[k];
+    x[k] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+  }
+  {
+    const float send = b4 ? x[0] : x[1];
+    const float keep = b4 ? x[1] : x[0];
+    float y = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+    y += __shfl_xor_sync(0xffffffffu, y, 2);
+    y += __shfl_xor_sync(0xffffffffu, y, 1);
+    *out8 = y;
+  }
+  float z = v[8];
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+  *out9 = z;
+}
+
+__global__ void __launch_bounds__(kRasterThreads)
+    k_render_bwd(const Rec* __restrict__ srec, const uint2* __restrict__ ranges, const uint32_t* __restrict__ n_isect,
+                 uint32_t cap, int W, int H, int TX, float bg0, float bg1, float bg2, const float* __restrict__ image,
+                 const float* __restrict__ target, const float* __restrict__ T_final,
+                 const uint32_t* __restrict__ n_contrib, float* __restrict__ grad2d, int64_t n_pad,
+                 float* __restrict__ loss, float inv3P, uint32_t* __restrict__ dev_status) {
+  __shared__ __align__(128) Rec s_rec[2][kBatch];
+  __shared__ __align__(8) uint64_t s_bar[2];
+  __shared__ float s_red[kRasterThreads / 32];
+  __shared__ uint32_t s_max[kRasterThreads / 32];
+
+  const int tile = blockIdx.x;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int pxi, pyi;
+  pixel_of_thread(tile, TX, pxi, pyi);
+  const bool inside = pxi < W && pyi < H;
+  const float px = float(pxi) + 0.5f, py = float(pyi) + 0.5f;
+
+  // per-pixel loss gradient
+  float g0 = 0.0f, g1 = 0.0f, g2 = 0.0f, T = 1.0f, lsum = 0.0f;
+  uint32_t nc = 0;
+  if (inside) {
+    const size_t P = size_t(W) * H;
+    const size_t pix = size_t(pyi) * W + pxi;
+    const float c0 = image[pix], c1 = image[P + pix], c2 = image[2 * P + pix];
+    const float t0 = target[pix], t1 = target[P + pix], t2 = target[2 * P + pix];
+    g0 = (c0 > t0) ? inv3P : ((c0 < t0) ? -inv3P : 0.0f);
+    g1 = (c1 > t1) ? inv3P : ((c1 < t1) ? -inv3P : 0.0f);
+    g2 = (c2 > t2) ? inv3P : ((c2 < t2) ? -inv3P : 0.0f);
+    lsum = fabsf(c0 - t0) + fabsf(c1 - t1) + fabsf(c2 - t2);
+    T = T_final[pix];
+    nc = n_contrib[pix];
+  }
+  // CTA loss partial and the largest n_contrib
+  float ls = lsum;
+  uint32_t mx = nc;
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) {
+    ls += __shfl_xor_sync(0xffffffffu, ls, o);
+    mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  }
+  const uint32_t warp_max = mx;
+  if (lane == 0) {
+    s_red[warp] = ls;
+    s_max[warp] = mx;
+  }
+  __syncthreads();
+  uint32_t n_max = 0;
+  if (threadIdx.x == 0) {
+    float t = 0.0f;
+    for (int w = 0; w < kRasterThreads / 32; ++w) t += s_red[w];
+    atomicAdd(loss, t * inv3P);
+  }
+#pragma unroll
+  for (int w = 0; w < kRasterThreads / 32; ++w) n_max = max(n_max, s_max[w]);
+
+  const uint32_t K = min(*n_isect, cap);
+  const uint2 rg = ranges[tile];
+  const uint32_t start = min(rg.x, K), end = min(max(rg.y, rg.x), K);
+  n_max = min(n_max, end - start);
+  if (n_max == 0) return;
+
+  BatchStager st{srec + start, n_max, s_rec[0], s_rec[1], s_bar};
+  const int nb = int((n_max + kBatch - 1) / kBatch);
+  if (threadIdx.x == 0) {
+    mbar_init(&s_bar[0], 1);
+    mbar_init(&s_bar[1], 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  // batches are consumed last to first; use u counts consumption order
+  if (threadIdx.x == 0) {
+    st.issue(nb - 1, 0);
+    if (nb > 1) st.issue(nb - 2, 1);
+  }
+  float acc0 = bg0, acc1 = bg1, acc2 = bg2;
+  float* gp = grad2d;
+  for (int u = 0; u < nb; ++u) {
+    const int b = nb - 1 - u;
+    const int slot = u & 1;
+    mbar_wait(&s_bar[slot], uint32_t((u >> 1) & 1), dev_status);
+    const Rec* R = st.buffer(slot);
+    const uint32_t pos0 = uint32_t(b) * kBatch;
+    const int cnt = int(st.count(b));
+    // this warp only needs entries below its largest n_contrib
+    const int jmax = int(min(uint32_t(cnt), warp_max > pos0 ? warp_max - pos0 : 0u));
+    for (int j = jmax - 1; j >= 0; --j) {
+      const uint32_t pos = pos0 + uint32_t(j);
+      float v[9];
+      bool contrib = false;
+      const float4 ra = R[j].a;
+      const float4 rb = R[j].b;
+      const float4 rc = R[j].c;
+      if (pos < nc) {
+        const float dx = __fsub_rn(px, ra.x), dy = __fsub_rn(py, ra.y);
+        const float power = conic_power(dx, dy, ra.z, ra.w, rb.x);
+        if (!(power > 0.0f) && !(power < kPowerSkip)) {
+          const float e = gs_expf_core(power);
+          const float vv = __fmul_rn(rb.y, e);
+          const bool clamped = !(vv < kAlphaMax);
+          const float alpha = clamped ? kAlphaMax : vv;
+          if (!(alpha < kAlphaMin)) {
+            contrib = true;
+            const float Ti = T / (1.0f - alpha);
+            const float wgt = alpha * Ti;
+            v[6] = g0 * wgt;
+            v[7] = g1 * wgt;
+            v[8] = g2 * wgt;
+            const float dLda = Ti * (g0 * (rb.z - acc0) + g1 * (rb.w - acc1) + g2 * (rc.x - acc2));
+            acc0 = alpha * rb.z + (1.0f - alpha) * acc0;
+            acc1 = alpha * rb.w + (1.0f - alpha) * acc1;
+            acc2 = alpha * rc.x + (1.0f - alpha) * acc2;
+            T = Ti;
+            const float dLdp = clamped ? 0.0f : dLda * alpha;
+            v[5] = clamped ? 0.0f : dLda * e;
+            // power = ca dx^2 + cb dx dy + cc dy^2 with (ca, cb, cc) = (-A/2, -B, -C/2)
+            v[0] = -dLdp * (2.0f * ra.z * dx + ra.w * dy);  // d/d mean x (dx = px - mx)
+            v[1] = -dLdp * (ra.w * dx + 2.0f * rb.x * dy);  // d/d mean y
+            v[2] = -0.5f * dLdp * dx * dx;                  // d/dA
+            v[3] = -dLdp * dx * dy;                         // d/dB
+            v[4] = -0.5f * dLdp * dy * dy;                  // d/dC
+          }
+        }
+      }
+      if (!contrib) {
+#pragma unroll
+        for (int q = 0; q < 9; ++q) v[q] = 0.0f;
+      }
+      if (__any_sync(0xffffffffu, contrib)) {
+        float s8, s9;
+        warp_reduce9(v, &s8, &s9);
+        const uint32_t gid = __float_as_uint(rc.y);
+        if ((lane & 3) == 0) atomicAdd(gp + int64_t(lane >> 2) * n_pad + gid, s8);
+        if (lane == 1) atomicAdd(gp + int64_t(8) * n_pad + gid, s9);
+      }
+    }
+    __syncthreads();
+    if (u + 2 < nb) {
+      if (threadIdx.x == 0) st.issue(nb - 1 - (u + 2), slot);
+    }
+  }
+}
+
+__global__ void k_zero4(float4* __restrict__ p, int64_t n4, float* __restrict__ scalar) {
+  const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+  for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n4; i += stride)
+    p[i] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+  if (blockIdx.x == 0 && threadIdx.x == 0 && scalar) *scalar = 0.0f;
+}
+
+}  // namespace gs
+
+extern "C" gs_status gs_render_bwd(gs_dims dims, const gs_camera* cam, const gs_bins* bins, uint32_t capacity_K,
+                                   const float bg[3], const float* image, const float* target, const float* T_final,
+                                   const uint32_t* n_contrib, float* grad2d, float* loss_out, uint32_t* dev_status,
+                                   cudaStream_t stream) {
+  using namespace gs;
+  if (!dims_ok(dims) || !camera_ok(cam) || !bins || !bg || !image || !target || !T_final || !n_contrib || !grad2d ||
+      !loss_out || !dev_status)
+    return GS_ERR_INVALID_ARG;
+  if (!bins->rec || !bins->ranges || !bins->n_isect || capacity_K == 0) return GS_ERR_INVALID_ARG;
+  if (!aligned(bins->rec, 16) || !aligned(bins->ranges, 8) || !aligned(grad2d, 16)) return GS_ERR_INVALID_ARG;
+  const int64_t n4 = int64_t(GS_N_GRAD2D) * dims.n_pad / 4;
+  k_zero4<<<grid_for(n4, 256, kSmCount * 8), 256, 0, stream>>>(reinterpret_cast<float4*>(grad2d), n4, loss_out);
+  const int TX = (cam->width + kTile - 1) / kTile;
+  const int64_t tiles = n_tiles(cam);
+  const float inv3P = float(1.0 / (3.0 * double(cam->width) * double(cam->height)));
+  k_render_bwd<<<int(tiles), kRasterThreads, 0, stream>>>(
+      reinterpret_cast<const Rec*>(bins->rec), reinterpret_cast<const uint2*>(bins->ranges), bins->n_isect,
+      capacity_K, cam->width, cam->height, TX, bg[0], bg[1], bg[2], image, target, T_final, n_contrib, grad2d,
+      dims.n_pad, loss_out, inv3P, dev_status);
+  return launch_status();
+}

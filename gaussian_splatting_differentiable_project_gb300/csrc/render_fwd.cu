@@ -1,0 +1,118 @@
+// gs_render_fwd: per-tile front-to-back alpha compositing.
+//
+// One CTA per 16x16 tile, one thread per pixel.  The tile's sorted records are
+// staged into shared memory in batches of 256 (12 KB) by cp.async.bulk with two
+// mbarrier-tracked buffers, so the next batch streams in while the current one is
+// composited; every thread reads the same record (shared-memory broadcast).  A
+// pixel stops at its transmittance threshold; the CTA stops loading once
+// __syncthreads_count reports no live pixel.
+#include "api_util.h"
+#include "raster_common.cuh"
+
+namespace gs {
+
+__global__ void __launch_bounds__(kRasterThreads)
+    k_render_fwd(const Rec* __restrict__ srec, const uint2* __restrict__ ranges, const uint32_t* __restrict__ n_isect,
+                 uint32_t cap, int W, int H, int TX, float bg0, float bg1, float bg2, float* __restrict__ image,
+                 float* __restrict__ T_final, uint32_t* __restrict__ n_contrib, uint32_t* __restrict__ dev_status) {
+  __shared__ __align__(128) Rec s_rec[2][kBatch];
+  __shared__ __align__(8) uint64_t s_bar[2];
+
+  const int tile = blockIdx.x;
+  int pxi, pyi;
+  pixel_of_thread(tile, TX, pxi, pyi);
+  const bool inside = pxi < W && pyi < H;
+  const float px = float(pxi) + 0.5f, py = float(pyi) + 0.5f;
+
+  const uint32_t K = min(*n_isect, cap);
+  const uint2 rg = ranges[tile];
+  const uint32_t start = min(rg.x, K), end = min(max(rg.y, rg.x), K);
+  const uint32_t n = end - start;
+
+  float T = 1.0f, C0 = 0.0f, C1 = 0.0f, C2 = 0.0f;
+  uint32_t last = 0;
+  bool done = !inside;
+
+  if (n > 0) {
+    BatchStager st{srec + start, n, s_rec[0], s_rec[1], s_bar};
+    const int nb = int((n + kBatch - 1) / kBatch);
+    if (threadIdx.x == 0) {
+      mbar_init(&s_bar[0], 1);
+      mbar_init(&s_bar[1], 1);
+      fence_mbar_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      st.issue(0, 0);
+      if (nb > 1) st.issue(1, 1);
+    }
+    int issued = nb < 2 ? nb : 2;
+    for (int b = 0; b < nb; ++b) {
+      const int slot = b & 1;
+      mbar_wait(&s_bar[slot], uint32_t((b >> 1) & 1), dev_status);
+      const Rec* R = st.buffer(slot);
+      const int cnt = int(st.count(b));
+      const uint32_t pos0 = uint32_t(b) * kBatch;
+      if (!done) {
+        for (int j = 0; j < cnt; ++j) {
+          const float4 ra = R[j].a;  // mx, my, ca, cb
+          const float dx = __fsub_rn(px, ra.x), dy = __fsub_rn(py, ra.y);
+          const float4 rb = R[j].b;  // cc, o, r, g
+          const float power = conic_power(dx, dy, ra.z, ra.w, rb.x);
+          if (power > 0.0f || power < kPowerSkip) continue;
+          const float v = __fmul_rn(rb.y, gs_expf_core(power));
+          const float alpha = (v < kAlphaMax) ? v : kAlphaMax;
+          if (alpha < kAlphaMin) continue;
+          const float Tn = __fmul_rn(T, __fsub_rn(1.0f, alpha));
+          if (Tn < kTMin) {
+            done = true;
+            break;
+          }
+          const float w = __fmul_rn(alpha, T);
+          const float cb = R[j].c.x;
+          C0 = __fmaf_rn(rb.z, w, C0);
+          C1 = __fmaf_rn(rb.w, w, C1);
+          C2 = __fmaf_rn(cb, w, C2);
+          T = Tn;
+          last = pos0 + uint32_t(j) + 1u;
+        }
+      }
+      const int alive = __syncthreads_count(!done);
+      if (alive == 0) {
+        // no pixel needs more: drain copies still in flight before the CTA exits
+        for (int q = b + 1; q < issued; ++q) mbar_wait(&s_bar[q & 1], uint32_t((q >> 1) & 1), dev_status);
+        break;
+      }
+      if (b + 2 < nb) {
+        if (threadIdx.x == 0) st.issue(b + 2, slot);
+        issued = b + 3;
+      }
+    }
+  }
+  if (inside) {
+    const size_t P = size_t(W) * H;
+    const size_t pix = size_t(pyi) * W + pxi;
+    image[pix] = __fmaf_rn(T, bg0, C0);
+    image[P + pix] = __fmaf_rn(T, bg1, C1);
+    image[2 * P + pix] = __fmaf_rn(T, bg2, C2);
+    T_final[pix] = T;
+    n_contrib[pix] = last;
+  }
+}
+
+}  // namespace gs
+
+extern "C" gs_status gs_render_fwd(const gs_camera* cam, const gs_bins* bins, uint32_t capacity_K, const float bg[3],
+                                   float* image, float* T_final, uint32_t* n_contrib, uint32_t* dev_status,
+                                   cudaStream_t stream) {
+  using namespace gs;
+  if (!camera_ok(cam) || !bins || !bg || !image || !T_final || !n_contrib || !dev_status) return GS_ERR_INVALID_ARG;
+  if (!bins->rec || !bins->ranges || !bins->n_isect || capacity_K == 0) return GS_ERR_INVALID_ARG;
+  if (!aligned(bins->rec, 16) || !aligned(bins->ranges, 8)) return GS_ERR_INVALID_ARG;
+  const int TX = (cam->width + kTile - 1) / kTile;
+  const int64_t tiles = n_tiles(cam);
+  k_render_fwd<<<int(tiles), kRasterThreads, 0, stream>>>(
+      reinterpret_cast<const Rec*>(bins->rec), reinterpret_cast<const uint2*>(bins->ranges), bins->n_isect,
+      capacity_K, cam->width, cam->height, TX, bg[0], bg[1], bg[2], image, T_final, n_contrib, dev_status);
+  return launch_status();
+}

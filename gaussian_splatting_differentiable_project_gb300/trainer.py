@@ -1,0 +1,77 @@
+"""Buffers and call order of one training step (one camera view per step).
+
+The step is the six C-ABI calls in order: project -> bin_sort -> render_fwd ->
+render_bwd -> project_bwd -> adam_step, all enqueued on one CUDA stream with no
+host synchronisation inside the step.  Parameters, Adam moments and every
+transient buffer stay resident on the device; the device status word is read
+only when the caller asks for it.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from . import (BinBuffers, ProjBuffers, N_GRAD2D, adam_step, bin_sort, project, project_bwd, render_bwd, render_fwd,
+               status_str)
+
+
+class Trainer:
+    def __init__(self, params, n: int, width: int, height: int, capacity: int, lr_plane, betas=(0.9, 0.999),
+                 eps: float = 1e-15, bg=(0.0, 0.0, 0.0), device="cuda"):
+        import torch
+        if isinstance(params, np.ndarray):
+            params = torch.from_numpy(np.ascontiguousarray(params, np.float32))
+        self.params = params.to(device=device, dtype=torch.float32).contiguous()
+        self.n = int(n)
+        self.n_pad = int(self.params.shape[1])
+        self.width, self.height = int(width), int(height)
+        self.m = torch.zeros_like(self.params)
+        self.v = torch.zeros_like(self.params)
+        self.grads = torch.empty_like(self.params)
+        self.grad2d = torch.empty((N_GRAD2D, self.n_pad), dtype=torch.float32, device=device)
+        self.proj = ProjBuffers(self.n_pad, device)
+        self.bins = BinBuffers(self.n, capacity, width, height, device)
+        self.image = torch.empty((3, height, width), dtype=torch.float32, device=device)
+        self.T_final = torch.empty((height, width), dtype=torch.float32, device=device)
+        self.n_contrib = torch.empty((height, width), dtype=torch.int32, device=device)
+        self.loss = torch.zeros(1, dtype=torch.float32, device=device)
+        self.status = torch.zeros(1, dtype=torch.int32, device=device)
+        self.lr_plane = np.asarray(lr_plane, np.float64)
+        self.beta1, self.beta2 = float(betas[0]), float(betas[1])
+        self.eps = float(eps)
+        self.bg = tuple(float(x) for x in bg)
+        self.t = 0
+
+    # the stages ------------------------------------------------------------------
+    def forward(self, cam: dict, stream=None) -> None:
+        project(self.n, self.params, cam, self.proj, self.status, stream)
+        bin_sort(self.n, self.n_pad, self.proj, cam, self.bins, self.status, stream)
+        render_fwd(cam, self.bins, self.bg, self.image, self.T_final, self.n_contrib, self.status, stream)
+
+    def backward(self, cam: dict, target, stream=None) -> None:
+        render_bwd(self.n, self.n_pad, cam, self.bins, self.bg, self.image, target, self.T_final, self.n_contrib,
+                   self.grad2d, self.loss, self.status, stream)
+        project_bwd(self.n, self.params, cam, self.proj, self.grad2d, self.grads, self.status, stream)
+
+    def optimizer_step(self, stream=None) -> None:
+        self.t += 1
+        adam_step(self.n, self.params, self.grads, self.m, self.v, self.lr_plane, self.beta1, self.beta2, self.eps,
+                  self.t, stream)
+
+    def step(self, cam: dict, target, stream=None) -> None:
+        """One optimisation step for one view: forward, backward, Adam."""
+        self.forward(cam, stream)
+        self.backward(cam, target, stream)
+        self.optimizer_step(stream)
+
+    # host-side reads (synchronise) -----------------------------------------------
+    def n_isect(self) -> int:
+        return int(self.bins.n_isect[0].item()) & 0xFFFFFFFF
+
+    def check_status(self) -> int:
+        s = int(self.status[0].item()) & 0xFFFFFFFF
+        return s
+
+    def raise_on_status(self) -> None:
+        s = self.check_status()
+        if s:
+            raise RuntimeError(f"device status {s}: {status_str(s)}")

@@ -160,6 +160,16 @@ class BlobField:
             g -= (e / (s * s))[:, None] * d
         return f, g
 
+    def value_grad_torch(self, x):
+        import torch
+        c = torch.as_tensor(self.centres, dtype=x.dtype, device=x.device)     # (B, 3)
+        s2 = torch.as_tensor(self.sigmas, dtype=x.dtype, device=x.device) ** 2  # (B,)
+        d = x[:, None, :] - c[None]                                              # (n, B, 3)
+        e = torch.exp(-(d * d).sum(-1) / (2.0 * s2))                              # (n, B)
+        f = e.sum(1) - 0.5
+        g = -((e / s2)[:, :, None] * d).sum(1)
+        return f, g
+
 
 @dataclass
 class TurbulenceField:
@@ -184,19 +194,39 @@ class TurbulenceField:
         g = (np.cos(arg) * a) @ k
         return f, g
 
+    def value_grad_torch(self, x):
+        import torch
+        k = torch.as_tensor(2.0 * math.pi * self.nu[:, None] * self.u, dtype=x.dtype, device=x.device)
+        ph = torch.as_tensor(self.phase, dtype=x.dtype, device=x.device)
+        a = torch.as_tensor(1.0 / self.nu, dtype=x.dtype, device=x.device)
+        arg = x @ k.T + ph
+        return torch.sin(arg) @ a, (torch.cos(arg) * a) @ k
+
 
 def sample_level_set(field, n: int, rng: np.random.Generator, jitter: float = 0.002,
-                     newton_steps: int = 8, tol: float = 1e-5, chunk: int = 1 << 18) -> np.ndarray:
+                     newton_steps: int = 8, tol: float = 1e-5, chunk: int = 1 << 18, device=None) -> np.ndarray:
     """Points on the zero level set: uniform candidates in [-1,1]^3, Newton steps
-    x <- x - f grad f / |grad f|^2, keep |f| < tol inside the cube, then jitter."""
+    x <- x - f grad f / |grad f|^2, keep |f| < tol inside the cube, then jitter.
+    The candidates and jitter come from ``rng``; with ``device`` (a torch device)
+    the Newton iterations run in torch fp64 there instead of numpy."""
     out, have = [], 0
     while have < n:
         x = rng.uniform(-1.0, 1.0, (chunk, 3))
-        for _ in range(newton_steps):
-            f, g = field.value_grad(x)
-            gg = np.einsum("ij,ij->i", g, g)
-            x = x - (f / np.maximum(gg, 1e-30))[:, None] * g
-        f, _ = field.value_grad(x)
+        if device is None:
+            for _ in range(newton_steps):
+                f, g = field.value_grad(x)
+                gg = np.einsum("ij,ij->i", g, g)
+                x = x - (f / np.maximum(gg, 1e-30))[:, None] * g
+            f, _ = field.value_grad(x)
+        else:
+            import torch
+            xt = torch.as_tensor(x, dtype=torch.float64, device=device)
+            for _ in range(newton_steps):
+                f, g = field.value_grad_torch(xt)
+                gg = (g * g).sum(1)
+                xt = xt - (f / torch.clamp(gg, min=1e-30))[:, None] * g
+            f, _ = field.value_grad_torch(xt)
+            x, f = xt.cpu().numpy(), f.cpu().numpy()
         ok = (np.abs(f) < tol) & np.all(np.abs(x) <= 1.0, axis=1)
         x = x[ok]
         out.append(x)
@@ -215,14 +245,17 @@ def knn_log_scale(points: np.ndarray, k: int = 3) -> np.ndarray:
 
 
 def isosurface_scene(field_seed: int, sample_seed: int, n: int, kind: str = "blobs",
-                     n_pad: int | None = None) -> np.ndarray:
+                     n_pad: int | None = None, device=None) -> np.ndarray:
     """Isosurface scene: means on the level set of the seeded field, kNN log-scales
     on all three axes, quaternions identity + N(0, 0.1^2) normalised, opacity
     logits 0.1 N(0,1), SH DC U(-1,1) and higher bands N(0, 0.05^2)."""
     field = BlobField.make(field_seed) if kind == "blobs" else TurbulenceField.make(field_seed)
     rng = np.random.default_rng(sample_seed)
-    chunk = 1 << 18 if kind == "blobs" else 1 << 15
-    means = sample_level_set(field, n, rng, chunk=chunk)
+    if device is None:
+        chunk = 1 << 18 if kind == "blobs" else 1 << 15
+    else:
+        chunk = 1 << 21 if kind == "blobs" else 1 << 18
+    means = sample_level_set(field, n, rng, chunk=chunk, device=device)
     ls = knn_log_scale(means)
     log_scales = np.repeat(ls[:, None], 3, axis=1)
     q = np.zeros((n, 4))
@@ -267,22 +300,23 @@ def cameras_for(cfg: Config) -> list[dict]:
     return fibonacci_cameras(cfg.n_views, cfg.width, cfg.height)
 
 
-def scene_for(cfg: Config, seed: int = 0, n: int | None = None) -> np.ndarray:
+def scene_for(cfg: Config, seed: int = 0, n: int | None = None, device=None) -> np.ndarray:
     """Model parameters for a config (``n`` overrides the Gaussian count for
-    reduced-size parity cases of the same generator)."""
+    reduced-size parity cases of the same generator; ``device`` runs the level-set
+    Newton iterations in torch on that device)."""
     n = cfg.n if n is None else n
     if cfg.kind == "cube":
         return random_cube_scene(seed, n)
-    return isosurface_scene(seed, 1000 + seed, n, cfg.kind)
+    return isosurface_scene(seed, 1000 + seed, n, cfg.kind, device=device)
 
 
-def target_scene_for(cfg: Config, seed: int = 0, n: int | None = None) -> np.ndarray:
+def target_scene_for(cfg: Config, seed: int = 0, n: int | None = None, device=None) -> np.ndarray:
     """The second seeded Gaussian set whose renders are the targets: for the
     isosurface configs the same surface sampled with another seed."""
     n = cfg.n if n is None else n
     if cfg.kind == "cube":
         return random_cube_scene(seed + 1, n)
-    return isosurface_scene(seed, 2000 + seed, n, cfg.kind)
+    return isosurface_scene(seed, 2000 + seed, n, cfg.kind, device=device)
 
 
 def offset_target(image: np.ndarray, seed: int, lo: float = 0.05, hi: float = 0.15) -> np.ndarray:

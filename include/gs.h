@@ -1,0 +1,261 @@
+/*
+ * gs.h -- C ABI of the GB300 (sm_103a) 3D Gaussian Splatting training step.
+ *
+ * One optimisation step of a scene of anisotropic 3D Gaussians (mean,
+ * scale + quaternion covariance, degree-3 SH colour, opacity) for one camera:
+ *
+ *   gs_project      EWA projection + SH colour, one thread per Gaussian
+ *   gs_bin_sort     tile binning: (tile, depth) keys, onesweep radix sort, per-tile
+ *                   ranges, records gathered into sorted order
+ *   gs_render_fwd   per-tile front-to-back alpha compositing with early termination
+ *   gs_render_bwd   L1 loss gradient and the reverse-order compositing backward
+ *   gs_project_bwd  chain rule from the 2D gradients to the 59 parameters
+ *   gs_adam_step    fused Adam update over every parameter plane
+ *
+ * The method is the one "Toward Distributed 3D Gaussian Splatting for
+ * High-Resolution Isosurface Visualization" (section III) trains and "Scaling 3D
+ * Gaussian Splatting with Distributed Compute" describes stage by stage: the
+ * Gaussian representation and its 59 parameters (memory-wall section), projection
+ * as per-Gaussian work and rasterisation as per-pixel work (section on what gsplat
+ * distributes), the projected record and SH evaluated before compositing (step
+ * walkthrough), tile intersection lists (trace section), gradients flowing back to
+ * mean, covariance, colour and opacity, and Adam per parameter.  Thresholds and
+ * formulas the pages do not print follow the 3DGS method they cite (Kerbl et al.
+ * 2023); each reading is stated at the call it affects.
+ *
+ * Conventions for every call
+ *   - Ownership: the caller owns every buffer (device memory unless stated) and the
+ *     stream.  The library never allocates, frees or synchronises.
+ *   - Asynchrony: every call only enqueues kernels on `stream` and returns.
+ *   - Errors: argument errors (null or misaligned pointers, bad sizes) are
+ *     returned at once as a gs_status and nothing is enqueued.  A failed launch
+ *     returns GS_ERR_CUDA.  Errors detected on the device (intersection capacity
+ *     exceeded, non-finite parameters, a bounded wait that ran out) are OR-ed into
+ *     the caller's device word `dev_status` (bits of gs_status) and the kernels
+ *     return normally: nothing traps.  Read dev_status after the step.
+ *   - Precision: fp32 everywhere.  Quantities that decide an integer (radius, tile
+ *     rect, depth key, compositing decisions) follow a frozen fp32 operation
+ *     sequence with a Cody-Waite exponential, so they are reproducible bit for bit
+ *     by a plain CPU implementation of the same sequence.
+ *
+ * Parameter layout (`params`, `grads`, `m`, `v`): 59 fp32 planes of stride n_pad
+ * (n_pad a multiple of 256, entries [n, n_pad) are padding):
+ *   0-2 mean mu, 3-5 log-scale, 6-9 quaternion (w, x, y, z), 10 opacity logit,
+ *   11 + 3k + ch: SH coefficient k (< 16) of colour channel ch.
+ */
+#ifndef GS_H
+#define GS_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define GS_N_PLANES 59
+#define GS_TILE 16          /* tile edge in pixels */
+#define GS_REC_FLOATS 12    /* projected record: 48 bytes */
+#define GS_N_GRAD2D 9       /* 2D gradient planes */
+
+typedef enum gs_status {
+  GS_OK = 0,
+  GS_ERR_INVALID_ARG = 1, /* returned: bad pointer, size or alignment */
+  GS_ERR_CUDA = 2,        /* returned: a kernel launch failed */
+  GS_ERR_CAPACITY = 4,    /* device: more tile intersections than capacity_K */
+  GS_ERR_TIMEOUT = 8,     /* device: a bounded inter-block wait gave up */
+  GS_ERR_NONFINITE = 16   /* device: a Gaussian with NaN/Inf parameters (culled) */
+} gs_status;
+
+/* Pinhole camera.  R is the world->camera rotation (row-major) and t the
+ * translation, with camera axes x right, y down, z forward.  fx, fy, cx, cy in
+ * pixels; pixel (i, j) has its centre at (i + 0.5, j + 0.5).  campos is the camera
+ * centre in world space (for the SH view direction).  Gaussians with camera-space
+ * z <= near_z are culled. */
+typedef struct gs_camera {
+  float R[9];
+  float t[3];
+  float fx, fy, cx, cy;
+  int32_t width, height;
+  float campos[3];
+  float near_z;
+} gs_camera;
+
+/* n Gaussians stored in planes of stride n_pad (n_pad % 256 == 0, n <= n_pad). */
+typedef struct gs_dims {
+  int64_t n;
+  int64_t n_pad;
+} gs_dims;
+
+/* Per-Gaussian projection output (device arrays of n_pad entries, caller-owned).
+ *   rec    12 floats per Gaussian (16-byte aligned): mean2d x, y; (ca, cb, cc) =
+ *          (-A/2, -B, -C/2) for the conic [[A, B], [B, C]] (inverse 2D covariance),
+ *          so that power = ca dx^2 + cb dx dy + cc dy^2; opacity; r, g, b; the
+ *          Gaussian's index (uint32 bits); 2 unused.  The pages' projected record
+ *          (means2d, depth, conic, opacity, colour) minus depth and radius, which
+ *          are kept in their own arrays.
+ *   depth  camera-space z.
+ *   radius pixel radius ceil(3 sqrt(lambda_max)), 0 if culled.
+ *   rect   2 uint32 per Gaussian: (tx0 | ty0 << 16, tx1 | ty1 << 16), inclusive tile
+ *          bounds of the box [mean - r, mean + r].
+ *   count  number of tiles in rect, 0 if culled. */
+typedef struct gs_proj {
+  float* rec;
+  float* depth;
+  int32_t* radius;
+  uint32_t* rect;
+  uint32_t* count;
+} gs_proj;
+
+/* Tile bins (device arrays, caller-owned).
+ *   keys     capacity_K uint64 keys (tile << 32 | fp32 depth bits), sorted.
+ *   ids      capacity_K uint32 Gaussian indices in key order (ties by index).
+ *   rec      capacity_K records (12 floats, 16-byte aligned) in key order.
+ *   ranges   2 uint32 per tile: [start, end) of the tile's entries.
+ *   n_isect  1 uint32: the total number of tile intersections K of this view
+ *            (may exceed capacity_K, in which case GS_ERR_CAPACITY is raised
+ *            and only the first capacity_K entries exist). */
+typedef struct gs_bins {
+  uint64_t* keys;
+  uint32_t* ids;
+  float* rec;
+  uint32_t* ranges;
+  uint32_t* n_isect;
+} gs_bins;
+
+/* ---------------------------------------------------------------------------
+ * gs_project -- projection of every Gaussian for one camera.
+ * "Scaling 3D Gaussian Splatting with Distributed Compute", step walkthrough
+ * (project locally: 2D means, depths, conics, radii, visibility; SH evaluated to
+ * RGB before compositing).  Per Gaussian: t = R mu + t; cull if t.z <= near_z;
+ * Sigma = M M^T with M = R(q / |q|) diag(exp(log-scale)); 2D covariance
+ * J W Sigma W^T J^T + 0.3 I with the perspective Jacobian J at the mean (abscissae
+ * clamped to 1.3 x the half field of view); conic = its inverse; radius =
+ * ceil(3 sqrt(mid + sqrt(max(0.1, mid^2 - det)))); tile rect of the box
+ * [mean - r, mean + r], culled if empty; opacity = sigmoid(logit); colour =
+ * max(0, sum_k Y_k(dir) sh_k + 0.5) with real SH (Condon-Shortley phase) at the
+ * unit direction from campos to mu.
+ *   params  59 x n_pad fp32 (read).   proj: outputs (write), n_pad entries each.
+ *   dev_status: device uint32 (GS_ERR_NONFINITE may be OR-ed in).
+ * Errors: GS_ERR_INVALID_ARG for null/misaligned pointers, n < 0, n > n_pad,
+ * n_pad % 256 != 0, width/height <= 0 or not finite intrinsics.  n == 0 is a no-op. */
+gs_status gs_project(gs_dims dims, const float* params, const gs_camera* cam, gs_proj proj,
+                     uint32_t* dev_status, cudaStream_t stream);
+
+/* Bytes of device scratch gs_bin_sort needs for n Gaussians, capacity_K
+ * intersections and the camera's tile grid. */
+size_t gs_bin_sort_workspace_bytes(gs_dims dims, uint32_t capacity_K, int32_t width, int32_t height);
+
+/* ---------------------------------------------------------------------------
+ * gs_bin_sort -- tile binning.  "Scaling 3D Gaussian Splatting with Distributed
+ * Compute", memory-wall section (per-tile sorted lists of Gaussian-to-pixel
+ * intersections) and trace section (one tile-intersection pass per Gaussian, one
+ * offset pass per intersection).  Exclusive scan of count -> K; each visible
+ * Gaussian emits one key (tile_id << 32 | fp32 bits of depth) per tile of its rect
+ * in index order; a stable onesweep LSD radix sort (8-bit digits, decoupled
+ * look-back with a bounded wait) over the low 32 + ceil(log2 tiles) key bits; tile
+ * ranges; records gathered into key order.  The result per tile is the ordered
+ * subsequence of the global (depth, index) order of the Gaussians whose rect
+ * contains the tile.
+ *   proj      output of gs_project (read).
+ *   workspace device scratch of at least gs_bin_sort_workspace_bytes(), 256-byte
+ *             aligned; contents need not be initialised and are clobbered.
+ *   bins      outputs (write); keys/ids/rec hold capacity_K entries.
+ * Errors: GS_ERR_INVALID_ARG as for gs_project, plus capacity_K == 0 or > 2^30,
+ * workspace too small or misaligned.  K > capacity_K sets GS_ERR_CAPACITY on the
+ * device; the look-back wait running out sets GS_ERR_TIMEOUT. */
+gs_status gs_bin_sort(gs_dims dims, const gs_proj* proj, const gs_camera* cam, uint32_t capacity_K,
+                      gs_bins bins, void* workspace, size_t workspace_bytes, uint32_t* dev_status,
+                      cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * gs_render_fwd -- per-tile front-to-back alpha compositing.  "Scaling 3D
+ * Gaussian Splatting with Distributed Compute", section on what gsplat
+ * distributes (rasterisation is per-pixel work per camera) and trace section
+ * (tiled rasteriser).  For each pixel over its tile's sorted entries, T = 1:
+ * power = ca dx^2 + cb dx dy + cc dy^2 with d = pixel centre - mean2d; skip if
+ * power > 0; alpha = min(0.99, o exp(power)); skip if alpha < 1/255; stop,
+ * without compositing, if T (1 - alpha) < 1e-4; else C += rgb alpha T and
+ * T *= 1 - alpha.  Output C + T bg.
+ *   bins       from gs_bin_sort (read).   bg: 3 floats (host).
+ *   image      3 x H x W fp32 (channel planes), T_final H x W fp32,
+ *   n_contrib  H x W uint32: entries iterated up to the last composited (write).
+ * Errors: GS_ERR_INVALID_ARG for null/misaligned pointers or bad sizes. */
+gs_status gs_render_fwd(const gs_camera* cam, const gs_bins* bins, uint32_t capacity_K, const float bg[3],
+                        float* image, float* T_final, uint32_t* n_contrib, uint32_t* dev_status,
+                        cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * gs_render_bwd -- L1 loss and the compositing backward.  "Scaling 3D Gaussian
+ * Splatting with Distributed Compute", objective and gradient-descent section
+ * (L1 term between render and ground truth; gradients flow back to mean,
+ * covariance, colour and opacity) and step walkthrough (loss computed locally,
+ * gradients back through the same stages).  loss = mean |C - C*| over the 3 H W
+ * values, dL/dC = sign(C - C*) / (3 H W).  Each pixel walks its composited
+ * entries in reverse, recovering T by division by (1 - alpha), and produces per
+ * entry the partials of the loss with respect to mean2d (x, y), the conic (A, B,
+ * C), opacity and colour (r, g, b); partials of a warp are summed by shuffles
+ * and added to grad2d with global atomics (summation order is not fixed).
+ *   image, T_final, n_contrib: outputs of gs_render_fwd (read).
+ *   target    3 x H x W fp32 (read).
+ *   grad2d    9 x n_pad fp32 (write; zeroed by this call first), planes
+ *             (d mx, d my, d A, d B, d C, d opacity, d r, d g, d b).
+ *   loss_out  1 fp32 (write; zeroed first).
+ * Errors: as gs_render_fwd. */
+gs_status gs_render_bwd(gs_dims dims, const gs_camera* cam, const gs_bins* bins, uint32_t capacity_K,
+                        const float bg[3], const float* image, const float* target, const float* T_final,
+                        const uint32_t* n_contrib, float* grad2d, float* loss_out, uint32_t* dev_status,
+                        cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * gs_project_bwd -- chain rule of gs_project.  "Scaling 3D Gaussian Splatting
+ * with Distributed Compute", objective section (gradients reach mu, Sigma, c and
+ * alpha as they would the weights of a network).  conic -> 2D covariance ->
+ * (Jacobian, Sigma); Jacobian and mean2d -> camera-space mean -> mu; Sigma -> M ->
+ * (rotation -> normalised quaternion -> quaternion, scale -> log-scale); sigmoid
+ * -> logit; colour -> SH coefficients and view direction -> mu.  Clamped colour
+ * channels and clamped Jacobian abscissae pass zero gradient; radius and rect are
+ * constants.  Culled Gaussians and padding get zero gradients.
+ *   params 59 x n_pad (read); proj from gs_project (read); grad2d 9 x n_pad (read);
+ *   grads  59 x n_pad fp32 (write, every entry).
+ * Errors: as gs_project. */
+gs_status gs_project_bwd(gs_dims dims, const float* params, const gs_camera* cam, const gs_proj* proj,
+                         const float* grad2d, float* grads, uint32_t* dev_status, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * gs_adam_step -- fused Adam over all 59 planes (padding included).  "Scaling 3D
+ * Gaussian Splatting with Distributed Compute", DDP background (two moments per
+ * parameter) and step walkthrough (Adam over the rank's own parameters).
+ *   m = beta1 m + (1 - beta1) g;  v = beta2 v + (1 - beta2) g^2;
+ *   p -= (lr[plane] / (1 - beta1^t)) m / (sqrt(v) / sqrt(1 - beta2^t) + eps)
+ * The hyperparameters arrive in fp64; 1 - beta, the bias corrections and the
+ * per-plane step sizes are formed on the host in fp64 and rounded to fp32 once
+ * (so that, e.g., 1 - 0.999 is not taken from an fp32 0.999).
+ *   params, m, v: 59 x n_pad fp32 (read and write, 16-byte aligned);
+ *   grads 59 x n_pad (read); lr_plane: 59 floats (host); t >= 1 the step count.
+ * Errors: GS_ERR_INVALID_ARG for null/misaligned pointers, bad sizes, t < 1 or
+ * betas outside [0, 1). */
+gs_status gs_adam_step(gs_dims dims, float* params, const float* grads, float* m, float* v,
+                       const float lr_plane[GS_N_PLANES], double beta1, double beta2, double eps, int64_t t,
+                       cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * gs_util_expf -- the library's fp32 exponential (Cody-Waite reduction, degree-7
+ * Taylor polynomial, 2^k scaling; the one every compositing decision uses), on n
+ * device floats, so that callers can check it against another implementation.
+ * Errors: GS_ERR_INVALID_ARG for null pointers or n < 0. */
+gs_status gs_util_expf(const float* x, float* y, int64_t n, cudaStream_t stream);
+
+/* Static description of a status value (several bits: the lowest set one). */
+const char* gs_status_str(uint32_t status);
+
+/* Library version, e.g. "gs-gb300 0.1 sm_103a". */
+const char* gs_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GS_H */

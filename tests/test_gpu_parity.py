@@ -1,0 +1,332 @@
+"""GPU <-> oracle parity, stage by stage, through the C ABI.
+
+Both sides get identical seeded inputs from gs_inputs.  Tolerances:
+  * integer, index and key outputs (radius, rect, count, keys, ids, ranges,
+    n_contrib): bit-exact;
+  * projected records, images, T_final: within 1e-5 absolute (the frozen fp32
+    sequence makes them bit-exact; the count of exact matches is asserted too);
+  * 2D and parameter gradients: within 1e-4 relative with an absolute floor of
+    1e-6 x the largest magnitude of that gradient plane (the stated 1e-6 floor is
+    absolute at the tiny config, whose per-pixel loss gradient is 1/(3*128*128);
+    the floor is kept in proportion as the images grow);
+  * Adam: |dp| <= 1e-5 |p_ref| + 1e-7.
+"""
+import numpy as np
+import pytest
+
+import gs_inputs as gi
+import oracle
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+import gaussian_splatting_differentiable_project_gb300 as gs  # noqa: E402
+
+DEV = "cuda"
+
+
+# ----------------------------------------------------------------------------- helpers
+
+def _status():
+    return torch.zeros(1, dtype=torch.int32, device=DEV)
+
+
+def _u32(t):
+    return t.cpu().numpy().view(np.uint32)
+
+
+def _grad_close(got, ref, rtol=1e-4, floor=1e-6, what=""):
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    scale = np.maximum(np.abs(ref).max(axis=-1, keepdims=True), 1e-30)
+    bad = np.abs(got - ref) > rtol * np.abs(ref) + floor * scale
+    assert not bad.any(), f"{what}: {bad.sum()} of {bad.size} outside tolerance; worst " \
+                          f"{np.max(np.abs(got - ref) / (rtol * np.abs(ref) + floor * scale))}"
+
+
+def _scene(name, n=None, seed=0):
+    cfg = gi.CONFIGS[name]
+    P = gi.scene_for(cfg, seed=seed, n=n)
+    return cfg, P, (n or cfg.n)
+
+
+def _cam_for(cfg, view=0, W=None, H=None):
+    if cfg.kind == "cube":
+        return gi.camera((0.0, 0.0, 3.0), W or cfg.width, H or cfg.height)
+    cams = gi.fibonacci_cameras(cfg.n_views, W or cfg.width, H or cfg.height)
+    return cams[view]
+
+
+def _gpu_forward(P, n, cam, capacity=1 << 20):
+    W, H = cam["width"], cam["height"]
+    tr = gs.Trainer(P, n, W, H, capacity=capacity, lr_plane=gi.lr_planes())
+    tr.forward(cam)
+    torch.cuda.synchronize()
+    return tr
+
+
+CASES = [
+    ("tiny", None, None, None),          # 4,096 Gaussians, 128x128
+    ("tiny", 3000, 72, 56),              # ragged tiles on both axes, n not a multiple of 256
+    ("iso1m_512", 60_000, 256, 192),     # isosurface generator at reduced size
+]
+
+
+@pytest.fixture(scope="module", params=CASES, ids=[f"{c[0]}-{c[1]}-{c[2]}x{c[3]}" for c in CASES])
+def case(request):
+    name, n, W, H = request.param
+    cfg, P, n = _scene(name, n)
+    cam = _cam_for(cfg, 3 if cfg.kind != "cube" else 0, W, H)
+    ref_proj = oracle.project(P, n, cam, 32)
+    tr = _gpu_forward(P, n, cam)
+    return {"cfg": cfg, "P": P, "n": n, "cam": cam, "ref_proj": ref_proj, "tr": tr}
+
+
+# ----------------------------------------------------------------------------- exp
+
+def test_expf_bitwise_equal_to_oracle():
+    x = np.concatenate([np.linspace(-90, 90, 200_001, dtype=np.float32),
+                        np.random.default_rng(0).uniform(-6, 0, 100_000).astype(np.float32),
+                        np.array([0.0, -0.0, np.nan, np.inf, -np.inf, 88.0, -87.0], np.float32)])
+    xd = torch.from_numpy(x).to(DEV)
+    yd = torch.empty_like(xd)
+    gs.util_expf(xd, yd)
+    y = yd.cpu().numpy()
+    yr = oracle.expf(x)
+    same = (y.view(np.uint32) == yr.view(np.uint32)) | (np.isnan(y) & np.isnan(yr))
+    assert same.all(), x[~same][:10]
+
+
+# ----------------------------------------------------------------------------- projection
+
+def test_project_parity(case):
+    tr, ref, n = case["tr"], case["ref_proj"], case["n"]
+    assert tr.check_status() == 0
+    count = _u32(tr.proj.count)[:n]
+    np.testing.assert_array_equal(count, ref["count"])
+    vis = ref["count"] > 0
+    assert vis.sum() > 0.5 * n
+    np.testing.assert_array_equal(tr.proj.radius.cpu().numpy()[:n][vis], ref["radius"][vis])
+    rect = _u32(tr.proj.rect)[:n]
+    r = ref["rect"]
+    np.testing.assert_array_equal(rect[vis, 0], (r[vis, 0] | (r[vis, 1] << 16)).astype(np.uint32))
+    np.testing.assert_array_equal(rect[vis, 1], (r[vis, 2] | (r[vis, 3] << 16)).astype(np.uint32))
+    depth = tr.proj.depth.cpu().numpy()[:n]
+    np.testing.assert_array_equal(depth[vis].view(np.uint32), ref["depth"][vis].view(np.uint32))
+    rec = tr.proj.rec.cpu().numpy()[:n]
+    exp = np.stack([ref["mean2d"][:, 0], ref["mean2d"][:, 1], -0.5 * ref["conic"][:, 0], -ref["conic"][:, 1],
+                    -0.5 * ref["conic"][:, 2], ref["opacity"], ref["rgb"][:, 0], ref["rgb"][:, 1],
+                    ref["rgb"][:, 2]], 1).astype(np.float32)
+    got = rec[:, :9]
+    assert np.max(np.abs(got[vis] - exp[vis])) <= 1e-5 * np.maximum(1, np.abs(exp[vis])).max()
+    exact = np.mean(got[vis].view(np.uint32) == exp[vis].view(np.uint32))
+    assert exact == 1.0, f"only {exact:.6f} of projected record values are bit-exact"
+    np.testing.assert_array_equal(rec[vis, 9].view(np.uint32), np.nonzero(vis)[0].astype(np.uint32))
+
+
+# ----------------------------------------------------------------------------- binning
+
+def test_bin_sort_parity(case):
+    tr, ref, cam = case["tr"], case["ref_proj"], case["cam"]
+    tl = oracle.tile_lists(ref, cam["width"], cam["height"])
+    K = tr.n_isect()
+    assert K == tl["K"]
+    keys = tr.bins.keys.cpu().numpy()[:K].view(np.uint64)
+    ids = _u32(tr.bins.ids)[:K]
+    np.testing.assert_array_equal(keys, tl["keys"])
+    np.testing.assert_array_equal(ids, tl["ids"])
+    np.testing.assert_array_equal(_u32(tr.bins.ranges), tl["ranges"])
+    # records gathered into key order are the projected records of those ids
+    srec = tr.bins.rec.cpu().numpy()[:K]
+    prec = tr.proj.rec.cpu().numpy()
+    np.testing.assert_array_equal(srec.view(np.uint32), prec[ids].view(np.uint32))
+
+
+def test_bin_sort_deterministic(case):
+    tr, cam = case["tr"], case["cam"]
+    keys0 = tr.bins.keys.clone()
+    ids0 = tr.bins.ids.clone()
+    img0 = tr.image.clone()
+    tr.forward(cam)
+    torch.cuda.synchronize()
+    K = tr.n_isect()
+    assert torch.equal(tr.bins.keys[:K], keys0[:K])
+    assert torch.equal(tr.bins.ids[:K], ids0[:K])
+    assert torch.equal(tr.image, img0)
+
+
+# ----------------------------------------------------------------------------- forward
+
+def test_render_fwd_parity(case):
+    tr, ref, cam = case["tr"], case["ref_proj"], case["cam"]
+    rd = oracle.render(ref, cam["width"], cam["height"])
+    img = tr.image.cpu().numpy()
+    assert np.max(np.abs(img - rd["image"])) <= 1e-5
+    assert np.max(np.abs(tr.T_final.cpu().numpy() - rd["T_final"])) <= 1e-5
+    np.testing.assert_array_equal(_u32(tr.n_contrib), rd["n_contrib"])
+    assert np.array_equal(img.view(np.uint32), rd["image"].view(np.uint32)), "image not bit-exact"
+
+
+# ----------------------------------------------------------------------------- backward
+
+def _target_for(case):
+    cam = case["cam"]
+    rd = oracle.render(case["ref_proj"], cam["width"], cam["height"])
+    return gi.offset_target(rd["image"], seed=7)
+
+
+def test_render_bwd_parity(case):
+    tr, ref, cam, n = case["tr"], case["ref_proj"], case["cam"], case["n"]
+    W, H = cam["width"], cam["height"]
+    target = _target_for(case)
+    rd = oracle.render(ref, W, H, target=target)
+    tgt = torch.from_numpy(target).to(DEV)
+    tr.forward(cam)
+    tr.backward(cam, tgt)
+    torch.cuda.synchronize()
+    assert tr.check_status() == 0
+    g2 = tr.grad2d.cpu().numpy()[:, :n]
+    _grad_close(g2, rd["grad2d"], what="grad2d")
+    assert abs(float(tr.loss.item()) - rd["loss"]) <= 1e-5 * rd["loss"]
+    # padding gets no gradient
+    assert not tr.grad2d[:, n:].any()
+
+
+def test_project_bwd_parity(case):
+    """Seeded stand-in 2D gradients fed to both sides isolate the chain rule."""
+    tr, P, cam, n = case["tr"], case["P"], case["cam"], case["n"]
+    g2 = gi.random_grad2d(11, n, P.shape[1])
+    ref = oracle.project_bwd(P, n, cam, g2[:, :n], prec=32)
+    g2d = torch.from_numpy(g2).to(DEV)
+    st = _status()
+    gs.project(n, tr.params, cam, tr.proj, st)
+    gs.project_bwd(n, tr.params, cam, tr.proj, g2d, tr.grads, st)
+    torch.cuda.synchronize()
+    got = tr.grads.cpu().numpy()
+    _grad_close(got[:, :n], ref, what="param grads")
+    assert not np.any(got[:, n:])
+
+
+def test_adam_parity():
+    rng = np.random.default_rng(5)
+    n, n_pad = 1000, 1024
+    p = rng.normal(size=(59, n_pad)).astype(np.float32)
+    g = (rng.normal(size=(59, n_pad)) * 10.0 ** rng.integers(-7, 0, (59, n_pad))).astype(np.float32)
+    m = (rng.normal(size=(59, n_pad)) * 1e-3).astype(np.float32)
+    v = (rng.uniform(size=(59, n_pad)) * 1e-6).astype(np.float32)
+    lr = gi.lr_planes()
+    t = 5
+    pr, mr, vr = oracle.adam(p.astype(np.float64), g.astype(np.float64), m.astype(np.float64),
+                             v.astype(np.float64), lr, 0.9, 0.999, 1e-15, t)
+    pd, gd, md, vd = (torch.from_numpy(a.copy()).to(DEV) for a in (p, g, m, v))
+    gs.adam_step(n, pd, gd, md, vd, lr, 0.9, 0.999, 1e-15, t)
+    torch.cuda.synchronize()
+    assert np.all(np.abs(pd.cpu().numpy() - pr) <= 1e-5 * np.abs(pr) + 1e-7)
+    assert np.all(np.abs(md.cpu().numpy() - mr) <= 1e-5 * np.abs(mr) + 1e-12)
+    assert np.all(np.abs(vd.cpu().numpy() - vr) <= 1e-5 * np.abs(vr) + 1e-15)
+
+
+def test_whole_step_end_to_end(case):
+    """The whole chain from the same parameters: every stage against the oracle's
+    chain; Adam is compared where the gradient is not within its tolerance of 0
+    (at t = 1 an update is lr sign(g), so a near-zero g has no defined sign)."""
+    P, cam, n = case["P"], case["cam"], case["n"]
+    W, H = cam["width"], cam["height"]
+    target = _target_for(case)
+    z = np.zeros((59, P.shape[1]))
+    ref = oracle.step(P, n, cam, target, z, z, 1, gi.lr_planes())
+    tr = gs.Trainer(P, n, W, H, capacity=1 << 20, lr_plane=gi.lr_planes())
+    tr.step(cam, torch.from_numpy(target).to(DEV))
+    torch.cuda.synchronize()
+    assert tr.check_status() == 0
+    _grad_close(tr.grad2d.cpu().numpy()[:, :n], ref["render"]["grad2d"], what="grad2d")
+    gref = ref["grads"][:, :n]
+    _grad_close(tr.grads.cpu().numpy()[:, :n], gref, rtol=2e-4, floor=2e-6, what="param grads")
+    p = tr.params.cpu().numpy()[:, :n].astype(np.float64)
+    pr = ref["params"][:, :n]
+    scale = np.abs(gref).max(axis=1, keepdims=True)
+    defined = np.abs(gref) > 1e-3 * scale
+    assert defined.mean() > 0.5
+    bad = (np.abs(p - pr) > 1e-5 * np.abs(pr) + 1e-7) & defined
+    assert not bad.any(), bad.sum()
+
+
+# ----------------------------------------------------------------------------- edge cases
+
+def test_empty_scene_all_culled():
+    """Every Gaussian behind the camera: K = 0, background image, zero gradients."""
+    cfg = gi.CONFIGS["tiny"]
+    P = gi.scene_for(cfg, n=500)
+    P[2, :500] = 50.0          # far behind the camera at z = +3 looking down -z
+    cam = gi.camera((0.0, 0.0, 3.0), 64, 48)
+    tr = gs.Trainer(P, 500, 64, 48, capacity=1024, lr_plane=gi.lr_planes(), bg=(0.2, 0.4, 0.6))
+    tgt = torch.zeros((3, 48, 64), device=DEV)
+    tr.step(cam, tgt)
+    torch.cuda.synchronize()
+    assert tr.check_status() == 0
+    assert tr.n_isect() == 0
+    img = tr.image.cpu().numpy()
+    np.testing.assert_array_equal(img[0], np.float32(0.2))
+    np.testing.assert_array_equal(img[2], np.float32(0.6))
+    assert not tr.grads.any()
+
+
+def test_capacity_overflow_is_flagged_not_written():
+    cfg = gi.CONFIGS["tiny"]
+    P = gi.scene_for(cfg)
+    cam = _cam_for(cfg)
+    tr = gs.Trainer(P, cfg.n, 128, 128, capacity=1000, lr_plane=gi.lr_planes())
+    guard = torch.full((4096,), -7, dtype=torch.int64, device=DEV)   # allocated after the bins
+    tr.forward(cam)
+    torch.cuda.synchronize()
+    assert tr.check_status() & gs.GS_ERR_CAPACITY
+    assert tr.n_isect() > 1000
+    assert torch.all(guard == -7)
+
+
+def test_nonfinite_parameters_are_flagged_and_culled():
+    cfg = gi.CONFIGS["tiny"]
+    P = gi.scene_for(cfg, n=600)
+    P[0, 5] = np.nan
+    P[4, 9] = np.inf
+    P[20, 11] = np.nan     # an SH coefficient
+    cam = _cam_for(cfg)
+    tr = _gpu_forward(P, 600, cam)
+    assert tr.check_status() & gs.GS_ERR_NONFINITE
+    count = _u32(tr.proj.count)
+    assert count[5] == 0 and count[9] == 0 and count[11] == 0
+    ref = oracle.project(P, 600, cam, 32)
+    np.testing.assert_array_equal(count[:600], ref["count"])
+    assert np.isfinite(tr.image.cpu().numpy()).all()
+
+
+def test_large_gaussian_spanning_many_tiles():
+    """One Gaussian covering the whole image plus small ones: long per-Gaussian key
+    runs and a tile list longer than one shared-memory batch."""
+    cam = gi.camera((0.0, 0.0, 3.0), 200, 120)
+    rng = np.random.default_rng(3)
+    n = 900
+    means = np.column_stack([rng.uniform(-0.8, 0.8, n), rng.uniform(-0.5, 0.5, n), rng.uniform(-0.1, 0.1, n)])
+    ls = np.full((n, 3), -2.6)
+    ls[0] = 0.3      # huge
+    q = np.tile([1.0, 0, 0, 0], (n, 1))
+    logits = rng.normal(-1.5, 0.3, n)       # low opacity: long lists before termination
+    sh = np.zeros((n, 16, 3))
+    sh[:, 0] = rng.uniform(-1, 1, (n, 3))
+    P = gi.pack(means, ls, q, logits, sh)
+    ref = oracle.project(P, n, cam, 32)
+    assert ref["count"][0] == gs.n_tiles(200, 120)
+    tr = _gpu_forward(P, n, cam)
+    tl = oracle.tile_lists(ref, 200, 120)
+    assert (np.diff(tl["ranges"], axis=1).max()) > 256
+    K = tr.n_isect()
+    np.testing.assert_array_equal(tr.bins.keys.cpu().numpy()[:K].view(np.uint64), tl["keys"])
+    rd = oracle.render(ref, 200, 120, target=gi.offset_target(oracle.render(ref, 200, 120)["image"], 2))
+    assert np.array_equal(tr.image.cpu().numpy().view(np.uint32), rd["image"].view(np.uint32))
+    tgt = torch.from_numpy(gi.offset_target(oracle.render(ref, 200, 120)["image"], 2)).to(DEV)
+    tr.backward(cam, tgt)
+    torch.cuda.synchronize()
+    _grad_close(tr.grad2d.cpu().numpy()[:, :n], rd["grad2d"], what="grad2d")
