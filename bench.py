@@ -1,0 +1,494 @@
+#!/usr/bin/env python
+"""Train steps/s of the GB300 3DGS step (fwd + bwd + Adam, one view per step).
+
+Workload (default): 4M-Gaussian blob isosurface at 2048x2048 with 448 orbit views,
+SH degree 3, fp32; step s trains view s mod 448 against that view's target image
+(a render of the same surface sampled with another seed).  Every input is seeded
+and synthetic and resident on the GPU before the timed region; parameters, Adam
+state and targets (22.5 GB) exceed L2 many times over, so no flush is needed.
+
+One JSON line is printed (rank 0).  Besides the device-timed value it carries:
+  e2e           the same steps through the public API with each step's target
+                copied from pinned host memory and its loss read back;
+  roofline      for the kernel with the largest share of step time;
+  cpu_baseline  the CPU oracle timed on this host on a bounded sample;
+  stages_ms     per-stage device time per step (CUDA events on the stream);
+  clocks        SM clocks and throttle reasons sampled during the timed region.
+
+``--impl reference`` times the CPU oracle instead (the reference arm of this
+build), each step a bounded sample of the same workload scaled to full steps.
+Multi-GPU runs are independent replicas (the step does not shard).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import gs_inputs as gi  # noqa: E402
+
+METRIC = "train steps/s (fwd+bwd+Adam, 1 view) at 4M Gaussians 2048²; % of roofline"
+STAGES = ["project", "bin_sort", "render_fwd", "render_bwd", "project_bwd", "adam"]
+
+
+def parse():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=448)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--config", default="iso4m_2048", choices=sorted(gi.CONFIGS))
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--capacity-slack", type=float, default=1.15)
+    return ap.parse_args()
+
+
+# ----------------------------------------------------------------------------- distributed
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def dist_init(ws):
+    if ws <= 1:
+        return None
+    import torch.distributed as dist
+    os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+    dist.init_process_group("nccl")
+    return dist
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        smax = max((num(r[2]) for r in rows if num(r[2]) is not None), default=None)
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[k] for r in rows for k in range(4) if r[5 + k].lower().startswith("active")})
+        load = [s for s in sm if smax and s > 0.5 * smax] or sm
+        return {"sm_mhz": statistics.median(load) if load else None, "sm_max_mhz": smax, "reasons": reasons,
+                "samples": len(rows), "power_w_max": max((num(r[3]) or 0.0) for r in rows)}
+
+
+# ----------------------------------------------------------------------------- roofline model
+
+def passes_for(width, height):
+    tiles = (-(-width // 16)) * (-(-height // 16))
+    b = 0
+    while (1 << b) < tiles:
+        b += 1
+    return (32 + b + 7) // 8
+
+
+def stage_bytes(N, n_pad, V, K, P, passes):
+    """Algorithmic DRAM bytes of each stage per step (the traffic the method needs
+    with the data layout used: SoA planes, 48-byte records, 8+4-byte keys)."""
+    return {
+        # all N: 11 geometric planes + depth/radius/rect/count; visible: 48 SH + record
+        "project": 64 * N + 240 * V,
+        # counts twice, rect+depth of the visible, keys+ids emitted, each radix pass
+        # reads and writes keys+ids, then keys/ids read and 48-byte records gathered
+        "bin_sort": 8 * N + 12 * V + (12 + 24 * passes + 12 + 96) * K,
+        # records once per tile, image + T + n_contrib written
+        "render_fwd": 48 * K + 20 * P,
+        # grad2d cleared, records once per tile, image/target/T/n_contrib read
+        "render_bwd": 36 * n_pad + 48 * K + 32 * P,
+        # all: count + 59 gradient planes written; visible: 59 params + 9 grad2d read
+        "project_bwd": 240 * N + 272 * V,
+        # p, g, m, v read; p, m, v written
+        "adam": 59 * n_pad * 28,
+    }
+
+
+# FP32 operations per iterated (pixel, entry) pair, counting an FMA as 2 and the
+# exponential as the 11 operations of its Cody-Waite + degree-7 evaluation.
+FLOP_FWD_PAIR = 41
+FLOP_BWD_PAIR = 75
+
+
+def fp32_peak_tflops(sm_mhz):
+    # 152 SMs x 128 FP32 lanes x 2 FLOP per FMA per clock
+    return 152 * 128 * 2 * sm_mhz * 1e6 / 1e12
+
+
+# ----------------------------------------------------------------------------- CPU oracle leg
+
+class OracleSample:
+    """Full-step oracle time estimated from a bounded sample of one view's step.
+
+    Per-Gaussian stages (projection, projection backward, Adam) run on every
+    frac_g-th Gaussian and are scaled by frac_g.  Binning and compositing (forward
+    and backward) run on a band of ``band_rows`` tile rows through the image centre,
+    given only the Gaussians whose tile rect meets the band, and are scaled by the
+    number of tile rows over band_rows."""
+
+    def __init__(self, P, n, cam, frac_g: int, band_rows: int):
+        import oracle
+        oracle.build()
+        self.oracle = oracle
+        W, H = int(cam["width"]), int(cam["height"])
+        self.TY = -(-H // 16)
+        self.frac_g, self.rows, self.W, self.cam = frac_g, band_rows, W, cam
+        sub = np.ascontiguousarray(P[:, : n : frac_g])
+        self.n_sub = sub.shape[1]
+        self.sub = np.zeros((59, gi.n_pad_of(self.n_sub)), np.float32)
+        self.sub[:, : self.n_sub] = sub
+        r0 = (self.TY - band_rows) // 2
+        band = dict(cam)
+        band["height"] = band_rows * 16
+        band["cy"] = np.float32(float(cam["cy"]) - 16 * r0)
+        pr = oracle.project(P, n, band, 32)
+        keep = np.nonzero(pr["count"] > 0)[0]
+        self.band_proj = {"proj16": np.ascontiguousarray(pr["proj16"][keep]),
+                          "iproj6": np.ascontiguousarray(pr["iproj6"][keep])}
+        self.band_target = np.full((3, band_rows * 16, W), 0.5, np.float32)
+        self.g2 = np.full((9, self.n_sub), 1e-6)
+        self.z = np.zeros((59, self.n_sub))
+        self.desc = (f"oracle on every {frac_g}th Gaussian (projection, projection backward, Adam; scaled "
+                     f"x{frac_g}) and on {band_rows} of {self.TY} tile rows of view 0 with the Gaussians that "
+                     f"touch them (binning, compositing forward and backward; scaled x{self.TY / band_rows:g}), "
+                     f"summed to one full step")
+
+    def seconds(self) -> float:
+        o = self.oracle
+        t0 = time.perf_counter()
+        o.project(self.sub, self.n_sub, self.cam, 32)
+        t1 = time.perf_counter()
+        o.render(self.band_proj, self.W, self.rows * 16, target=self.band_target)
+        t2 = time.perf_counter()
+        o.project_bwd(self.sub, self.n_sub, self.cam, self.g2, 32)
+        t3 = time.perf_counter()
+        o.adam(self.sub[:, : self.n_sub].astype(np.float64), self.z + 1e-6, self.z, self.z, gi.lr_planes(),
+               0.9, 0.999, 1e-15, 1)
+        t4 = time.perf_counter()
+        return (t1 - t0 + t3 - t2 + t4 - t3) * self.frac_g + (t2 - t1) * self.TY / self.rows
+
+
+def _torch_dev():
+    try:
+        import torch
+        return "cuda" if torch.cuda.is_available() else "cpu"
+    except ImportError:
+        return None
+
+
+def run_reference(args, cfg, rank):
+    """Reference arm: the CPU oracle, each step a bounded sample scaled to a full step."""
+    if rank != 0:
+        return
+    cams = gi.cameras_for(cfg)
+    P = gi.scene_for(cfg, seed=args.seed, device=_torch_dev() if cfg.n >= 1_000_000 else None)
+    smp = OracleSample(P, cfg.n, cams[0], frac_g=256, band_rows=1)
+    per = []
+    for s in range(args.warmup + args.steps):
+        sec = smp.seconds()
+        if s >= args.warmup:
+            per.append(sec)
+    val = 1.0 / float(np.mean(per))
+    line = {
+        "impl": "reference", "metric": METRIC, "value": val, "unit": "steps/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 / val, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64 (fp32 decisions)", "data": "synthetic",
+        "config": _config_dict(cfg),
+        "cpu_baseline": {"value": val, "unit": "steps/s", "cores": smp.oracle.threads(), "kind": "oracle",
+                         "sample": smp.desc},
+        "e2e": {"value": val, "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def _config_dict(cfg):
+    return {"workload": f"{cfg.name}: {cfg.description}; one view per step, views in orbit order",
+            "n_gaussians": cfg.n, "width": cfg.width, "height": cfg.height, "views": cfg.n_views,
+            "sh_degree": 3, "l2": "inputs larger than L2 (parameters + Adam state + targets >> 129 MB); no flush"}
+
+
+# ----------------------------------------------------------------------------- GPU arm
+
+def run_gb300(args, cfg, ws, rank, local):
+    import torch
+    import gaussian_splatting_differentiable_project_gb300 as gs
+
+    dist = dist_init(ws)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    t_setup = time.time()
+    gs.load()
+    P = gi.scene_for(cfg, seed=args.seed, device=dev)
+    Pt = gi.target_scene_for(cfg, seed=args.seed, device=dev)
+    cams = gi.cameras_for(cfg)
+    V_views = len(cams)
+    W, H = cfg.width, cfg.height
+    n, n_pad = cfg.n, P.shape[1]
+    passes = passes_for(W, H)
+
+    # capacity: project every view (model and target sets) and take the largest K
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    Pd = torch.from_numpy(P).to(dev)
+    Ptd = torch.from_numpy(Pt).to(dev)
+    proj = gs.ProjBuffers(n_pad, dev)
+    kmax, Ks, Vs = 0, [], []
+    for cam in cams:
+        for which in (Ptd, Pd):
+            gs.project(n, which, cam, proj, st)
+            k = int(proj.count[:n].sum().item())
+            kmax = max(kmax, k)
+            if which is Pd:
+                Ks.append(k)
+                Vs.append(int((proj.count[:n] > 0).sum().item()))
+    capacity = int(kmax * args.capacity_slack) + 4096
+    del proj
+
+    # targets: forward renders of the target set, one per view
+    rend = gs.Trainer(Ptd, n, W, H, capacity, gi.lr_planes(), device=dev)
+    targets = torch.empty((V_views, 3, H, W), dtype=torch.float32, device=dev)
+    for v, cam in enumerate(cams):
+        rend.forward(cam)
+        targets[v].copy_(rend.image)
+    torch.cuda.synchronize()
+    rend.raise_on_status()
+    del rend, Ptd
+
+    tr = gs.Trainer(Pd, n, W, H, capacity, gi.lr_planes(), device=dev)
+    del Pd
+    # per-view work statistics (forward on the initial parameters)
+    E = []
+    for cam in cams:
+        tr.forward(cam)
+        E.append(int(tr.n_contrib.to(torch.int64).sum().item()))
+    torch.cuda.synchronize()
+    tr.raise_on_status()
+    setup_s = time.time() - t_setup
+
+    def step(s, events=None):
+        v = s % V_views
+        cam = cams[v]
+        if events is None:
+            tr.step(cam, targets[v])
+            return
+        e = events
+        e[0].record()
+        gs.project(tr.n, tr.params, cam, tr.proj, tr.status)
+        e[1].record()
+        gs.bin_sort(tr.n, tr.n_pad, tr.proj, cam, tr.bins, tr.status)
+        e[2].record()
+        gs.render_fwd(cam, tr.bins, tr.bg, tr.image, tr.T_final, tr.n_contrib, tr.status)
+        e[3].record()
+        gs.render_bwd(tr.n, tr.n_pad, cam, tr.bins, tr.bg, tr.image, targets[v], tr.T_final, tr.n_contrib,
+                      tr.grad2d, tr.loss, tr.status)
+        e[4].record()
+        gs.project_bwd(tr.n, tr.params, cam, tr.proj, tr.grad2d, tr.grads, tr.status)
+        e[5].record()
+        tr.optimizer_step()
+        e[6].record()
+
+    for s in range(args.warmup):
+        step(s)
+    torch.cuda.synchronize()
+
+    # ---------------------------------------------------------------- timed region
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(K)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record()
+    for s in range(K):
+        step(args.warmup + s, ev[s])
+    t_end.record()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clk = clocks.stop()
+    ms = t_start.elapsed_time(t_end)
+    if dist:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    tr.raise_on_status()
+    stage_ms = {name: float(np.mean([ev[s][i].elapsed_time(ev[s][i + 1]) for s in range(K)]))
+                for i, name in enumerate(STAGES)}
+    value = ws * K / (ms / 1e3)
+
+    # ---------------------------------------------------------------- e2e leg
+    e2e = None
+    if not args.no_e2e:
+        host_t = torch.empty_like(targets, device="cpu").pin_memory()
+        host_t.copy_(targets)
+        del targets
+        torch.cuda.empty_cache()
+        tgt_dev = torch.empty((3, H, W), dtype=torch.float32, device=dev)
+        loss_host = torch.empty(K, dtype=torch.float32).pin_memory()
+        torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        for s in range(K):
+            v = (args.warmup + s) % V_views
+            tgt_dev.copy_(host_t[v], non_blocking=True)
+            tr.step(cams[v], tgt_dev)
+            loss_host[s:s + 1].copy_(tr.loss, non_blocking=True)
+        b.record()
+        torch.cuda.synchronize()
+        ms_e2e = a.elapsed_time(b)
+        if dist:
+            t = torch.tensor([ms_e2e], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ms_e2e = float(t.item())
+        e2e = {"value": ws * K / (ms_e2e / 1e3), "unit": "steps/s", "h2d_bytes_per_step": 3 * H * W * 4,
+               "d2h_bytes_per_step": 4, "ms_per_step": ms_e2e / K}
+        del host_t
+
+    if rank != 0:
+        return
+
+    # ---------------------------------------------------------------- roofline
+    views = [(args.warmup + s) % V_views for s in range(K)]
+    Kmean = float(np.mean([Ks[v] for v in views]))
+    Vmean = float(np.mean([Vs[v] for v in views]))
+    Emean = float(np.mean([E[v] for v in views]))
+    Pix = W * H
+    byt = stage_bytes(n, n_pad, Vmean, Kmean, Pix, passes)
+    peak_bw = _peak("hbm_gbs", 6800.0)
+    sm_mhz = clk.get("sm_max_mhz") or 2070.0
+    peak_fp32 = fp32_peak_tflops(sm_mhz)
+    flops = {"render_fwd": FLOP_FWD_PAIR * Emean, "render_bwd": FLOP_BWD_PAIR * Emean}
+    per_stage = {}
+    t_star = 0.0
+    for name in STAGES:
+        tb = byt[name] / (peak_bw * 1e9)
+        tf = flops.get(name, 0.0) / (peak_fp32 * 1e12)
+        t_star += max(tb, tf)
+        t_meas = stage_ms[name] / 1e3
+        bound = "alu" if tf > tb else "hbm"
+        per_stage[name] = {"ms": stage_ms[name], "bound": bound,
+                           "gbs": byt[name] / t_meas / 1e9, "tflops": flops.get(name, 0.0) / t_meas / 1e12,
+                           "frac": max(tb, tf) / t_meas}
+    dom = max(STAGES, key=lambda s: stage_ms[s])
+    d = per_stage[dom]
+    if d["bound"] == "hbm":
+        roof = {"kernel": dom, "bound": "hbm", "achieved": d["gbs"], "peak": peak_bw, "unit": "GB/s",
+                "frac": d["gbs"] / peak_bw, "traffic": None, "peak_source": _peak_src("hbm_gbs")}
+    else:
+        roof = {"kernel": dom, "bound": "alu", "achieved": d["tflops"], "peak": peak_fp32, "unit": "TFLOP/s",
+                "frac": d["tflops"] / peak_fp32, "traffic": None,
+                "peak_source": f"152 SMs x 128 FP32 lanes x 2 x {sm_mhz:.0f} MHz"}
+
+    cpu = None
+    if not args.no_cpu_baseline and ws == 1:
+        try:
+            cpu = cpu_baseline(cfg, P, cams[0], tr, W, H)
+        except Exception as exc:  # the baseline is reported, never required
+            cpu = {"value": None, "unit": "steps/s", "kind": "oracle", "error": repr(exc)}
+
+    launches_per_step = 1 + (4 + passes) + 1 + 2 + 1 + 1
+    line = {
+        "metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": ws, "steps": K, "warmup": args.warmup,
+        "ms_per_step": ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic",
+        "config": dict(_config_dict(cfg), parallelism=f"replicas{ws}", capacity_K=capacity,
+                       K_mean=Kmean, visible_mean=Vmean, pairs_bwd_mean=Emean),
+        "roofline": roof,
+        "step_roofline_frac": t_star / (ms / K / 1e3),
+        "stages_ms": stage_ms, "stages": per_stage,
+        "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches_per_step * K,
+        "clocks": clk, "setup_s": setup_s,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def _peak(key, fallback):
+    try:
+        return float(json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))[key])
+    except (OSError, KeyError, ValueError):
+        return fallback
+
+
+def _peak_src(key):
+    return "of measured" if os.path.exists(os.path.join(ROOT, "MEASURED_PEAKS.json")) else "of fallback"
+
+
+def cpu_baseline(cfg, P, cam, tr, W, H):
+    rows = max(1, (-(-H // 16)) // 16)
+    smp = OracleSample(P, cfg.n, cam, frac_g=8, band_rows=rows)
+    sec = smp.seconds()
+    return {"value": 1.0 / sec, "unit": "steps/s", "cores": smp.oracle.threads(), "kind": "oracle",
+            "sample": smp.desc, "seconds_per_step": sec}
+
+
+def main():
+    args = parse()
+    ws, rank, local = dist_env()
+    cfg = gi.CONFIGS[args.config]
+    if args.impl == "reference":
+        run_reference(args, cfg, rank)
+        return
+    run_gb300(args, cfg, ws, rank, local)
+
+
+if __name__ == "__main__":
+    main()

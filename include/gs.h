@@ -113,7 +113,8 @@ typedef struct gs_proj {
  *   keys     capacity_K uint64 keys (tile << 32 | fp32 depth bits), sorted.
  *   ids      capacity_K uint32 Gaussian indices in key order (ties by index).
  *   rec      capacity_K records (12 floats, 16-byte aligned) in key order.
- *   ranges   2 uint32 per tile: [start, end) of the tile's entries.
+ *   ranges   2 uint32 per tile: [start, end) of the tile's entries; [0, 0) for a
+ *            tile with no entries.
  *   n_isect  1 uint32: the total number of tile intersections K of this view
  *            (may exceed capacity_K, in which case GS_ERR_CAPACITY is raised
  *            and only the first capacity_K entries exist). */
