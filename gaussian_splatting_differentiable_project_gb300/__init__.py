@@ -31,6 +31,7 @@ GS_ERR_CUDA = 2
 GS_ERR_CAPACITY = 4
 GS_ERR_TIMEOUT = 8
 GS_ERR_NONFINITE = 16
+GS_ERR_SCRATCH_LIMIT = 32
 
 _lock = threading.Lock()
 _lib = None
@@ -86,6 +87,9 @@ def load(build_if_missing: bool = True):
         lib.gs_bin_sort.argtypes = [GsDims, ctypes.POINTER(GsProj), ctypes.POINTER(GsCamera), ctypes.c_uint32,
                                     GsBins, P, ctypes.c_size_t, P, P]
         lib.gs_bin_sort.restype = st
+        lib.gs_bin_sort_noalloc.argtypes = [GsDims, ctypes.POINTER(GsProj), ctypes.POINTER(GsCamera),
+                                            ctypes.c_uint32, GsBins, P, P]
+        lib.gs_bin_sort_noalloc.restype = st
         lib.gs_render_fwd.argtypes = [ctypes.POINTER(GsCamera), ctypes.POINTER(GsBins), ctypes.c_uint32,
                                       ctypes.POINTER(ctypes.c_float), P, P, P, P, P]
         lib.gs_render_fwd.restype = st
@@ -204,6 +208,16 @@ def bin_sort(n: int, n_pad: int, proj: ProjBuffers, cam: dict, bins: BinBuffers,
     _check(load().gs_bin_sort(dims(n, n_pad), ctypes.byref(pc), ctypes.byref(cc), bins.capacity, bins.c(),
                               ctypes.c_void_p(bins.ws_ptr()), bins.ws_bytes, _p(dev_status), _stream(stream)),
            "gs_bin_sort")
+
+
+def bin_sort_noalloc(n: int, n_pad: int, proj: ProjBuffers, cam: dict, bins: BinBuffers, dev_status,
+                     stream=None) -> None:
+    """gs_bin_sort with the library's fixed scratch instead of bins.workspace (for
+    callers that may not allocate device memory; see include/gs.h for the limits)."""
+    cc = camera(cam)
+    pc = proj.c()
+    _check(load().gs_bin_sort_noalloc(dims(n, n_pad), ctypes.byref(pc), ctypes.byref(cc), bins.capacity, bins.c(),
+                                      _p(dev_status), _stream(stream)), "gs_bin_sort_noalloc")
 
 
 def _bg(bg):

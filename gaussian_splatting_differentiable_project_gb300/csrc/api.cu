@@ -27,6 +27,7 @@ extern "C" const char* gs_status_str(uint32_t status) {
   if (status & GS_ERR_CAPACITY) return "tile intersections exceed capacity";
   if (status & GS_ERR_TIMEOUT) return "bounded device wait gave up";
   if (status & GS_ERR_NONFINITE) return "non-finite Gaussian parameters";
+  if (status & GS_ERR_SCRATCH_LIMIT) return "sizes exceed the fixed scratch of gs_bin_sort_noalloc";
   return "unknown status";
 }
 

@@ -14,6 +14,8 @@
 //                     ticket order, scatter through shared memory
 //   k_bs_ranges_gather per intersection: tile [start, end) and the 48-byte record
 //                     gathered into key order
+#include <mutex>
+
 #include "api_util.h"
 #include "gs_common.cuh"
 
@@ -417,4 +419,58 @@ extern "C" gs_status gs_bin_sort(gs_dims dims, const gs_proj* proj, const gs_cam
                                             reinterpret_cast<const float4*>(proj->rec),
                                             reinterpret_cast<float4*>(bins.rec), reinterpret_cast<uint2*>(bins.ranges));
   return launch_status();
+}
+
+// ---------------------------------------------------------------------------
+// gs_bin_sort_noalloc: the same binning for callers that may not allocate device
+// memory, e.g. code running inside a host callback or a real-time loop whose
+// memory is reserved up front, or a host that forbids device allocation after
+// start-up.  The sort's scratch lives in the file-scope array below, which every
+// GPU that loads this library holds until the process exits.  Its size covers
+// n <= GS_NOALLOC_MAX_N Gaussians, capacity_K <= GS_NOALLOC_MAX_K intersections
+// and up to GS_NOALLOC_MAX_TILES tiles (six radix passes).
+namespace gs {
+
+constexpr size_t na_align(size_t x) { return (x + 255) & ~size_t(255); }
+
+// The workspace layout of sort_layout() at the maximum sizes.
+constexpr size_t kNoAllocBytes =
+    na_align(size_t(GS_NOALLOC_MAX_K) * 8) + na_align(size_t(GS_NOALLOC_MAX_K) * 4) +
+    na_align(size_t((GS_NOALLOC_MAX_N + kScanBlock - 1) / kScanBlock) * 8) + na_align(size_t(kMaxPasses) * 256 * 4) +
+    na_align(size_t(kMaxPasses) * 4) +
+    na_align(size_t(6) * size_t((GS_NOALLOC_MAX_K + kPart - 1) / kPart) * 256 * 4);
+static_assert(kNoAllocBytes == 14172416, "fixed scratch size changed");
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocBytes];
+
+constexpr int kNoAllocMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[kNoAllocMaxDevices] = {};
+
+}  // namespace gs
+
+extern "C" gs_status gs_bin_sort_noalloc(gs_dims dims, const gs_proj* proj, const gs_camera* cam,
+                                         uint32_t capacity_K, gs_bins bins, uint32_t* dev_status,
+                                         cudaStream_t stream) {
+  using namespace gs;
+  if (!dims_ok(dims) || !camera_ok(cam)) return GS_ERR_INVALID_ARG;
+  const int64_t tiles = n_tiles(cam);
+  if (dims.n > GS_NOALLOC_MAX_N || capacity_K > GS_NOALLOC_MAX_K || tiles > GS_NOALLOC_MAX_TILES)
+    return GS_ERR_SCRATCH_LIMIT;
+  const size_t need = sort_layout(dims.n, capacity_K, tiles).total;
+  if (need > kNoAllocBytes) return GS_ERR_SCRATCH_LIMIT;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoAllocMaxDevices) return GS_ERR_CUDA;
+  void* scratch = nullptr;
+  {
+    // once per device, with that device current: the device address of the array
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+      void* p = nullptr;
+      if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return GS_ERR_CUDA;
+      g_noalloc_ptr[dev] = p;
+    }
+    scratch = g_noalloc_ptr[dev];
+  }
+  return gs_bin_sort(dims, proj, cam, capacity_K, bins, scratch, kNoAllocBytes, dev_status, stream);
 }

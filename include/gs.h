@@ -66,7 +66,8 @@ typedef enum gs_status {
   GS_ERR_CUDA = 2,        /* returned: a kernel launch failed */
   GS_ERR_CAPACITY = 4,    /* device: more tile intersections than capacity_K */
   GS_ERR_TIMEOUT = 8,     /* device: a bounded inter-block wait gave up */
-  GS_ERR_NONFINITE = 16   /* device: a Gaussian with NaN/Inf parameters (culled) */
+  GS_ERR_NONFINITE = 16,  /* device: a Gaussian with NaN/Inf parameters (culled) */
+  GS_ERR_SCRATCH_LIMIT = 32 /* returned: sizes exceed gs_bin_sort_noalloc's fixed scratch */
 } gs_status;
 
 /* Pinhole camera.  R is the world->camera rotation (row-major) and t the
@@ -241,6 +242,31 @@ gs_status gs_project_bwd(gs_dims dims, const float* params, const gs_camera* cam
 gs_status gs_adam_step(gs_dims dims, float* params, const float* grads, float* m, float* v,
                        const float lr_plane[GS_N_PLANES], double beta1, double beta2, double eps, int64_t t,
                        cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * gs_bin_sort_noalloc -- gs_bin_sort for callers that must not allocate device
+ * memory (for example code that runs where cudaMalloc is not allowed or not
+ * wanted after start-up: host callbacks, a render loop with all memory reserved
+ * in advance, embedders whose allocator owns the GPU).  The paper has no
+ * counterpart; this is a library convenience.  Results are identical to
+ * gs_bin_sort's.
+ *   Scratch: a fixed array inside the library (about 13.5 MiB), held by every GPU
+ *   that loads the library until the process exits.  It is used in place of the
+ *   workspace argument; the caller still passes proj and bins.
+ *   Limits: n <= GS_NOALLOC_MAX_N, capacity_K <= GS_NOALLOC_MAX_K, at most
+ *   GS_NOALLOC_MAX_TILES tiles; larger sizes return GS_ERR_SCRATCH_LIMIT and
+ *   nothing is enqueued.
+ *   The first call on a device looks up the array's device address (with that
+ *   device current); make that first call before any stream capture.
+ *   Every call on a device shares the one array: calls whose kernels overlap on
+ *   the GPU (other streams, other host threads) race and corrupt each other.
+ *   Serialise them.  Each call clears what must start at zero itself.
+ * Errors: as gs_bin_sort, plus GS_ERR_SCRATCH_LIMIT. */
+#define GS_NOALLOC_MAX_N (1 << 22)
+#define GS_NOALLOC_MAX_K (1 << 20)
+#define GS_NOALLOC_MAX_TILES (1 << 16)
+gs_status gs_bin_sort_noalloc(gs_dims dims, const gs_proj* proj, const gs_camera* cam, uint32_t capacity_K,
+                              gs_bins bins, uint32_t* dev_status, cudaStream_t stream);
 
 /* ---------------------------------------------------------------------------
  * gs_util_expf -- the library's fp32 exponential (Cody-Waite reduction, degree-7
