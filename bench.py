@@ -354,10 +354,12 @@ def run_gb300(args, cfg, ws, rank, local):
     torch.cuda.synchronize()
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
+    torch.cuda.nvtx.range_push("timed")
     t_start.record()
     for s in range(K):
         step(args.warmup + s, ev[s])
     t_end.record()
+    torch.cuda.nvtx.range_pop()
     torch.cuda.synchronize()
     if dist:
         dist.barrier()

@@ -132,13 +132,25 @@ __global__ void __launch_bounds__(kRasterThreads)
     const int cnt = int(st.count(b));
     // this warp only needs entries below its largest n_contrib
     const int jmax = int(min(uint32_t(cnt), warp_max > pos0 ? warp_max - pos0 : 0u));
+    const float4* Rf = reinterpret_cast<const float4*>(R);
+    float4 pa, pb, pc;
+    if (jmax > 0) {
+      pa = Rf[3 * (jmax - 1)];
+      pb = Rf[3 * (jmax - 1) + 1];
+      pc = Rf[3 * (jmax - 1) + 2];
+    }
     for (int j = jmax - 1; j >= 0; --j) {
       const uint32_t pos = pos0 + uint32_t(j);
       float v[9];
       bool contrib = false;
-      const float4 ra = R[j].a;
-      const float4 rb = R[j].b;
-      const float4 rc = R[j].c;
+      const float4 ra = pa;  // next (lower) record loaded one entry ahead
+      const float4 rb = pb;
+      const float4 rc = pc;
+      if (j > 0) {
+        pa = Rf[3 * (j - 1)];
+        pb = Rf[3 * (j - 1) + 1];
+        pc = Rf[3 * (j - 1) + 2];
+      }
       if (pos < nc) {
         const float dx = __fsub_rn(px, ra.x), dy = __fsub_rn(py, ra.y);
         const float power = conic_power(dx, dy, ra.z, ra.w, rb.x);
@@ -149,7 +161,7 @@ __global__ void __launch_bounds__(kRasterThreads)
           const float alpha = clamped ? kAlphaMax : vv;
           if (!(alpha < kAlphaMin)) {
             contrib = true;
-            const float Ti = T / (1.0f - alpha);
+            const float Ti = __fdividef(T, 1.0f - alpha);
             const float wgt = alpha * Ti;
             v[6] = g0 * wgt;
             v[7] = g1 * wgt;

@@ -53,28 +53,43 @@ __global__ void __launch_bounds__(kRasterThreads)
       const Rec* R = st.buffer(slot);
       const int cnt = int(st.count(b));
       const uint32_t pos0 = uint32_t(b) * kBatch;
-      if (!done) {
+      // Warp-uniform walk over the batch: every lane steps through the same j and
+      // takes its skip / stop decisions as predicates, so the warp stays converged
+      // (per-lane continue/break let the lanes drift apart and run serially).
+      // The next record is loaded from shared memory one entry ahead.
+      if (!__all_sync(0xffffffffu, done)) {
+        const float4* Rf = reinterpret_cast<const float4*>(R);
+        float4 na = Rf[0], nb = Rf[1];
+        float nc2 = Rf[2].x;
         for (int j = 0; j < cnt; ++j) {
-          const float4 ra = R[j].a;  // mx, my, ca, cb
-          const float dx = __fsub_rn(px, ra.x), dy = __fsub_rn(py, ra.y);
-          const float4 rb = R[j].b;  // cc, o, r, g
-          const float power = conic_power(dx, dy, ra.z, ra.w, rb.x);
-          if (power > 0.0f || power < kPowerSkip) continue;
-          const float v = __fmul_rn(rb.y, gs_expf_core(power));
-          const float alpha = (v < kAlphaMax) ? v : kAlphaMax;
-          if (alpha < kAlphaMin) continue;
-          const float Tn = __fmul_rn(T, __fsub_rn(1.0f, alpha));
-          if (Tn < kTMin) {
-            done = true;
-            break;
+          const float4 ra = na;  // mx, my, ca, cb
+          const float4 rb = nb;  // cc, o, r, g
+          const float cb = nc2;  // b
+          if (j + 1 < cnt) {
+            na = Rf[3 * (j + 1)];
+            nb = Rf[3 * (j + 1) + 1];
+            nc2 = Rf[3 * (j + 1) + 2].x;
           }
-          const float w = __fmul_rn(alpha, T);
-          const float cb = R[j].c.x;
-          C0 = __fmaf_rn(rb.z, w, C0);
-          C1 = __fmaf_rn(rb.w, w, C1);
-          C2 = __fmaf_rn(cb, w, C2);
-          T = Tn;
-          last = pos0 + uint32_t(j) + 1u;
+          const float dx = __fsub_rn(px, ra.x), dy = __fsub_rn(py, ra.y);
+          const float power = conic_power(dx, dy, ra.z, ra.w, rb.x);
+          if (!done && !(power > 0.0f) && !(power < kPowerSkip)) {
+            const float v = __fmul_rn(rb.y, gs_expf_core(power));
+            const float alpha = (v < kAlphaMax) ? v : kAlphaMax;
+            if (!(alpha < kAlphaMin)) {
+              const float Tn = __fmul_rn(T, __fsub_rn(1.0f, alpha));
+              if (Tn < kTMin) {
+                done = true;
+              } else {
+                const float w = __fmul_rn(alpha, T);
+                C0 = __fmaf_rn(rb.z, w, C0);
+                C1 = __fmaf_rn(rb.w, w, C1);
+                C2 = __fmaf_rn(cb, w, C2);
+                T = Tn;
+                last = pos0 + uint32_t(j) + 1u;
+              }
+            }
+          }
+          if ((j & 3) == 3 && __all_sync(0xffffffffu, done)) break;
         }
       }
       const int alive = __syncthreads_count(!done);
