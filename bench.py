@@ -52,6 +52,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--capacity-slack", type=float, default=1.15)
+    ap.add_argument("--views", type=int, default=0,
+                    help="use only the first N orbit views (profiling runs; 0 = all)")
     return ap.parse_args()
 
 
@@ -274,6 +276,8 @@ def run_gb300(args, cfg, ws, rank, local):
     P = gi.scene_for(cfg, seed=args.seed, device=dev)
     Pt = gi.target_scene_for(cfg, seed=args.seed, device=dev)
     cams = gi.cameras_for(cfg)
+    if args.views > 0:
+        cams = cams[: args.views]
     V_views = len(cams)
     W, H = cfg.width, cfg.height
     n, n_pad = cfg.n, P.shape[1]

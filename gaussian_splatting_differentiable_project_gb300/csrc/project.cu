@@ -6,6 +6,21 @@
 
 namespace gs {
 
+// Skip radius r of a record: at every pixel with |dx| > r or |dy| > r the entry's
+// fp32 power is below the rasteriser's -5.6 skip threshold, so the entry would be
+// skipped there anyway.  lam >= the largest eigenvalue of the 2D covariance (it is
+// the radius eigenvalue, with its 0.1 floor), so the exact inverse has smallest
+// eigenvalue mu_min >= 1/lam and power <= -|d|^2 / (2 lam).  The fp32 conic differs
+// from the exact inverse by a common factor (the rounded determinant) and a few ulp
+// per entry, together below 0.2% of mu_min while lam <= 1424 (r <= 128 px, which
+// bounds mu_max / mu_min by lam / 0.3); the fp32 power adds a few ulp of
+// mu_max |d|^2.  r = sqrt(11.536 lam) + 0.1 keeps the exact power below -5.77 and
+// covers both; beyond 128 px the radius is +inf (never skip).
+__device__ __forceinline__ float skip_radius(float lam) {
+  const float r = sqrtf(11.536f * lam) + 0.1f;
+  return r <= 128.0f ? r : __int_as_float(0x7f7fffff);
+}
+
 __global__ void __launch_bounds__(256)
     k_project(const float* __restrict__ P, int64_t n, int64_t n_pad, CamDev cam, float4* __restrict__ rec,
               float* __restrict__ depth, int32_t* __restrict__ radius, uint2* __restrict__ rect,
@@ -33,7 +48,7 @@ __global__ void __launch_bounds__(256)
     if (vis) {
       rec[3 * i + 0] = make_float4(g.mx, g.my, __fmul_rn(-0.5f, g.A), -g.B);
       rec[3 * i + 1] = make_float4(__fmul_rn(-0.5f, g.C), o, rgb[0], rgb[1]);
-      rec[3 * i + 2] = make_float4(rgb[2], __uint_as_float(uint32_t(i)), 0.0f, 0.0f);
+      rec[3 * i + 2] = make_float4(rgb[2], __uint_as_float(uint32_t(i)), skip_radius(g.lam), 0.0f);
       depth[i] = g.tz;
       radius[i] = g.radius;
       rect[i] = make_uint2(uint32_t(g.tx0) | (uint32_t(g.ty0) << 16), uint32_t(g.tx1) | (uint32_t(g.ty1) << 16));

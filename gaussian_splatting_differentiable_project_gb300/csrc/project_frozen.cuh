@@ -69,6 +69,7 @@ struct Geo {
   float T0[3], T1[3];      // rows of J W
   float a, b, c, det;      // 2D covariance (+0.3) and its determinant
   float A, B, C;           // conic
+  float lam;               // radius eigenvalue mid + sqrt(max(0.1, mid^2 - det))
   float mx, my;            // mean2d
   int radius;
   int tx0, ty0, tx1, ty1;
@@ -192,6 +193,7 @@ __device__ __forceinline__ void project_geo(const float* __restrict__ P, int64_t
   const float mid = __fmul_rn(0.5f, __fadd_rn(g.a, g.c));
   const float disc = __fmaf_rn(mid, mid, -g.det);
   const float lam = __fadd_rn(mid, __fsqrt_rn((0.1f < disc) ? disc : 0.1f));
+  g.lam = lam;
   float rf = ceilf(__fmul_rn(3.0f, __fsqrt_rn(lam)));
   if (rf > 16777216.0f) rf = 16777216.0f;
   g.mx = __fmaf_rn(cam.fx, g.u, cam.cx);

@@ -1,24 +1,59 @@
 // Shared pieces of the forward and backward rasterisers: tile/pixel mapping and
 // the bulk-copy (cp.async.bulk + mbarrier) staging of record batches into shared
-// memory.  Each CTA owns one 16x16 tile, one thread per pixel; warp w covers the
-// 8x4 pixel block (w & 1, w >> 1) of the tile so that a Gaussian's footprint
-// touches few warps.
+// memory.  Each CTA owns one 8x8 quarter of a 16x16 tile, one thread per pixel,
+// two warps of 8x4 pixels each, and walks the whole tile's record list.  Small
+// CTAs keep the coupling between warps (one barrier per batch) to two warps and
+// let up to 32 CTAs share an SM, so a quarter whose pixels finish early frees its
+// slot instead of idling until the slowest pixel of a 256-pixel tile is done.
 #pragma once
 
 #include "gs_common.cuh"
 
 namespace gs {
 
-constexpr int kRasterThreads = 256;
-constexpr int kBatch = 256;                          // records per shared-memory batch
-constexpr uint32_t kBatchBytes = kBatch * sizeof(Rec);  // 12 KB
+constexpr int kRasterThreads = 64;                   // one 8x8 quarter tile
+constexpr int kCtasPerTile = 4;
+constexpr int kBatch = 64;                           // records per shared-memory batch
+constexpr uint32_t kBatchBytes = kBatch * sizeof(Rec);  // 3 KB
 constexpr int kWaitLimit = 1 << 24;                  // bounded mbarrier wait (iterations)
 
-__device__ __forceinline__ void pixel_of_thread(int tile, int TX, int& px, int& py) {
+__device__ __forceinline__ int tile_of_block() { return int(blockIdx.x) / kCtasPerTile; }
+
+__device__ __forceinline__ void pixel_of_thread(int TX, int& px, int& py) {
+  const int tile = tile_of_block(), q = int(blockIdx.x) % kCtasPerTile;
   const int tx = tile % TX, ty = tile / TX;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  px = tx * kTile + (warp & 1) * 8 + (lane & 7);
-  py = ty * kTile + (warp >> 1) * 4 + (lane >> 3);
+  px = tx * kTile + (q & 1) * 8 + (lane & 7);
+  py = ty * kTile + (q >> 1) * 8 + warp * 4 + (lane >> 3);
+}
+
+// Pixel-centre bounds of this warp's 8x4 block.
+__device__ __forceinline__ void warp_block_bounds(int TX, float& x0, float& x1, float& y0, float& y1) {
+  const int tile = tile_of_block(), q = int(blockIdx.x) % kCtasPerTile;
+  const int warp = threadIdx.x >> 5;
+  const float bx = float((tile % TX) * kTile + (q & 1) * 8);
+  const float by = float((tile / TX) * kTile + (q >> 1) * 8 + warp * 4);
+  x0 = bx + 0.5f;
+  x1 = bx + 7.5f;
+  y0 = by + 0.5f;
+  y1 = by + 3.5f;
+}
+
+// Lane-parallel culling of 32 entries [j0, j0 + 32) of a staged batch against the
+// warp's block: bit l set if entry j0 + l may reach one of the warp's pixels, i.e.
+// the block is within the entry's skip radius of its mean on both axes.  A cleared
+// bit is an entry every lane of the warp would skip (power below the skip
+// threshold), so walking only the set bits changes no decision.
+__device__ __forceinline__ uint32_t warp_cull(const Rec* R, int j0, int cnt, float x0, float x1, float y0,
+                                              float y1) {
+  const int j = j0 + (threadIdx.x & 31);
+  bool near = false;
+  if (j < cnt) {
+    const float2 m = *reinterpret_cast<const float2*>(&R[j].a);
+    const float r = R[j].c.z;
+    near = !(m.x < x0 - r || m.x > x1 + r || m.y < y0 - r || m.y > y1 + r);
+  }
+  return __ballot_sync(0xffffffffu, near);
 }
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {

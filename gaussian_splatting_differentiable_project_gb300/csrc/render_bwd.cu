@@ -1,7 +1,7 @@
 // gs_render_bwd: L1 loss gradient and the compositing backward.
 //
-// One CTA per tile, one thread per pixel, the tile's records staged in reverse
-// batches by cp.async.bulk (as in the forward).  Each pixel walks its composited
+// One CTA per 8x8 quarter tile, one thread per pixel, the tile's records staged in
+// reverse batches by cp.async.bulk (as in the forward).  Each pixel walks its composited
 // entries back to front, recovering the transmittance before each entry by
 // division by (1 - alpha) and carrying the normalised colour of everything
 // behind it.  Per entry each lane holds nine partials; a warp that has any
@@ -57,12 +57,14 @@ __global__ void __launch_bounds__(kRasterThreads)
   __shared__ float s_red[kRasterThreads / 32];
   __shared__ uint32_t s_max[kRasterThreads / 32];
 
-  const int tile = blockIdx.x;
+  const int tile = tile_of_block();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   int pxi, pyi;
-  pixel_of_thread(tile, TX, pxi, pyi);
+  pixel_of_thread(TX, pxi, pyi);
   const bool inside = pxi < W && pyi < H;
   const float px = float(pxi) + 0.5f, py = float(pyi) + 0.5f;
+  float bx0, bx1, by0, by1;
+  warp_block_bounds(TX, bx0, bx1, by0, by1);
 
   // per-pixel loss gradient
   float g0 = 0.0f, g1 = 0.0f, g2 = 0.0f, T = 1.0f, lsum = 0.0f;
@@ -132,66 +134,62 @@ __global__ void __launch_bounds__(kRasterThreads)
     const int cnt = int(st.count(b));
     // this warp only needs entries below its largest n_contrib
     const int jmax = int(min(uint32_t(cnt), warp_max > pos0 ? warp_max - pos0 : 0u));
-    const float4* Rf = reinterpret_cast<const float4*>(R);
-    float4 pa, pb, pc;
-    if (jmax > 0) {
-      pa = Rf[3 * (jmax - 1)];
-      pb = Rf[3 * (jmax - 1) + 1];
-      pc = Rf[3 * (jmax - 1) + 2];
-    }
-    for (int j = jmax - 1; j >= 0; --j) {
-      const uint32_t pos = pos0 + uint32_t(j);
-      float v[9];
-      bool contrib = false;
-      const float4 ra = pa;  // next (lower) record loaded one entry ahead
-      const float4 rb = pb;
-      const float4 rc = pc;
-      if (j > 0) {
-        pa = Rf[3 * (j - 1)];
-        pb = Rf[3 * (j - 1) + 1];
-        pc = Rf[3 * (j - 1) + 2];
-      }
-      if (pos < nc) {
-        const float dx = __fsub_rn(px, ra.x), dy = __fsub_rn(py, ra.y);
-        const float power = conic_power(dx, dy, ra.z, ra.w, rb.x);
-        if (!(power > 0.0f) && !(power < kPowerSkip)) {
-          const float e = gs_expf_core(power);
-          const float vv = __fmul_rn(rb.y, e);
-          const bool clamped = !(vv < kAlphaMax);
-          const float alpha = clamped ? kAlphaMax : vv;
-          if (!(alpha < kAlphaMin)) {
-            contrib = true;
-            const float Ti = __fdividef(T, 1.0f - alpha);
-            const float wgt = alpha * Ti;
-            v[6] = g0 * wgt;
-            v[7] = g1 * wgt;
-            v[8] = g2 * wgt;
-            const float dLda = Ti * (g0 * (rb.z - acc0) + g1 * (rb.w - acc1) + g2 * (rc.x - acc2));
-            acc0 = alpha * rb.z + (1.0f - alpha) * acc0;
-            acc1 = alpha * rb.w + (1.0f - alpha) * acc1;
-            acc2 = alpha * rc.x + (1.0f - alpha) * acc2;
-            T = Ti;
-            const float dLdp = clamped ? 0.0f : dLda * alpha;
-            v[5] = clamped ? 0.0f : dLda * e;
-            // power = ca dx^2 + cb dx dy + cc dy^2 with (ca, cb, cc) = (-A/2, -B, -C/2)
-            v[0] = -dLdp * (2.0f * ra.z * dx + ra.w * dy);  // d/d mean x (dx = px - mx)
-            v[1] = -dLdp * (ra.w * dx + 2.0f * rb.x * dy);  // d/d mean y
-            v[2] = -0.5f * dLdp * dx * dx;                  // d/dA
-            v[3] = -dLdp * dx * dy;                         // d/dB
-            v[4] = -0.5f * dLdp * dy * dy;                  // d/dC
+    // 32 entries at a time, from the top: cull against the warp's block with one
+    // ballot, then walk the set bits from the highest down.
+    for (int j0 = ((jmax - 1) >> 5) << 5; j0 >= 0 && jmax > 0; j0 -= 32) {
+      uint32_t mask = warp_cull(R, j0, jmax, bx0, bx1, by0, by1);
+      while (mask) {
+        const int hb = 31 - __clz(mask);
+        mask &= ~(1u << hb);
+        const int j = j0 + hb;
+        const uint32_t pos = pos0 + uint32_t(j);
+        float v[9];
+        bool contrib = false;
+        const float4 ra = R[j].a;
+        const float4 rb = R[j].b;
+        const float4 rc = R[j].c;
+        if (pos < nc) {
+          const float dx = __fsub_rn(px, ra.x), dy = __fsub_rn(py, ra.y);
+          const float power = conic_power(dx, dy, ra.z, ra.w, rb.x);
+          if (!(power > 0.0f) && !(power < kPowerSkip)) {
+            const float e = gs_expf_core(power);
+            const float vv = __fmul_rn(rb.y, e);
+            const bool clamped = !(vv < kAlphaMax);
+            const float alpha = clamped ? kAlphaMax : vv;
+            if (!(alpha < kAlphaMin)) {
+              contrib = true;
+              const float Ti = __fdividef(T, 1.0f - alpha);
+              const float wgt = alpha * Ti;
+              v[6] = g0 * wgt;
+              v[7] = g1 * wgt;
+              v[8] = g2 * wgt;
+              const float dLda = Ti * (g0 * (rb.z - acc0) + g1 * (rb.w - acc1) + g2 * (rc.x - acc2));
+              acc0 = alpha * rb.z + (1.0f - alpha) * acc0;
+              acc1 = alpha * rb.w + (1.0f - alpha) * acc1;
+              acc2 = alpha * rc.x + (1.0f - alpha) * acc2;
+              T = Ti;
+              const float dLdp = clamped ? 0.0f : dLda * alpha;
+              v[5] = clamped ? 0.0f : dLda * e;
+              // power = ca dx^2 + cb dx dy + cc dy^2 with (ca, cb, cc) = (-A/2, -B, -C/2)
+              v[0] = -dLdp * (2.0f * ra.z * dx + ra.w * dy);  // d/d mean x (dx = px - mx)
+              v[1] = -dLdp * (ra.w * dx + 2.0f * rb.x * dy);  // d/d mean y
+              v[2] = -0.5f * dLdp * dx * dx;                  // d/dA
+              v[3] = -dLdp * dx * dy;                         // d/dB
+              v[4] = -0.5f * dLdp * dy * dy;                  // d/dC
+            }
           }
         }
-      }
-      if (!contrib) {
-#pragma unroll
-        for (int q = 0; q < 9; ++q) v[q] = 0.0f;
-      }
-      if (__any_sync(0xffffffffu, contrib)) {
-        float s8, s9;
-        warp_reduce9(v, &s8, &s9);
-        const uint32_t gid = __float_as_uint(rc.y);
-        if ((lane & 3) == 0) atomicAdd(gp + int64_t(lane >> 2) * n_pad + gid, s8);
-        if (lane == 1) atomicAdd(gp + int64_t(8) * n_pad + gid, s9);
+        if (!contrib) {
+  #pragma unroll
+          for (int q = 0; q < 9; ++q) v[q] = 0.0f;
+        }
+        if (__any_sync(0xffffffffu, contrib)) {
+          float s8, s9;
+          warp_reduce9(v, &s8, &s9);
+          const uint32_t gid = __float_as_uint(rc.y);
+          if ((lane & 3) == 0) atomicAdd(gp + int64_t(lane >> 2) * n_pad + gid, s8);
+          if (lane == 1) atomicAdd(gp + int64_t(8) * n_pad + gid, s9);
+        }
       }
     }
     __syncthreads();
@@ -225,7 +223,7 @@ extern "C" gs_status gs_render_bwd(gs_dims dims, const gs_camera* cam, const gs_
   const int TX = (cam->width + kTile - 1) / kTile;
   const int64_t tiles = n_tiles(cam);
   const float inv3P = float(1.0 / (3.0 * double(cam->width) * double(cam->height)));
-  k_render_bwd<<<int(tiles), kRasterThreads, 0, stream>>>(
+  k_render_bwd<<<int(tiles * kCtasPerTile), kRasterThreads, 0, stream>>>(
       reinterpret_cast<const Rec*>(bins->rec), reinterpret_cast<const uint2*>(bins->ranges), bins->n_isect,
       capacity_K, cam->width, cam->height, TX, bg[0], bg[1], bg[2], image, target, T_final, n_contrib, grad2d,
       dims.n_pad, loss_out, inv3P, dev_status);

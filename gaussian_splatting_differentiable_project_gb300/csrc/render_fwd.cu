@@ -1,11 +1,11 @@
 // gs_render_fwd: per-tile front-to-back alpha compositing.
 //
-// One CTA per 16x16 tile, one thread per pixel.  The tile's sorted records are
-// staged into shared memory in batches of 256 (12 KB) by cp.async.bulk with two
-// mbarrier-tracked buffers, so the next batch streams in while the current one is
-// composited; every thread reads the same record (shared-memory broadcast).  A
-// pixel stops at its transmittance threshold; the CTA stops loading once
-// __syncthreads_count reports no live pixel.
+// One CTA per 8x8 quarter of a 16x16 tile, one thread per pixel.  The tile's
+// sorted records are staged into shared memory in batches of 64 (3 KB) by
+// cp.async.bulk with two mbarrier-tracked buffers, so the next batch streams in
+// while the current one is composited; every thread reads the same record
+// (shared-memory broadcast).  A pixel stops at its transmittance threshold; the
+// CTA stops loading once __syncthreads_count reports no live pixel.
 #include "api_util.h"
 #include "raster_common.cuh"
 
@@ -18,11 +18,13 @@ __global__ void __launch_bounds__(kRasterThreads)
   __shared__ __align__(128) Rec s_rec[2][kBatch];
   __shared__ __align__(8) uint64_t s_bar[2];
 
-  const int tile = blockIdx.x;
+  const int tile = tile_of_block();
   int pxi, pyi;
-  pixel_of_thread(tile, TX, pxi, pyi);
+  pixel_of_thread(TX, pxi, pyi);
   const bool inside = pxi < W && pyi < H;
   const float px = float(pxi) + 0.5f, py = float(pyi) + 0.5f;
+  float bx0, bx1, by0, by1;
+  warp_block_bounds(TX, bx0, bx1, by0, by1);
 
   const uint32_t K = min(*n_isect, cap);
   const uint2 rg = ranges[tile];
@@ -53,43 +55,39 @@ __global__ void __launch_bounds__(kRasterThreads)
       const Rec* R = st.buffer(slot);
       const int cnt = int(st.count(b));
       const uint32_t pos0 = uint32_t(b) * kBatch;
-      // Warp-uniform walk over the batch: every lane steps through the same j and
-      // takes its skip / stop decisions as predicates, so the warp stays converged
-      // (per-lane continue/break let the lanes drift apart and run serially).
-      // The next record is loaded from shared memory one entry ahead.
+      // Warp-uniform walk over the batch: 32 entries at a time are culled against
+      // the warp's 8x4 block by one ballot, then the warp steps through the set
+      // bits in order; every lane takes its skip / stop decisions as predicates,
+      // so the warp stays converged.
       if (!__all_sync(0xffffffffu, done)) {
-        const float4* Rf = reinterpret_cast<const float4*>(R);
-        float4 na = Rf[0], nb = Rf[1];
-        float nc2 = Rf[2].x;
-        for (int j = 0; j < cnt; ++j) {
-          const float4 ra = na;  // mx, my, ca, cb
-          const float4 rb = nb;  // cc, o, r, g
-          const float cb = nc2;  // b
-          if (j + 1 < cnt) {
-            na = Rf[3 * (j + 1)];
-            nb = Rf[3 * (j + 1) + 1];
-            nc2 = Rf[3 * (j + 1) + 2].x;
-          }
-          const float dx = __fsub_rn(px, ra.x), dy = __fsub_rn(py, ra.y);
-          const float power = conic_power(dx, dy, ra.z, ra.w, rb.x);
-          if (!done && !(power > 0.0f) && !(power < kPowerSkip)) {
-            const float v = __fmul_rn(rb.y, gs_expf_core(power));
-            const float alpha = (v < kAlphaMax) ? v : kAlphaMax;
-            if (!(alpha < kAlphaMin)) {
-              const float Tn = __fmul_rn(T, __fsub_rn(1.0f, alpha));
-              if (Tn < kTMin) {
-                done = true;
-              } else {
-                const float w = __fmul_rn(alpha, T);
-                C0 = __fmaf_rn(rb.z, w, C0);
-                C1 = __fmaf_rn(rb.w, w, C1);
-                C2 = __fmaf_rn(cb, w, C2);
-                T = Tn;
-                last = pos0 + uint32_t(j) + 1u;
+        for (int j0 = 0; j0 < cnt; j0 += 32) {
+          uint32_t mask = warp_cull(R, j0, cnt, bx0, bx1, by0, by1);
+          while (mask) {
+            const int j = j0 + __ffs(mask) - 1;
+            mask &= mask - 1u;
+            const float4 ra = R[j].a;  // mx, my, ca, cb
+            const float4 rb = R[j].b;  // cc, o, r, g
+            const float dx = __fsub_rn(px, ra.x), dy = __fsub_rn(py, ra.y);
+            const float power = conic_power(dx, dy, ra.z, ra.w, rb.x);
+            if (!done && !(power > 0.0f) && !(power < kPowerSkip)) {
+              const float v = __fmul_rn(rb.y, gs_expf_core(power));
+              const float alpha = (v < kAlphaMax) ? v : kAlphaMax;
+              if (!(alpha < kAlphaMin)) {
+                const float Tn = __fmul_rn(T, __fsub_rn(1.0f, alpha));
+                if (Tn < kTMin) {
+                  done = true;
+                } else {
+                  const float w = __fmul_rn(alpha, T);
+                  C0 = __fmaf_rn(rb.z, w, C0);
+                  C1 = __fmaf_rn(rb.w, w, C1);
+                  C2 = __fmaf_rn(R[j].c.x, w, C2);
+                  T = Tn;
+                  last = pos0 + uint32_t(j) + 1u;
+                }
               }
             }
           }
-          if ((j & 3) == 3 && __all_sync(0xffffffffu, done)) break;
+          if (__all_sync(0xffffffffu, done)) break;
         }
       }
       const int alive = __syncthreads_count(!done);
@@ -126,7 +124,7 @@ extern "C" gs_status gs_render_fwd(const gs_camera* cam, const gs_bins* bins, ui
   if (!aligned(bins->rec, 16) || !aligned(bins->ranges, 8)) return GS_ERR_INVALID_ARG;
   const int TX = (cam->width + kTile - 1) / kTile;
   const int64_t tiles = n_tiles(cam);
-  k_render_fwd<<<int(tiles), kRasterThreads, 0, stream>>>(
+  k_render_fwd<<<int(tiles * kCtasPerTile), kRasterThreads, 0, stream>>>(
       reinterpret_cast<const Rec*>(bins->rec), reinterpret_cast<const uint2*>(bins->ranges), bins->n_isect,
       capacity_K, cam->width, cam->height, TX, bg[0], bg[1], bg[2], image, T_final, n_contrib, dev_status);
   return launch_status();
