@@ -7,9 +7,10 @@
 //                     ranges (so the workspace needs no initialisation)
 //   k_bs_scan_sums    one block: exclusive scan of the block sums -> K
 //   k_bs_emit         per Gaussian, its offset (block scan + block prefix) and one
-//                     key per tile of its rect, in index order; digit histograms
-//                     of every radix pass accumulated on the way
-//   k_bs_onesweep     one launch per 8-bit digit: stable ranking of 4096 keys per
+//                     key per tile of its rect, in index order, staged through
+//                     shared memory for coalesced writes; digit histograms of
+//                     every radix pass accumulated on the way
+//   k_bs_onesweep     one launch per 8-bit digit: stable ranking of 2048 keys per
 //                     CTA, decoupled look-back (bounded wait) across CTAs taken in
 //                     ticket order, scatter through shared memory
 //   k_bs_ranges_gather per intersection: tile [start, end) and the 48-byte record
@@ -26,7 +27,7 @@ constexpr int kScanItems = 16;
 constexpr int kScanBlock = kScanThreads * kScanItems;  // Gaussians per scan block
 constexpr int kSortThreads = 256;
 constexpr int kSortWarps = kSortThreads / 32;
-constexpr int kSortItems = 16;
+constexpr int kSortItems = 8;
 constexpr int kPart = kSortThreads * kSortItems;  // keys per onesweep partition
 constexpr int kMaxPasses = 8;
 constexpr uint32_t kFlagAgg = 1u << 30;
@@ -78,12 +79,14 @@ inline SortLayout sort_layout(int64_t n, uint32_t cap, int64_t tiles) {
 }
 
 // ------------------------------------------------------------------ memory order helpers
-__device__ __forceinline__ void st_release(uint32_t* p, uint32_t v) {
-  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+// Look-back words hold flag and count in one 32-bit word and publish nothing
+// else, so relaxed (L2-coherent, unfenced) accesses suffice.
+__device__ __forceinline__ void st_relaxed(uint32_t* p, uint32_t v) {
+  asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
-__device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
+__device__ __forceinline__ uint32_t ld_relaxed(const uint32_t* p) {
   uint32_t v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
 }
 
@@ -164,45 +167,66 @@ __global__ void __launch_bounds__(1024)
   }
 }
 
+constexpr int kEmitStage = 2048;  // keys staged in shared memory per write-out chunk
+
+// Emission: a block owns Gaussians [block * 4096, +4096) and the contiguous output
+// range [block_prefix, block_prefix + block total).  It walks them in 16 rounds of
+// 256 (one Gaussian per thread, coalesced reads); a block scan of the round's
+// counts gives each Gaussian's offset, and the round's keys are staged through
+// shared memory in chunks of kEmitStage so that they leave in contiguous,
+// coalesced runs.  The digit histograms of every radix pass are accumulated on
+// the way out.
 __global__ void __launch_bounds__(kScanThreads)
     k_bs_emit(const uint32_t* __restrict__ count, const uint2* __restrict__ rect, const float* __restrict__ depth,
               int64_t n, const uint64_t* __restrict__ block_prefix, uint64_t* __restrict__ keys,
               uint32_t* __restrict__ ids, uint32_t cap, int TX, int passes, uint32_t* __restrict__ hist) {
   __shared__ uint32_t s_warp[8];
   __shared__ uint32_t s_hist[kMaxPasses * 256];
+  __shared__ uint64_t s_key[kEmitStage];
+  __shared__ uint32_t s_id[kEmitStage];
   for (int k = threadIdx.x; k < passes * 256; k += kScanThreads) s_hist[k] = 0;
-  // blocked arrangement: thread t owns Gaussians [base + 16 t, base + 16 t + 16)
-  const int64_t base = int64_t(blockIdx.x) * kScanBlock + int64_t(threadIdx.x) * kScanItems;
-  uint32_t c[kScanItems];
-  uint32_t s = 0;
-#pragma unroll
-  for (int it = 0; it < kScanItems; ++it) {
-    const int64_t i = base + it;
-    c[it] = (i < n) ? count[i] : 0u;
-    s += c[it];
-  }
-  const uint32_t excl = block_excl_scan_256(s, s_warp, nullptr);  // also orders the s_hist clear
-  uint64_t off = block_prefix[blockIdx.x] + excl;
+  uint64_t round_base = block_prefix[blockIdx.x];
+  const int64_t base = int64_t(blockIdx.x) * kScanBlock;
 #pragma unroll 1
-  for (int it = 0; it < kScanItems; ++it) {
-    if (c[it] == 0) continue;
-    const int64_t i = base + it;
-    const uint2 r = rect[i];
-    const uint32_t tx0 = r.x & 0xFFFFu, ty0 = r.x >> 16, tx1 = r.y & 0xFFFFu, ty1 = r.y >> 16;
-    const uint64_t zb = uint64_t(__float_as_uint(depth[i]));
-    for (uint32_t ty = ty0; ty <= ty1; ++ty) {
-      for (uint32_t tx = tx0; tx <= tx1; ++tx) {
-        if (off < cap) {
-          const uint64_t key = (uint64_t(ty * uint32_t(TX) + tx) << 32) | zb;
-          keys[off] = key;
-          ids[off] = uint32_t(i);
+  for (int r = 0; r < kScanItems; ++r) {
+    const int64_t i = base + int64_t(r) * kScanThreads + threadIdx.x;
+    const uint32_t c = (i < n) ? count[i] : 0u;
+    uint32_t tx0 = 0, ty0 = 0, w = 1;
+    uint32_t zb = 0;
+    if (c) {
+      const uint2 rc = rect[i];
+      tx0 = rc.x & 0xFFFFu;
+      ty0 = rc.x >> 16;
+      w = (rc.y & 0xFFFFu) - tx0 + 1u;
+      zb = __float_as_uint(depth[i]);
+    }
+    uint32_t total;
+    const uint32_t off = block_excl_scan_256(c, s_warp, &total);  // also orders s_hist clear
+#pragma unroll 1
+    for (uint32_t c0 = 0; c0 < total; c0 += kEmitStage) {
+      // this thread's keys k in [0, c) whose round offset off + k lies in the chunk
+      const uint32_t lo = (c0 > off) ? c0 - off : 0u;
+      const uint32_t hi = min(c, (c0 + kEmitStage > off) ? c0 + kEmitStage - off : 0u);
+      for (uint32_t k = lo; k < hi; ++k) {
+        const uint32_t ty = ty0 + k / w, tx = tx0 + k % w;
+        s_key[off + k - c0] = (uint64_t(ty * uint32_t(TX) + tx) << 32) | zb;
+        s_id[off + k - c0] = uint32_t(i);
+      }
+      __syncthreads();
+      const uint32_t m = min(uint32_t(kEmitStage), total - c0);
+      for (uint32_t q = threadIdx.x; q < m; q += kScanThreads) {
+        const uint64_t o = round_base + c0 + q;
+        if (o < cap) {
+          const uint64_t key = s_key[q];
+          keys[o] = key;
+          ids[o] = s_id[q];
           for (int p = 0; p < passes; ++p) atomicAdd(&s_hist[p * 256 + int((key >> (8 * p)) & 0xFFu)], 1u);
         }
-        ++off;
       }
+      __syncthreads();
     }
+    round_base += total;
   }
-  __syncthreads();
   for (int k = threadIdx.x; k < passes * 256; k += kScanThreads) {
     const uint32_t v = s_hist[k];
     if (v) atomicAdd(&hist[k], v);
@@ -275,7 +299,7 @@ __global__ void __launch_bounds__(kSortThreads)
     tot += c;
   }
   uint32_t* mine = look + size_t(part) * 256 + d;
-  st_release(mine, (part == 0 ? kFlagInc : kFlagAgg) | tot);
+  st_relaxed(mine, (part == 0 ? kFlagInc : kFlagAgg) | tot);
 
   const uint32_t gstart = block_excl_scan_256(hist[d], s_warp, nullptr);
   const uint32_t lstart = block_excl_scan_256(tot, s_warp, nullptr);
@@ -285,7 +309,7 @@ __global__ void __launch_bounds__(kSortThreads)
     int64_t j = int64_t(part) - 1;
     int spins = 0;
     for (;;) {
-      const uint32_t w = ld_acquire(look + size_t(j) * 256 + d);
+      const uint32_t w = ld_relaxed(look + size_t(j) * 256 + d);
       const uint32_t f = w & ~kCountMask;
       if (f == 0u) {
         if (++spins > kSpinLimit) {
@@ -299,7 +323,7 @@ __global__ void __launch_bounds__(kSortThreads)
       if (f == kFlagInc || j == 0) break;
       --j;
     }
-    st_release(mine, kFlagInc | (excl + tot));
+    st_relaxed(mine, kFlagInc | (excl + tot));
   }
   s_gbase[d] = gstart + excl;
   s_lstart[d] = lstart;
@@ -439,7 +463,7 @@ constexpr size_t kNoAllocBytes =
     na_align(size_t((GS_NOALLOC_MAX_N + kScanBlock - 1) / kScanBlock) * 8) + na_align(size_t(kMaxPasses) * 256 * 4) +
     na_align(size_t(kMaxPasses) * 4) +
     na_align(size_t(6) * size_t((GS_NOALLOC_MAX_K + kPart - 1) / kPart) * 256 * 4);
-static_assert(kNoAllocBytes == 14172416, "fixed scratch size changed");
+static_assert(kNoAllocBytes == 15745280, "fixed scratch size changed");
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocBytes];
 

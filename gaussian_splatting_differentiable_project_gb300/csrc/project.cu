@@ -21,7 +21,7 @@ __device__ __forceinline__ float skip_radius(float lam) {
   return r <= 128.0f ? r : __int_as_float(0x7f7fffff);
 }
 
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(256, 2)
     k_project(const float* __restrict__ P, int64_t n, int64_t n_pad, CamDev cam, float4* __restrict__ rec,
               float* __restrict__ depth, int32_t* __restrict__ radius, uint2* __restrict__ rect,
               uint32_t* __restrict__ count, uint32_t* __restrict__ dev_status) {

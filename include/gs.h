@@ -252,7 +252,7 @@ gs_status gs_adam_step(gs_dims dims, float* params, const float* grads, float* m
  * in advance, embedders whose allocator owns the GPU).  The paper has no
  * counterpart; this is a library convenience.  Results are identical to
  * gs_bin_sort's.
- *   Scratch: a fixed array inside the library (about 13.5 MiB), held by every GPU
+ *   Scratch: a fixed array inside the library (15.0 MiB), held by every GPU
  *   that loads the library until the process exits.  It is used in place of the
  *   workspace argument; the caller still passes proj and bins.
  *   Limits: n <= GS_NOALLOC_MAX_N, capacity_K <= GS_NOALLOC_MAX_K, at most
