@@ -6,18 +6,24 @@
 
 namespace gs {
 
-// Skip radius r of a record: at every pixel with |dx| > r or |dy| > r the entry's
-// fp32 power is below the rasteriser's -5.6 skip threshold, so the entry would be
-// skipped there anyway.  lam >= the largest eigenvalue of the 2D covariance (it is
-// the radius eigenvalue, with its 0.1 floor), so the exact inverse has smallest
-// eigenvalue mu_min >= 1/lam and power <= -|d|^2 / (2 lam).  The fp32 conic differs
-// from the exact inverse by a common factor (the rounded determinant) and a few ulp
-// per entry, together below 0.2% of mu_min while lam <= 1424 (r <= 128 px, which
-// bounds mu_max / mu_min by lam / 0.3); the fp32 power adds a few ulp of
-// mu_max |d|^2.  r = sqrt(11.536 lam) + 0.1 keeps the exact power below -5.77 and
-// covers both; beyond 128 px the radius is +inf (never skip).
-__device__ __forceinline__ float skip_radius(float lam) {
-  const float r = sqrtf(11.536f * lam) + 0.1f;
+// Skip radius r of a record: at every pixel whose distance from the mean exceeds
+// r the entry is skipped by the rasteriser anyway (alpha below 1/255, or power
+// below the -5.6 skip threshold), so a warp whose pixels all lie farther than r
+// may skip the entry without changing any decision.
+//   lam >= the largest eigenvalue of the 2D covariance (the radius eigenvalue, with
+//   its 0.1 floor), so the exact inverse gives power <= -|d|^2 / (2 lam).  alpha =
+//   o e^power < 1/255 wherever power < -L with L = ln(255 o) (never above 5.54 <
+//   5.6).  r^2 = 2.06 lam (L + 0.05) keeps the exact power below -(L + 0.05) by 3%:
+//   the fp32 conic differs from the exact inverse by below 0.2% of mu_min while
+//   lam <= 1424 (r <= 128 px, which bounds mu_max / mu_min by lam / 0.3), the fp32
+//   power by a few ulp of mu_max |d|^2 (< 0.02 here) and the fp32 exponential and
+//   product by a few ulp, all inside the 0.05 margin.  An opacity at most
+//   0.999/255 is never composited (alpha <= o < 1/255): r = -inf (skip everywhere).
+//   Beyond 128 px: +inf (never skip).
+__device__ __forceinline__ float skip_radius(float lam, float o) {
+  if (!(o * 255.0f > 0.999f)) return -__int_as_float(0x7f7fffff);
+  const float L = logf(255.0f * o) + 0.05f;
+  const float r = sqrtf(2.06f * lam * L) + 0.1f;
   return r <= 128.0f ? r : __int_as_float(0x7f7fffff);
 }
 
@@ -48,7 +54,7 @@ __global__ void __launch_bounds__(256, 2)
     if (vis) {
       rec[3 * i + 0] = make_float4(g.mx, g.my, __fmul_rn(-0.5f, g.A), -g.B);
       rec[3 * i + 1] = make_float4(__fmul_rn(-0.5f, g.C), o, rgb[0], rgb[1]);
-      rec[3 * i + 2] = make_float4(rgb[2], __uint_as_float(uint32_t(i)), skip_radius(g.lam), 0.0f);
+      rec[3 * i + 2] = make_float4(rgb[2], __uint_as_float(uint32_t(i)), skip_radius(g.lam, o), 0.0f);
       depth[i] = g.tz;
       radius[i] = g.radius;
       rect[i] = make_uint2(uint32_t(g.tx0) | (uint32_t(g.ty0) << 16), uint32_t(g.tx1) | (uint32_t(g.ty1) << 16));

@@ -41,7 +41,7 @@ __device__ __forceinline__ void warp_block_bounds(int TX, float& x0, float& x1, 
 
 // Lane-parallel culling of 32 entries [j0, j0 + 32) of a staged batch against the
 // warp's block: bit l set if entry j0 + l may reach one of the warp's pixels, i.e.
-// the block is within the entry's skip radius of its mean on both axes.  A cleared
+// the block is within the entry's skip radius of its mean.  A cleared
 // bit is an entry every lane of the warp would skip (power below the skip
 // threshold), so walking only the set bits changes no decision.
 __device__ __forceinline__ uint32_t warp_cull(const Rec* R, int j0, int cnt, float x0, float x1, float y0,
@@ -51,7 +51,10 @@ __device__ __forceinline__ uint32_t warp_cull(const Rec* R, int j0, int cnt, flo
   if (j < cnt) {
     const float2 m = *reinterpret_cast<const float2*>(&R[j].a);
     const float r = R[j].c.z;
-    near = !(m.x < x0 - r || m.x > x1 + r || m.y < y0 - r || m.y > y1 + r);
+    // Euclidean distance from the mean to the block of pixel centres
+    const float ex = fmaxf(fmaxf(x0 - m.x, m.x - x1), 0.0f);
+    const float ey = fmaxf(fmaxf(y0 - m.y, m.y - y1), 0.0f);
+    near = (r >= 0.0f) && (ex * ex + ey * ey <= r * r);
   }
   return __ballot_sync(0xffffffffu, near);
 }

@@ -94,9 +94,9 @@ typedef struct gs_dims {
  *   rec    12 floats per Gaussian (16-byte aligned): mean2d x, y; (ca, cb, cc) =
  *          (-A/2, -B, -C/2) for the conic [[A, B], [B, C]] (inverse 2D covariance),
  *          so that power = ca dx^2 + cb dx dy + cc dy^2; opacity; r, g, b; the
- *          Gaussian's index (uint32 bits); a skip radius (beyond it on either axis
- *          the entry's alpha is below the compositing threshold; +FLT_MAX if not
- *          bounded); 1 unused.  The pages' projected record
+ *          Gaussian's index (uint32 bits); a skip radius (at pixels farther than it
+ *          from the mean the entry's alpha is below the compositing threshold;
+ *          +FLT_MAX if not bounded, -FLT_MAX if never composited); 1 unused.  The pages' projected record
  *          (means2d, depth, conic, opacity, colour) minus depth and radius, which
  *          are kept in their own arrays.
  *   depth  camera-space z.
