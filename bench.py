@@ -436,12 +436,13 @@ def run_gb300(args, cfg, ws, rank, local):
                            "frac": max(tb, tf) / t_meas}
     dom = max(STAGES, key=lambda s: stage_ms[s])
     d = per_stage[dom]
+    traffic = measured_traffic({"render_fwd": "k_render_fwd", "render_bwd": "k_render_bwd"}.get(dom, ""))
     if d["bound"] == "hbm":
         roof = {"kernel": dom, "bound": "hbm", "achieved": d["gbs"], "peak": peak_bw, "unit": "GB/s",
-                "frac": d["gbs"] / peak_bw, "traffic": None, "peak_source": _peak_src("hbm_gbs")}
+                "frac": d["gbs"] / peak_bw, "traffic": traffic, "peak_source": _peak_src("hbm_gbs")}
     else:
         roof = {"kernel": dom, "bound": "alu", "achieved": d["tflops"], "peak": peak_fp32, "unit": "TFLOP/s",
-                "frac": d["tflops"] / peak_fp32, "traffic": None,
+                "frac": d["tflops"] / peak_fp32, "traffic": traffic,
                 "peak_source": f"152 SMs x 128 FP32 lanes x 2 x {sm_mhz:.0f} MHz"}
 
     cpu = None
@@ -465,6 +466,28 @@ def run_gb300(args, cfg, ws, rank, local):
         "clocks": clk, "setup_s": setup_s,
     }
     print(json.dumps(line), flush=True)
+
+
+def measured_traffic(kernel: str):
+    """DRAM bytes per launch of ``kernel`` from profiles/dram_traffic.md, or None if the
+    kernel's sources changed since that capture (fingerprint mismatch) or it has none."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "dram_traffic.md")
+    if not os.path.exists(path):
+        return None
+    for line in open(path):
+        cells = [c.strip() for c in line.strip().strip("|").split("|")]
+        if len(cells) != 6 or cells[0] != kernel:
+            continue
+        h = hashlib.sha256()
+        try:
+            for f in cells[1].split():
+                h.update(open(os.path.join(ROOT, "gaussian_splatting_differentiable_project_gb300", "csrc", f),
+                              "rb").read())
+        except OSError:
+            return None
+        return int(cells[5]) if h.hexdigest()[:16] == cells[2] else None
+    return None
 
 
 def _peak(key, fallback):
