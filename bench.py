@@ -38,7 +38,8 @@ sys.path.insert(0, ROOT)
 import gs_inputs as gi  # noqa: E402
 
 METRIC = "train steps/s (fwd+bwd+Adam, 1 view) at 4M Gaussians 2048²; % of roofline"
-STAGES = ["project", "bin_sort", "render_fwd", "render_bwd", "project_bwd", "adam"]
+STAGES_SEPARATE = ["project", "bin_sort", "render_fwd", "render_bwd", "project_bwd", "adam"]
+STAGES_FUSED = ["project", "bin_sort", "render_fwd", "render_bwd", "project_bwd_adam"]
 
 
 def parse():
@@ -52,6 +53,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--capacity-slack", type=float, default=1.15)
+    ap.add_argument("--separate", action="store_true",
+                    help="run the projection backward and Adam as two calls instead of gs_project_bwd_adam")
     ap.add_argument("--views", type=int, default=0,
                     help="use only the first N orbit views (profiling runs; 0 = all)")
     return ap.parse_args()
@@ -157,6 +160,19 @@ def stage_bytes(N, n_pad, V, K, P, passes):
         # p, g, m, v read; p, m, v written
         "adam": 59 * n_pad * 28,
     }
+
+
+# Bytes the fused projection backward + Adam actually moves: count, 9 grad2d of the
+# visible, p, m, v read and written for every parameter (the gradient planes are
+# never written).  The step roofline still charges rows a5 + a6 their own bytes.
+def fused_bytes(N, n_pad, V):
+    return 4 * N + 36 * V + 59 * n_pad * 24
+
+
+# Rows of the step each measured stage covers.
+STAGE_ROWS = {"project": ["project"], "bin_sort": ["bin_sort"], "render_fwd": ["render_fwd"],
+              "render_bwd": ["render_bwd"], "project_bwd": ["project_bwd"], "adam": ["adam"],
+              "project_bwd_adam": ["project_bwd", "adam"]}
 
 
 # FP32 operations per iterated (pixel, entry) pair, counting an FMA as 2 and the
@@ -310,7 +326,8 @@ def run_gb300(args, cfg, ws, rank, local):
     rend.raise_on_status()
     del rend, Ptd
 
-    tr = gs.Trainer(Pd, n, W, H, capacity, gi.lr_planes(), device=dev)
+    tr = gs.Trainer(Pd, n, W, H, capacity, gi.lr_planes(), device=dev, fused=not args.separate)
+    STAGES = STAGES_SEPARATE if args.separate else STAGES_FUSED
     del Pd
     # per-view work statistics (forward on the initial parameters)
     E = []
@@ -338,10 +355,16 @@ def run_gb300(args, cfg, ws, rank, local):
         gs.render_bwd(tr.n, tr.n_pad, cam, tr.bins, tr.bg, tr.image, targets[v], tr.T_final, tr.n_contrib,
                       tr.grad2d, tr.loss, tr.status)
         e[4].record()
-        gs.project_bwd(tr.n, tr.params, cam, tr.proj, tr.grad2d, tr.grads, tr.status)
-        e[5].record()
-        tr.optimizer_step()
-        e[6].record()
+        if args.separate:
+            gs.project_bwd(tr.n, tr.params, cam, tr.proj, tr.grad2d, tr.grads, tr.status)
+            e[5].record()
+            tr.optimizer_step()
+            e[6].record()
+        else:
+            tr.t += 1
+            gs.project_bwd_adam(tr.n, tr.params, cam, tr.proj, tr.grad2d, tr.m, tr.v, tr.lr_plane, tr.beta1,
+                                tr.beta2, tr.eps, tr.t, tr.status)
+            e[5].record()
 
     for s in range(args.warmup):
         step(s)
@@ -349,7 +372,7 @@ def run_gb300(args, cfg, ws, rank, local):
 
     # ---------------------------------------------------------------- timed region
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(K)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(STAGES) + 1)] for _ in range(K)]
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
@@ -425,15 +448,19 @@ def run_gb300(args, cfg, ws, rank, local):
     flops = {"render_fwd": FLOP_FWD_PAIR * Emean, "render_bwd": FLOP_BWD_PAIR * Emean}
     per_stage = {}
     t_star = 0.0
+    row_t = {}
+    for row in STAGE_ROWS["project_bwd_adam"] + ["project", "bin_sort", "render_fwd", "render_bwd"]:
+        row_t[row] = max(byt[row] / (peak_bw * 1e9), flops.get(row, 0.0) / (peak_fp32 * 1e12))
+    t_star = sum(row_t.values())
     for name in STAGES:
-        tb = byt[name] / (peak_bw * 1e9)
-        tf = flops.get(name, 0.0) / (peak_fp32 * 1e12)
-        t_star += max(tb, tf)
+        rows = STAGE_ROWS[name]
         t_meas = stage_ms[name] / 1e3
-        bound = "alu" if tf > tb else "hbm"
-        per_stage[name] = {"ms": stage_ms[name], "bound": bound,
-                           "gbs": byt[name] / t_meas / 1e9, "tflops": flops.get(name, 0.0) / t_meas / 1e12,
-                           "frac": max(tb, tf) / t_meas}
+        t_rows = sum(row_t[r] for r in rows)
+        moved = fused_bytes(n, n_pad, Vmean) if name == "project_bwd_adam" else sum(byt[r] for r in rows)
+        fl = sum(flops.get(r, 0.0) for r in rows)
+        bound = "alu" if fl / (peak_fp32 * 1e12) > moved / (peak_bw * 1e9) else "hbm"
+        per_stage[name] = {"ms": stage_ms[name], "bound": bound, "rows": rows,
+                           "gbs": moved / t_meas / 1e9, "tflops": fl / t_meas / 1e12, "frac": t_rows / t_meas}
     dom = max(STAGES, key=lambda s: stage_ms[s])
     d = per_stage[dom]
     traffic = measured_traffic({"render_fwd": "k_render_fwd", "render_bwd": "k_render_bwd"}.get(dom, ""))
@@ -452,7 +479,7 @@ def run_gb300(args, cfg, ws, rank, local):
         except Exception as exc:  # the baseline is reported, never required
             cpu = {"value": None, "unit": "steps/s", "kind": "oracle", "error": repr(exc)}
 
-    launches_per_step = 1 + (4 + passes) + 1 + 2 + 1 + 1
+    launches_per_step = 1 + (4 + passes) + 1 + 2 + (2 if args.separate else 1)
     line = {
         "metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": ws, "steps": K, "warmup": args.warmup,
         "ms_per_step": ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,

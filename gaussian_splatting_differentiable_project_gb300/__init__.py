@@ -8,7 +8,8 @@ present, the calls raise.
 
 Entry points (same names as the C ABI, without the ``gs_`` prefix):
 ``project``, ``bin_sort``, ``render_fwd``, ``render_bwd``, ``project_bwd``,
-``adam_step``, plus ``util_expf`` and ``bin_sort_workspace_bytes``.
+``adam_step``, the fused ``project_bwd_adam``, plus ``bin_sort_noalloc``,
+``util_expf`` and ``bin_sort_workspace_bytes``.
 """
 from __future__ import annotations
 
@@ -101,6 +102,10 @@ def load(build_if_missing: bool = True):
         lib.gs_adam_step.argtypes = [GsDims, P, P, P, P, ctypes.POINTER(ctypes.c_float), ctypes.c_double,
                                      ctypes.c_double, ctypes.c_double, ctypes.c_int64, P]
         lib.gs_adam_step.restype = st
+        lib.gs_project_bwd_adam.argtypes = [GsDims, P, ctypes.POINTER(GsCamera), ctypes.POINTER(GsProj), P, P, P,
+                                            ctypes.POINTER(ctypes.c_float), ctypes.c_double, ctypes.c_double,
+                                            ctypes.c_double, ctypes.c_int64, P, P]
+        lib.gs_project_bwd_adam.restype = st
         lib.gs_util_expf.argtypes = [P, P, ctypes.c_int64, P]
         lib.gs_util_expf.restype = st
         lib.gs_status_str.argtypes = [ctypes.c_uint32]
@@ -253,6 +258,17 @@ def adam_step(n: int, params, grads, m, v, lr_plane, beta1: float, beta2: float,
     lr = (ctypes.c_float * N_PLANES)(*[float(x) for x in lr_plane])
     _check(load().gs_adam_step(dims(n, params.shape[1]), _p(params), _p(grads), _p(m), _p(v), lr, float(beta1),
                                float(beta2), float(eps), int(t), _stream(stream)), "gs_adam_step")
+
+
+def project_bwd_adam(n: int, params, cam: dict, proj: ProjBuffers, grad2d, m, v, lr_plane, beta1: float,
+                     beta2: float, eps: float, t: int, dev_status, stream=None) -> None:
+    """Projection backward and Adam step ``t`` in one pass (no gradient planes)."""
+    cc = camera(cam)
+    pc = proj.c()
+    lr = (ctypes.c_float * N_PLANES)(*[float(x) for x in lr_plane])
+    _check(load().gs_project_bwd_adam(dims(n, params.shape[1]), _p(params), ctypes.byref(cc), ctypes.byref(pc),
+                                      _p(grad2d), _p(m), _p(v), lr, float(beta1), float(beta2), float(eps), int(t),
+                                      _p(dev_status), _stream(stream)), "gs_project_bwd_adam")
 
 
 def util_expf(x, y, stream=None) -> None:

@@ -1,0 +1,40 @@
+// Adam element update shared by gs_adam_step and the fused projection backward +
+// Adam, so that both paths apply the same fp32 expression.
+#pragma once
+
+#include <cmath>
+
+#include "gs_common.cuh"
+
+namespace gs {
+
+// Hyperparameters as the kernels use them: beta, 1 - beta, the bias corrections
+// and lr / (1 - beta1^t) are formed on the host in fp64 and rounded to fp32 once.
+struct AdamParams {
+  float step[kPlanes];  // lr[plane] / (1 - beta1^t)
+  float b1, c1, b2, c2, eps, inv_sqrt_bc2;
+};
+
+inline bool make_adam_params(const float lr_plane[kPlanes], double beta1, double beta2, double eps, int64_t t,
+                             AdamParams& a) {
+  if (t < 1 || !(beta1 >= 0.0 && beta1 < 1.0) || !(beta2 >= 0.0 && beta2 < 1.0) || !(eps >= 0.0)) return false;
+  const double bc1 = 1.0 - std::pow(beta1, double(t));
+  const double bc2 = 1.0 - std::pow(beta2, double(t));
+  for (int k = 0; k < kPlanes; ++k) a.step[k] = float(double(lr_plane[k]) / bc1);
+  a.b1 = float(beta1);
+  a.c1 = float(1.0 - beta1);
+  a.b2 = float(beta2);
+  a.c2 = float(1.0 - beta2);
+  a.eps = float(eps);
+  a.inv_sqrt_bc2 = float(1.0 / std::sqrt(bc2));
+  return true;
+}
+
+// m = b1 m + (1 - b1) g; v = b2 v + (1 - b2) g^2; p -= step m / (sqrt(v) / sqrt(bc2) + eps)
+__device__ __forceinline__ void adam_elem(float& p, float& m, float& v, float g, float step, const AdamParams& a) {
+  m = a.b1 * m + a.c1 * g;
+  v = a.b2 * v + a.c2 * g * g;
+  p -= step * m / (sqrtf(v) * a.inv_sqrt_bc2 + a.eps);
+}
+
+}  // namespace gs

@@ -6,6 +6,7 @@
 // Reads the 59 parameter planes and 9 gradient planes, writes 59 gradient
 // planes; every access is coalesced across the warp.
 #include "api_util.h"
+#include "adam_common.cuh"
 #include "project_frozen.cuh"
 
 namespace gs {
@@ -33,159 +34,244 @@ __device__ __forceinline__ void sh_basis_grad(float x, float y, float z, int k, 
   }
 }
 
+// Gradients of one Gaussian from its nine 2D gradients: the 11 geometric ones
+// (mean, log-scale, quaternion, opacity logit) and the factors of the 48 SH ones
+// (d L / d sh[k][ch] = Y[k] gcol[ch]).  Returns false for culled Gaussians and
+// padding (all gradients zero).
+struct ChainOut {
+  float geo[11];
+  float Y[16];
+  float gcol[3];
+};
+
+template <bool kReadOnly = true>
+__device__ __forceinline__ bool chain_rule(const float* P, int64_t n, int64_t n_pad, int64_t i, const CamDev& cam,
+                                           const uint32_t* __restrict__ count, const float* __restrict__ g2,
+                                           ChainOut& o) {
+  Geo g;
+  g.visible = false;
+  if (i < n && count[i] > 0u) project_geo<kReadOnly>(P, n_pad, i, cam, g);
+  if (!g.visible) return false;
+  float gq2[9];
+#pragma unroll
+  for (int q = 0; q < 9; ++q) gq2[q] = __ldg(g2 + int64_t(q) * n_pad + i);
+  const float gmx = gq2[0], gmy = gq2[1], gA = gq2[2], gB = gq2[3], gC = gq2[4], go = gq2[5];
+
+  // ---- colour: SH coefficients and the view direction
+  float d[3], len;
+  view_dir(g.mux, g.muy, g.muz, cam, d, &len);
+  float Y[16];
+  sh_basis(d[0], d[1], d[2], Y);
+  float acc[3] = {0.f, 0.f, 0.f};
+  float h[3][3] = {{0.f, 0.f, 0.f}, {0.f, 0.f, 0.f}, {0.f, 0.f, 0.f}};
+#pragma unroll
+  for (int k = 0; k < 16; ++k) {
+    float dY[3];
+    sh_basis_grad(d[0], d[1], d[2], k, dY);
+#pragma unroll
+    for (int ch = 0; ch < 3; ++ch) {
+      const float sh = ldp<kReadOnly>(P, n_pad, 11 + 3 * k + ch, i);
+      acc[ch] = (k == 0) ? __fmul_rn(Y[0], sh) : __fmaf_rn(Y[k], sh, acc[ch]);
+      h[ch][0] += sh * dY[0];
+      h[ch][1] += sh * dY[1];
+      h[ch][2] += sh * dY[2];
+    }
+  }
+  float gcol[3];
+#pragma unroll
+  for (int ch = 0; ch < 3; ++ch) gcol[ch] = (__fadd_rn(acc[ch], 0.5f) < 0.0f) ? 0.0f : gq2[6 + ch];
+#pragma unroll
+  for (int k = 0; k < 16; ++k) o.Y[k] = Y[k];
+#pragma unroll
+  for (int ch = 0; ch < 3; ++ch) o.gcol[ch] = gcol[ch];
+  float gd[3];
+#pragma unroll
+  for (int e = 0; e < 3; ++e) gd[e] = gcol[0] * h[0][e] + gcol[1] * h[1][e] + gcol[2] * h[2][e];
+  const float dotd = gd[0] * d[0] + gd[1] * d[1] + gd[2] * d[2];
+  const float inv_len = 1.0f / len;
+  float gmu[3];
+#pragma unroll
+  for (int e = 0; e < 3; ++e) gmu[e] = (gd[e] - d[e] * dotd) * inv_len;
+
+  // ---- opacity
+  const float op = opacity_of(ldp<kReadOnly>(P, n_pad, 10, i));
+  o.geo[10] = go * op * (1.0f - op);
+
+  // ---- conic (A, B, C) -> 2D covariance (a, b, c)
+  const float a = g.a, b = g.b, c = g.c;
+  const float id2 = 1.0f / (g.det * g.det);
+  const float ga = (-gA * c * c + gB * b * c - gC * b * b) * id2;
+  const float gb = (2.0f * gA * b * c - gB * (a * c + b * b) + 2.0f * gC * a * b) * id2;
+  const float gc = (-gA * b * b + gB * a * b - gC * a * a) * id2;
+
+  // ---- (a, b, c) -> rows of T = J W and Sigma
+  const float Sg[3][3] = {{g.S00, g.S01, g.S02}, {g.S01, g.S11, g.S12}, {g.S02, g.S12, g.S22}};
+  float ST0[3], ST1[3];
+#pragma unroll
+  for (int r = 0; r < 3; ++r) {
+    ST0[r] = Sg[r][0] * g.T0[0] + Sg[r][1] * g.T0[1] + Sg[r][2] * g.T0[2];
+    ST1[r] = Sg[r][0] * g.T1[0] + Sg[r][1] * g.T1[1] + Sg[r][2] * g.T1[2];
+  }
+  float gT0[3], gT1[3];
+#pragma unroll
+  for (int j = 0; j < 3; ++j) {
+    gT0[j] = 2.0f * ga * ST0[j] + gb * ST1[j];
+    gT1[j] = gb * ST0[j] + 2.0f * gc * ST1[j];
+  }
+  // symmetrised dL/dSigma (gS + gS^T)
+  float gSs[3][3];
+#pragma unroll
+  for (int r = 0; r < 3; ++r)
+#pragma unroll
+    for (int q = 0; q < 3; ++q)
+      gSs[r][q] = 2.0f * ga * g.T0[r] * g.T0[q] + gb * (g.T0[r] * g.T1[q] + g.T1[r] * g.T0[q]) +
+                  2.0f * gc * g.T1[r] * g.T1[q];
+
+  // ---- T = J W -> Jacobian entries -> camera-space mean
+  const float* W = cam.R;
+  float gJ00 = 0.f, gJ02 = 0.f, gJ11 = 0.f, gJ12 = 0.f;
+#pragma unroll
+  for (int j = 0; j < 3; ++j) {
+    gJ00 += gT0[j] * W[j];
+    gJ02 += gT0[j] * W[6 + j];
+    gJ11 += gT1[j] * W[3 + j];
+    gJ12 += gT1[j] * W[6 + j];
+  }
+  const float fx = cam.fx, fy = cam.fy, tz = g.tz;
+  const float itz = 1.0f / tz, itz2 = itz * itz;
+  float gtx = 0.f, gty = 0.f, gtz = -(fx * gJ00 + fy * gJ11) * itz2;
+  if (!g.clamp_x) {
+    gtx -= fx * gJ02 * itz2;
+    gtz += 2.0f * fx * g.uc * gJ02 * itz2;
+  } else {
+    gtz += fx * g.uc * gJ02 * itz2;
+  }
+  if (!g.clamp_y) {
+    gty -= fy * gJ12 * itz2;
+    gtz += 2.0f * fy * g.vc * gJ12 * itz2;
+  } else {
+    gtz += fy * g.vc * gJ12 * itz2;
+  }
+  gtx += gmx * fx * itz;
+  gty += gmy * fy * itz;
+  gtz -= (gmx * fx * g.tx + gmy * fy * g.ty) * itz2;
+#pragma unroll
+  for (int e = 0; e < 3; ++e) gmu[e] += W[e] * gtx + W[3 + e] * gty + W[6 + e] * gtz;
+#pragma unroll
+  for (int e = 0; e < 3; ++e) o.geo[e] = gmu[e];
+
+  // ---- Sigma = M M^T -> M -> scale and rotation
+  float gM[9];
+#pragma unroll
+  for (int r = 0; r < 3; ++r)
+#pragma unroll
+    for (int k = 0; k < 3; ++k)
+      gM[3 * r + k] = gSs[r][0] * g.M[k] + gSs[r][1] * g.M[3 + k] + gSs[r][2] * g.M[6 + k];
+#pragma unroll
+  for (int k = 0; k < 3; ++k) {
+    const float gs = gM[k] * g.Rq[k] + gM[3 + k] * g.Rq[3 + k] + gM[6 + k] * g.Rq[6 + k];
+    o.geo[3 + k] = gs * g.s[k];
+  }
+  float gR[9];
+#pragma unroll
+  for (int r = 0; r < 3; ++r)
+#pragma unroll
+    for (int k = 0; k < 3; ++k) gR[3 * r + k] = gM[3 * r + k] * g.s[k];
+  const float w = g.qw, x = g.qx, y = g.qy, z = g.qz;
+  float gq[4];
+  gq[0] = 2.f * (-z * gR[1] + y * gR[2] + z * gR[3] - x * gR[5] - y * gR[6] + x * gR[7]);
+  gq[1] = 2.f * (y * gR[1] + z * gR[2] + y * gR[3] - 2.f * x * gR[4] - w * gR[5] + z * gR[6] + w * gR[7] -
+                 2.f * x * gR[8]);
+  gq[2] = 2.f * (-2.f * y * gR[0] + x * gR[1] + w * gR[2] + x * gR[3] + z * gR[5] - w * gR[6] + z * gR[7] -
+                 2.f * y * gR[8]);
+  gq[3] = 2.f * (-2.f * z * gR[0] - w * gR[1] + x * gR[2] + w * gR[3] - 2.f * z * gR[4] + y * gR[5] + x * gR[6] +
+                 y * gR[7]);
+  const float dq = gq[0] * w + gq[1] * x + gq[2] * y + gq[3] * z;
+  const float iqn = 1.0f / g.qn;
+  o.geo[6] = (gq[0] - w * dq) * iqn;
+  o.geo[7] = (gq[1] - x * dq) * iqn;
+  o.geo[8] = (gq[2] - y * dq) * iqn;
+  o.geo[9] = (gq[3] - z * dq) * iqn;
+  return true;
+}
+
 __global__ void __launch_bounds__(256)
     k_project_bwd(const float* __restrict__ P, int64_t n, int64_t n_pad, CamDev cam, const uint32_t* __restrict__ count,
                   const float* __restrict__ g2, float* __restrict__ G) {
   const int64_t stride = int64_t(gridDim.x) * blockDim.x;
   for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n_pad; i += stride) {
-    Geo g;
-    g.visible = false;
-    if (i < n && count[i] > 0u) project_geo(P, n_pad, i, cam, g);
-    if (!g.visible) {
+    ChainOut o;
+    if (!chain_rule(P, n, n_pad, i, cam, count, g2, o)) {
 #pragma unroll 4
       for (int pl = 0; pl < kPlanes; ++pl) G[int64_t(pl) * n_pad + i] = 0.0f;
       continue;
     }
-    float gq2[9];
 #pragma unroll
-    for (int q = 0; q < 9; ++q) gq2[q] = __ldg(g2 + int64_t(q) * n_pad + i);
-    const float gmx = gq2[0], gmy = gq2[1], gA = gq2[2], gB = gq2[3], gC = gq2[4], go = gq2[5];
-
-    // ---- colour: SH coefficients and the view direction
-    float d[3], len;
-    view_dir(g.mux, g.muy, g.muz, cam, d, &len);
-    float Y[16];
-    sh_basis(d[0], d[1], d[2], Y);
-    float acc[3] = {0.f, 0.f, 0.f};
-    float h[3][3] = {{0.f, 0.f, 0.f}, {0.f, 0.f, 0.f}, {0.f, 0.f, 0.f}};
-#pragma unroll
-    for (int k = 0; k < 16; ++k) {
-      float dY[3];
-      sh_basis_grad(d[0], d[1], d[2], k, dY);
-#pragma unroll
-      for (int ch = 0; ch < 3; ++ch) {
-        const float sh = ldp(P, n_pad, 11 + 3 * k + ch, i);
-        acc[ch] = (k == 0) ? __fmul_rn(Y[0], sh) : __fmaf_rn(Y[k], sh, acc[ch]);
-        h[ch][0] += sh * dY[0];
-        h[ch][1] += sh * dY[1];
-        h[ch][2] += sh * dY[2];
-      }
-    }
-    float gcol[3];
-#pragma unroll
-    for (int ch = 0; ch < 3; ++ch) gcol[ch] = (__fadd_rn(acc[ch], 0.5f) < 0.0f) ? 0.0f : gq2[6 + ch];
+    for (int pl = 0; pl < 11; ++pl) G[int64_t(pl) * n_pad + i] = o.geo[pl];
 #pragma unroll
     for (int k = 0; k < 16; ++k)
 #pragma unroll
-      for (int ch = 0; ch < 3; ++ch) G[int64_t(11 + 3 * k + ch) * n_pad + i] = Y[k] * gcol[ch];
-    float gd[3];
-#pragma unroll
-    for (int e = 0; e < 3; ++e) gd[e] = gcol[0] * h[0][e] + gcol[1] * h[1][e] + gcol[2] * h[2][e];
-    const float dotd = gd[0] * d[0] + gd[1] * d[1] + gd[2] * d[2];
-    const float inv_len = 1.0f / len;
-    float gmu[3];
-#pragma unroll
-    for (int e = 0; e < 3; ++e) gmu[e] = (gd[e] - d[e] * dotd) * inv_len;
+      for (int ch = 0; ch < 3; ++ch) G[int64_t(11 + 3 * k + ch) * n_pad + i] = o.Y[k] * o.gcol[ch];
+  }
+}
 
-    // ---- opacity
-    const float o = opacity_of(ldp(P, n_pad, 10, i));
-    G[int64_t(10) * n_pad + i] = go * o * (1.0f - o);
+// Fused projection backward + Adam: a CTA takes 256 consecutive Gaussians.  Phase 1:
+// each thread derives its Gaussian's gradient factors (11 geometric gradients, the
+// 16 SH basis values and 3 colour factors; zeros for culled Gaussians and padding)
+// into shared memory.  Phase 2: the CTA streams the 59 planes x 256 parameters as
+// float4 (p, m, v read and written once) and applies the Adam element update with
+// gradients rebuilt from shared memory, so the gradient planes are never written or
+// read.  A CTA's Gaussians occupy whole 1 KB lines of every plane (n_pad and the
+// block start are multiples of 256) that no other CTA touches, and phase 1 reads
+// them before phase 2 writes them.
+constexpr int kFusedBlock = 256;
 
-    // ---- conic (A, B, C) -> 2D covariance (a, b, c)
-    const float a = g.a, b = g.b, c = g.c;
-    const float id2 = 1.0f / (g.det * g.det);
-    const float ga = (-gA * c * c + gB * b * c - gC * b * b) * id2;
-    const float gb = (2.0f * gA * b * c - gB * (a * c + b * b) + 2.0f * gC * a * b) * id2;
-    const float gc = (-gA * b * b + gB * a * b - gC * a * a) * id2;
-
-    // ---- (a, b, c) -> rows of T = J W and Sigma
-    const float Sg[3][3] = {{g.S00, g.S01, g.S02}, {g.S01, g.S11, g.S12}, {g.S02, g.S12, g.S22}};
-    float ST0[3], ST1[3];
+__global__ void __launch_bounds__(kFusedBlock, 2)
+    k_project_bwd_adam(float* P, int64_t n, int64_t n_pad, CamDev cam, const uint32_t* __restrict__ count,
+                       const float* __restrict__ g2, float* M, float* V, AdamParams a) {
+  __shared__ float s_geo[11][kFusedBlock];
+  __shared__ float s_Y[16][kFusedBlock];
+  __shared__ float s_gc[3][kFusedBlock];
+  const int tid = threadIdx.x;
+  for (int64_t b0 = int64_t(blockIdx.x) * kFusedBlock; b0 < n_pad; b0 += int64_t(gridDim.x) * kFusedBlock) {
+    {
+      ChainOut o;
+      const bool vis = chain_rule<false>(P, n, n_pad, b0 + tid, cam, count, g2, o);
 #pragma unroll
-    for (int r = 0; r < 3; ++r) {
-      ST0[r] = Sg[r][0] * g.T0[0] + Sg[r][1] * g.T0[1] + Sg[r][2] * g.T0[2];
-      ST1[r] = Sg[r][0] * g.T1[0] + Sg[r][1] * g.T1[1] + Sg[r][2] * g.T1[2];
+      for (int k = 0; k < 11; ++k) s_geo[k][tid] = vis ? o.geo[k] : 0.0f;
+#pragma unroll
+      for (int k = 0; k < 16; ++k) s_Y[k][tid] = vis ? o.Y[k] : 0.0f;
+#pragma unroll
+      for (int k = 0; k < 3; ++k) s_gc[k][tid] = vis ? o.gcol[k] : 0.0f;
     }
-    float gT0[3], gT1[3];
+    __syncthreads();
+    constexpr int kRow4 = kFusedBlock / 4;  // float4 per plane row of the block
+#pragma unroll 4
+    for (int e4 = tid; e4 < kPlanes * kRow4; e4 += kFusedBlock) {
+      const int pl = e4 / kRow4, q = (e4 % kRow4) * 4;
+      const int64_t base = int64_t(pl) * n_pad + b0 + q;
+      float4 pp = *reinterpret_cast<const float4*>(P + base);
+      float4 mm = *reinterpret_cast<const float4*>(M + base);
+      float4 vv = *reinterpret_cast<const float4*>(V + base);
+      float g[4];
+      if (pl < 11) {
 #pragma unroll
-    for (int j = 0; j < 3; ++j) {
-      gT0[j] = 2.0f * ga * ST0[j] + gb * ST1[j];
-      gT1[j] = gb * ST0[j] + 2.0f * gc * ST1[j];
+        for (int k = 0; k < 4; ++k) g[k] = s_geo[pl][q + k];
+      } else {
+        const int kk = (pl - 11) / 3, ch = (pl - 11) % 3;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) g[k] = s_Y[kk][q + k] * s_gc[ch][q + k];
+      }
+      const float step = a.step[pl];
+      adam_elem(pp.x, mm.x, vv.x, g[0], step, a);
+      adam_elem(pp.y, mm.y, vv.y, g[1], step, a);
+      adam_elem(pp.z, mm.z, vv.z, g[2], step, a);
+      adam_elem(pp.w, mm.w, vv.w, g[3], step, a);
+      *reinterpret_cast<float4*>(P + base) = pp;
+      *reinterpret_cast<float4*>(M + base) = mm;
+      *reinterpret_cast<float4*>(V + base) = vv;
     }
-    // symmetrised dL/dSigma (gS + gS^T)
-    float gSs[3][3];
-#pragma unroll
-    for (int r = 0; r < 3; ++r)
-#pragma unroll
-      for (int q = 0; q < 3; ++q)
-        gSs[r][q] = 2.0f * ga * g.T0[r] * g.T0[q] + gb * (g.T0[r] * g.T1[q] + g.T1[r] * g.T0[q]) +
-                    2.0f * gc * g.T1[r] * g.T1[q];
-
-    // ---- T = J W -> Jacobian entries -> camera-space mean
-    const float* W = cam.R;
-    float gJ00 = 0.f, gJ02 = 0.f, gJ11 = 0.f, gJ12 = 0.f;
-#pragma unroll
-    for (int j = 0; j < 3; ++j) {
-      gJ00 += gT0[j] * W[j];
-      gJ02 += gT0[j] * W[6 + j];
-      gJ11 += gT1[j] * W[3 + j];
-      gJ12 += gT1[j] * W[6 + j];
-    }
-    const float fx = cam.fx, fy = cam.fy, tz = g.tz;
-    const float itz = 1.0f / tz, itz2 = itz * itz;
-    float gtx = 0.f, gty = 0.f, gtz = -(fx * gJ00 + fy * gJ11) * itz2;
-    if (!g.clamp_x) {
-      gtx -= fx * gJ02 * itz2;
-      gtz += 2.0f * fx * g.uc * gJ02 * itz2;
-    } else {
-      gtz += fx * g.uc * gJ02 * itz2;
-    }
-    if (!g.clamp_y) {
-      gty -= fy * gJ12 * itz2;
-      gtz += 2.0f * fy * g.vc * gJ12 * itz2;
-    } else {
-      gtz += fy * g.vc * gJ12 * itz2;
-    }
-    gtx += gmx * fx * itz;
-    gty += gmy * fy * itz;
-    gtz -= (gmx * fx * g.tx + gmy * fy * g.ty) * itz2;
-#pragma unroll
-    for (int e = 0; e < 3; ++e) gmu[e] += W[e] * gtx + W[3 + e] * gty + W[6 + e] * gtz;
-#pragma unroll
-    for (int e = 0; e < 3; ++e) G[int64_t(e) * n_pad + i] = gmu[e];
-
-    // ---- Sigma = M M^T -> M -> scale and rotation
-    float gM[9];
-#pragma unroll
-    for (int r = 0; r < 3; ++r)
-#pragma unroll
-      for (int k = 0; k < 3; ++k)
-        gM[3 * r + k] = gSs[r][0] * g.M[k] + gSs[r][1] * g.M[3 + k] + gSs[r][2] * g.M[6 + k];
-#pragma unroll
-    for (int k = 0; k < 3; ++k) {
-      const float gs = gM[k] * g.Rq[k] + gM[3 + k] * g.Rq[3 + k] + gM[6 + k] * g.Rq[6 + k];
-      G[int64_t(3 + k) * n_pad + i] = gs * g.s[k];
-    }
-    float gR[9];
-#pragma unroll
-    for (int r = 0; r < 3; ++r)
-#pragma unroll
-      for (int k = 0; k < 3; ++k) gR[3 * r + k] = gM[3 * r + k] * g.s[k];
-    const float w = g.qw, x = g.qx, y = g.qy, z = g.qz;
-    float gq[4];
-    gq[0] = 2.f * (-z * gR[1] + y * gR[2] + z * gR[3] - x * gR[5] - y * gR[6] + x * gR[7]);
-    gq[1] = 2.f * (y * gR[1] + z * gR[2] + y * gR[3] - 2.f * x * gR[4] - w * gR[5] + z * gR[6] + w * gR[7] -
-                   2.f * x * gR[8]);
-    gq[2] = 2.f * (-2.f * y * gR[0] + x * gR[1] + w * gR[2] + x * gR[3] + z * gR[5] - w * gR[6] + z * gR[7] -
-                   2.f * y * gR[8]);
-    gq[3] = 2.f * (-2.f * z * gR[0] - w * gR[1] + x * gR[2] + w * gR[3] - 2.f * z * gR[4] + y * gR[5] + x * gR[6] +
-                   y * gR[7]);
-    const float dq = gq[0] * w + gq[1] * x + gq[2] * y + gq[3] * z;
-    const float iqn = 1.0f / g.qn;
-    G[int64_t(6) * n_pad + i] = (gq[0] - w * dq) * iqn;
-    G[int64_t(7) * n_pad + i] = (gq[1] - x * dq) * iqn;
-    G[int64_t(8) * n_pad + i] = (gq[2] - y * dq) * iqn;
-    G[int64_t(9) * n_pad + i] = (gq[3] - z * dq) * iqn;
+    __syncthreads();
   }
 }
 
@@ -199,5 +285,22 @@ extern "C" gs_status gs_project_bwd(gs_dims dims, const float* params, const gs_
   if (!aligned(params, 16) || !aligned(grads, 16) || !aligned(grad2d, 16)) return GS_ERR_INVALID_ARG;
   const int blocks = grid_for(dims.n_pad, 256, kSmCount * 64);
   k_project_bwd<<<blocks, 256, 0, stream>>>(params, dims.n, dims.n_pad, cam_dev(*cam), proj->count, grad2d, grads);
+  return launch_status();
+}
+
+extern "C" gs_status gs_project_bwd_adam(gs_dims dims, float* params, const gs_camera* cam, const gs_proj* proj,
+                                         const float* grad2d, float* m, float* v, const float lr_plane[GS_N_PLANES],
+                                         double beta1, double beta2, double eps, int64_t t, uint32_t* dev_status,
+                                         cudaStream_t stream) {
+  using namespace gs;
+  if (!dims_ok(dims) || !camera_ok(cam) || !params || !proj || !proj->count || !grad2d || !m || !v || !lr_plane ||
+      !dev_status)
+    return GS_ERR_INVALID_ARG;
+  if (!aligned(params, 16) || !aligned(grad2d, 16) || !aligned(m, 16) || !aligned(v, 16)) return GS_ERR_INVALID_ARG;
+  AdamParams a;
+  if (!make_adam_params(lr_plane, beta1, beta2, eps, t, a)) return GS_ERR_INVALID_ARG;
+  const int blocks = grid_for(dims.n_pad, kFusedBlock, kSmCount * 64);
+  k_project_bwd_adam<<<blocks, kFusedBlock, 0, stream>>>(params, dims.n, dims.n_pad, cam_dev(*cam), proj->count, grad2d, m,
+                                                 v, a);
   return launch_status();
 }

@@ -75,22 +75,26 @@ struct Geo {
   int tx0, ty0, tx1, ty1;
 };
 
-__device__ __forceinline__ float ldp(const float* __restrict__ P, int64_t n_pad, int plane, int64_t i) {
-  return __ldg(P + int64_t(plane) * n_pad + i);
+// Parameter load.  kReadOnly uses the read-only data path; kernels that also write
+// the parameter planes (the fused projection backward + Adam) use plain loads.
+template <bool kReadOnly = true>
+__device__ __forceinline__ float ldp(const float* P, int64_t n_pad, int plane, int64_t i) {
+  if (kReadOnly) return __ldg(P + int64_t(plane) * n_pad + i);
+  return P[int64_t(plane) * n_pad + i];
 }
 
 // Geometry: everything but opacity and colour.  Sets visible = false when the
 // Gaussian is culled (behind the near plane, degenerate quaternion, det <= 0,
 // empty tile rect) and nonfinite when a geometric parameter or derived value is
 // NaN/Inf.
-__device__ __forceinline__ void project_geo(const float* __restrict__ P, int64_t n_pad, int64_t i,
-                                            const CamDev& cam, Geo& g) {
+template <bool kReadOnly = true>
+__device__ __forceinline__ void project_geo(const float* P, int64_t n_pad, int64_t i, const CamDev& cam, Geo& g) {
   g.visible = false;
   g.nonfinite = false;
   g.clamp_x = g.clamp_y = false;
   float pv[11];
 #pragma unroll
-  for (int pl = 0; pl < 11; ++pl) pv[pl] = ldp(P, n_pad, pl, i);
+  for (int pl = 0; pl < 11; ++pl) pv[pl] = ldp<kReadOnly>(P, n_pad, pl, i);
   bool fin = true;
 #pragma unroll
   for (int pl = 0; pl < 11; ++pl) fin = fin && isfinite(pv[pl]);

@@ -10,13 +10,13 @@ from __future__ import annotations
 
 import numpy as np
 
-from . import (BinBuffers, ProjBuffers, N_GRAD2D, adam_step, bin_sort, project, project_bwd, render_bwd, render_fwd,
-               status_str)
+from . import (BinBuffers, ProjBuffers, N_GRAD2D, adam_step, bin_sort, project, project_bwd, project_bwd_adam,
+               render_bwd, render_fwd, status_str)
 
 
 class Trainer:
     def __init__(self, params, n: int, width: int, height: int, capacity: int, lr_plane, betas=(0.9, 0.999),
-                 eps: float = 1e-15, bg=(0.0, 0.0, 0.0), device="cuda"):
+                 eps: float = 1e-15, bg=(0.0, 0.0, 0.0), device="cuda", fused: bool = True):
         import torch
         if isinstance(params, np.ndarray):
             params = torch.from_numpy(np.ascontiguousarray(params, np.float32))
@@ -39,6 +39,7 @@ class Trainer:
         self.beta1, self.beta2 = float(betas[0]), float(betas[1])
         self.eps = float(eps)
         self.bg = tuple(float(x) for x in bg)
+        self.fused = bool(fused)
         self.t = 0
 
     # the stages ------------------------------------------------------------------
@@ -58,10 +59,19 @@ class Trainer:
                   self.t, stream)
 
     def step(self, cam: dict, target, stream=None) -> None:
-        """One optimisation step for one view: forward, backward, Adam."""
+        """One optimisation step for one view: forward, backward, Adam.  With
+        ``fused`` the projection backward and Adam run as one call and the gradient
+        planes (``grads``) are not written."""
         self.forward(cam, stream)
-        self.backward(cam, target, stream)
-        self.optimizer_step(stream)
+        if not self.fused:
+            self.backward(cam, target, stream)
+            self.optimizer_step(stream)
+            return
+        render_bwd(self.n, self.n_pad, cam, self.bins, self.bg, self.image, target, self.T_final, self.n_contrib,
+                   self.grad2d, self.loss, self.status, stream)
+        self.t += 1
+        project_bwd_adam(self.n, self.params, cam, self.proj, self.grad2d, self.m, self.v, self.lr_plane, self.beta1,
+                         self.beta2, self.eps, self.t, self.status, stream)
 
     # host-side reads (synchronise) -----------------------------------------------
     def n_isect(self) -> int:

@@ -11,6 +11,7 @@
  *   gs_render_bwd   L1 loss gradient and the reverse-order compositing backward
  *   gs_project_bwd  chain rule from the 2D gradients to the 59 parameters
  *   gs_adam_step    fused Adam update over every parameter plane
+ *   (gs_project_bwd_adam: the last two in one pass)
  *
  * The method is the one "Toward Distributed 3D Gaussian Splatting for
  * High-Resolution Isosurface Visualization" (section III) trains and "Scaling 3D
@@ -244,6 +245,21 @@ gs_status gs_project_bwd(gs_dims dims, const float* params, const gs_camera* cam
 gs_status gs_adam_step(gs_dims dims, float* params, const float* grads, float* m, float* v,
                        const float lr_plane[GS_N_PLANES], double beta1, double beta2, double eps, int64_t t,
                        cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * gs_project_bwd_adam -- gs_project_bwd followed by gs_adam_step in one pass, without
+ * materialising the 59 gradient planes.  Same arithmetic as the two calls (each
+ * thread derives its Gaussian's gradients in registers and applies the Adam element
+ * update of gs_adam_step to all 59 of its parameters, culled and padding ones with
+ * gradient 0), so it moves 1456 instead of 2164 bytes per Gaussian.  Use the two
+ * separate calls when the gradients themselves are wanted.
+ *   params  59 x n_pad (read, then updated in place); proj, grad2d as for
+ *   gs_project_bwd; m, v, lr_plane, beta1, beta2, eps, t as for gs_adam_step.
+ * Errors: the union of gs_project_bwd's and gs_adam_step's. */
+gs_status gs_project_bwd_adam(gs_dims dims, float* params, const gs_camera* cam, const gs_proj* proj,
+                              const float* grad2d, float* m, float* v, const float lr_plane[GS_N_PLANES],
+                              double beta1, double beta2, double eps, int64_t t, uint32_t* dev_status,
+                              cudaStream_t stream);
 
 /* ---------------------------------------------------------------------------
  * gs_bin_sort_noalloc -- gs_bin_sort for callers that must not allocate device

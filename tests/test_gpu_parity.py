@@ -251,22 +251,25 @@ def test_adam_parity():
     assert np.all(np.abs(vd.cpu().numpy() - vr) <= 1e-6 * (np.abs(0.999 * v64) + np.abs(0.001 * g64 * g64)) + 1e-30)
 
 
-def test_whole_step_end_to_end(case):
+@pytest.mark.parametrize("fused", [False, True], ids=["separate", "fused"])
+def test_whole_step_end_to_end(case, fused):
     """The whole chain from the same parameters: every stage against the oracle's
     chain; Adam is compared where the gradient is not within its tolerance of 0
-    (at t = 1 an update is lr sign(g), so a near-zero g has no defined sign)."""
+    (at t = 1 an update is lr sign(g), so a near-zero g has no defined sign).
+    ``fused`` runs the projection backward and Adam as gs_project_bwd_adam."""
     P, cam, n = case["P"], case["cam"], case["n"]
     W, H = cam["width"], cam["height"]
     target = _target_for(case)
     z = np.zeros((59, P.shape[1]))
     ref = oracle.step(P, n, cam, target, z, z, 1, gi.lr_planes())
-    tr = gs.Trainer(P, n, W, H, capacity=1 << 20, lr_plane=gi.lr_planes())
+    tr = gs.Trainer(P, n, W, H, capacity=1 << 20, lr_plane=gi.lr_planes(), fused=fused)
     tr.step(cam, torch.from_numpy(target).to(DEV))
     torch.cuda.synchronize()
     assert tr.check_status() == 0
     _grad_close(tr.grad2d.cpu().numpy()[:, :n], ref["render"]["grad2d"], what="grad2d")
     gref = ref["grads"][:, :n]
-    _grad_close(tr.grads.cpu().numpy()[:, :n], gref, rtol=2e-4, floor=2e-6, what="param grads")
+    if not fused:
+        _grad_close(tr.grads.cpu().numpy()[:, :n], gref, rtol=2e-4, floor=2e-6, what="param grads")
     p = tr.params.cpu().numpy()[:, :n].astype(np.float64)
     pr = ref["params"][:, :n]
     # the sign of g (hence the t = 1 update) is certain where |g| exceeds the gradient
@@ -278,6 +281,33 @@ def test_whole_step_end_to_end(case):
     assert defined.mean() > 0.2
     bad = (np.abs(p - pr) > 1e-5 * np.abs(pr) + 1e-7) & defined
     assert not bad.any(), bad.sum()
+    # padding is never moved
+    assert not tr.params[:, n:].any()
+
+
+def test_fused_project_bwd_adam_equals_separate_calls(case):
+    """gs_project_bwd_adam applies the same fp32 arithmetic as gs_project_bwd then
+    gs_adam_step: parameters and moments agree to an ulp or so, over three steps
+    with nonzero moments (seeded 2D gradients as input)."""
+    P, cam, n = case["P"], case["cam"], case["n"]
+    n_pad = P.shape[1]
+    W, H = cam["width"], cam["height"]
+    lr = gi.lr_planes()
+    a = gs.Trainer(P, n, W, H, capacity=1 << 20, lr_plane=lr, fused=False)
+    b = gs.Trainer(P, n, W, H, capacity=1 << 20, lr_plane=lr, fused=True)
+    st = _status()
+    for t in range(1, 4):
+        g2 = torch.from_numpy(gi.random_grad2d(100 + t, n, n_pad)).to(DEV)
+        gs.project(n, a.params, cam, a.proj, st)
+        gs.project_bwd(n, a.params, cam, a.proj, g2, a.grads, st)
+        gs.adam_step(n, a.params, a.grads, a.m, a.v, lr, 0.9, 0.999, 1e-15, t)
+        gs.project(n, b.params, cam, b.proj, st)
+        gs.project_bwd_adam(n, b.params, cam, b.proj, g2, b.m, b.v, lr, 0.9, 0.999, 1e-15, t, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    for x, y in ((a.params, b.params), (a.m, b.m), (a.v, b.v)):
+        x, y = x.cpu().numpy().astype(np.float64), y.cpu().numpy().astype(np.float64)
+        assert np.all(np.abs(x - y) <= 4e-7 * np.abs(x) + 1e-30)
 
 
 # ----------------------------------------------------------------------------- edge cases
@@ -288,16 +318,22 @@ def test_empty_scene_all_culled():
     P = gi.scene_for(cfg, n=500)
     P[2, :500] = 50.0          # far behind the camera at z = +3 looking down -z
     cam = gi.camera((0.0, 0.0, 3.0), 64, 48)
-    tr = gs.Trainer(P, 500, 64, 48, capacity=1024, lr_plane=gi.lr_planes(), bg=(0.2, 0.4, 0.6))
     tgt = torch.zeros((3, 48, 64), device=DEV)
-    tr.step(cam, tgt)
-    torch.cuda.synchronize()
-    assert tr.check_status() == 0
-    assert tr.n_isect() == 0
-    img = tr.image.cpu().numpy()
-    np.testing.assert_array_equal(img[0], np.float32(0.2))
-    np.testing.assert_array_equal(img[2], np.float32(0.6))
-    assert not tr.grads.any()
+    for fused in (False, True):
+        tr = gs.Trainer(P, 500, 64, 48, capacity=1024, lr_plane=gi.lr_planes(), bg=(0.2, 0.4, 0.6), fused=fused)
+        p0 = tr.params.clone()
+        tr.step(cam, tgt)
+        torch.cuda.synchronize()
+        assert tr.check_status() == 0
+        assert tr.n_isect() == 0
+        img = tr.image.cpu().numpy()
+        np.testing.assert_array_equal(img[0], np.float32(0.2))
+        np.testing.assert_array_equal(img[2], np.float32(0.6))
+        if not fused:
+            assert not tr.grads.any()
+        # zero gradients: zero moments, parameters unchanged
+        assert not tr.m.any() and not tr.v.any()
+        assert torch.equal(tr.params, p0)
 
 
 def test_capacity_overflow_is_flagged_not_written():
