@@ -89,6 +89,8 @@ def _load():
             for name in ("or_render_f32", "or_render_f64"):
                 getattr(lib, name).argtypes = [i64, P, P, ctypes.c_int, ctypes.c_int, P, P, P, P, P, P, P]
             lib.or_project_bwd.argtypes = [P, i64, i64, ctypes.POINTER(OrCamera), ctypes.c_int, P, P]
+            lib.or_ssim.argtypes = [ctypes.c_int, ctypes.c_int, P, P, ctypes.c_double, P]
+            lib.or_ssim.restype = ctypes.c_double
             lib.or_adam.argtypes = [P, P, P, P, ctypes.c_int, i64, P, ctypes.c_double, ctypes.c_double,
                                     ctypes.c_double, i64]
             _lib = lib
@@ -206,6 +208,19 @@ def project_bwd(params: np.ndarray, n: int, cam: dict, grad2d: np.ndarray, prec:
     _load().or_project_bwd(_ptr(params), n, params.shape[1], ctypes.byref(cam_c), int(prec),
                            _ptr(g2), _ptr(grads))
     return grads
+
+
+def ssim(x, y, lam: float = 1.0):
+    """Mean SSIM of x against y (3 x H x W; 11x11 Gaussian window, sigma 1.5, C1 =
+    0.01^2, C2 = 0.03^2, zero padding) and the gradient of lam (1 - SSIM) with
+    respect to x, in fp64."""
+    x = _c(x, np.float64)
+    y = _c(y, np.float64)
+    C, H, W = x.shape
+    assert C == 3 and y.shape == x.shape
+    g = np.zeros_like(x)
+    val = _load().or_ssim(W, H, _ptr(x), _ptr(y), float(lam), _ptr(g))
+    return float(val), g
 
 
 def adam(p, g, m, v, lr_plane, beta1: float, beta2: float, eps: float, t: int):

@@ -811,6 +811,103 @@ void project_bwd_one(const float* params, int64_t n_pad, int64_t i, const OrCame
   for (int e = 0; e < 3; ++e) out[e] = gmu[e];
 }
 
+// --------------------------------------------------------------------------------
+// SSIM (Wang et al. 2004) with an 11x11 Gaussian window (sigma 1.5), C1 = 0.01^2,
+// C2 = 0.03^2, zero padding outside the image, averaged over all pixels and
+// channels: the D-SSIM term of the objective ("Scaling 3D Gaussian Splatting with
+// Distributed Compute", objective paragraph: a weighted L1 plus D-SSIM; the formula
+// was lost from the page, read here as (1 - lambda) L1 + lambda (1 - SSIM)).
+// Everything in fp64 by direct summation of the 121-tap window.
+struct SsimOut {
+  double ssim;
+};
+
+void ssim_window(double w[11][11]) {
+  double g[11], sum = 0.0;
+  for (int k = 0; k < 11; ++k) {
+    const double d = double(k - 5);
+    g[k] = std::exp(-d * d / (2.0 * 1.5 * 1.5));
+    sum += g[k];
+  }
+  for (int a = 0; a < 11; ++a)
+    for (int b = 0; b < 11; ++b) w[a][b] = (g[a] / sum) * (g[b] / sum);
+}
+
+// L = lambda (1 - mean SSIM); returns mean SSIM and dL/dx (3 x H x W).
+double ssim_and_grad(int W, int H, const double* x, const double* y, double lambda, double* dLdx) {
+  const double C1 = 0.01 * 0.01, C2 = 0.03 * 0.03;
+  double w[11][11];
+  ssim_window(w);
+  const int64_t P = int64_t(W) * H;
+  std::vector<double> A(3 * P), B(3 * P), C(3 * P), S(3 * P);
+  // local statistics and the partial derivatives of S at every pixel
+  parallel_for(3 * int64_t(H), [&](int64_t r0, int64_t r1) {
+    for (int64_t cr = r0; cr < r1; ++cr) {
+      const int c = int(cr / H), i = int(cr % H);
+      const double* xc = x + c * P;
+      const double* yc = y + c * P;
+      for (int j = 0; j < W; ++j) {
+        double mx = 0, my = 0, exx = 0, eyy = 0, exy = 0;
+        for (int a = -5; a <= 5; ++a) {
+          const int ii = i + a;
+          if (ii < 0 || ii >= H) continue;
+          for (int b = -5; b <= 5; ++b) {
+            const int jj = j + b;
+            if (jj < 0 || jj >= W) continue;
+            const double g = w[a + 5][b + 5];
+            const double xv = xc[int64_t(ii) * W + jj], yv = yc[int64_t(ii) * W + jj];
+            mx += g * xv;
+            my += g * yv;
+            exx += g * xv * xv;
+            eyy += g * yv * yv;
+            exy += g * xv * yv;
+          }
+        }
+        const double sxx = exx - mx * mx, syy = eyy - my * my, sxy = exy - mx * my;
+        const double n1 = 2 * mx * my + C1, n2 = 2 * sxy + C2;
+        const double d1 = mx * mx + my * my + C1, d2 = sxx + syy + C2;
+        const double s = n1 * n2 / (d1 * d2);
+        const double dS_dmx = 2 * my * n2 / (d1 * d2) - s * 2 * mx / d1;
+        const double dS_dsxx = -s / d2;
+        const double dS_dsxy = 2 * n1 / (d1 * d2);
+        const double dLdS = -lambda / double(3 * P);
+        const int64_t q = c * P + int64_t(i) * W + j;
+        S[q] = s;
+        A[q] = dLdS * (dS_dmx - 2 * mx * dS_dsxx - my * dS_dsxy);
+        B[q] = dLdS * dS_dsxx;
+        C[q] = dLdS * dS_dsxy;
+      }
+    }
+  });
+  // dL/dx(p) = sum_q G(q - p) [A(q) + 2 x(p) B(q) + y(p) C(q)], q over the image
+  parallel_for(3 * int64_t(H), [&](int64_t r0, int64_t r1) {
+    for (int64_t cr = r0; cr < r1; ++cr) {
+      const int c = int(cr / H), i = int(cr % H);
+      for (int j = 0; j < W; ++j) {
+        double ga = 0, gb = 0, gc = 0;
+        for (int a = -5; a <= 5; ++a) {
+          const int ii = i + a;
+          if (ii < 0 || ii >= H) continue;
+          for (int b = -5; b <= 5; ++b) {
+            const int jj = j + b;
+            if (jj < 0 || jj >= W) continue;
+            const double g = w[a + 5][b + 5];
+            const int64_t q = c * P + int64_t(ii) * W + jj;
+            ga += g * A[q];
+            gb += g * B[q];
+            gc += g * C[q];
+          }
+        }
+        const int64_t p = c * P + int64_t(i) * W + j;
+        dLdx[p] = ga + 2 * x[p] * gb + y[p] * gc;
+      }
+    }
+  });
+  double sum = 0;
+  for (double v : S) sum += v;
+  return sum / double(3 * P);
+}
+
 }  // namespace
 
 // ==================================================================================
@@ -921,6 +1018,12 @@ void or_project_bwd(const float* params, int64_t n, int64_t n_pad, const OrCamer
       for (int k = 0; k < kPlanes; ++k) grads[int64_t(k) * n + i] = out[k];
     }
   });
+}
+
+// SSIM of image x against y (3 x H x W each, fp64) and the gradient of
+// lambda (1 - SSIM) with respect to x; returns the mean SSIM.
+double or_ssim(int W, int H, const double* x, const double* y, double lambda, double* dLdx) {
+  return ssim_and_grad(W, H, x, y, lambda, dLdx);
 }
 
 // Adam, textbook form in fp64: m = b1 m + (1-b1) g; v = b2 v + (1-b2) g^2;

@@ -521,3 +521,63 @@ def test_adam_first_step_is_signed_lr():
     for b1, b2 in ((0.9, 0.999), (0.0, 0.5)):
         p, _, _ = oracle.adam(p0, g, np.zeros_like(p0), np.zeros_like(p0), lr, b1, b2, 1e-15, 1)
         np.testing.assert_allclose(p, p0 - lr[:, None] * np.sign(g), rtol=1e-12)
+
+
+# ----------------------------------------------------------------------------- SSIM
+
+def _ssim_stats_scipy(x, y):
+    """Local means and (co)variances from scipy: 11x11 window from scipy's Gaussian
+    (std 1.5, normalised), zero padding outside the image."""
+    nd = pytest.importorskip("scipy.ndimage")
+    windows = pytest.importorskip("scipy.signal.windows")
+    g = windows.gaussian(11, std=1.5)
+    w = np.outer(g, g)
+    w /= w.sum()
+    f = lambda a: nd.correlate(a, w, mode="constant", cval=0.0)
+    mx, my = f(x), f(y)
+    return mx, my, f(x * x) - mx * mx, f(y * y) - my * my, f(x * y) - mx * my
+
+
+def test_ssim_identity_and_symmetry():
+    """SSIM(x, x) = 1 with zero gradient (its maximum); SSIM(x, y) = SSIM(y, x)."""
+    rng = np.random.default_rng(0)
+    x = rng.uniform(0, 1, (3, 30, 26))
+    y = rng.uniform(0, 1, (3, 30, 26))
+    s, g = oracle.ssim(x, x)
+    assert abs(s - 1.0) < 1e-14 and np.abs(g).max() < 1e-14
+    assert abs(oracle.ssim(x, y)[0] - oracle.ssim(y, x)[0]) < 1e-14
+
+
+def test_ssim_reduces_to_library_statistics():
+    """With y = 0 the index is C1/(mu_x^2 + C1) * C2/(s_xx + C2); with y = a x it is
+    (2a mu^2 + C1)/((1+a^2) mu^2 + C1) * (2a s + C2)/((1+a^2) s + C2); local statistics
+    from scipy's correlate with zero padding."""
+    rng = np.random.default_rng(1)
+    x = rng.uniform(0, 1, (3, 33, 29))
+    C1, C2 = 0.01 ** 2, 0.03 ** 2
+    for a in (0.0, 0.6, 1.7):
+        y = a * x
+        ref = []
+        for c in range(3):
+            mx, _, sxx, _, _ = _ssim_stats_scipy(x[c], y[c])
+            ref.append((2 * a * mx * mx + C1) / ((1 + a * a) * mx * mx + C1)
+                       * (2 * a * sxx + C2) / ((1 + a * a) * sxx + C2))
+        assert abs(oracle.ssim(x, y)[0] - np.mean(ref)) < 1e-12, a
+
+
+def test_ssim_gradient_matches_finite_differences():
+    """d/dx of lambda (1 - SSIM) against central differences at every pixel of a small
+    image (borders included)."""
+    rng = np.random.default_rng(2)
+    x = rng.uniform(0.1, 0.9, (3, 14, 12))
+    y = np.clip(x + rng.normal(0, 0.2, x.shape), 0, 1)
+    lam = 0.2
+    _, g = oracle.ssim(x, y, lam)
+    h = 1e-6
+    fd = np.zeros_like(x)
+    for idx in np.ndindex(x.shape):
+        xp, xm = x.copy(), x.copy()
+        xp[idx] += h
+        xm[idx] -= h
+        fd[idx] = lam * ((1 - oracle.ssim(xp, y)[0]) - (1 - oracle.ssim(xm, y)[0])) / (2 * h)
+    np.testing.assert_allclose(g, fd, rtol=1e-5, atol=1e-9 * np.abs(g).max())
