@@ -87,7 +87,8 @@ def _load():
             lib.or_tile_lists_f32.argtypes = [i64, P, P, ctypes.c_int, ctypes.c_int, P, P, P, i64]
             lib.or_tile_lists_f32.restype = i64
             for name in ("or_render_f32", "or_render_f64"):
-                getattr(lib, name).argtypes = [i64, P, P, ctypes.c_int, ctypes.c_int, P, P, P, P, P, P, P]
+                getattr(lib, name).argtypes = [i64, P, P, ctypes.c_int, ctypes.c_int, P, P, P, P, P, P, P,
+                                               ctypes.c_double, P]
             lib.or_project_bwd.argtypes = [P, i64, i64, ctypes.POINTER(OrCamera), ctypes.c_int, P, P]
             lib.or_ssim.argtypes = [ctypes.c_int, ctypes.c_int, P, P, ctypes.c_double, P]
             lib.or_ssim.restype = ctypes.c_double
@@ -169,11 +170,13 @@ def tile_lists(proj: dict, width: int, height: int, cap: int | None = None) -> d
     return {"K": int(K), "keys": keys[:min(K, cap)], "ids": ids[:min(K, cap)], "ranges": ranges}
 
 
-def render(proj: dict, width: int, height: int, bg=(0.0, 0.0, 0.0), target=None, prec: int = 32) -> dict:
+def render(proj: dict, width: int, height: int, bg=(0.0, 0.0, 0.0), target=None, prec: int = 32,
+           l1_weight: float = 1.0, dLdC_extra=None) -> dict:
     """Front-to-back compositing of every pixel over its tile's list; with a
-    target, also the L1 loss (mean over 3 P values) and the per-Gaussian 2D
-    gradients (9 x n fp64: d mx, d my, d A, d B, d C, d o, d r, d g, d b) from the
-    suffix-sum backward."""
+    target, also the loss l1_weight * mean |C - C*| (over 3 P values) and the
+    per-Gaussian 2D gradients (9 x n fp64: d mx, d my, d A, d B, d C, d o, d r, d g,
+    d b) from the suffix-sum backward, with dLdC_extra (3 x H x W fp64) added to the
+    loss gradient if given."""
     n = proj["proj16"].shape[0]
     dt = np.float32 if prec == 32 else np.float64
     P = width * height
@@ -188,8 +191,9 @@ def render(proj: dict, width: int, height: int, bg=(0.0, 0.0, 0.0), target=None,
         grad2d = np.zeros((9, n), np.float64)
         loss = np.zeros(1, np.float64)
     f = _load().or_render_f32 if prec == 32 else _load().or_render_f64
+    extra = None if dLdC_extra is None else _c(dLdC_extra, np.float64).reshape(3, height, width)
     f(n, _ptr(_c(proj["proj16"], dt)), _ptr(proj["iproj6"]), width, height, _ptr(bg_a), _ptr(tgt),
-      _ptr(image), _ptr(T_final), _ptr(n_contrib), _ptr(grad2d), _ptr(loss))
+      _ptr(image), _ptr(T_final), _ptr(n_contrib), _ptr(grad2d), _ptr(loss), float(l1_weight), _ptr(extra))
     out = {"image": image, "T_final": T_final, "n_contrib": n_contrib}
     if target is not None:
         out["grad2d"] = grad2d
@@ -236,11 +240,19 @@ def adam(p, g, m, v, lr_plane, beta1: float, beta2: float, eps: float, t: int):
 
 
 def step(params, n: int, cam: dict, target, m, v, t: int, lr_plane, beta1=0.9, beta2=0.999, eps=1e-15,
-         bg=(0.0, 0.0, 0.0)) -> dict:
-    """One whole optimisation step for one view, stage by stage."""
+         bg=(0.0, 0.0, 0.0), dssim: float = 0.0) -> dict:
+    """One whole optimisation step for one view, stage by stage; with dssim = lambda
+    > 0 the loss is (1 - lambda) L1 + lambda (1 - SSIM)."""
     pr = project(params, n, cam, 32)
     W, H = int(cam["width"]), int(cam["height"])
-    rd = render(pr, W, H, bg, target, 32)
+    if dssim > 0.0:
+        img = render(pr, W, H, bg, None, 32)["image"]
+        s_val, extra = ssim(img.astype(np.float64), np.asarray(target, np.float64), dssim)
+        rd = render(pr, W, H, bg, target, 32, l1_weight=1.0 - dssim, dLdC_extra=extra)
+        rd["ssim"] = s_val
+        rd["loss"] += dssim * (1.0 - s_val)
+    else:
+        rd = render(pr, W, H, bg, target, 32)
     grads = project_bwd(params, n, cam, rd["grad2d"], 32)
     n_pad = params.shape[1]
     gfull = np.zeros((N_PLANES, n_pad), np.float64)

@@ -583,10 +583,12 @@ std::vector<Splat<S>> splats_from(int64_t n, const S* proj16, const int32_t* ipr
 }
 
 // Forward (and optionally backward) over all tiles.
+// The loss is l1_weight * mean |C - C*|; its gradient dL/dC = l1_weight sign(C - C*)
+// / (3P) plus dLdC_extra (another loss term's gradient, e.g. D-SSIM), if given.
 template <class S>
 void render_all(int64_t n, const S* proj16, const int32_t* iproj6, int W, int H, const S* bg_in,
                 const S* target, S* image, S* T_final, uint32_t* n_contrib, double* grad2d,
-                double* loss) {
+                double* loss, double l1_weight = 1.0, const double* dLdC_extra = nullptr) {
   const int TX = (W + kTile - 1) / kTile, TY = (H + kTile - 1) / kTile;
   std::vector<Splat<S>> sp = splats_from<S>(n, proj16, iproj6);
   auto lists = build_tile_lists<S>(sp, TX, TY);
@@ -623,7 +625,7 @@ void render_all(int64_t n, const S* proj16, const int32_t* iproj6, int W, int H,
               const double sg = (out[ch] > target[ch * P + pix]) ? 1.0 : ((out[ch] < target[ch * P + pix]) ? -1.0 : 0.0);
               lsum += std::fabs(double(out[ch]) - double(target[ch * P + pix]));
               (void)r;
-              dLdC[ch] = sg * inv3P;
+              dLdC[ch] = l1_weight * sg * inv3P + (dLdC_extra ? dLdC_extra[ch * P + pix] : 0.0);
             }
             render_pixel_bwd<S>(sp, L, double(xx) + 0.5, double(yy) + 0.5, bgd, cs, dLdC,
                                 entry_grads[size_t(t)].data());
@@ -644,7 +646,7 @@ void render_all(int64_t n, const S* proj16, const int32_t* iproj6, int W, int H,
     }
     double l = 0.0;
     for (double v : tile_loss) l += v;
-    if (loss) *loss = l * inv3P;
+    if (loss) *loss = l1_weight * l * inv3P;
   }
 }
 
@@ -994,13 +996,16 @@ int64_t or_tile_lists_f32(int64_t n, const float* proj16, const int32_t* iproj6,
 // grad2d is 9 x n: (d mx, d my, d A, d B, d C, d o, d r, d g, d b).
 void or_render_f32(int64_t n, const float* proj16, const int32_t* iproj6, int W, int H, const float* bg,
                    const float* target, float* image, float* T_final, uint32_t* n_contrib,
-                   double* grad2d, double* loss) {
-  render_all<float>(n, proj16, iproj6, W, H, bg, target, image, T_final, n_contrib, grad2d, loss);
+                   double* grad2d, double* loss, double l1_weight, const double* dLdC_extra) {
+  render_all<float>(n, proj16, iproj6, W, H, bg, target, image, T_final, n_contrib, grad2d, loss, l1_weight,
+                    dLdC_extra);
 }
 void or_render_f64(int64_t n, const double* proj16, const int32_t* iproj6, int W, int H,
                    const double* bg, const double* target, double* image, double* T_final,
-                   uint32_t* n_contrib, double* grad2d, double* loss) {
-  render_all<double>(n, proj16, iproj6, W, H, bg, target, image, T_final, n_contrib, grad2d, loss);
+                   uint32_t* n_contrib, double* grad2d, double* loss, double l1_weight,
+                   const double* dLdC_extra) {
+  render_all<double>(n, proj16, iproj6, W, H, bg, target, image, T_final, n_contrib, grad2d, loss, l1_weight,
+                     dLdC_extra);
 }
 
 // Projection backward: grad2d (9 x n, fp64) -> grads (59 x n, fp64).  prec selects

@@ -581,3 +581,43 @@ def test_ssim_gradient_matches_finite_differences():
         xm[idx] -= h
         fd[idx] = lam * ((1 - oracle.ssim(xp, y)[0]) - (1 - oracle.ssim(xm, y)[0])) / (2 * h)
     np.testing.assert_allclose(g, fd, rtol=1e-5, atol=1e-9 * np.abs(g).max())
+
+
+def test_whole_step_gradient_with_dssim_matches_finite_differences():
+    """(1 - lambda) L1 + lambda (1 - SSIM): the render backward with the SSIM image
+    gradient added, then the projection backward, equals central differences of the
+    whole fp64 forward.  The steps change no compositing decision (n_contrib is the
+    same at +h and -h), so the loss is smooth across each difference."""
+    P, n, cam = _fd_scene(n=3, seed=9)
+    lam = 0.2
+    pr = oracle.project(P, n, cam, 64)
+    img = oracle.render(pr, 32, 32, prec=64)["image"]
+    tgt = gi.offset_target(img, seed=6)
+    _, extra = oracle.ssim(img, tgt, lam)
+    assert np.abs(extra).max() > 0
+    rd = oracle.render(pr, 32, 32, target=tgt, prec=64, l1_weight=1 - lam, dLdC_extra=extra)
+    an = oracle.project_bwd(P, n, cam, rd["grad2d"], prec=64)
+
+    def loss(Pm):
+        p = oracle.project(Pm, n, cam, 64)
+        r = oracle.render(p, 32, 32, target=tgt, prec=64, l1_weight=1 - lam)
+        np.testing.assert_array_equal(r["n_contrib"], rd["n_contrib"])
+        return r["loss"] + lam * (1 - oracle.ssim(r["image"], tgt)[0])
+
+    def central(i, pl, h):
+        x0 = float(P[pl, i])
+        Pp, Pm_ = P.copy(), P.copy()
+        Pp[pl, i] = np.float32(x0 + h)
+        Pm_[pl, i] = np.float32(x0 - h)
+        he = (float(Pp[pl, i]) - float(Pm_[pl, i])) / 2
+        return (loss(Pp) - loss(Pm_)) / (2 * he), he
+
+    for i in range(n):
+        for pl in (0, 1, 2, 3, 6, 10, 11, 14, 20, 58):
+            h = 1e-3 * max(abs(float(P[pl, i])), 0.05)
+            # Richardson: the central difference is D + c he^2 + O(he^4); two step
+            # sizes remove the he^2 term
+            d1, e1 = central(i, pl, h)
+            d2, e2 = central(i, pl, h / 2)
+            fd = (d2 * e1 * e1 - d1 * e2 * e2) / (e1 * e1 - e2 * e2)
+            assert abs(fd - an[pl, i]) <= 2e-4 * abs(fd) + 2e-7 * np.abs(an).max(), (i, pl, fd, an[pl, i])
