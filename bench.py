@@ -57,6 +57,8 @@ def parse():
                     help="run the projection backward and Adam as two calls instead of gs_project_bwd_adam")
     ap.add_argument("--views", type=int, default=0,
                     help="use only the first N orbit views (profiling runs; 0 = all)")
+    ap.add_argument("--dssim", type=float, default=0.0,
+                    help="D-SSIM weight lambda: the loss becomes (1 - lambda) L1 + lambda (1 - SSIM) (0 = L1)")
     return ap.parse_args()
 
 
@@ -69,13 +71,43 @@ def dist_env():
     return ws, rank, local
 
 
-def dist_init(ws):
+def dist_init(ws, backend="nccl"):
     if ws <= 1:
         return None
     import torch.distributed as dist
     os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
-    dist.init_process_group("nccl")
+    dist.init_process_group(backend)
     return dist
+
+
+def max_over_ranks(dist, x: float, device=None) -> float:
+    """The largest of every rank's x (x itself without a process group)."""
+    if dist is None:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def time_replicas(dist, body, sync, device=None) -> float:
+    """Milliseconds of ``body`` on the slowest rank.  Every rank synchronises its
+    device and meets the others at a barrier before and after; ``body`` returns its
+    own duration in ms (CUDA events on the GPU)."""
+    sync()
+    if dist:
+        dist.barrier()
+    ms = body()
+    sync()
+    if dist:
+        dist.barrier()
+    return max_over_ranks(dist, ms, device)
+
+
+def whole_job_rate(ws: int, steps: int, ms: float) -> float:
+    """Steps per second of the whole job: every rank runs ``steps`` independent
+    steps, the job takes the slowest rank's ``ms``."""
+    return ws * steps / (ms / 1e3)
 
 
 # ----------------------------------------------------------------------------- clocks
@@ -142,7 +174,7 @@ def passes_for(width, height):
     return (32 + b + 7) // 8
 
 
-def stage_bytes(N, n_pad, V, K, P, passes):
+def stage_bytes(N, n_pad, V, K, P, passes, dssim=False):
     """Algorithmic DRAM bytes of each stage per step (the traffic the method needs
     with the data layout used: SoA planes, 48-byte records, 8+4-byte keys)."""
     return {
@@ -153,8 +185,12 @@ def stage_bytes(N, n_pad, V, K, P, passes):
         "bin_sort": 8 * N + 12 * V + (12 + 24 * passes + 12 + 96) * K,
         # records once per tile, image + T + n_contrib written
         "render_fwd": 48 * K + 20 * P,
-        # grad2d cleared, records once per tile, image/target/T/n_contrib read
-        "render_bwd": 36 * n_pad + 48 * K + 32 * P,
+        # grad2d cleared, records once per tile, image/target/T/n_contrib read (and
+        # the D-SSIM image gradient when that term is on)
+        "render_bwd": 36 * n_pad + 48 * K + (44 if dssim else 32) * P,
+        # D-SSIM: image + target read, 15 maps (3 partials, 2 means per channel)
+        # written; the maps, image and target read again, the image gradient written
+        "ssim": 180 * P,
         # all: count + 59 gradient planes written; visible: 59 params + 9 grad2d read
         "project_bwd": 240 * N + 272 * V,
         # p, g, m, v read; p, m, v written
@@ -172,13 +208,18 @@ def fused_bytes(N, n_pad, V):
 # Rows of the step each measured stage covers.
 STAGE_ROWS = {"project": ["project"], "bin_sort": ["bin_sort"], "render_fwd": ["render_fwd"],
               "render_bwd": ["render_bwd"], "project_bwd": ["project_bwd"], "adam": ["adam"],
-              "project_bwd_adam": ["project_bwd", "adam"]}
+              "project_bwd_adam": ["project_bwd", "adam"], "ssim": ["ssim"]}
 
 
 # FP32 operations per iterated (pixel, entry) pair, counting an FMA as 2 and the
 # exponential as the 11 operations of its Cody-Waite + degree-7 evaluation.
 FLOP_FWD_PAIR = 41
 FLOP_BWD_PAIR = 75
+# FP32 operations per pixel of the D-SSIM forward and backward over 3 channels.  Per
+# channel, forward: horizontal pass 158 (42 staged rows per 32 output rows; per 4
+# outputs 42 products and 5 moments x 44 FMAs), vertical 110, SSIM partials 35;
+# backward: folding the means 14, horizontal 87, vertical 66, combine 6.
+FLOP_SSIM_PIX = 3 * (158 + 110 + 35 + 14 + 87 + 66 + 6)
 
 
 def fp32_peak_tflops(sm_mhz):
@@ -326,8 +367,10 @@ def run_gb300(args, cfg, ws, rank, local):
     rend.raise_on_status()
     del rend, Ptd
 
-    tr = gs.Trainer(Pd, n, W, H, capacity, gi.lr_planes(), device=dev, fused=not args.separate)
-    STAGES = STAGES_SEPARATE if args.separate else STAGES_FUSED
+    tr = gs.Trainer(Pd, n, W, H, capacity, gi.lr_planes(), device=dev, fused=not args.separate, dssim=args.dssim)
+    STAGES = list(STAGES_SEPARATE if args.separate else STAGES_FUSED)
+    if args.dssim > 0:
+        STAGES.insert(STAGES.index("render_bwd"), "ssim")
     del Pd
     # per-view work statistics (forward on the initial parameters)
     E = []
@@ -352,19 +395,27 @@ def run_gb300(args, cfg, ws, rank, local):
         e[2].record()
         gs.render_fwd(cam, tr.bins, tr.bg, tr.image, tr.T_final, tr.n_contrib, tr.status)
         e[3].record()
+        k = 4
+        extra = None
+        if args.dssim > 0:
+            gs.ssim_fwd(tr.image, targets[v], tr.dssim, tr.ssim_maps, tr.ssim_val)
+            gs.ssim_bwd(tr.image, targets[v], tr.ssim_maps, tr.dLdC)
+            extra = tr.dLdC
+            e[k].record()
+            k += 1
         gs.render_bwd(tr.n, tr.n_pad, cam, tr.bins, tr.bg, tr.image, targets[v], tr.T_final, tr.n_contrib,
-                      tr.grad2d, tr.loss, tr.status)
-        e[4].record()
+                      tr.grad2d, tr.loss, tr.status, l1_weight=1.0 - tr.dssim, dLdC_extra=extra)
+        e[k].record()
         if args.separate:
             gs.project_bwd(tr.n, tr.params, cam, tr.proj, tr.grad2d, tr.grads, tr.status)
-            e[5].record()
+            e[k + 1].record()
             tr.optimizer_step()
-            e[6].record()
+            e[k + 2].record()
         else:
             tr.t += 1
             gs.project_bwd_adam(tr.n, tr.params, cam, tr.proj, tr.grad2d, tr.m, tr.v, tr.lr_plane, tr.beta1,
                                 tr.beta2, tr.eps, tr.t, tr.status)
-            e[5].record()
+            e[k + 1].record()
 
     for s in range(args.warmup):
         step(s)
@@ -376,30 +427,25 @@ def run_gb300(args, cfg, ws, rank, local):
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
-    if dist:
-        dist.barrier()
-    torch.cuda.synchronize()
-    t_start = torch.cuda.Event(enable_timing=True)
-    t_end = torch.cuda.Event(enable_timing=True)
-    torch.cuda.nvtx.range_push("timed")
-    t_start.record()
-    for s in range(K):
-        step(args.warmup + s, ev[s])
-    t_end.record()
-    torch.cuda.nvtx.range_pop()
-    torch.cuda.synchronize()
-    if dist:
-        dist.barrier()
+
+    def timed():
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        torch.cuda.nvtx.range_push("timed")
+        t_start.record()
+        for s in range(K):
+            step(args.warmup + s, ev[s])
+        t_end.record()
+        torch.cuda.nvtx.range_pop()
+        torch.cuda.synchronize()
+        return t_start.elapsed_time(t_end)
+
+    ms = time_replicas(dist, timed, torch.cuda.synchronize, dev)
     clk = clocks.stop()
-    ms = t_start.elapsed_time(t_end)
-    if dist:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
     tr.raise_on_status()
     stage_ms = {name: float(np.mean([ev[s][i].elapsed_time(ev[s][i + 1]) for s in range(K)]))
                 for i, name in enumerate(STAGES)}
-    value = ws * K / (ms / 1e3)
+    value = whole_job_rate(ws, K, ms)
 
     # ---------------------------------------------------------------- e2e leg
     e2e = None
@@ -409,27 +455,26 @@ def run_gb300(args, cfg, ws, rank, local):
         del targets
         torch.cuda.empty_cache()
         tgt_dev = torch.empty((3, H, W), dtype=torch.float32, device=dev)
-        loss_host = torch.empty(K, dtype=torch.float32).pin_memory()
-        torch.cuda.synchronize()
-        if dist:
-            dist.barrier()
-        a = torch.cuda.Event(enable_timing=True)
-        b = torch.cuda.Event(enable_timing=True)
-        a.record()
-        for s in range(K):
-            v = (args.warmup + s) % V_views
-            tgt_dev.copy_(host_t[v], non_blocking=True)
-            tr.step(cams[v], tgt_dev)
-            loss_host[s:s + 1].copy_(tr.loss, non_blocking=True)
-        b.record()
-        torch.cuda.synchronize()
-        ms_e2e = a.elapsed_time(b)
-        if dist:
-            t = torch.tensor([ms_e2e], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ms_e2e = float(t.item())
-        e2e = {"value": ws * K / (ms_e2e / 1e3), "unit": "steps/s", "h2d_bytes_per_step": 3 * H * W * 4,
-               "d2h_bytes_per_step": 4, "ms_per_step": ms_e2e / K}
+        loss_host = torch.empty((K, 2), dtype=torch.float32).pin_memory()
+
+        def timed_e2e():
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record()
+            for s in range(K):
+                v = (args.warmup + s) % V_views
+                tgt_dev.copy_(host_t[v], non_blocking=True)
+                tr.step(cams[v], tgt_dev)
+                loss_host[s, 0:1].copy_(tr.loss, non_blocking=True)
+                if args.dssim > 0:
+                    loss_host[s, 1:2].copy_(tr.ssim_val, non_blocking=True)
+            b.record()
+            torch.cuda.synchronize()
+            return a.elapsed_time(b)
+
+        ms_e2e = time_replicas(dist, timed_e2e, torch.cuda.synchronize, dev)
+        e2e = {"value": whole_job_rate(ws, K, ms_e2e), "unit": "steps/s", "h2d_bytes_per_step": 3 * H * W * 4,
+               "d2h_bytes_per_step": 8 if args.dssim > 0 else 4, "ms_per_step": ms_e2e / K}
         del host_t
 
     if rank != 0:
@@ -441,15 +486,18 @@ def run_gb300(args, cfg, ws, rank, local):
     Vmean = float(np.mean([Vs[v] for v in views]))
     Emean = float(np.mean([E[v] for v in views]))
     Pix = W * H
-    byt = stage_bytes(n, n_pad, Vmean, Kmean, Pix, passes)
+    byt = stage_bytes(n, n_pad, Vmean, Kmean, Pix, passes, dssim=args.dssim > 0)
     peak_bw = _peak("hbm_gbs", 6800.0)
     sm_mhz = clk.get("sm_max_mhz") or 2070.0
     peak_fp32 = fp32_peak_tflops(sm_mhz)
-    flops = {"render_fwd": FLOP_FWD_PAIR * Emean, "render_bwd": FLOP_BWD_PAIR * Emean}
+    flops = {"render_fwd": FLOP_FWD_PAIR * Emean, "render_bwd": FLOP_BWD_PAIR * Emean, "ssim": FLOP_SSIM_PIX * Pix}
     per_stage = {}
     t_star = 0.0
     row_t = {}
-    for row in STAGE_ROWS["project_bwd_adam"] + ["project", "bin_sort", "render_fwd", "render_bwd"]:
+    rows_all = STAGE_ROWS["project_bwd_adam"] + ["project", "bin_sort", "render_fwd", "render_bwd"]
+    if args.dssim > 0:
+        rows_all.append("ssim")
+    for row in rows_all:
         row_t[row] = max(byt[row] / (peak_bw * 1e9), flops.get(row, 0.0) / (peak_fp32 * 1e12))
     t_star = sum(row_t.values())
     for name in STAGES:
@@ -479,12 +527,13 @@ def run_gb300(args, cfg, ws, rank, local):
         except Exception as exc:  # the baseline is reported, never required
             cpu = {"value": None, "unit": "steps/s", "kind": "oracle", "error": repr(exc)}
 
-    launches_per_step = 1 + (4 + passes) + 1 + 2 + (2 if args.separate else 1)
+    launches_per_step = 1 + (4 + passes) + 1 + 2 + (2 if args.separate else 1) + (3 if args.dssim > 0 else 0)
     line = {
         "metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": ws, "steps": K, "warmup": args.warmup,
         "ms_per_step": ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32", "data": "synthetic",
         "config": dict(_config_dict(cfg), parallelism=f"replicas{ws}", capacity_K=capacity,
+                       objective=(f"{1 - args.dssim:g} L1 + {args.dssim:g} (1 - SSIM)" if args.dssim > 0 else "L1"),
                        K_mean=Kmean, visible_mean=Vmean, pairs_bwd_mean=Emean),
         "roofline": roof,
         "step_roofline_frac": t_star / (ms / K / 1e3),

@@ -25,6 +25,7 @@ N_PLANES = 59
 TILE = 16
 REC_FLOATS = 12
 N_GRAD2D = 9
+SSIM_MAPS = 15  # planes of gs_ssim_fwd's maps: 3 partials and 2 local means per channel
 
 GS_OK = 0
 GS_ERR_INVALID_ARG = 1
@@ -95,7 +96,7 @@ def load(build_if_missing: bool = True):
                                       ctypes.POINTER(ctypes.c_float), P, P, P, P, P]
         lib.gs_render_fwd.restype = st
         lib.gs_render_bwd.argtypes = [GsDims, ctypes.POINTER(GsCamera), ctypes.POINTER(GsBins), ctypes.c_uint32,
-                                      ctypes.POINTER(ctypes.c_float), P, P, P, P, P, P, P, P]
+                                      ctypes.POINTER(ctypes.c_float), P, P, P, P, ctypes.c_float, P, P, P, P, P]
         lib.gs_render_bwd.restype = st
         lib.gs_project_bwd.argtypes = [GsDims, P, ctypes.POINTER(GsCamera), ctypes.POINTER(GsProj), P, P, P, P]
         lib.gs_project_bwd.restype = st
@@ -106,6 +107,10 @@ def load(build_if_missing: bool = True):
                                             ctypes.POINTER(ctypes.c_float), ctypes.c_double, ctypes.c_double,
                                             ctypes.c_double, ctypes.c_int64, P, P]
         lib.gs_project_bwd_adam.restype = st
+        lib.gs_ssim_fwd.argtypes = [ctypes.c_int32, ctypes.c_int32, P, P, ctypes.c_float, P, P, P]
+        lib.gs_ssim_fwd.restype = st
+        lib.gs_ssim_bwd.argtypes = [ctypes.c_int32, ctypes.c_int32, P, P, P, P, P]
+        lib.gs_ssim_bwd.restype = st
         lib.gs_util_expf.argtypes = [P, P, ctypes.c_int64, P]
         lib.gs_util_expf.restype = st
         lib.gs_status_str.argtypes = [ctypes.c_uint32]
@@ -237,12 +242,27 @@ def render_fwd(cam: dict, bins: BinBuffers, bg, image, T_final, n_contrib, dev_s
 
 
 def render_bwd(n: int, n_pad: int, cam: dict, bins: BinBuffers, bg, image, target, T_final, n_contrib, grad2d,
-               loss, dev_status, stream=None) -> None:
+               loss, dev_status, stream=None, l1_weight: float = 1.0, dLdC_extra=None) -> None:
     cc = camera(cam)
     bc = bins.c()
+    extra = _p(dLdC_extra) if dLdC_extra is not None else None
     _check(load().gs_render_bwd(dims(n, n_pad), ctypes.byref(cc), ctypes.byref(bc), bins.capacity, _bg(bg),
-                                _p(image), _p(target), _p(T_final), _p(n_contrib), _p(grad2d), _p(loss),
-                                _p(dev_status), _stream(stream)), "gs_render_bwd")
+                                _p(image), _p(target), _p(T_final), _p(n_contrib), float(l1_weight), extra,
+                                _p(grad2d), _p(loss), _p(dev_status), _stream(stream)), "gs_render_bwd")
+
+
+def ssim_fwd(image, target, lam: float, maps, ssim_out, stream=None) -> None:
+    """Mean SSIM of image (3 x H x W) against target into ssim_out, and the partial
+    derivatives of lam (1 - SSIM) and local means into maps (SSIM_MAPS x H x W)."""
+    _, H, W = image.shape
+    _check(load().gs_ssim_fwd(W, H, _p(image), _p(target), float(lam), _p(maps), _p(ssim_out), _stream(stream)),
+           "gs_ssim_fwd")
+
+
+def ssim_bwd(image, target, maps, dLdC, stream=None) -> None:
+    """d[lam (1 - SSIM)] / d image into dLdC (3 x H x W), from ssim_fwd's maps."""
+    _, H, W = image.shape
+    _check(load().gs_ssim_bwd(W, H, _p(image), _p(target), _p(maps), _p(dLdC), _stream(stream)), "gs_ssim_bwd")
 
 
 def project_bwd(n: int, params, cam: dict, proj: ProjBuffers, grad2d, grads, dev_status, stream=None) -> None:

@@ -54,7 +54,7 @@ __global__ void __launch_bounds__(256, 2)
     if (vis) {
       rec[3 * i + 0] = make_float4(g.mx, g.my, __fmul_rn(-0.5f, g.A), -g.B);
       rec[3 * i + 1] = make_float4(__fmul_rn(-0.5f, g.C), o, rgb[0], rgb[1]);
-      rec[3 * i + 2] = make_float4(rgb[2], __uint_as_float(uint32_t(i)), skip_radius(g.lam, o), 0.0f);
+      rec[3 * i + 2] = make_float4(rgb[2], __uint_as_float(uint32_t(i)), skip_radius(g.lam, o), g.tz);
       depth[i] = g.tz;
       radius[i] = g.radius;
       rect[i] = make_uint2(uint32_t(g.tx0) | (uint32_t(g.ty0) << 16), uint32_t(g.tx1) | (uint32_t(g.ty1) << 16));

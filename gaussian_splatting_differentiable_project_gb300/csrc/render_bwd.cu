@@ -51,7 +51,8 @@ __global__ void __launch_bounds__(kRasterThreads)
                  uint32_t cap, int W, int H, int TX, float bg0, float bg1, float bg2, const float* __restrict__ image,
                  const float* __restrict__ target, const float* __restrict__ T_final,
                  const uint32_t* __restrict__ n_contrib, float* __restrict__ grad2d, int64_t n_pad,
-                 float* __restrict__ loss, float inv3P, uint32_t* __restrict__ dev_status) {
+                 float* __restrict__ loss, float inv3P, float l1w, const float* __restrict__ dLdC_extra,
+                 uint32_t* __restrict__ dev_status) {
   __shared__ __align__(128) Rec s_rec[2][kBatch];
   __shared__ __align__(8) uint64_t s_bar[2];
   __shared__ float s_red[kRasterThreads / 32];
@@ -74,9 +75,16 @@ __global__ void __launch_bounds__(kRasterThreads)
     const size_t pix = size_t(pyi) * W + pxi;
     const float c0 = image[pix], c1 = image[P + pix], c2 = image[2 * P + pix];
     const float t0 = target[pix], t1 = target[P + pix], t2 = target[2 * P + pix];
-    g0 = (c0 > t0) ? inv3P : ((c0 < t0) ? -inv3P : 0.0f);
-    g1 = (c1 > t1) ? inv3P : ((c1 < t1) ? -inv3P : 0.0f);
-    g2 = (c2 > t2) ? inv3P : ((c2 < t2) ? -inv3P : 0.0f);
+    // d(l1w L1)/dC = l1w sign(C - C*) / (3 H W), plus any other loss term's gradient
+    const float w1 = l1w * inv3P;
+    g0 = (c0 > t0) ? w1 : ((c0 < t0) ? -w1 : 0.0f);
+    g1 = (c1 > t1) ? w1 : ((c1 < t1) ? -w1 : 0.0f);
+    g2 = (c2 > t2) ? w1 : ((c2 < t2) ? -w1 : 0.0f);
+    if (dLdC_extra) {
+      g0 += dLdC_extra[pix];
+      g1 += dLdC_extra[P + pix];
+      g2 += dLdC_extra[2 * P + pix];
+    }
     lsum = fabsf(c0 - t0) + fabsf(c1 - t1) + fabsf(c2 - t2);
     T = T_final[pix];
     nc = n_contrib[pix];
@@ -99,7 +107,7 @@ __global__ void __launch_bounds__(kRasterThreads)
   if (threadIdx.x == 0) {
     float t = 0.0f;
     for (int w = 0; w < kRasterThreads / 32; ++w) t += s_red[w];
-    atomicAdd(loss, t * inv3P);
+    atomicAdd(loss, t * (l1w * inv3P));
   }
 #pragma unroll
   for (int w = 0; w < kRasterThreads / 32; ++w) n_max = max(n_max, s_max[w]);
@@ -210,14 +218,15 @@ __global__ void k_zero4(float4* __restrict__ p, int64_t n4, float* __restrict__ 
 
 extern "C" gs_status gs_render_bwd(gs_dims dims, const gs_camera* cam, const gs_bins* bins, uint32_t capacity_K,
                                    const float bg[3], const float* image, const float* target, const float* T_final,
-                                   const uint32_t* n_contrib, float* grad2d, float* loss_out, uint32_t* dev_status,
-                                   cudaStream_t stream) {
+                                   const uint32_t* n_contrib, float l1_weight, const float* dLdC_extra, float* grad2d,
+                                   float* loss_out, uint32_t* dev_status, cudaStream_t stream) {
   using namespace gs;
   if (!dims_ok(dims) || !camera_ok(cam) || !bins || !bg || !image || !target || !T_final || !n_contrib || !grad2d ||
       !loss_out || !dev_status)
     return GS_ERR_INVALID_ARG;
   if (!bins->rec || !bins->ranges || !bins->n_isect || capacity_K == 0) return GS_ERR_INVALID_ARG;
   if (!aligned(bins->rec, 16) || !aligned(bins->ranges, 8) || !aligned(grad2d, 16)) return GS_ERR_INVALID_ARG;
+  if (!(l1_weight >= 0.0f) || !std::isfinite(l1_weight)) return GS_ERR_INVALID_ARG;
   const int64_t n4 = int64_t(GS_N_GRAD2D) * dims.n_pad / 4;
   k_zero4<<<grid_for(n4, 256, kSmCount * 8), 256, 0, stream>>>(reinterpret_cast<float4*>(grad2d), n4, loss_out);
   const int TX = (cam->width + kTile - 1) / kTile;
@@ -226,6 +235,6 @@ extern "C" gs_status gs_render_bwd(gs_dims dims, const gs_camera* cam, const gs_
   k_render_bwd<<<int(tiles * kCtasPerTile), kRasterThreads, 0, stream>>>(
       reinterpret_cast<const Rec*>(bins->rec), reinterpret_cast<const uint2*>(bins->ranges), bins->n_isect,
       capacity_K, cam->width, cam->height, TX, bg[0], bg[1], bg[2], image, target, T_final, n_contrib, grad2d,
-      dims.n_pad, loss_out, inv3P, dev_status);
+      dims.n_pad, loss_out, inv3P, l1_weight, dLdC_extra, dev_status);
   return launch_status();
 }

@@ -1,0 +1,253 @@
+// D-SSIM term of the objective: SSIM with an 11x11 Gaussian window (sigma 1.5,
+// separable), C1 = 0.01^2, C2 = 0.03^2, zero padding, averaged over 3 H W values.
+//
+// Both kernels take a 32x32 output tile per 256-thread CTA, one channel at a time: the
+// planes they filter are staged with a 5-pixel halo (42x42, zero outside the image),
+// a horizontal 11-tap pass writes the 42 staged rows x 32 columns, and a vertical pass
+// finishes in registers.  In each pass a thread produces 4 adjacent outputs from a
+// 14-value window held in registers, so a staged value is read once per 4 outputs.
+//
+// gs_ssim_fwd: the local means, variances and covariance, then per pixel the partial
+//   derivatives of S times dL/dS = -lambda / (3 H W):
+//     a = dL/dS dS/dmu_x,  b = dL/dS dS/ds_xx,  c = dL/dS dS/ds_xy,
+//   stored with the local means mu_x, mu_y; the CTA adds its share of mean S.  The
+//   moments are taken about a shift per CTA and channel (the tile-centre value of each
+//   image; the zero padding is staged as 0 - shift): the window weights sum to 1, so the
+//   variance and covariance do not change, while E[x^2] - mu^2 no longer cancels in flat
+//   regions (exactly zero there).
+// gs_ssim_bwd: with s_x, s_y a shift of its own (the tile-centre values again),
+//     dL/dx_j = sum_i g_ij [a_i + 2 (x_j - mu_x,i) b_i + (y_j - mu_y,i) c_i]
+//             = G * A + 2 (x_j - s_x) (G * b) + (y_j - s_y) (G * c),
+//     A = a - 2 (mu_x - s_x) b - (mu_y - s_y) c,
+//   (the window is symmetric, so the transposed filter is G itself).  Folding the means
+//   in about the shift rather than about zero keeps the terms that cancel small.
+#include <cmath>
+
+#include "api_util.h"
+#include "gs_common.cuh"
+
+namespace gs {
+
+constexpr int kSsimTile = 32;                      // output tile edge
+constexpr int kSsimHalo = 5;                       // window radius
+constexpr int kSsimIn = kSsimTile + 2 * kSsimHalo; // 42 staged rows / columns
+constexpr int kSsimInStride = 43;                  // odd: a warp's 14-wide windows hit distinct banks
+constexpr int kSsimHStride = 33;                   // horizontal-pass rows: conflict-free column stores
+constexpr int kSsimGroup = 4;                      // outputs per thread per pass
+constexpr int kSsimWin = kSsimGroup + 10;          // values a group of 4 outputs reads
+constexpr int kSsimThreads = 256;
+constexpr int kSsimHItems = kSsimIn * (kSsimTile / kSsimGroup);  // 42 rows x 8 column groups
+constexpr float kC1 = 0.01f * 0.01f;
+constexpr float kC2 = 0.03f * 0.03f;
+static_assert(kSsimThreads == kSsimTile * (kSsimTile / kSsimGroup), "one vertical group per thread");
+
+struct SsimWindow {
+  float g[11];  // normalised 1D Gaussian, sigma 1.5
+};
+
+inline SsimWindow ssim_window() {
+  SsimWindow w;
+  double sum = 0.0, g[11];
+  for (int k = 0; k < 11; ++k) {
+    const double d = double(k - 5);
+    g[k] = std::exp(-d * d / 4.5);
+    sum += g[k];
+  }
+  for (int k = 0; k < 11; ++k) w.g[k] = float(g[k] / sum);
+  return w;
+}
+
+// Stage NQ planes of channel c (plane q at base[q] + c P) with the halo into
+// s[q][42][43]; values outside the image are 0, and shift[q] is subtracted from all.
+template <int NQ>
+__device__ __forceinline__ void ssim_stage(float (*s)[kSsimIn][kSsimInStride], const float* const* base, int W,
+                                           int H, int64_t P, int c, int ox, int oy, const float* shift) {
+  for (int k = threadIdx.x; k < kSsimIn * kSsimIn; k += kSsimThreads) {
+    const int r = k / kSsimIn, col = k - r * kSsimIn;
+    const int gy = oy - kSsimHalo + r, gx = ox - kSsimHalo + col;
+    const bool in = gx >= 0 && gx < W && gy >= 0 && gy < H;
+    const int64_t e = int64_t(c) * P + int64_t(gy) * W + gx;
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) s[q][r][col] = (in ? base[q][e] : 0.0f) - shift[q];
+  }
+}
+
+// out[j] += sum_t g[t] v[j + t] for the 4 outputs of a group.
+__device__ __forceinline__ void ssim_tap4(float (&out)[kSsimGroup], const float (&v)[kSsimWin], const SsimWindow& w) {
+#pragma unroll
+  for (int k = 0; k < kSsimWin; ++k)
+#pragma unroll
+    for (int j = 0; j < kSsimGroup; ++j)
+      if (k - j >= 0 && k - j < 11) out[j] = fmaf(w.g[k - j], v[k], out[j]);
+}
+
+__global__ void __launch_bounds__(kSsimThreads)
+    k_ssim_fwd(const float* __restrict__ x, const float* __restrict__ y, int W, int H, SsimWindow w, float dLdS,
+               float inv3P, float* __restrict__ maps, float* __restrict__ ssim_out) {
+  __shared__ float s_in[2][kSsimIn][kSsimInStride];
+  __shared__ float s_h[5][kSsimIn][kSsimHStride];
+  __shared__ float s_red[kSsimThreads / 32];
+  const int ox = blockIdx.x * kSsimTile, oy = blockIdx.y * kSsimTile;
+  const int64_t P = int64_t(W) * H;
+  const int vcol = threadIdx.x % kSsimTile, vrow = (threadIdx.x / kSsimTile) * kSsimGroup;
+  const int64_t centre = int64_t(min(oy + kSsimTile / 2, H - 1)) * W + min(ox + kSsimTile / 2, W - 1);
+  float ssum = 0.0f;
+  for (int c = 0; c < 3; ++c) {
+    const float shift[2] = {x[c * P + centre], y[c * P + centre]};
+    const float* planes[2] = {x, y};
+    ssim_stage<2>(s_in, planes, W, H, P, c, ox, oy, shift);
+    __syncthreads();
+    // horizontal: moments of the shifted values (x, y, x^2, y^2, x y) along rows
+    for (int i = threadIdx.x; i < kSsimHItems; i += kSsimThreads) {
+      const int r = i % kSsimIn, c0 = (i / kSsimIn) * kSsimGroup;
+      float a[kSsimWin], b[kSsimWin], aa[kSsimWin], bb[kSsimWin], ab[kSsimWin];
+#pragma unroll
+      for (int k = 0; k < kSsimWin; ++k) {
+        a[k] = s_in[0][r][c0 + k];
+        b[k] = s_in[1][r][c0 + k];
+        aa[k] = a[k] * a[k];
+        bb[k] = b[k] * b[k];
+        ab[k] = a[k] * b[k];
+      }
+      float m[5][kSsimGroup] = {};
+      ssim_tap4(m[0], a, w);
+      ssim_tap4(m[1], b, w);
+      ssim_tap4(m[2], aa, w);
+      ssim_tap4(m[3], bb, w);
+      ssim_tap4(m[4], ab, w);
+#pragma unroll
+      for (int q = 0; q < 5; ++q)
+#pragma unroll
+        for (int j = 0; j < kSsimGroup; ++j) s_h[q][r][c0 + j] = m[q][j];
+    }
+    __syncthreads();
+    // vertical: 4 rows of one column per thread
+    float m[5][kSsimGroup] = {};
+#pragma unroll
+    for (int q = 0; q < 5; ++q) {
+      float v[kSsimWin];
+#pragma unroll
+      for (int k = 0; k < kSsimWin; ++k) v[k] = s_h[q][vrow + k][vcol];
+      ssim_tap4(m[q], v, w);
+    }
+#pragma unroll
+    for (int j = 0; j < kSsimGroup; ++j) {
+      const int px = ox + vcol, py = oy + vrow + j;
+      if (px >= W || py >= H) continue;
+      const float mx = shift[0] + m[0][j], my = shift[1] + m[1][j];
+      const float sxx = m[2][j] - m[0][j] * m[0][j], syy = m[3][j] - m[1][j] * m[1][j];
+      const float sxy = m[4][j] - m[0][j] * m[1][j];
+      const float n1 = 2.f * mx * my + kC1, n2 = 2.f * sxy + kC2;
+      const float d1 = mx * mx + my * my + kC1, d2 = sxx + syy + kC2;
+      const float id = 1.0f / (d1 * d2);
+      const float S = n1 * n2 * id;
+      const float dS_dmx = 2.f * my * n2 * id - S * 2.f * mx / d1;
+      const float dS_dsxx = -S / d2;
+      const float dS_dsxy = 2.f * n1 * id;
+      const int64_t e = int64_t(py) * W + px;
+      maps[(0 + c) * P + e] = dLdS * dS_dmx;
+      maps[(3 + c) * P + e] = dLdS * dS_dsxx;
+      maps[(6 + c) * P + e] = dLdS * dS_dsxy;
+      maps[(9 + c) * P + e] = mx;
+      maps[(12 + c) * P + e] = my;
+      ssum += S;
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) ssum += __shfl_xor_sync(0xffffffffu, ssum, o);
+  if ((threadIdx.x & 31) == 0) s_red[threadIdx.x >> 5] = ssum;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float t = 0.f;
+    for (int k = 0; k < kSsimThreads / 32; ++k) t += s_red[k];
+    atomicAdd(ssim_out, t * inv3P);
+  }
+}
+
+__global__ void __launch_bounds__(kSsimThreads)
+    k_ssim_bwd(const float* __restrict__ x, const float* __restrict__ y, int W, int H, SsimWindow w,
+               const float* __restrict__ maps, float* __restrict__ dLdx) {
+  __shared__ float s_in[3][kSsimIn][kSsimInStride];
+  __shared__ float s_h[3][kSsimIn][kSsimHStride];
+  const int ox = blockIdx.x * kSsimTile, oy = blockIdx.y * kSsimTile;
+  const int64_t P = int64_t(W) * H;
+  const int vcol = threadIdx.x % kSsimTile, vrow = (threadIdx.x / kSsimTile) * kSsimGroup;
+  const int64_t centre = int64_t(min(oy + kSsimTile / 2, H - 1)) * W + min(ox + kSsimTile / 2, W - 1);
+  for (int c = 0; c < 3; ++c) {
+    const float sx = x[c * P + centre], sy = y[c * P + centre];
+    // stage A (about the shift), b and c of this channel with the halo; zero outside
+    for (int k = threadIdx.x; k < kSsimIn * kSsimIn; k += kSsimThreads) {
+      const int r = k / kSsimIn, col = k - r * kSsimIn;
+      const int gy = oy - kSsimHalo + r, gx = ox - kSsimHalo + col;
+      float va = 0.f, vb = 0.f, vc = 0.f;
+      if (gx >= 0 && gx < W && gy >= 0 && gy < H) {
+        const int64_t e = int64_t(c) * P + int64_t(gy) * W + gx;
+        vb = maps[3 * P + e];
+        vc = maps[6 * P + e];
+        va = maps[e] - 2.f * (maps[9 * P + e] - sx) * vb - (maps[12 * P + e] - sy) * vc;
+      }
+      s_in[0][r][col] = va;
+      s_in[1][r][col] = vb;
+      s_in[2][r][col] = vc;
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < kSsimHItems; i += kSsimThreads) {
+      const int r = i % kSsimIn, c0 = (i / kSsimIn) * kSsimGroup;
+#pragma unroll
+      for (int q = 0; q < 3; ++q) {
+        float v[kSsimWin];
+#pragma unroll
+        for (int k = 0; k < kSsimWin; ++k) v[k] = s_in[q][r][c0 + k];
+        float o[kSsimGroup] = {};
+        ssim_tap4(o, v, w);
+#pragma unroll
+        for (int j = 0; j < kSsimGroup; ++j) s_h[q][r][c0 + j] = o[j];
+      }
+    }
+    __syncthreads();
+    float g[3][kSsimGroup] = {};
+#pragma unroll
+    for (int q = 0; q < 3; ++q) {
+      float v[kSsimWin];
+#pragma unroll
+      for (int k = 0; k < kSsimWin; ++k) v[k] = s_h[q][vrow + k][vcol];
+      ssim_tap4(g[q], v, w);
+    }
+#pragma unroll
+    for (int j = 0; j < kSsimGroup; ++j) {
+      const int px = ox + vcol, py = oy + vrow + j;
+      if (px >= W || py >= H) continue;
+      const int64_t e = int64_t(c) * P + int64_t(py) * W + px;
+      dLdx[e] = g[0][j] + 2.f * (x[e] - sx) * g[1][j] + (y[e] - sy) * g[2][j];
+    }
+    __syncthreads();
+  }
+}
+
+__global__ void k_zero1(float* p) { *p = 0.0f; }
+
+}  // namespace gs
+
+extern "C" gs_status gs_ssim_fwd(int32_t width, int32_t height, const float* image, const float* target,
+                                 float lambda, float* maps, float* ssim_out, cudaStream_t stream) {
+  using namespace gs;
+  if (width <= 0 || height <= 0 || !image || !target || !maps || !ssim_out || !(lambda >= 0.0f) ||
+      !std::isfinite(lambda))
+    return GS_ERR_INVALID_ARG;
+  const double P = double(width) * double(height);
+  k_zero1<<<1, 1, 0, stream>>>(ssim_out);
+  const dim3 grid((width + kSsimTile - 1) / kSsimTile, (height + kSsimTile - 1) / kSsimTile);
+  k_ssim_fwd<<<grid, kSsimThreads, 0, stream>>>(image, target, width, height, ssim_window(), float(-double(lambda) / (3.0 * P)),
+                                       float(1.0 / (3.0 * P)), maps, ssim_out);
+  return launch_status();
+}
+
+extern "C" gs_status gs_ssim_bwd(int32_t width, int32_t height, const float* image, const float* target,
+                                 const float* maps, float* dLdC, cudaStream_t stream) {
+  using namespace gs;
+  if (width <= 0 || height <= 0 || !image || !target || !maps || !dLdC) return GS_ERR_INVALID_ARG;
+  const dim3 grid((width + kSsimTile - 1) / kSsimTile, (height + kSsimTile - 1) / kSsimTile);
+  k_ssim_bwd<<<grid, kSsimThreads, 0, stream>>>(image, target, width, height, ssim_window(), maps, dLdC);
+  return launch_status();
+}

@@ -2,7 +2,9 @@
 
 The step is the six C-ABI calls in order: project -> bin_sort -> render_fwd ->
 render_bwd -> project_bwd -> adam_step, all enqueued on one CUDA stream with no
-host synchronisation inside the step.  Parameters, Adam moments and every
+host synchronisation inside the step.  With a D-SSIM weight lambda > 0 the loss is
+(1 - lambda) L1 + lambda (1 - SSIM): ssim_fwd and ssim_bwd run between render_fwd
+and render_bwd, and render_bwd adds their image gradient to the weighted L1 one.  Parameters, Adam moments and every
 transient buffer stay resident on the device; the device status word is read
 only when the caller asks for it.
 """
@@ -10,13 +12,13 @@ from __future__ import annotations
 
 import numpy as np
 
-from . import (BinBuffers, ProjBuffers, N_GRAD2D, adam_step, bin_sort, project, project_bwd, project_bwd_adam,
-               render_bwd, render_fwd, status_str)
+from . import (BinBuffers, ProjBuffers, N_GRAD2D, SSIM_MAPS, adam_step, bin_sort, project, project_bwd, project_bwd_adam,
+               render_bwd, render_fwd, ssim_bwd, ssim_fwd, status_str)
 
 
 class Trainer:
     def __init__(self, params, n: int, width: int, height: int, capacity: int, lr_plane, betas=(0.9, 0.999),
-                 eps: float = 1e-15, bg=(0.0, 0.0, 0.0), device="cuda", fused: bool = True):
+                 eps: float = 1e-15, bg=(0.0, 0.0, 0.0), device="cuda", fused: bool = True, dssim: float = 0.0):
         import torch
         if isinstance(params, np.ndarray):
             params = torch.from_numpy(np.ascontiguousarray(params, np.float32))
@@ -40,6 +42,13 @@ class Trainer:
         self.eps = float(eps)
         self.bg = tuple(float(x) for x in bg)
         self.fused = bool(fused)
+        self.dssim = float(dssim)
+        if not (0.0 <= self.dssim <= 1.0):
+            raise ValueError(f"D-SSIM weight must lie in [0, 1], got {dssim}")
+        if self.dssim > 0.0:
+            self.ssim_maps = torch.empty((SSIM_MAPS, height, width), dtype=torch.float32, device=device)
+            self.dLdC = torch.empty((3, height, width), dtype=torch.float32, device=device)
+            self.ssim_val = torch.zeros(1, dtype=torch.float32, device=device)
         self.t = 0
 
     # the stages ------------------------------------------------------------------
@@ -48,9 +57,19 @@ class Trainer:
         bin_sort(self.n, self.n_pad, self.proj, cam, self.bins, self.status, stream)
         render_fwd(cam, self.bins, self.bg, self.image, self.T_final, self.n_contrib, self.status, stream)
 
-    def backward(self, cam: dict, target, stream=None) -> None:
+    def loss_backward(self, cam: dict, target, stream=None) -> None:
+        """The loss and its gradient with respect to the projected quantities
+        (grad2d): the D-SSIM term first when lambda > 0, then the render backward."""
+        extra = None
+        if self.dssim > 0.0:
+            ssim_fwd(self.image, target, self.dssim, self.ssim_maps, self.ssim_val, stream)
+            ssim_bwd(self.image, target, self.ssim_maps, self.dLdC, stream)
+            extra = self.dLdC
         render_bwd(self.n, self.n_pad, cam, self.bins, self.bg, self.image, target, self.T_final, self.n_contrib,
-                   self.grad2d, self.loss, self.status, stream)
+                   self.grad2d, self.loss, self.status, stream, l1_weight=1.0 - self.dssim, dLdC_extra=extra)
+
+    def backward(self, cam: dict, target, stream=None) -> None:
+        self.loss_backward(cam, target, stream)
         project_bwd(self.n, self.params, cam, self.proj, self.grad2d, self.grads, self.status, stream)
 
     def optimizer_step(self, stream=None) -> None:
@@ -67,13 +86,19 @@ class Trainer:
             self.backward(cam, target, stream)
             self.optimizer_step(stream)
             return
-        render_bwd(self.n, self.n_pad, cam, self.bins, self.bg, self.image, target, self.T_final, self.n_contrib,
-                   self.grad2d, self.loss, self.status, stream)
+        self.loss_backward(cam, target, stream)
         self.t += 1
         project_bwd_adam(self.n, self.params, cam, self.proj, self.grad2d, self.m, self.v, self.lr_plane, self.beta1,
                          self.beta2, self.eps, self.t, self.status, stream)
 
     # host-side reads (synchronise) -----------------------------------------------
+    def total_loss(self) -> float:
+        """(1 - lambda) L1 + lambda (1 - SSIM) of the last step (L1 alone for lambda = 0)."""
+        v = float(self.loss[0].item())
+        if self.dssim > 0.0:
+            v += self.dssim * (1.0 - float(self.ssim_val[0].item()))
+        return v
+
     def n_isect(self) -> int:
         return int(self.bins.n_isect[0].item()) & 0xFFFFFFFF
 

@@ -97,9 +97,9 @@ typedef struct gs_dims {
  *          so that power = ca dx^2 + cb dx dy + cc dy^2; opacity; r, g, b; the
  *          Gaussian's index (uint32 bits); a skip radius (at pixels farther than it
  *          from the mean the entry's alpha is below the compositing threshold;
- *          +FLT_MAX if not bounded, -FLT_MAX if never composited); 1 unused.  The pages' projected record
- *          (means2d, depth, conic, opacity, colour) minus depth and radius, which
- *          are kept in their own arrays.
+ *          +FLT_MAX if not bounded, -FLT_MAX if never composited); camera-space z
+ *          (as in depth).  The pages' projected record (means2d, depth, conic,
+ *          opacity, colour) minus the radius, which is kept in its own array.
  *   depth  camera-space z.
  *   radius pixel radius ceil(3 sqrt(lambda_max)), 0 if culled.
  *   rect   2 uint32 per Gaussian: (tx0 | ty0 << 16, tx1 | ty1 << 16), inclusive tile
@@ -193,26 +193,50 @@ gs_status gs_render_fwd(const gs_camera* cam, const gs_bins* bins, uint32_t capa
                         cudaStream_t stream);
 
 /* ---------------------------------------------------------------------------
- * gs_render_bwd -- L1 loss and the compositing backward.  "Scaling 3D Gaussian
- * Splatting with Distributed Compute", objective and gradient-descent section
- * (L1 term between render and ground truth; gradients flow back to mean,
- * covariance, colour and opacity) and step walkthrough (loss computed locally,
- * gradients back through the same stages).  loss = mean |C - C*| over the 3 H W
- * values, dL/dC = sign(C - C*) / (3 H W).  Each pixel walks its composited
- * entries in reverse, recovering T by division by (1 - alpha), and produces per
- * entry the partials of the loss with respect to mean2d (x, y), the conic (A, B,
- * C), opacity and colour (r, g, b); partials of a warp are summed by shuffles
- * and added to grad2d with global atomics (summation order is not fixed).
+ * gs_render_bwd -- loss gradient and the compositing backward.  "Scaling 3D
+ * Gaussian Splatting with Distributed Compute", objective and gradient-descent
+ * section (a weighted L1 and D-SSIM objective between render and ground truth;
+ * gradients flow back to mean, covariance, colour and opacity) and step walkthrough
+ * (loss computed locally, gradients back through the same stages).
+ * dL/dC = l1_weight sign(C - C*) / (3 H W) + dLdC_extra (if non-null, e.g. the D-SSIM
+ * term's gradient from gs_ssim_bwd); loss_out = l1_weight mean |C - C*| over the
+ * 3 H W values.  Each pixel walks its composited entries in reverse, recovering T
+ * by division by (1 - alpha), and produces per entry the partials of the loss with
+ * respect to mean2d (x, y), the conic (A, B, C), opacity and colour (r, g, b);
+ * partials of a warp are summed by shuffles and added to grad2d with global
+ * atomics (summation order is not fixed).
  *   image, T_final, n_contrib: outputs of gs_render_fwd (read).
- *   target    3 x H x W fp32 (read).
- *   grad2d    9 x n_pad fp32 (write; zeroed by this call first), planes
- *             (d mx, d my, d A, d B, d C, d opacity, d r, d g, d b).
- *   loss_out  1 fp32 (write; zeroed first).
- * Errors: as gs_render_fwd. */
+ *   target      3 x H x W fp32 (read).
+ *   l1_weight   weight of the L1 term (1 for the L1 objective, 1 - lambda with D-SSIM).
+ *   dLdC_extra  3 x H x W fp32 added to the loss gradient, or null.
+ *   grad2d      9 x n_pad fp32 (write; zeroed by this call first), planes
+ *               (d mx, d my, d A, d B, d C, d opacity, d r, d g, d b).
+ *   loss_out    1 fp32 (write; zeroed first).
+ * Errors: as gs_render_fwd, plus a negative or non-finite l1_weight. */
 gs_status gs_render_bwd(gs_dims dims, const gs_camera* cam, const gs_bins* bins, uint32_t capacity_K,
                         const float bg[3], const float* image, const float* target, const float* T_final,
-                        const uint32_t* n_contrib, float* grad2d, float* loss_out, uint32_t* dev_status,
-                        cudaStream_t stream);
+                        const uint32_t* n_contrib, float l1_weight, const float* dLdC_extra, float* grad2d,
+                        float* loss_out, uint32_t* dev_status, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * gs_ssim_fwd / gs_ssim_bwd -- the D-SSIM term.  "Scaling 3D Gaussian Splatting
+ * with Distributed Compute", objective paragraph (a weighted combination of an L1
+ * term and a D-SSIM term; the formula did not survive on the page, read as
+ * (1 - lambda) L1 + lambda (1 - SSIM)).  SSIM after Wang et al. 2004: an 11x11
+ * Gaussian window (sigma 1.5, separable), C1 = 0.01^2, C2 = 0.03^2, zero padding
+ * outside the image, averaged over the 3 H W values.
+ * gs_ssim_fwd: ssim_out = mean SSIM of image against target (1 fp32, zeroed first);
+ *   maps (GS_SSIM_MAPS x H x W fp32, caller-owned scratch) receives, per pixel and
+ *   channel, the derivatives of lambda (1 - SSIM) with respect to the local mean of
+ *   the image, its variance and the covariance (planes 0-2, 3-5, 6-8), and the local
+ *   means of image and target (planes 9-11, 12-14).
+ * gs_ssim_bwd: dLdC (3 x H x W fp32, write) = d[lambda (1 - SSIM)] / d image, from maps.
+ * Errors: GS_ERR_INVALID_ARG for null pointers, non-positive sizes, lambda < 0. */
+#define GS_SSIM_MAPS 15
+gs_status gs_ssim_fwd(int32_t width, int32_t height, const float* image, const float* target, float lambda,
+                      float* maps, float* ssim_out, cudaStream_t stream);
+gs_status gs_ssim_bwd(int32_t width, int32_t height, const float* image, const float* target, const float* maps,
+                      float* dLdC, cudaStream_t stream);
 
 /* ---------------------------------------------------------------------------
  * gs_project_bwd -- chain rule of gs_project.  "Scaling 3D Gaussian Splatting

@@ -78,6 +78,18 @@ def test_argument_errors_are_returned_without_a_gpu():
     r = lib.gs_adam_step(gs.dims(10, 256), ctypes.c_void_p(16), ctypes.c_void_p(16), ctypes.c_void_p(16),
                          ctypes.c_void_p(16), lr, 0.9, 0.999, 1e-15, 0, None)
     assert r == gs.GS_ERR_INVALID_ARG
+    # ssim: negative lambda, empty image, null output
+    p = ctypes.c_void_p(16)
+    assert lib.gs_ssim_fwd(64, 64, p, p, -0.1, p, p, None) == gs.GS_ERR_INVALID_ARG
+    assert lib.gs_ssim_fwd(0, 64, p, p, 0.2, p, p, None) == gs.GS_ERR_INVALID_ARG
+    assert lib.gs_ssim_bwd(64, 64, p, p, p, None, None) == gs.GS_ERR_INVALID_ARG
+    # render backward: negative or non-finite L1 weight
+    bins = gs.GsBins(16, 16, 16, 16, 16)
+    bg = (ctypes.c_float * 3)(0, 0, 0)
+    for w in (-1.0, float("nan"), float("inf")):
+        r = lib.gs_render_bwd(gs.dims(10, 256), ctypes.byref(cam), ctypes.byref(bins), 1000, bg, p, p, p, p, w, None,
+                              p, p, p, None)
+        assert r == gs.GS_ERR_INVALID_ARG, w
 
 
 def test_product_package_has_no_oracle_or_cpu_path():
@@ -100,3 +112,14 @@ def test_workspace_query_scales(n):
     b = lib.gs_bin_sort_workspace_bytes(gs.dims(n, pad), 1 << 24, 2048, 2048)
     assert 0 < a < b
     assert b >= (1 << 24) * 12
+
+
+def test_binding_constants_match_the_header():
+    import gaussian_splatting_differentiable_project_gb300 as gs
+    src = open(os.path.join(ROOT, "include", "gs.h")).read()
+    defs = dict(re.findall(r"#define (GS_[A-Z0-9_]+) (\d+)\b", src))
+    assert int(defs["GS_N_PLANES"]) == gs.N_PLANES
+    assert int(defs["GS_TILE"]) == gs.TILE
+    assert int(defs["GS_REC_FLOATS"]) == gs.REC_FLOATS
+    assert int(defs["GS_N_GRAD2D"]) == gs.N_GRAD2D
+    assert int(defs["GS_SSIM_MAPS"]) == gs.SSIM_MAPS

@@ -140,6 +140,8 @@ def test_project_parity(case):
     exact = np.mean(got[vis].view(np.uint32) == exp[vis].view(np.uint32))
     assert exact == 1.0, f"only {exact:.6f} of projected record values are bit-exact"
     np.testing.assert_array_equal(rec[vis, 9].view(np.uint32), np.nonzero(vis)[0].astype(np.uint32))
+    # the record's last slot carries the depth (the binning's sort keys read it there)
+    np.testing.assert_array_equal(rec[vis, 11].view(np.uint32), ref["depth"][vis].view(np.uint32))
 
 
 # ----------------------------------------------------------------------------- binning
@@ -308,6 +310,128 @@ def test_fused_project_bwd_adam_equals_separate_calls(case):
     for x, y in ((a.params, b.params), (a.m, b.m), (a.v, b.v)):
         x, y = x.cpu().numpy().astype(np.float64), y.cpu().numpy().astype(np.float64)
         assert np.all(np.abs(x - y) <= 4e-7 * np.abs(x) + 1e-30)
+
+
+# ----------------------------------------------------------------------------- D-SSIM
+
+def _ssim_gpu(x, y, lam):
+    xd = torch.from_numpy(np.ascontiguousarray(x, np.float32)).to(DEV)
+    yd = torch.from_numpy(np.ascontiguousarray(y, np.float32)).to(DEV)
+    _, H, W = x.shape
+    maps = torch.full((gs.SSIM_MAPS, H, W), float("nan"), dtype=torch.float32, device=DEV)
+    s = torch.full((1,), float("nan"), dtype=torch.float32, device=DEV)
+    g = torch.full((3, H, W), float("nan"), dtype=torch.float32, device=DEV)
+    gs.ssim_fwd(xd, yd, lam, maps, s)
+    gs.ssim_bwd(xd, yd, maps, g)
+    torch.cuda.synchronize()
+    return float(s.item()), g.cpu().numpy().astype(np.float64)
+
+
+def _ssim_grad_close(got, ref, lam, P):
+    """fp32 against fp64.  The gradient's natural unit is lambda / (3 P).  The kernels
+    take the window moments about a per-tile shift and fold the local means in about
+    a shift too, so flat regions cancel exactly.  Elsewhere single terms of the
+    filtered sums are large: the luminance factor divides by mu_x^2 + mu_y^2 + C1 >=
+    1e-4 and the contrast-structure factor by the variances + C2 >= 9e-4, so in dark
+    or smooth regions a term reaches hundreds of units while their sum is far smaller,
+    and 121-tap fp32 sums of them keep about 1e-5 of the image's largest gradient.
+    Allowed: 1e-4 relative plus 1e-4 of the larger of the unit and the largest
+    gradient magnitude (the 2D-gradient tests scale their floor with the group's
+    largest value the same way)."""
+    unit = lam / (3.0 * P)
+    tol = 1e-4 * np.abs(ref) + 1e-4 * max(unit, float(np.abs(ref).max()))
+    bad = ~(np.abs(got - ref) <= tol)
+    assert not bad.any(), (int(bad.sum()), float(np.nanmax(np.abs(got - ref) / unit)), float(np.abs(ref).max() / unit))
+
+
+SSIM_SHAPES = [(37, 53), (128, 128), (5, 7), (1, 1), (300, 200)]
+
+
+@pytest.mark.parametrize("H,W", SSIM_SHAPES, ids=[f"{h}x{w}" for h, w in SSIM_SHAPES])
+def test_ssim_parity_random_images(H, W):
+    """Mean SSIM within 1e-5 and the gradient of lambda (1 - SSIM) per value, on
+    seeded images with ragged 16x16 tiles, images smaller than the window and a
+    single pixel."""
+    rng = np.random.default_rng(H * 1000 + W)
+    x = rng.uniform(0, 1, (3, H, W)).astype(np.float32)
+    y = np.clip(x + rng.normal(0, 0.15, x.shape), 0, 1).astype(np.float32)
+    s_ref, g_ref = oracle.ssim(x, y, 0.2)
+    s, g = _ssim_gpu(x, y, 0.2)
+    assert abs(s - s_ref) <= 1e-5, (s, s_ref)
+    _ssim_grad_close(g, g_ref, 0.2, H * W)
+
+
+def test_ssim_identical_and_flat_images():
+    """SSIM(x, x) = 1 with zero gradient (its maximum), on a textured image and on a
+    flat one (variances exactly zero); a flat image against a different flat image."""
+    rng = np.random.default_rng(3)
+    x = rng.uniform(0, 1, (3, 40, 24)).astype(np.float32)
+    for a, b in ((x, x), (np.full_like(x, 0.3), np.full_like(x, 0.3)), (np.full_like(x, 0.3), np.full_like(x, 0.7))):
+        s_ref, g_ref = oracle.ssim(a, b, 0.2)
+        s, g = _ssim_gpu(a, b, 0.2)
+        assert abs(s - s_ref) <= 1e-5, (s, s_ref)
+        _ssim_grad_close(g, g_ref, 0.2, a.shape[1] * a.shape[2])
+
+
+def test_ssim_parity_on_renders(case):
+    """The images the step feeds it: a render against its offset target."""
+    cam = case["cam"]
+    W, H = cam["width"], cam["height"]
+    img = oracle.render(case["ref_proj"], W, H)["image"]
+    tgt = _target_for(case)
+    s_ref, g_ref = oracle.ssim(img, tgt, 0.2)
+    s, g = _ssim_gpu(img, tgt, 0.2)
+    assert abs(s - s_ref) <= 1e-5, (s, s_ref)
+    _ssim_grad_close(g, g_ref, 0.2, W * H)
+
+
+@pytest.mark.parametrize("fused", [False, True], ids=["separate", "fused"])
+def test_whole_step_with_dssim_end_to_end(case, fused):
+    """(1 - lambda) L1 + lambda (1 - SSIM) with lambda = 0.2: loss, 2D gradients and
+    the Adam update against the oracle's step with the same objective."""
+    P, cam, n = case["P"], case["cam"], case["n"]
+    W, H = cam["width"], cam["height"]
+    target = _target_for(case)
+    z = np.zeros((59, P.shape[1]))
+    ref = oracle.step(P, n, cam, target, z, z, 1, gi.lr_planes(), dssim=0.2)
+    tr = gs.Trainer(P, n, W, H, capacity=1 << 20, lr_plane=gi.lr_planes(), fused=fused, dssim=0.2)
+    tr.step(cam, torch.from_numpy(target).to(DEV))
+    torch.cuda.synchronize()
+    assert tr.check_status() == 0
+    assert abs(tr.total_loss() - ref["render"]["loss"]) <= 1e-5 * abs(ref["render"]["loss"])
+    assert abs(float(tr.ssim_val.item()) - ref["render"]["ssim"]) <= 1e-5
+    _grad_close(tr.grad2d.cpu().numpy()[:, :n], ref["render"]["grad2d"], what="grad2d")
+    gref = ref["grads"][:, :n]
+    if not fused:
+        _grad_close(tr.grads.cpu().numpy()[:, :n], gref, rtol=2e-4, floor=2e-6, what="param grads")
+    p = tr.params.cpu().numpy()[:, :n].astype(np.float64)
+    pr = ref["params"][:, :n]
+    gscale = np.zeros((59, 1))
+    for a, b in GROUPS_59:
+        gscale[a:b] = np.abs(gref[a:b]).max()
+    defined = np.abs(gref) > 1e-3 * gscale
+    assert defined.mean() > 0.2
+    bad = (np.abs(p - pr) > 1e-5 * np.abs(pr) + 1e-7) & defined
+    assert not bad.any(), bad.sum()
+
+
+def test_render_bwd_extra_image_gradient(case):
+    """The render backward driven only by a given dL/dC image (L1 weight 0): the 2D
+    gradients are the oracle's for the same image gradient, and the loss is 0."""
+    tr, ref, cam, n = case["tr"], case["ref_proj"], case["cam"], case["n"]
+    W, H = cam["width"], cam["height"]
+    target = _target_for(case)
+    extra = np.random.default_rng(21).normal(0.0, 1.0 / (3 * W * H), (3, H, W)).astype(np.float32)
+    rd = oracle.render(ref, W, H, target=target, l1_weight=0.0, dLdC_extra=extra)
+    tr.forward(cam)
+    st = _status()
+    gs.render_bwd(n, tr.n_pad, cam, tr.bins, tr.bg, tr.image, torch.from_numpy(target).to(DEV), tr.T_final,
+                  tr.n_contrib, tr.grad2d, tr.loss, st, l1_weight=0.0,
+                  dLdC_extra=torch.from_numpy(extra).to(DEV))
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert float(tr.loss.item()) == 0.0
+    _grad_close(tr.grad2d.cpu().numpy()[:, :n], rd["grad2d"], what="grad2d")
 
 
 # ----------------------------------------------------------------------------- edge cases
