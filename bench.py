@@ -167,11 +167,12 @@ class ClockSampler:
 # ----------------------------------------------------------------------------- roofline model
 
 def passes_for(width, height):
+    """Radix passes of the tile sort: ceil(tile bits / 8)."""
     tiles = (-(-width // 16)) * (-(-height // 16))
     b = 0
     while (1 << b) < tiles:
         b += 1
-    return (32 + b + 7) // 8
+    return (b + 7) // 8
 
 
 def stage_bytes(N, n_pad, V, K, P, passes, dssim=False):
@@ -180,9 +181,11 @@ def stage_bytes(N, n_pad, V, K, P, passes, dssim=False):
     return {
         # all N: 11 geometric planes + depth/radius/rect/count; visible: 48 SH + record
         "project": 64 * N + 240 * V,
-        # counts twice, rect+depth of the visible, keys+ids emitted, each radix pass
-        # reads and writes keys+ids, then keys/ids read and 48-byte records gathered
-        "bin_sort": 8 * N + 12 * V + (12 + 24 * passes + 12 + 96) * K,
+        # counts twice; visible: depth read, (depth, index) written, 4 depth passes of
+        # 16 bytes, sorted index + count read twice and rect once; per intersection
+        # (tile, index) emitted, each tile pass reads and writes 16 bytes, then tile
+        # key + index read, 48-byte record gathered and written, 64-bit key written
+        "bin_sort": 8 * N + 100 * V + (8 + 16 * passes + 112) * K,
         # records once per tile, image + T + n_contrib written
         "render_fwd": 48 * K + 20 * P,
         # grad2d cleared, records once per tile, image/target/T/n_contrib read (and
@@ -527,7 +530,7 @@ def run_gb300(args, cfg, ws, rank, local):
         except Exception as exc:  # the baseline is reported, never required
             cpu = {"value": None, "unit": "steps/s", "kind": "oracle", "error": repr(exc)}
 
-    launches_per_step = 1 + (4 + passes) + 1 + 2 + (2 if args.separate else 1) + (3 if args.dssim > 0 else 0)
+    launches_per_step = 1 + (9 + passes) + 1 + 2 + (2 if args.separate else 1) + (3 if args.dssim > 0 else 0)
     line = {
         "metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": ws, "steps": K, "warmup": args.warmup,
         "ms_per_step": ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,

@@ -5,7 +5,7 @@
  * scale + quaternion covariance, degree-3 SH colour, opacity) for one camera:
  *
  *   gs_project      EWA projection + SH colour, one thread per Gaussian
- *   gs_bin_sort     tile binning: (tile, depth) keys, onesweep radix sort, per-tile
+ *   gs_bin_sort     tile binning: (tile, depth) order by onesweep radix sorts, per-tile
  *                   ranges, records gathered into sorted order
  *   gs_render_fwd   per-tile front-to-back alpha compositing with early termination
  *   gs_render_bwd   L1 loss gradient and the reverse-order compositing backward
@@ -157,13 +157,15 @@ size_t gs_bin_sort_workspace_bytes(gs_dims dims, uint32_t capacity_K, int32_t wi
  * gs_bin_sort -- tile binning.  "Scaling 3D Gaussian Splatting with Distributed
  * Compute", memory-wall section (per-tile sorted lists of Gaussian-to-pixel
  * intersections) and trace section (one tile-intersection pass per Gaussian, one
- * offset pass per intersection).  Exclusive scan of count -> K; each visible
- * Gaussian emits one key (tile_id << 32 | fp32 bits of depth) per tile of its rect
- * in index order; a stable onesweep LSD radix sort (8-bit digits, decoupled
- * look-back with a bounded wait) over the low 32 + ceil(log2 tiles) key bits; tile
- * ranges; records gathered into key order.  The result per tile is the ordered
- * subsequence of the global (depth, index) order of the Gaussians whose rect
- * contains the tile.
+ * offset pass per intersection).  The result is that of a stable sort of one key
+ * (tile_id << 32 | fp32 bits of depth) per tile of each visible Gaussian's rect,
+ * emitted in index order: per tile, the ordered subsequence of the global (depth,
+ * index) order of the Gaussians whose rect contains the tile.  It is computed by
+ * two stable onesweep LSD radix sorts (8-bit digits, decoupled look-back with a
+ * bounded wait): the visible Gaussians by depth bits (4 passes), then one
+ * (tile, index) pair per intersection, emitted in depth order, by tile
+ * (ceil(log2 tiles / 8) passes); then tile ranges, the 64-bit keys and the
+ * records gathered into key order.
  *   proj      output of gs_project (read).
  *   workspace device scratch of at least gs_bin_sort_workspace_bytes(), 256-byte
  *             aligned; contents need not be initialised and are clobbered.
@@ -292,8 +294,8 @@ gs_status gs_project_bwd_adam(gs_dims dims, float* params, const gs_camera* cam,
  * in advance, embedders whose allocator owns the GPU).  The paper has no
  * counterpart; this is a library convenience.  Results are identical to
  * gs_bin_sort's.
- *   Scratch: a fixed array inside the library (15.0 MiB), held by every GPU
- *   that loads the library until the process exits.  It is used in place of the
+ *   Scratch: a fixed array inside the library (68.5 MiB), held by every GPU
+ *   that calls this entry point until the process exits.  It is used in place of the
  *   workspace argument; the caller still passes proj and bins.
  *   Limits: n <= GS_NOALLOC_MAX_N, capacity_K <= GS_NOALLOC_MAX_K, at most
  *   GS_NOALLOC_MAX_TILES tiles; larger sizes return GS_ERR_SCRATCH_LIMIT and
