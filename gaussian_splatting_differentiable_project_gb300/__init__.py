@@ -299,4 +299,4 @@ def version() -> str:
     return load().gs_version().decode()
 
 
-from .trainer import Trainer  # noqa: E402  (re-export)
+from .trainer import HostTargets, Trainer  # noqa: E402  (re-export)

@@ -225,15 +225,72 @@ __global__ void __launch_bounds__(256)
 // block start are multiples of 256) that no other CTA touches, and phase 1 reads
 // them before phase 2 writes them.
 constexpr int kFusedBlock = 256;
+constexpr int kChunkPlanes = 8;                                       // planes per streamed chunk
+constexpr int kChunks = (kPlanes + kChunkPlanes - 1) / kChunkPlanes;  // 8
+constexpr int kRow4 = kFusedBlock / 4;                                // float4 per plane row of a group
+constexpr size_t kChunkBytes = size_t(kChunkPlanes) * kRow4 * 16;     // one array's share of a chunk
+constexpr size_t kFusedDynSmem = 2 * 3 * kChunkBytes;                 // p, m, v, double-buffered: 48 KB
 
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst));
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Streams the parameters and moments of one group through shared memory in chunks of
+// kChunkPlanes planes: p, m and v of chunk c land in buffer c & 1.
+struct ChunkStream {
+  float4* buf;  // [2][3][kChunkPlanes][kRow4]
+  __device__ __forceinline__ float4* at(int b, int arr) const {
+    return buf + (size_t(b) * 3 + arr) * (kChunkPlanes * kRow4);
+  }
+  // every thread: issue its share of chunk c of group b0 into buffer b, one commit group
+  __device__ __forceinline__ void issue(int c, int b, const float* P, const float* M, const float* V, int64_t n_pad,
+                                        int64_t b0) const {
+    const int pl0 = c * kChunkPlanes;
+    const int np = min(kChunkPlanes, kPlanes - pl0);
+    for (int e = threadIdx.x; e < np * kRow4; e += kFusedBlock) {
+      const int64_t g = int64_t(pl0 + e / kRow4) * n_pad + b0 + int64_t(e % kRow4) * 4;
+      cp_async16(at(b, 0) + e, P + g);
+      cp_async16(at(b, 1) + e, M + g);
+      cp_async16(at(b, 2) + e, V + g);
+    }
+    cp_async_commit();
+  }
+};
+
+// Fused projection backward + Adam over groups of 256 Gaussians.  Phase 1: one thread
+// per Gaussian runs the chain rule and leaves 30 factors in shared memory (11
+// geometric gradients, 16 SH basis values, 3 colour factors; an SH coefficient's
+// gradient is basis value x colour factor).  Phase 2: the 59 planes of the group
+// stream through shared memory in chunks of 8 planes (cp.async, double-buffered,
+// the first two chunks issued before phase 1 so that the chain rule overlaps the
+// loads); each element gets its gradient from the factors and the Adam update, and
+// p, m, v are written back.  The gradient planes are never written.
 __global__ void __launch_bounds__(kFusedBlock, 2)
     k_project_bwd_adam(float* P, int64_t n, int64_t n_pad, CamDev cam, const uint32_t* __restrict__ count,
                        const float* __restrict__ g2, float* M, float* V, AdamParams a) {
   __shared__ float s_geo[11][kFusedBlock];
   __shared__ float s_Y[16][kFusedBlock];
   __shared__ float s_gc[3][kFusedBlock];
+  extern __shared__ __align__(16) unsigned char fused_smem[];
+  const ChunkStream cs{reinterpret_cast<float4*>(fused_smem)};
   const int tid = threadIdx.x;
-  for (int64_t b0 = int64_t(blockIdx.x) * kFusedBlock; b0 < n_pad; b0 += int64_t(gridDim.x) * kFusedBlock) {
+  const int64_t gstride = int64_t(gridDim.x) * kFusedBlock;
+  int64_t b0 = int64_t(blockIdx.x) * kFusedBlock;
+  if (b0 < n_pad) {
+    cs.issue(0, 0, P, M, V, n_pad, b0);
+    cs.issue(1, 1, P, M, V, n_pad, b0);
+  }
+  for (; b0 < n_pad; b0 += gstride) {
+    // the next group's first two chunks are issued into the buffers that this
+    // group's last two chunks free, so its loads overlap this group's tail and the
+    // next chain rule
+    const bool has_next = b0 + gstride < n_pad;
     {
       ChainOut o;
       const bool vis = chain_rule<false>(P, n, n_pad, b0 + tid, cam, count, g2, o);
@@ -244,34 +301,47 @@ __global__ void __launch_bounds__(kFusedBlock, 2)
 #pragma unroll
       for (int k = 0; k < 3; ++k) s_gc[k][tid] = vis ? o.gcol[k] : 0.0f;
     }
-    __syncthreads();
-    constexpr int kRow4 = kFusedBlock / 4;  // float4 per plane row of the block
-#pragma unroll 4
-    for (int e4 = tid; e4 < kPlanes * kRow4; e4 += kFusedBlock) {
-      const int pl = e4 / kRow4, q = (e4 % kRow4) * 4;
-      const int64_t base = int64_t(pl) * n_pad + b0 + q;
-      float4 pp = *reinterpret_cast<const float4*>(P + base);
-      float4 mm = *reinterpret_cast<const float4*>(M + base);
-      float4 vv = *reinterpret_cast<const float4*>(V + base);
-      float g[4];
-      if (pl < 11) {
+#pragma unroll 1
+    for (int c = 0; c < kChunks; ++c) {
+      if (c + 1 < kChunks || has_next)
+        cp_async_wait<1>();
+      else
+        cp_async_wait<0>();
+      __syncthreads();  // chunk c landed for every thread; phase 1 factors visible
+      const int b = c & 1;
+      const int pl0 = c * kChunkPlanes;
+      const int np = min(kChunkPlanes, kPlanes - pl0);
+      const float4* sp = cs.at(b, 0);
+      const float4* sm = cs.at(b, 1);
+      const float4* sv = cs.at(b, 2);
+      for (int e = tid; e < np * kRow4; e += kFusedBlock) {
+        const int pl = pl0 + e / kRow4, q = (e % kRow4) * 4;
+        float4 pp = sp[e], mm = sm[e], vv = sv[e];
+        float g[4];
+        if (pl < 11) {
 #pragma unroll
-        for (int k = 0; k < 4; ++k) g[k] = s_geo[pl][q + k];
-      } else {
-        const int kk = (pl - 11) / 3, ch = (pl - 11) % 3;
+          for (int k = 0; k < 4; ++k) g[k] = s_geo[pl][q + k];
+        } else {
+          const int kk = (pl - 11) / 3, ch = (pl - 11) % 3;
 #pragma unroll
-        for (int k = 0; k < 4; ++k) g[k] = s_Y[kk][q + k] * s_gc[ch][q + k];
+          for (int k = 0; k < 4; ++k) g[k] = s_Y[kk][q + k] * s_gc[ch][q + k];
+        }
+        const float step = a.step[pl];
+        adam_elem(pp.x, mm.x, vv.x, g[0], step, a);
+        adam_elem(pp.y, mm.y, vv.y, g[1], step, a);
+        adam_elem(pp.z, mm.z, vv.z, g[2], step, a);
+        adam_elem(pp.w, mm.w, vv.w, g[3], step, a);
+        const int64_t base = int64_t(pl) * n_pad + b0 + q;
+        *reinterpret_cast<float4*>(P + base) = pp;
+        *reinterpret_cast<float4*>(M + base) = mm;
+        *reinterpret_cast<float4*>(V + base) = vv;
       }
-      const float step = a.step[pl];
-      adam_elem(pp.x, mm.x, vv.x, g[0], step, a);
-      adam_elem(pp.y, mm.y, vv.y, g[1], step, a);
-      adam_elem(pp.z, mm.z, vv.z, g[2], step, a);
-      adam_elem(pp.w, mm.w, vv.w, g[3], step, a);
-      *reinterpret_cast<float4*>(P + base) = pp;
-      *reinterpret_cast<float4*>(M + base) = mm;
-      *reinterpret_cast<float4*>(V + base) = vv;
+      __syncthreads();  // buffer b free
+      if (c + 2 < kChunks)
+        cs.issue(c + 2, b, P, M, V, n_pad, b0);
+      else if (has_next)
+        cs.issue(c + 2 - kChunks, b, P, M, V, n_pad, b0 + gstride);
     }
-    __syncthreads();
   }
 }
 
@@ -299,8 +369,15 @@ extern "C" gs_status gs_project_bwd_adam(gs_dims dims, float* params, const gs_c
   if (!aligned(params, 16) || !aligned(grad2d, 16) || !aligned(m, 16) || !aligned(v, 16)) return GS_ERR_INVALID_ARG;
   AdamParams a;
   if (!make_adam_params(lr_plane, beta1, beta2, eps, t, a)) return GS_ERR_INVALID_ARG;
-  const int blocks = grid_for(dims.n_pad, kFusedBlock, kSmCount * 64);
-  k_project_bwd_adam<<<blocks, kFusedBlock, 0, stream>>>(params, dims.n, dims.n_pad, cam_dev(*cam), proj->count, grad2d, m,
-                                                 v, a);
+  static bool attr_set = false;
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(k_project_bwd_adam, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kFusedDynSmem)) !=
+        cudaSuccess)
+      return GS_ERR_CUDA;
+    attr_set = true;
+  }
+  const int blocks = grid_for(dims.n_pad / kFusedBlock, 1, kSmCount * 2);
+  k_project_bwd_adam<<<blocks, kFusedBlock, kFusedDynSmem, stream>>>(params, dims.n, dims.n_pad, cam_dev(*cam),
+                                                                     proj->count, grad2d, m, v, a);
   return launch_status();
 }

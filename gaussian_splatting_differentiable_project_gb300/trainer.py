@@ -16,6 +16,46 @@ from . import (BinBuffers, ProjBuffers, N_GRAD2D, SSIM_MAPS, adam_step, bin_sort
                render_bwd, render_fwd, ssim_bwd, ssim_fwd, status_str)
 
 
+class HostTargets:
+    """Double-buffered upload of per-step targets (3 x H x W fp32, pinned host memory).
+
+    ``put`` starts the upload of a host target into a free device slot on a copy
+    stream of its own and returns the slot; ``get`` orders a compute stream after that
+    upload; ``release`` marks the slot free once the work enqueued so far on the
+    compute stream is done.  The upload for the next step thus runs while the current
+    step computes."""
+
+    def __init__(self, shape, device="cuda", slots: int = 2):
+        import torch
+        self.bufs = [torch.empty(shape, dtype=torch.float32, device=device) for _ in range(slots)]
+        self.copied = [torch.cuda.Event() for _ in range(slots)]
+        self.consumed = [torch.cuda.Event() for _ in range(slots)]
+        self.used = [False] * slots
+        self.stream = torch.cuda.Stream(device=device)
+        self.next = 0
+
+    def put(self, host) -> int:
+        import torch
+        k = self.next
+        self.next = (k + 1) % len(self.bufs)
+        with torch.cuda.stream(self.stream):
+            if self.used[k]:
+                self.stream.wait_event(self.consumed[k])
+            self.bufs[k].copy_(host, non_blocking=True)
+            self.copied[k].record(self.stream)
+        self.used[k] = True
+        return k
+
+    def get(self, k: int, stream=None):
+        import torch
+        (stream or torch.cuda.current_stream()).wait_event(self.copied[k])
+        return self.bufs[k]
+
+    def release(self, k: int, stream=None) -> None:
+        import torch
+        self.consumed[k].record(stream or torch.cuda.current_stream())
+
+
 class Trainer:
     def __init__(self, params, n: int, width: int, height: int, capacity: int, lr_plane, betas=(0.9, 0.999),
                  eps: float = 1e-15, bg=(0.0, 0.0, 0.0), device="cuda", fused: bool = True, dssim: float = 0.0):
@@ -90,6 +130,11 @@ class Trainer:
         self.t += 1
         project_bwd_adam(self.n, self.params, cam, self.proj, self.grad2d, self.m, self.v, self.lr_plane, self.beta1,
                          self.beta2, self.eps, self.t, self.status, stream)
+
+    def step_staged(self, cam: dict, targets: HostTargets, slot: int, stream=None) -> None:
+        """``step`` against the target uploaded into ``slot`` of ``targets``."""
+        self.step(cam, targets.get(slot, stream), stream)
+        targets.release(slot, stream)
 
     # host-side reads (synchronise) -----------------------------------------------
     def total_loss(self) -> float:
