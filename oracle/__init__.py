@@ -19,6 +19,7 @@ against closed forms, invariants, library routines and finite differences.
 from __future__ import annotations
 
 import ctypes
+import math
 import os
 import subprocess
 import threading
@@ -237,6 +238,49 @@ def adam(p, g, m, v, lr_plane, beta1: float, beta2: float, eps: float, t: int):
     lr = _c(lr_plane, np.float64)
     _load().or_adam(_ptr(p), _ptr(g), _ptr(m), _ptr(v), planes, stride, _ptr(lr), beta1, beta2, eps, int(t))
     return p, m, v
+
+
+def batch_hyper(batch: int, lr_plane, beta1: float, beta2: float, eps: float):
+    """Adam hyperparameters for a step over ``batch`` views ("Scaling 3D Gaussian
+    Splatting with Distributed Compute", batch-size section): learning rates times
+    sqrt(batch), epsilon divided by sqrt(batch), and each momentum coefficient by the
+    linearisation 1 - batch (1 - beta) of beta^batch (the page's formula did not
+    survive; this reading makes beta1 = 0.9 reach zero at batch 10, as the page
+    states), clamped at zero beyond that."""
+    s = math.sqrt(batch)
+    lr = np.asarray(lr_plane, np.float64) * s
+    return lr, max(0.0, 1.0 - batch * (1.0 - beta1)), max(0.0, 1.0 - batch * (1.0 - beta2)), eps / s
+
+
+def step_batch(params, n: int, cams, targets, m, v, t: int, lr_plane, beta1=0.9, beta2=0.999, eps=1e-15,
+               bg=(0.0, 0.0, 0.0), dssim: float = 0.0) -> dict:
+    """One optimisation step over several views: the loss is the mean of the per-view
+    losses, so each view's loss gradient carries 1 / batch; the per-view parameter
+    gradients are summed and one Adam step with ``batch_hyper`` follows."""
+    B = len(cams)
+    assert B >= 1 and len(targets) == B
+    n_pad = params.shape[1]
+    grads = np.zeros((N_PLANES, n_pad), np.float64)
+    loss = 0.0
+    views = []
+    for cam, target in zip(cams, targets):
+        pr = project(params, n, cam, 32)
+        W, H = int(cam["width"]), int(cam["height"])
+        if dssim > 0.0:
+            img = render(pr, W, H, bg, None, 32)["image"]
+            s_val, extra = ssim(img.astype(np.float64), np.asarray(target, np.float64), dssim / B)
+            rd = render(pr, W, H, bg, target, 32, l1_weight=(1.0 - dssim) / B, dLdC_extra=extra)
+            rd["ssim"] = s_val
+            rd["loss"] += dssim * (1.0 - s_val) / B
+        else:
+            rd = render(pr, W, H, bg, target, 32, l1_weight=1.0 / B)
+        grads[:, :n] += project_bwd(params, n, cam, rd["grad2d"], 32)
+        loss += rd["loss"]
+        views.append({"proj": pr, "render": rd})
+    lr_b, b1, b2, eps_b = batch_hyper(B, lr_plane, beta1, beta2, eps)
+    p1, m1, v1 = adam(params.astype(np.float64), grads, m, v, lr_b, b1, b2, eps_b, t)
+    return {"views": views, "grads": grads, "loss": loss, "params": p1, "m": m1, "v": v1,
+            "hyper": (lr_b, b1, b2, eps_b)}
 
 
 def step(params, n: int, cam: dict, target, m, v, t: int, lr_plane, beta1=0.9, beta2=0.999, eps=1e-15,

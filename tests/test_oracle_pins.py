@@ -621,3 +621,68 @@ def test_whole_step_gradient_with_dssim_matches_finite_differences():
             d2, e2 = central(i, pl, h / 2)
             fd = (d2 * e1 * e1 - d1 * e2 * e2) / (e1 * e1 - e2 * e2)
             assert abs(fd - an[pl, i]) <= 2e-4 * abs(fd) + 2e-7 * np.abs(an).max(), (i, pl, fd, an[pl, i])
+
+
+# ----------------------------------------------------------------------------- batched step
+
+def test_batch_hyperparameters_follow_the_pages():
+    """"Scaling 3D Gaussian Splatting with Distributed Compute", batch-size section:
+    learning rates grow as sqrt(BS), epsilon shrinks as 1/sqrt(BS), and the momentum
+    linearisation takes beta1 = 0.9 to zero at BS = 10 (held at zero beyond)."""
+    lr = np.full(59, 1e-3)
+    for B, b1, b2 in ((1, 0.9, 0.999), (4, 0.6, 0.996), (10, 0.0, 0.99)):
+        lr_b, c1, c2, e = oracle.batch_hyper(B, lr, 0.9, 0.999, 1e-15)
+        np.testing.assert_allclose(lr_b, 1e-3 * np.sqrt(B), rtol=1e-15)
+        assert abs(c1 - b1) < 1e-12 and abs(c2 - b2) < 1e-12, (B, c1, c2)
+        assert abs(e - 1e-15 / np.sqrt(B)) < 1e-30
+    assert oracle.batch_hyper(12, lr, 0.9, 0.999, 1e-15)[1] == 0.0
+
+
+def _two_views(seed=11):
+    P, n, cam = _fd_scene(n=6, seed=seed)
+    cam2 = gi.camera((-0.5, 0.35, 2.8), 32, 32)
+    pr1, pr2 = oracle.project(P, n, cam, 32), oracle.project(P, n, cam2, 32)
+    t1 = gi.offset_target(oracle.render(pr1, 32, 32)["image"], seed=21)
+    t2 = gi.offset_target(oracle.render(pr2, 32, 32)["image"], seed=22)
+    return P, n, [cam, cam2], [t1, t2]
+
+
+def test_batch_of_one_is_the_single_view_step():
+    P, n, cams, targets = _two_views()
+    z = np.zeros((59, P.shape[1]))
+    a = oracle.step(P, n, cams[0], targets[0], z, z, 1, gi.lr_planes())
+    b = oracle.step_batch(P, n, cams[:1], targets[:1], z, z, 1, gi.lr_planes())
+    np.testing.assert_array_equal(b["grads"], a["grads"])
+    for k in ("params", "m", "v"):
+        np.testing.assert_allclose(b[k], a[k], rtol=1e-15, atol=0)
+
+
+def test_batch_gradient_is_the_mean_of_view_gradients():
+    """The batch loss is the mean of the view losses, so its gradient is the mean of
+    the single-view gradients (a dropped 1/BS or a missing view fails)."""
+    P, n, cams, targets = _two_views()
+    z = np.zeros((59, P.shape[1]))
+    g1 = oracle.step(P, n, cams[0], targets[0], z, z, 1, gi.lr_planes())["grads"]
+    g2 = oracle.step(P, n, cams[1], targets[1], z, z, 1, gi.lr_planes())["grads"]
+    r = oracle.step_batch(P, n, cams, targets, z, z, 1, gi.lr_planes())
+    assert np.abs(g1 - g2).max() > 1e-3 * np.abs(g1).max()
+    np.testing.assert_allclose(r["grads"], 0.5 * (g1 + g2), rtol=1e-12, atol=1e-18)
+    l1 = oracle.step(P, n, cams[0], targets[0], z, z, 1, gi.lr_planes())["render"]["loss"]
+    l2 = oracle.step(P, n, cams[1], targets[1], z, z, 1, gi.lr_planes())["render"]["loss"]
+    assert abs(r["loss"] - 0.5 * (l1 + l2)) < 1e-12
+
+
+def test_batch_first_step_moves_by_sqrt_batch_lr():
+    """Four identical views: the gradient is the single view's, and the first Adam
+    step from zero moments moves each parameter by lr sqrt(4) sign(g) where |g| is
+    far above epsilon / sqrt(4)."""
+    P, n, cams, targets = _two_views()
+    z = np.zeros((59, P.shape[1]))
+    g = oracle.step(P, n, cams[0], targets[0], z, z, 1, gi.lr_planes())["grads"]
+    r = oracle.step_batch(P, n, [cams[0]] * 4, [targets[0]] * 4, z, z, 1, gi.lr_planes())
+    np.testing.assert_allclose(r["grads"], g, rtol=1e-12, atol=1e-18)
+    lr = np.asarray(gi.lr_planes(), np.float64)[:, None]
+    big = np.abs(g) > 1e-6  # epsilon / sqrt(4) is below 1e-9 of these
+    expect = P.astype(np.float64) - 2.0 * lr * np.sign(g)
+    assert big.sum() > 50
+    np.testing.assert_allclose(r["params"][big], expect[big], rtol=0, atol=1e-11)  # a flip moves by >= 2.5e-4
