@@ -39,6 +39,7 @@ sys.path.insert(0, ROOT)
 import gs_inputs as gi  # noqa: E402
 
 METRIC = "train steps/s (fwd+bwd+Adam, 1 view) at 4M Gaussians 2048²; % of roofline"
+METRIC_BATCH = "train steps/s ({B} views per step: fwd+bwd per view, one Adam) at 4M Gaussians 2048²"
 STAGES_SEPARATE = ["project", "bin_sort", "render_fwd", "render_bwd", "project_bwd", "adam"]
 STAGES_FUSED = ["project", "bin_sort", "render_fwd", "render_bwd", "project_bwd_adam"]
 
@@ -58,6 +59,9 @@ def parse():
                     help="run the projection backward and Adam as two calls instead of gs_project_bwd_adam")
     ap.add_argument("--views", type=int, default=0,
                     help="use only the first N orbit views (profiling runs; 0 = all)")
+    ap.add_argument("--batch", type=int, default=1,
+                    help="views per optimisation step (batch-size scaling of the Adam hyperparameters); the "
+                         "headline is one view per step")
     ap.add_argument("--dssim", type=float, default=0.0,
                     help="D-SSIM weight lambda: the loss becomes (1 - lambda) L1 + lambda (1 - SSIM) (0 = L1)")
     return ap.parse_args()
@@ -385,7 +389,16 @@ def run_gb300(args, cfg, ws, rank, local):
     tr.raise_on_status()
     setup_s = time.time() - t_setup
 
+    B = max(1, args.batch)
+
+    def views_of(s):
+        return [(s * B + k) % V_views for k in range(B)]
+
     def step(s, events=None):
+        if B > 1:
+            vs = views_of(s)
+            tr.step_batch([cams[v] for v in vs], [targets[v] for v in vs])
+            return
         v = s % V_views
         cam = cams[v]
         if events is None:
@@ -438,7 +451,7 @@ def run_gb300(args, cfg, ws, rank, local):
         torch.cuda.nvtx.range_push("timed")
         t_start.record()
         for s in range(K):
-            step(args.warmup + s, ev[s])
+            step(args.warmup + s, ev[s] if B == 1 else None)
         t_end.record()
         torch.cuda.nvtx.range_pop()
         torch.cuda.synchronize()
@@ -447,8 +460,8 @@ def run_gb300(args, cfg, ws, rank, local):
     ms = time_replicas(dist, timed, torch.cuda.synchronize, dev)
     clk = clocks.stop()
     tr.raise_on_status()
-    stage_ms = {name: float(np.mean([ev[s][i].elapsed_time(ev[s][i + 1]) for s in range(K)]))
-                for i, name in enumerate(STAGES)}
+    stage_ms = ({name: float(np.mean([ev[s][i].elapsed_time(ev[s][i + 1]) for s in range(K)]))
+                 for i, name in enumerate(STAGES)} if B == 1 else None)
     value = whole_job_rate(ws, K, ms)
 
     # ---------------------------------------------------------------- e2e leg
@@ -458,8 +471,8 @@ def run_gb300(args, cfg, ws, rank, local):
         host_t.copy_(targets)
         del targets
         torch.cuda.empty_cache()
-        staged = gs.HostTargets((3, H, W), dev)
-        loss_host = torch.empty((K, 2), dtype=torch.float32).pin_memory()
+        staged = gs.HostTargets((3, H, W), dev, slots=2 * B)
+        loss_host = torch.empty((K, max(2, B)), dtype=torch.float32).pin_memory()
 
         def timed_e2e():
             # each step's target is uploaded from pinned host memory on a copy stream
@@ -469,29 +482,35 @@ def run_gb300(args, cfg, ws, rank, local):
             b = torch.cuda.Event(enable_timing=True)
             a.record()
             staged.stream.wait_event(a)
-            slot = staged.put(host_t[args.warmup % V_views])
+            slots = [staged.put(host_t[v]) for v in views_of(args.warmup)]
             for s in range(K):
-                v = (args.warmup + s) % V_views
-                nxt = staged.put(host_t[(args.warmup + s + 1) % V_views]) if s + 1 < K else None
-                tr.step_staged(cams[v], staged, slot)
-                loss_host[s, 0:1].copy_(tr.loss, non_blocking=True)
-                if args.dssim > 0:
-                    loss_host[s, 1:2].copy_(tr.ssim_val, non_blocking=True)
-                slot = nxt
+                vs = views_of(args.warmup + s)
+                nxt = [staged.put(host_t[v]) for v in views_of(args.warmup + s + 1)] if s + 1 < K else None
+                if B == 1:
+                    tr.step_staged(cams[vs[0]], staged, slots[0])
+                    loss_host[s, 0:1].copy_(tr.loss, non_blocking=True)
+                    if args.dssim > 0:
+                        loss_host[s, 1:2].copy_(tr.ssim_val, non_blocking=True)
+                else:
+                    tr.step_batch([cams[v] for v in vs], [staged.get(sl) for sl in slots])
+                    for sl in slots:
+                        staged.release(sl)
+                    loss_host[s, :B].copy_(tr.batch_losses, non_blocking=True)
+                slots = nxt
             b.record()
             torch.cuda.synchronize()
             return a.elapsed_time(b)
 
         ms_e2e = time_replicas(dist, timed_e2e, torch.cuda.synchronize, dev)
-        e2e = {"value": whole_job_rate(ws, K, ms_e2e), "unit": "steps/s", "h2d_bytes_per_step": 3 * H * W * 4,
-               "d2h_bytes_per_step": 8 if args.dssim > 0 else 4, "ms_per_step": ms_e2e / K}
+        e2e = {"value": whole_job_rate(ws, K, ms_e2e), "unit": "steps/s", "h2d_bytes_per_step": B * 3 * H * W * 4,
+               "d2h_bytes_per_step": 4 * B if B > 1 else (8 if args.dssim > 0 else 4), "ms_per_step": ms_e2e / K}
         del host_t
 
     if rank != 0:
         return
 
     # ---------------------------------------------------------------- roofline
-    views = [(args.warmup + s) % V_views for s in range(K)]
+    views = [v for s in range(K) for v in views_of(args.warmup + s)]
     Kmean = float(np.mean([Ks[v] for v in views]))
     Vmean = float(np.mean([Vs[v] for v in views]))
     Emean = float(np.mean([E[v] for v in views]))
@@ -510,7 +529,10 @@ def run_gb300(args, cfg, ws, rank, local):
     for row in rows_all:
         row_t[row] = max(byt[row] / (peak_bw * 1e9), flops.get(row, 0.0) / (peak_fp32 * 1e12))
     t_star = sum(row_t.values())
-    for name in STAGES:
+    if B > 1:
+        # a batch step: every row but Adam once per view, Adam once
+        t_star = B * sum(t for r, t in row_t.items() if r != "adam") + row_t["adam"]
+    for name in (STAGES if B == 1 else []):
         rows = STAGE_ROWS[name]
         t_meas = stage_ms[name] / 1e3
         t_rows = sum(row_t[r] for r in rows)
@@ -519,16 +541,18 @@ def run_gb300(args, cfg, ws, rank, local):
         bound = "alu" if fl / (peak_fp32 * 1e12) > moved / (peak_bw * 1e9) else "hbm"
         per_stage[name] = {"ms": stage_ms[name], "bound": bound, "rows": rows,
                            "gbs": moved / t_meas / 1e9, "tflops": fl / t_meas / 1e12, "frac": t_rows / t_meas}
-    dom = max(STAGES, key=lambda s: stage_ms[s])
-    d = per_stage[dom]
-    traffic = measured_traffic({"render_fwd": "k_render_fwd", "render_bwd": "k_render_bwd"}.get(dom, ""))
-    if d["bound"] == "hbm":
-        roof = {"kernel": dom, "bound": "hbm", "achieved": d["gbs"], "peak": peak_bw, "unit": "GB/s",
-                "frac": d["gbs"] / peak_bw, "traffic": traffic, "peak_source": _peak_src("hbm_gbs")}
-    else:
-        roof = {"kernel": dom, "bound": "alu", "achieved": d["tflops"], "peak": peak_fp32, "unit": "TFLOP/s",
-                "frac": d["tflops"] / peak_fp32, "traffic": traffic,
-                "peak_source": f"152 SMs x 128 FP32 lanes x 2 x {sm_mhz:.0f} MHz"}
+    roof = None  # a batch step has no per-stage events (they are taken at one view per step)
+    if B == 1:
+        dom = max(STAGES, key=lambda s: stage_ms[s])
+        d = per_stage[dom]
+        traffic = measured_traffic({"render_fwd": "k_render_fwd", "render_bwd": "k_render_bwd"}.get(dom, ""))
+        if d["bound"] == "hbm":
+            roof = {"kernel": dom, "bound": "hbm", "achieved": d["gbs"], "peak": peak_bw, "unit": "GB/s",
+                    "frac": d["gbs"] / peak_bw, "traffic": traffic, "peak_source": _peak_src("hbm_gbs")}
+        else:
+            roof = {"kernel": dom, "bound": "alu", "achieved": d["tflops"], "peak": peak_fp32, "unit": "TFLOP/s",
+                    "frac": d["tflops"] / peak_fp32, "traffic": traffic,
+                    "peak_source": f"152 SMs x 128 FP32 lanes x 2 x {sm_mhz:.0f} MHz"}
 
     cpu = None
     if not args.no_cpu_baseline and ws == 1:
@@ -537,14 +561,16 @@ def run_gb300(args, cfg, ws, rank, local):
         except Exception as exc:  # the baseline is reported, never required
             cpu = {"value": None, "unit": "steps/s", "kind": "oracle", "error": repr(exc)}
 
-    launches_per_step = 1 + (9 + passes) + 1 + 2 + (2 if args.separate else 1) + (3 if args.dssim > 0 else 0)
+    per_view = 1 + (9 + passes) + 1 + 2 + 1 + (3 if args.dssim > 0 else 0)
+    launches_per_step = B * per_view + (1 if args.separate else 0)
     line = {
-        "metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": ws, "steps": K, "warmup": args.warmup,
+        "metric": METRIC if B == 1 else METRIC_BATCH.format(B=B), "value": value, "unit": "steps/s", "n_gpus": ws, "steps": K, "warmup": args.warmup,
         "ms_per_step": ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32", "data": "synthetic",
         "config": dict(_config_dict(cfg), parallelism=f"replicas{ws}", capacity_K=capacity,
                        objective=(f"{1 - args.dssim:g} L1 + {args.dssim:g} (1 - SSIM)" if args.dssim > 0 else "L1"),
-                       K_mean=Kmean, visible_mean=Vmean, pairs_bwd_mean=Emean),
+                       K_mean=Kmean, visible_mean=Vmean, pairs_bwd_mean=Emean, batch=B),
+        "views_per_s": value * B,
         "roofline": roof,
         "step_roofline_frac": t_star / (ms / K / 1e3),
         "stages_ms": stage_ms, "stages": per_stage,

@@ -100,10 +100,13 @@ def load(build_if_missing: bool = True):
         lib.gs_render_bwd.restype = st
         lib.gs_project_bwd.argtypes = [GsDims, P, ctypes.POINTER(GsCamera), ctypes.POINTER(GsProj), P, P, P, P]
         lib.gs_project_bwd.restype = st
+        lib.gs_project_bwd_accumulate.argtypes = [GsDims, P, ctypes.POINTER(GsCamera), ctypes.POINTER(GsProj), P, P,
+                                                  P, P]
+        lib.gs_project_bwd_accumulate.restype = st
         lib.gs_adam_step.argtypes = [GsDims, P, P, P, P, ctypes.POINTER(ctypes.c_float), ctypes.c_double,
                                      ctypes.c_double, ctypes.c_double, ctypes.c_int64, P]
         lib.gs_adam_step.restype = st
-        lib.gs_project_bwd_adam.argtypes = [GsDims, P, ctypes.POINTER(GsCamera), ctypes.POINTER(GsProj), P, P, P,
+        lib.gs_project_bwd_adam.argtypes = [GsDims, P, ctypes.POINTER(GsCamera), ctypes.POINTER(GsProj), P, P, P, P,
                                             ctypes.POINTER(ctypes.c_float), ctypes.c_double, ctypes.c_double,
                                             ctypes.c_double, ctypes.c_int64, P, P]
         lib.gs_project_bwd_adam.restype = st
@@ -272,6 +275,16 @@ def project_bwd(n: int, params, cam: dict, proj: ProjBuffers, grad2d, grads, dev
                                  _p(grad2d), _p(grads), _p(dev_status), _stream(stream)), "gs_project_bwd")
 
 
+def project_bwd_accumulate(n: int, params, cam: dict, proj: ProjBuffers, grad2d, grads, dev_status,
+                           stream=None) -> None:
+    """grads += the chain rule of this view's grad2d (a later view of a batch)."""
+    cc = camera(cam)
+    pc = proj.c()
+    _check(load().gs_project_bwd_accumulate(dims(n, params.shape[1]), _p(params), ctypes.byref(cc),
+                                            ctypes.byref(pc), _p(grad2d), _p(grads), _p(dev_status),
+                                            _stream(stream)), "gs_project_bwd_accumulate")
+
+
 def adam_step(n: int, params, grads, m, v, lr_plane, beta1: float, beta2: float, eps: float, t: int,
               stream=None) -> None:
     """Adam step number ``t`` (>= 1); bias corrections are formed inside the call."""
@@ -281,14 +294,16 @@ def adam_step(n: int, params, grads, m, v, lr_plane, beta1: float, beta2: float,
 
 
 def project_bwd_adam(n: int, params, cam: dict, proj: ProjBuffers, grad2d, m, v, lr_plane, beta1: float,
-                     beta2: float, eps: float, t: int, dev_status, stream=None) -> None:
-    """Projection backward and Adam step ``t`` in one pass (no gradient planes)."""
+                     beta2: float, eps: float, t: int, dev_status, stream=None, grads_in=None) -> None:
+    """Projection backward and Adam step ``t`` in one pass (no gradient planes);
+    ``grads_in``: gradients accumulated by earlier views of a batch, or None."""
     cc = camera(cam)
     pc = proj.c()
     lr = (ctypes.c_float * N_PLANES)(*[float(x) for x in lr_plane])
+    gin = _p(grads_in) if grads_in is not None else None
     _check(load().gs_project_bwd_adam(dims(n, params.shape[1]), _p(params), ctypes.byref(cc), ctypes.byref(pc),
-                                      _p(grad2d), _p(m), _p(v), lr, float(beta1), float(beta2), float(eps), int(t),
-                                      _p(dev_status), _stream(stream)), "gs_project_bwd_adam")
+                                      _p(grad2d), gin, _p(m), _p(v), lr, float(beta1), float(beta2), float(eps),
+                                      int(t), _p(dev_status), _stream(stream)), "gs_project_bwd_adam")
 
 
 def util_expf(x, y, stream=None) -> None:

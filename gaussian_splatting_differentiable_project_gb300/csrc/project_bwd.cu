@@ -195,23 +195,49 @@ __device__ __forceinline__ bool chain_rule(const float* P, int64_t n, int64_t n_
   return true;
 }
 
-__global__ void __launch_bounds__(256)
+// kAcc: add to G instead of overwriting it (culled Gaussians and padding untouched).
+template <bool kAcc>
+__global__ void __launch_bounds__(256, 2)
     k_project_bwd(const float* __restrict__ P, int64_t n, int64_t n_pad, CamDev cam, const uint32_t* __restrict__ count,
                   const float* __restrict__ g2, float* __restrict__ G) {
   const int64_t stride = int64_t(gridDim.x) * blockDim.x;
   for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n_pad; i += stride) {
     ChainOut o;
     if (!chain_rule(P, n, n_pad, i, cam, count, g2, o)) {
+      if (!kAcc) {
 #pragma unroll 4
-      for (int pl = 0; pl < kPlanes; ++pl) G[int64_t(pl) * n_pad + i] = 0.0f;
+        for (int pl = 0; pl < kPlanes; ++pl) G[int64_t(pl) * n_pad + i] = 0.0f;
+      }
       continue;
     }
+    if (!kAcc) {
 #pragma unroll
-    for (int pl = 0; pl < 11; ++pl) G[int64_t(pl) * n_pad + i] = o.geo[pl];
+      for (int pl = 0; pl < 11; ++pl) G[int64_t(pl) * n_pad + i] = o.geo[pl];
 #pragma unroll
-    for (int k = 0; k < 16; ++k)
+      for (int k = 0; k < 16; ++k)
 #pragma unroll
-      for (int ch = 0; ch < 3; ++ch) G[int64_t(11 + 3 * k + ch) * n_pad + i] = o.Y[k] * o.gcol[ch];
+        for (int ch = 0; ch < 3; ++ch) G[int64_t(11 + 3 * k + ch) * n_pad + i] = o.Y[k] * o.gcol[ch];
+      continue;
+    }
+    // accumulate: each group's old values are loaded before any of its stores (the
+    // compiler cannot reorder a later plane's load above an earlier plane's store,
+    // so one plane at a time would serialise 59 memory round trips)
+    {
+      float cur[11];
+#pragma unroll
+      for (int pl = 0; pl < 11; ++pl) cur[pl] = G[int64_t(pl) * n_pad + i];
+#pragma unroll
+      for (int pl = 0; pl < 11; ++pl) G[int64_t(pl) * n_pad + i] = cur[pl] + o.geo[pl];
+    }
+#pragma unroll
+    for (int k0 = 0; k0 < 16; k0 += 4) {
+      float cur[12];
+#pragma unroll
+      for (int q = 0; q < 12; ++q) cur[q] = G[int64_t(11 + 3 * k0 + q) * n_pad + i];
+#pragma unroll
+      for (int q = 0; q < 12; ++q)
+        G[int64_t(11 + 3 * k0 + q) * n_pad + i] = cur[q] + o.Y[k0 + q / 3] * o.gcol[q % 3];
+    }
   }
 }
 
@@ -229,7 +255,8 @@ constexpr int kChunkPlanes = 8;                                       // planes 
 constexpr int kChunks = (kPlanes + kChunkPlanes - 1) / kChunkPlanes;  // 8
 constexpr int kRow4 = kFusedBlock / 4;                                // float4 per plane row of a group
 constexpr size_t kChunkBytes = size_t(kChunkPlanes) * kRow4 * 16;     // one array's share of a chunk
-constexpr size_t kFusedDynSmem = 2 * 3 * kChunkBytes;                 // p, m, v, double-buffered: 48 KB
+// p, m, v (and the accumulated gradient when there is one), double-buffered: 48 / 64 KB
+constexpr size_t fused_dyn_smem(bool acc_in) { return 2 * (acc_in ? 4 : 3) * kChunkBytes; }
 
 __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
   const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst));
@@ -241,16 +268,19 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-// Streams the parameters and moments of one group through shared memory in chunks of
-// kChunkPlanes planes: p, m and v of chunk c land in buffer c & 1.
+// Streams the parameters and moments of one group (and the gradient accumulated by
+// earlier views when kAccIn) through shared memory in chunks of kChunkPlanes planes:
+// the arrays of chunk c land in buffer c & 1.
+template <bool kAccIn>
 struct ChunkStream {
-  float4* buf;  // [2][3][kChunkPlanes][kRow4]
+  static constexpr int kArrays = kAccIn ? 4 : 3;
+  float4* buf;  // [2][kArrays][kChunkPlanes][kRow4]
   __device__ __forceinline__ float4* at(int b, int arr) const {
-    return buf + (size_t(b) * 3 + arr) * (kChunkPlanes * kRow4);
+    return buf + (size_t(b) * kArrays + arr) * (kChunkPlanes * kRow4);
   }
   // every thread: issue its share of chunk c of group b0 into buffer b, one commit group
-  __device__ __forceinline__ void issue(int c, int b, const float* P, const float* M, const float* V, int64_t n_pad,
-                                        int64_t b0) const {
+  __device__ __forceinline__ void issue(int c, int b, const float* P, const float* M, const float* V,
+                                        const float* Gin, int64_t n_pad, int64_t b0) const {
     const int pl0 = c * kChunkPlanes;
     const int np = min(kChunkPlanes, kPlanes - pl0);
     for (int e = threadIdx.x; e < np * kRow4; e += kFusedBlock) {
@@ -258,6 +288,7 @@ struct ChunkStream {
       cp_async16(at(b, 0) + e, P + g);
       cp_async16(at(b, 1) + e, M + g);
       cp_async16(at(b, 2) + e, V + g);
+      if (kAccIn) cp_async16(at(b, 3) + e, Gin + g);
     }
     cp_async_commit();
   }
@@ -269,22 +300,25 @@ struct ChunkStream {
 // gradient is basis value x colour factor).  Phase 2: the 59 planes of the group
 // stream through shared memory in chunks of 8 planes (cp.async, double-buffered,
 // the first two chunks issued before phase 1 so that the chain rule overlaps the
-// loads); each element gets its gradient from the factors and the Adam update, and
+// loads); each element gets its gradient from the factors (plus, with kAccIn, the
+// gradient that earlier views of a batch accumulated in Gin) and the Adam update, and
 // p, m, v are written back.  The gradient planes are never written.
+template <bool kAccIn>
 __global__ void __launch_bounds__(kFusedBlock, 2)
     k_project_bwd_adam(float* P, int64_t n, int64_t n_pad, CamDev cam, const uint32_t* __restrict__ count,
-                       const float* __restrict__ g2, float* M, float* V, AdamParams a) {
+                       const float* __restrict__ g2, const float* __restrict__ Gin, float* M, float* V,
+                       AdamParams a) {
   __shared__ float s_geo[11][kFusedBlock];
   __shared__ float s_Y[16][kFusedBlock];
   __shared__ float s_gc[3][kFusedBlock];
   extern __shared__ __align__(16) unsigned char fused_smem[];
-  const ChunkStream cs{reinterpret_cast<float4*>(fused_smem)};
+  const ChunkStream<kAccIn> cs{reinterpret_cast<float4*>(fused_smem)};
   const int tid = threadIdx.x;
   const int64_t gstride = int64_t(gridDim.x) * kFusedBlock;
   int64_t b0 = int64_t(blockIdx.x) * kFusedBlock;
   if (b0 < n_pad) {
-    cs.issue(0, 0, P, M, V, n_pad, b0);
-    cs.issue(1, 1, P, M, V, n_pad, b0);
+    cs.issue(0, 0, P, M, V, Gin, n_pad, b0);
+    cs.issue(1, 1, P, M, V, Gin, n_pad, b0);
   }
   for (; b0 < n_pad; b0 += gstride) {
     // the next group's first two chunks are issued into the buffers that this
@@ -314,6 +348,7 @@ __global__ void __launch_bounds__(kFusedBlock, 2)
       const float4* sp = cs.at(b, 0);
       const float4* sm = cs.at(b, 1);
       const float4* sv = cs.at(b, 2);
+      const float4* sg = cs.at(b, kAccIn ? 3 : 2);
       for (int e = tid; e < np * kRow4; e += kFusedBlock) {
         const int pl = pl0 + e / kRow4, q = (e % kRow4) * 4;
         float4 pp = sp[e], mm = sm[e], vv = sv[e];
@@ -325,6 +360,13 @@ __global__ void __launch_bounds__(kFusedBlock, 2)
           const int kk = (pl - 11) / 3, ch = (pl - 11) % 3;
 #pragma unroll
           for (int k = 0; k < 4; ++k) g[k] = s_Y[kk][q + k] * s_gc[ch][q + k];
+        }
+        if (kAccIn) {
+          const float4 gi = sg[e];
+          g[0] += gi.x;
+          g[1] += gi.y;
+          g[2] += gi.z;
+          g[3] += gi.w;
         }
         const float step = a.step[pl];
         adam_elem(pp.x, mm.x, vv.x, g[0], step, a);
@@ -338,46 +380,77 @@ __global__ void __launch_bounds__(kFusedBlock, 2)
       }
       __syncthreads();  // buffer b free
       if (c + 2 < kChunks)
-        cs.issue(c + 2, b, P, M, V, n_pad, b0);
+        cs.issue(c + 2, b, P, M, V, Gin, n_pad, b0);
       else if (has_next)
-        cs.issue(c + 2 - kChunks, b, P, M, V, n_pad, b0 + gstride);
+        cs.issue(c + 2 - kChunks, b, P, M, V, Gin, n_pad, b0 + gstride);
     }
   }
 }
 
 }  // namespace gs
 
-extern "C" gs_status gs_project_bwd(gs_dims dims, const float* params, const gs_camera* cam, const gs_proj* proj,
-                                    const float* grad2d, float* grads, uint32_t* dev_status, cudaStream_t stream) {
+namespace {
+
+gs_status project_bwd_launch(gs_dims dims, const float* params, const gs_camera* cam, const gs_proj* proj,
+                             const float* grad2d, float* grads, uint32_t* dev_status, cudaStream_t stream, bool acc) {
   using namespace gs;
   if (!dims_ok(dims) || !camera_ok(cam) || !params || !proj || !proj->count || !grad2d || !grads || !dev_status)
     return GS_ERR_INVALID_ARG;
   if (!aligned(params, 16) || !aligned(grads, 16) || !aligned(grad2d, 16)) return GS_ERR_INVALID_ARG;
   const int blocks = grid_for(dims.n_pad, 256, kSmCount * 64);
-  k_project_bwd<<<blocks, 256, 0, stream>>>(params, dims.n, dims.n_pad, cam_dev(*cam), proj->count, grad2d, grads);
+  if (acc)
+    k_project_bwd<true><<<blocks, 256, 0, stream>>>(params, dims.n, dims.n_pad, cam_dev(*cam), proj->count, grad2d,
+                                                    grads);
+  else
+    k_project_bwd<false><<<blocks, 256, 0, stream>>>(params, dims.n, dims.n_pad, cam_dev(*cam), proj->count, grad2d,
+                                                     grads);
   return launch_status();
 }
 
-extern "C" gs_status gs_project_bwd_adam(gs_dims dims, float* params, const gs_camera* cam, const gs_proj* proj,
-                                         const float* grad2d, float* m, float* v, const float lr_plane[GS_N_PLANES],
-                                         double beta1, double beta2, double eps, int64_t t, uint32_t* dev_status,
-                                         cudaStream_t stream) {
+template <bool kAccIn>
+gs_status fused_launch(gs_dims dims, float* params, const gs_camera* cam, const gs_proj* proj, const float* grad2d,
+                       const float* grads_in, float* m, float* v, const gs::AdamParams& a, cudaStream_t stream) {
   using namespace gs;
-  if (!dims_ok(dims) || !camera_ok(cam) || !params || !proj || !proj->count || !grad2d || !m || !v || !lr_plane ||
-      !dev_status)
-    return GS_ERR_INVALID_ARG;
-  if (!aligned(params, 16) || !aligned(grad2d, 16) || !aligned(m, 16) || !aligned(v, 16)) return GS_ERR_INVALID_ARG;
-  AdamParams a;
-  if (!make_adam_params(lr_plane, beta1, beta2, eps, t, a)) return GS_ERR_INVALID_ARG;
   static bool attr_set = false;
+  const size_t smem = fused_dyn_smem(kAccIn);
   if (!attr_set) {
-    if (cudaFuncSetAttribute(k_project_bwd_adam, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kFusedDynSmem)) !=
+    if (cudaFuncSetAttribute(k_project_bwd_adam<kAccIn>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) !=
         cudaSuccess)
       return GS_ERR_CUDA;
     attr_set = true;
   }
   const int blocks = grid_for(dims.n_pad / kFusedBlock, 1, kSmCount * 2);
-  k_project_bwd_adam<<<blocks, kFusedBlock, kFusedDynSmem, stream>>>(params, dims.n, dims.n_pad, cam_dev(*cam),
-                                                                     proj->count, grad2d, m, v, a);
+  k_project_bwd_adam<kAccIn><<<blocks, kFusedBlock, smem, stream>>>(params, dims.n, dims.n_pad, cam_dev(*cam),
+                                                                     proj->count, grad2d, grads_in, m, v, a);
   return launch_status();
+}
+
+}  // namespace
+
+extern "C" gs_status gs_project_bwd(gs_dims dims, const float* params, const gs_camera* cam, const gs_proj* proj,
+                                    const float* grad2d, float* grads, uint32_t* dev_status, cudaStream_t stream) {
+  return project_bwd_launch(dims, params, cam, proj, grad2d, grads, dev_status, stream, false);
+}
+
+extern "C" gs_status gs_project_bwd_accumulate(gs_dims dims, const float* params, const gs_camera* cam,
+                                               const gs_proj* proj, const float* grad2d, float* grads,
+                                               uint32_t* dev_status, cudaStream_t stream) {
+  return project_bwd_launch(dims, params, cam, proj, grad2d, grads, dev_status, stream, true);
+}
+
+extern "C" gs_status gs_project_bwd_adam(gs_dims dims, float* params, const gs_camera* cam, const gs_proj* proj,
+                                         const float* grad2d, const float* grads_in, float* m, float* v,
+                                         const float lr_plane[GS_N_PLANES], double beta1, double beta2, double eps,
+                                         int64_t t, uint32_t* dev_status, cudaStream_t stream) {
+  using namespace gs;
+  if (!dims_ok(dims) || !camera_ok(cam) || !params || !proj || !proj->count || !grad2d || !m || !v || !lr_plane ||
+      !dev_status)
+    return GS_ERR_INVALID_ARG;
+  if (!aligned(params, 16) || !aligned(grad2d, 16) || !aligned(m, 16) || !aligned(v, 16) ||
+      (grads_in && !aligned(grads_in, 16)))
+    return GS_ERR_INVALID_ARG;
+  AdamParams a;
+  if (!make_adam_params(lr_plane, beta1, beta2, eps, t, a)) return GS_ERR_INVALID_ARG;
+  return grads_in ? fused_launch<true>(dims, params, cam, proj, grad2d, grads_in, m, v, a, stream)
+                  : fused_launch<false>(dims, params, cam, proj, grad2d, nullptr, m, v, a, stream);
 }

@@ -12,8 +12,21 @@ from __future__ import annotations
 
 import numpy as np
 
-from . import (BinBuffers, ProjBuffers, N_GRAD2D, SSIM_MAPS, adam_step, bin_sort, project, project_bwd, project_bwd_adam,
-               render_bwd, render_fwd, ssim_bwd, ssim_fwd, status_str)
+import math
+
+from . import (BinBuffers, ProjBuffers, N_GRAD2D, SSIM_MAPS, adam_step, bin_sort, project, project_bwd,
+               project_bwd_accumulate, project_bwd_adam, render_bwd, render_fwd, ssim_bwd, ssim_fwd, status_str)
+
+
+def batch_adam_hyper(batch: int, lr_plane, beta1: float, beta2: float, eps: float):
+    """Adam hyperparameters of a step over ``batch`` views ("Scaling 3D Gaussian
+    Splatting with Distributed Compute", batch-size section): learning rates scale
+    with sqrt(batch), epsilon with 1 / sqrt(batch), and the momentum coefficients
+    follow the linearisation 1 - batch (1 - beta) of beta^batch, held at zero where
+    it would go negative (beta1 = 0.9 reaches zero at batch 10)."""
+    root = math.sqrt(batch)
+    lr = np.asarray(lr_plane, np.float64) * root
+    return lr, max(0.0, 1.0 - batch * (1.0 - beta1)), max(0.0, 1.0 - batch * (1.0 - beta2)), eps / root
 
 
 class HostTargets:
@@ -97,16 +110,21 @@ class Trainer:
         bin_sort(self.n, self.n_pad, self.proj, cam, self.bins, self.status, stream)
         render_fwd(cam, self.bins, self.bg, self.image, self.T_final, self.n_contrib, self.status, stream)
 
-    def loss_backward(self, cam: dict, target, stream=None) -> None:
+    def loss_backward(self, cam: dict, target, stream=None, weight: float = 1.0, loss_out=None,
+                      ssim_out=None) -> None:
         """The loss and its gradient with respect to the projected quantities
-        (grad2d): the D-SSIM term first when lambda > 0, then the render backward."""
+        (grad2d): the D-SSIM term first when lambda > 0, then the render backward.
+        ``weight`` scales the whole loss (1 / batch for a view of a batch step);
+        ``loss_out`` / ``ssim_out`` default to the trainer's own scalars."""
         extra = None
         if self.dssim > 0.0:
-            ssim_fwd(self.image, target, self.dssim, self.ssim_maps, self.ssim_val, stream)
+            ssim_fwd(self.image, target, self.dssim * weight, self.ssim_maps,
+                     self.ssim_val if ssim_out is None else ssim_out, stream)
             ssim_bwd(self.image, target, self.ssim_maps, self.dLdC, stream)
             extra = self.dLdC
         render_bwd(self.n, self.n_pad, cam, self.bins, self.bg, self.image, target, self.T_final, self.n_contrib,
-                   self.grad2d, self.loss, self.status, stream, l1_weight=1.0 - self.dssim, dLdC_extra=extra)
+                   self.grad2d, self.loss if loss_out is None else loss_out, self.status, stream,
+                   l1_weight=(1.0 - self.dssim) * weight, dLdC_extra=extra)
 
     def backward(self, cam: dict, target, stream=None) -> None:
         self.loss_backward(cam, target, stream)
@@ -130,6 +148,46 @@ class Trainer:
         self.t += 1
         project_bwd_adam(self.n, self.params, cam, self.proj, self.grad2d, self.m, self.v, self.lr_plane, self.beta1,
                          self.beta2, self.eps, self.t, self.status, stream)
+
+    def step_batch(self, cams, targets, stream=None) -> None:
+        """One optimisation step over a batch of views: the loss is the mean of the
+        view losses.  The first view writes the gradient planes, later ones
+        accumulate into them, and the last view's projection backward runs fused with
+        Adam (adding the accumulated planes) under the batch-scaled hyperparameters;
+        with ``fused`` off the last view accumulates too and Adam runs on its own.
+        Per-view losses (weighted by 1 / batch) land in ``batch_losses``."""
+        import torch
+        B = len(cams)
+        if B < 1 or len(targets) != B:
+            raise ValueError("step_batch needs one target per camera")
+        if getattr(self, "batch_losses", None) is None or self.batch_losses.numel() != B:
+            self.batch_losses = torch.zeros(B, dtype=torch.float32, device=self.params.device)
+            if self.dssim > 0.0:
+                self.batch_ssim = torch.zeros(B, dtype=torch.float32, device=self.params.device)
+        lr_b, b1, b2, eps_b = batch_adam_hyper(B, self.lr_plane, self.beta1, self.beta2, self.eps)
+        self.t += 1
+        for k, (cam, target) in enumerate(zip(cams, targets)):
+            self.forward(cam, stream)
+            self.loss_backward(cam, target, stream, weight=1.0 / B, loss_out=self.batch_losses[k:k + 1],
+                               ssim_out=self.batch_ssim[k:k + 1] if self.dssim > 0.0 else None)
+            if self.fused and k == B - 1:
+                project_bwd_adam(self.n, self.params, cam, self.proj, self.grad2d, self.m, self.v, lr_b, b1, b2,
+                                 eps_b, self.t, self.status, stream, grads_in=self.grads if B > 1 else None)
+            elif k == 0:
+                project_bwd(self.n, self.params, cam, self.proj, self.grad2d, self.grads, self.status, stream)
+            else:
+                project_bwd_accumulate(self.n, self.params, cam, self.proj, self.grad2d, self.grads, self.status,
+                                       stream)
+        if not self.fused:
+            adam_step(self.n, self.params, self.grads, self.m, self.v, lr_b, b1, b2, eps_b, self.t, stream)
+
+    def batch_loss(self) -> float:
+        """The mean view loss of the last batch step (synchronises)."""
+        v = float(self.batch_losses.cpu().numpy().astype(np.float64).sum())
+        if self.dssim > 0.0:
+            s = self.batch_ssim.cpu().numpy().astype(np.float64)
+            v += self.dssim * float((1.0 - s).mean())
+        return v
 
     def step_staged(self, cam: dict, targets: HostTargets, slot: int, stream=None) -> None:
         """``step`` against the target uploaded into ``slot`` of ``targets``."""

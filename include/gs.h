@@ -11,7 +11,8 @@
  *   gs_render_bwd   L1 loss gradient and the reverse-order compositing backward
  *   gs_project_bwd  chain rule from the 2D gradients to the 59 parameters
  *   gs_adam_step    fused Adam update over every parameter plane
- *   (gs_project_bwd_adam: the last two in one pass)
+ *   (gs_project_bwd_adam: the last two in one pass; gs_project_bwd_accumulate sums
+ *   the gradients of several views of a batch)
  *
  * The method is the one "Toward Distributed 3D Gaussian Splatting for
  * High-Resolution Isosurface Visualization" (section III) trains and "Scaling 3D
@@ -256,6 +257,18 @@ gs_status gs_project_bwd(gs_dims dims, const float* params, const gs_camera* cam
                          const float* grad2d, float* grads, uint32_t* dev_status, cudaStream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * gs_project_bwd_accumulate -- gs_project_bwd adding into grads instead of
+ * overwriting it: grads += chain rule of this view's grad2d (entries of culled
+ * Gaussians and padding are left as they are).  For a step over a batch of views
+ * ("Scaling 3D Gaussian Splatting with Distributed Compute", batch-size section):
+ * the first view writes with gs_project_bwd, later ones accumulate, and each view's
+ * loss gradient carries its 1 / batch weight through gs_render_bwd's l1_weight.
+ *   grads  59 x n_pad fp32 (read and write).  Other arguments and errors as
+ *   gs_project_bwd. */
+gs_status gs_project_bwd_accumulate(gs_dims dims, const float* params, const gs_camera* cam, const gs_proj* proj,
+                                    const float* grad2d, float* grads, uint32_t* dev_status, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------
  * gs_adam_step -- fused Adam over all 59 planes (padding included).  "Scaling 3D
  * Gaussian Splatting with Distributed Compute", DDP background (two moments per
  * parameter) and step walkthrough (Adam over the rank's own parameters).
@@ -281,11 +294,14 @@ gs_status gs_adam_step(gs_dims dims, float* params, const float* grads, float* m
  * separate calls when the gradients themselves are wanted.
  *   params  59 x n_pad (read, then updated in place); proj, grad2d as for
  *   gs_project_bwd; m, v, lr_plane, beta1, beta2, eps, t as for gs_adam_step.
+ *   grads_in null, or 59 x n_pad fp32 (read, 16-byte aligned): gradients that earlier
+ *   views of a batch accumulated, added to this view's before the update (the last
+ *   view of a batch step; the batch's scaled hyperparameters are the caller's).
  * Errors: the union of gs_project_bwd's and gs_adam_step's. */
 gs_status gs_project_bwd_adam(gs_dims dims, float* params, const gs_camera* cam, const gs_proj* proj,
-                              const float* grad2d, float* m, float* v, const float lr_plane[GS_N_PLANES],
-                              double beta1, double beta2, double eps, int64_t t, uint32_t* dev_status,
-                              cudaStream_t stream);
+                              const float* grad2d, const float* grads_in, float* m, float* v,
+                              const float lr_plane[GS_N_PLANES], double beta1, double beta2, double eps, int64_t t,
+                              uint32_t* dev_status, cudaStream_t stream);
 
 /* ---------------------------------------------------------------------------
  * gs_bin_sort_noalloc -- gs_bin_sort for callers that must not allocate device

@@ -465,6 +465,67 @@ def test_staged_host_targets_feed_the_right_step(case):
     np.testing.assert_allclose(lb, la, rtol=1e-5)
 
 
+def _batch_cams(case, B=3):
+    cfg, cam = case["cfg"], case["cam"]
+    W, H = cam["width"], cam["height"]
+    if cfg.kind == "cube":
+        return [gi.camera(pos, W, H) for pos in ((0.0, 0.0, 3.0), (0.6, -0.4, 2.8), (-0.5, 0.5, 2.9))][:B]
+    cams = gi.fibonacci_cameras(cfg.n_views, W, H)
+    return [cams[k] for k in (3, 9, 20)][:B]
+
+
+@pytest.mark.parametrize("fused", [False, True], ids=["separate", "fused"])
+def test_batch_step_matches_oracle(case, fused):
+    """A step over three views ("Scaling 3D Gaussian Splatting with Distributed
+    Compute", batch-size section): the mean of the view losses, gradients summed
+    through gs_project_bwd_accumulate (or, fused, added inside gs_project_bwd_adam),
+    one Adam step with lr sqrt(3), eps / sqrt(3) and betas 1 - 3 (1 - beta)."""
+    P, n = case["P"], case["n"]
+    cams = _batch_cams(case)
+    targets = [gi.offset_target(oracle.render(oracle.project(P, n, c, 32), c["width"], c["height"])["image"],
+                                seed=60 + k) for k, c in enumerate(cams)]
+    z = np.zeros((59, P.shape[1]))
+    ref = oracle.step_batch(P, n, cams, targets, z, z, 1, gi.lr_planes())
+    W, H = cams[0]["width"], cams[0]["height"]
+    tr = gs.Trainer(P, n, W, H, capacity=1 << 20, lr_plane=gi.lr_planes(), fused=fused)
+    tr.step_batch(cams, [torch.from_numpy(t).to(DEV) for t in targets])
+    torch.cuda.synchronize()
+    assert tr.check_status() == 0
+    assert abs(tr.batch_loss() - ref["loss"]) <= 1e-5 * ref["loss"]
+    gref = ref["grads"][:, :n]
+    if not fused:
+        _grad_close(tr.grads.cpu().numpy()[:, :n], gref, rtol=2e-4, floor=2e-6, what="batch grads")
+    p = tr.params.cpu().numpy()[:, :n].astype(np.float64)
+    pr = ref["params"][:, :n]
+    gscale = np.zeros((59, 1))
+    for a, b in GROUPS_59:
+        gscale[a:b] = np.abs(gref[a:b]).max()
+    defined = np.abs(gref) > 1e-3 * gscale
+    assert defined.mean() > 0.2
+    bad = (np.abs(p - pr) > 1e-5 * np.abs(pr) + 1e-7) & defined
+    assert not bad.any(), bad.sum()
+    assert not tr.params[:, n:].any()
+
+
+def test_batch_of_one_is_the_single_view_step(case):
+    """step_batch with one view runs the same calls as step: the same parameters to
+    within the atomics' summation order."""
+    P, cam, n = case["P"], case["cam"], case["n"]
+    W, H = cam["width"], cam["height"]
+    tgt = torch.from_numpy(_target_for(case)).to(DEV)
+    a = gs.Trainer(P, n, W, H, capacity=1 << 20, lr_plane=gi.lr_planes())
+    b = gs.Trainer(P, n, W, H, capacity=1 << 20, lr_plane=gi.lr_planes())
+    a.step(cam, tgt)
+    b.step_batch([cam], [tgt])
+    torch.cuda.synchronize()
+    assert abs(b.batch_loss() - float(a.loss.item())) <= 1e-6 * float(a.loss.item())
+    x, y = a.params.cpu().numpy().astype(np.float64), b.params.cpu().numpy().astype(np.float64)
+    moved = np.abs(x - P.astype(np.float64)) > 0
+    assert moved.mean() > 0.2
+    close = np.abs(x - y) <= 1e-6 * np.abs(x) + 1e-7
+    assert close.mean() > 0.999, close.mean()
+
+
 # ----------------------------------------------------------------------------- edge cases
 
 def test_empty_scene_all_culled():
