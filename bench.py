@@ -62,6 +62,8 @@ def parse():
     ap.add_argument("--batch", type=int, default=1,
                     help="views per optimisation step (batch-size scaling of the Adam hyperparameters); the "
                          "headline is one view per step")
+    ap.add_argument("--graph", action="store_true",
+                    help="replay each view's step from a CUDA graph captured after the warm-up (one view per step)")
     ap.add_argument("--dssim", type=float, default=0.0,
                     help="D-SSIM weight lambda: the loss becomes (1 - lambda) L1 + lambda (1 - SSIM) (0 = L1)")
     return ap.parse_args()
@@ -437,6 +439,15 @@ def run_gb300(args, cfg, ws, rank, local):
     for s in range(args.warmup):
         step(s)
     torch.cuda.synchronize()
+    graphs = {}
+    if args.graph:
+        if B != 1 or args.separate:
+            raise SystemExit("--graph replays the fused one-view step")
+        for s in range(args.steps):
+            v = (args.warmup + s) % V_views
+            if v not in graphs:
+                graphs[v] = tr.capture_step(cams[v], targets[v])
+        torch.cuda.synchronize()
 
     # ---------------------------------------------------------------- timed region
     K = args.steps
@@ -451,7 +462,10 @@ def run_gb300(args, cfg, ws, rank, local):
         torch.cuda.nvtx.range_push("timed")
         t_start.record()
         for s in range(K):
-            step(args.warmup + s, ev[s] if B == 1 else None)
+            if graphs:
+                tr.replay(graphs[(args.warmup + s) % V_views])
+            else:
+                step(args.warmup + s, ev[s] if B == 1 else None)
         t_end.record()
         torch.cuda.nvtx.range_pop()
         torch.cuda.synchronize()
@@ -461,12 +475,13 @@ def run_gb300(args, cfg, ws, rank, local):
     clk = clocks.stop()
     tr.raise_on_status()
     stage_ms = ({name: float(np.mean([ev[s][i].elapsed_time(ev[s][i + 1]) for s in range(K)]))
-                 for i, name in enumerate(STAGES)} if B == 1 else None)
+                 for i, name in enumerate(STAGES)} if B == 1 and not graphs else None)
     value = whole_job_rate(ws, K, ms)
 
     # ---------------------------------------------------------------- e2e leg
     e2e = None
     if not args.no_e2e:
+        graphs.clear()  # they read the device-resident targets freed below
         host_t = torch.empty_like(targets, device="cpu").pin_memory()
         host_t.copy_(targets)
         del targets
@@ -532,7 +547,7 @@ def run_gb300(args, cfg, ws, rank, local):
     if B > 1:
         # a batch step: every row but Adam once per view, Adam once
         t_star = B * sum(t for r, t in row_t.items() if r != "adam") + row_t["adam"]
-    for name in (STAGES if B == 1 else []):
+    for name in (STAGES if stage_ms is not None else []):
         rows = STAGE_ROWS[name]
         t_meas = stage_ms[name] / 1e3
         t_rows = sum(row_t[r] for r in rows)
@@ -541,8 +556,8 @@ def run_gb300(args, cfg, ws, rank, local):
         bound = "alu" if fl / (peak_fp32 * 1e12) > moved / (peak_bw * 1e9) else "hbm"
         per_stage[name] = {"ms": stage_ms[name], "bound": bound, "rows": rows,
                            "gbs": moved / t_meas / 1e9, "tflops": fl / t_meas / 1e12, "frac": t_rows / t_meas}
-    roof = None  # a batch step has no per-stage events (they are taken at one view per step)
-    if B == 1:
+    roof = None  # batch and graph steps have no per-stage events
+    if stage_ms is not None:
         dom = max(STAGES, key=lambda s: stage_ms[s])
         d = per_stage[dom]
         traffic = measured_traffic({"render_fwd": "k_render_fwd", "render_bwd": "k_render_bwd"}.get(dom, ""))
@@ -561,7 +576,9 @@ def run_gb300(args, cfg, ws, rank, local):
         except Exception as exc:  # the baseline is reported, never required
             cpu = {"value": None, "unit": "steps/s", "kind": "oracle", "error": repr(exc)}
 
-    per_view = 1 + (9 + passes) + 1 + 2 + 1 + (3 if args.dssim > 0 else 0)
+    # project 1; binning 12 + p (prep, 3 scans, compact, 4 depth passes, sorted sums, emit,
+    # p tile passes, gather); forward 1; backward 2 (clear + raster); fused 1
+    per_view = 1 + (12 + passes) + 1 + 2 + 1 + (3 if args.dssim > 0 else 0) + (1 if args.graph else 0)
     launches_per_step = B * per_view + (1 if args.separate else 0)
     line = {
         "metric": METRIC if B == 1 else METRIC_BATCH.format(B=B), "value": value, "unit": "steps/s", "n_gpus": ws, "steps": K, "warmup": args.warmup,
@@ -569,7 +586,8 @@ def run_gb300(args, cfg, ws, rank, local):
         "dtype": "f32", "data": "synthetic",
         "config": dict(_config_dict(cfg), parallelism=f"replicas{ws}", capacity_K=capacity,
                        objective=(f"{1 - args.dssim:g} L1 + {args.dssim:g} (1 - SSIM)" if args.dssim > 0 else "L1"),
-                       K_mean=Kmean, visible_mean=Vmean, pairs_bwd_mean=Emean, batch=B),
+                       K_mean=Kmean, visible_mean=Vmean, pairs_bwd_mean=Emean, batch=B,
+                       cuda_graph=bool(graphs)),
         "views_per_s": value * B,
         "roofline": roof,
         "step_roofline_frac": t_star / (ms / K / 1e3),

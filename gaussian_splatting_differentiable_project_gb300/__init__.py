@@ -110,6 +110,12 @@ def load(build_if_missing: bool = True):
                                             ctypes.POINTER(ctypes.c_float), ctypes.c_double, ctypes.c_double,
                                             ctypes.c_double, ctypes.c_int64, P, P]
         lib.gs_project_bwd_adam.restype = st
+        lib.gs_project_bwd_adam_tdev.argtypes = [GsDims, P, ctypes.POINTER(GsCamera), ctypes.POINTER(GsProj), P, P, P,
+                                                 P, ctypes.POINTER(ctypes.c_float), ctypes.c_double, ctypes.c_double,
+                                                 ctypes.c_double, P, P, P]
+        lib.gs_project_bwd_adam_tdev.restype = st
+        lib.gs_step_counter_add.argtypes = [P, ctypes.c_int64, P]
+        lib.gs_step_counter_add.restype = st
         lib.gs_ssim_fwd.argtypes = [ctypes.c_int32, ctypes.c_int32, P, P, ctypes.c_float, P, P, P]
         lib.gs_ssim_fwd.restype = st
         lib.gs_ssim_bwd.argtypes = [ctypes.c_int32, ctypes.c_int32, P, P, P, P, P]
@@ -304,6 +310,24 @@ def project_bwd_adam(n: int, params, cam: dict, proj: ProjBuffers, grad2d, m, v,
     _check(load().gs_project_bwd_adam(dims(n, params.shape[1]), _p(params), ctypes.byref(cc), ctypes.byref(pc),
                                       _p(grad2d), gin, _p(m), _p(v), lr, float(beta1), float(beta2), float(eps),
                                       int(t), _p(dev_status), _stream(stream)), "gs_project_bwd_adam")
+
+
+def project_bwd_adam_tdev(n: int, params, cam: dict, proj: ProjBuffers, grad2d, m, v, lr_plane, beta1: float,
+                          beta2: float, eps: float, t_dev, dev_status, stream=None, grads_in=None) -> None:
+    """project_bwd_adam with the step count read from the device int64 ``t_dev`` when
+    the kernel runs (for CUDA graph capture)."""
+    cc = camera(cam)
+    pc = proj.c()
+    lr = (ctypes.c_float * N_PLANES)(*[float(x) for x in lr_plane])
+    gin = _p(grads_in) if grads_in is not None else None
+    _check(load().gs_project_bwd_adam_tdev(dims(n, params.shape[1]), _p(params), ctypes.byref(cc),
+                                           ctypes.byref(pc), _p(grad2d), gin, _p(m), _p(v), lr, float(beta1),
+                                           float(beta2), float(eps), _p(t_dev), _p(dev_status), _stream(stream)),
+           "gs_project_bwd_adam_tdev")
+
+
+def step_counter_add(counter, delta: int = 1, stream=None) -> None:
+    _check(load().gs_step_counter_add(_p(counter), int(delta), _stream(stream)), "gs_step_counter_add")
 
 
 def util_expf(x, y, stream=None) -> None:

@@ -15,18 +15,36 @@ struct AdamParams {
   float b1, c1, b2, c2, eps, inv_sqrt_bc2;
 };
 
-inline bool make_adam_params(const float lr_plane[kPlanes], double beta1, double beta2, double eps, int64_t t,
-                             AdamParams& a) {
-  if (t < 1 || !(beta1 >= 0.0 && beta1 < 1.0) || !(beta2 >= 0.0 && beta2 < 1.0) || !(eps >= 0.0)) return false;
-  const double bc1 = 1.0 - std::pow(beta1, double(t));
-  const double bc2 = 1.0 - std::pow(beta2, double(t));
+// Hyperparameters that do not change from step to step (a step count read from
+// device memory completes them inside a kernel; see k_project_bwd_adam).
+struct AdamHyper {
+  float lr[kPlanes];
+  double beta1, beta2, eps;
+};
+
+inline bool adam_hyper_ok(double beta1, double beta2, double eps) {
+  return (beta1 >= 0.0 && beta1 < 1.0) && (beta2 >= 0.0 && beta2 < 1.0) && (eps >= 0.0);
+}
+
+// The same fp64 formation on the host (a step count known there) and on the device
+// (a step count in device memory, for steps replayed from a CUDA graph).
+__host__ __device__ inline void form_adam_params(const float lr_plane[kPlanes], double beta1, double beta2,
+                                                 double eps, int64_t t, AdamParams& a) {
+  const double bc1 = 1.0 - ::pow(beta1, double(t));
+  const double bc2 = 1.0 - ::pow(beta2, double(t));
   for (int k = 0; k < kPlanes; ++k) a.step[k] = float(double(lr_plane[k]) / bc1);
   a.b1 = float(beta1);
   a.c1 = float(1.0 - beta1);
   a.b2 = float(beta2);
   a.c2 = float(1.0 - beta2);
   a.eps = float(eps);
-  a.inv_sqrt_bc2 = float(1.0 / std::sqrt(bc2));
+  a.inv_sqrt_bc2 = float(1.0 / ::sqrt(bc2));
+}
+
+inline bool make_adam_params(const float lr_plane[kPlanes], double beta1, double beta2, double eps, int64_t t,
+                             AdamParams& a) {
+  if (t < 1 || !adam_hyper_ok(beta1, beta2, eps)) return false;
+  form_adam_params(lr_plane, beta1, beta2, eps, t, a);
   return true;
 }
 

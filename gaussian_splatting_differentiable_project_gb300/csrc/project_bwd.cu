@@ -210,33 +210,33 @@ __global__ void __launch_bounds__(256, 2)
       }
       continue;
     }
-    if (!kAcc) {
+    if constexpr (!kAcc) {
 #pragma unroll
       for (int pl = 0; pl < 11; ++pl) G[int64_t(pl) * n_pad + i] = o.geo[pl];
 #pragma unroll
       for (int k = 0; k < 16; ++k)
 #pragma unroll
         for (int ch = 0; ch < 3; ++ch) G[int64_t(11 + 3 * k + ch) * n_pad + i] = o.Y[k] * o.gcol[ch];
-      continue;
-    }
-    // accumulate: each group's old values are loaded before any of its stores (the
-    // compiler cannot reorder a later plane's load above an earlier plane's store,
-    // so one plane at a time would serialise 59 memory round trips)
-    {
-      float cur[11];
+    } else {
+      // accumulate: each group's old values are loaded before any of its stores (the
+      // compiler cannot reorder a later plane's load above an earlier plane's store,
+      // so one plane at a time would serialise 59 memory round trips)
+      {
+        float cur[11];
 #pragma unroll
-      for (int pl = 0; pl < 11; ++pl) cur[pl] = G[int64_t(pl) * n_pad + i];
+        for (int pl = 0; pl < 11; ++pl) cur[pl] = G[int64_t(pl) * n_pad + i];
 #pragma unroll
-      for (int pl = 0; pl < 11; ++pl) G[int64_t(pl) * n_pad + i] = cur[pl] + o.geo[pl];
-    }
+        for (int pl = 0; pl < 11; ++pl) G[int64_t(pl) * n_pad + i] = cur[pl] + o.geo[pl];
+      }
 #pragma unroll
-    for (int k0 = 0; k0 < 16; k0 += 4) {
-      float cur[12];
+      for (int k0 = 0; k0 < 16; k0 += 4) {
+        float cur[12];
 #pragma unroll
-      for (int q = 0; q < 12; ++q) cur[q] = G[int64_t(11 + 3 * k0 + q) * n_pad + i];
+        for (int q = 0; q < 12; ++q) cur[q] = G[int64_t(11 + 3 * k0 + q) * n_pad + i];
 #pragma unroll
-      for (int q = 0; q < 12; ++q)
-        G[int64_t(11 + 3 * k0 + q) * n_pad + i] = cur[q] + o.Y[k0 + q / 3] * o.gcol[q % 3];
+        for (int q = 0; q < 12; ++q)
+          G[int64_t(11 + 3 * k0 + q) * n_pad + i] = cur[q] + o.Y[k0 + q / 3] * o.gcol[q % 3];
+      }
     }
   }
 }
@@ -303,11 +303,33 @@ struct ChunkStream {
 // loads); each element gets its gradient from the factors (plus, with kAccIn, the
 // gradient that earlier views of a batch accumulated in Gin) and the Adam update, and
 // p, m, v are written back.  The gradient planes are never written.
-template <bool kAccIn>
+// kDevT: the step count is read from t_dev and the Adam parameters are formed from
+// h in fp64 by one thread per CTA (for steps replayed from a CUDA graph, whose
+// kernel arguments are fixed); otherwise they arrive ready in a.
+template <bool kAccIn, bool kDevT>
 __global__ void __launch_bounds__(kFusedBlock, 2)
     k_project_bwd_adam(float* P, int64_t n, int64_t n_pad, CamDev cam, const uint32_t* __restrict__ count,
                        const float* __restrict__ g2, const float* __restrict__ Gin, float* M, float* V,
-                       AdamParams a) {
+                       AdamParams a_in, AdamHyper h, const int64_t* __restrict__ t_dev) {
+  __shared__ AdamParams s_adam;
+  if (kDevT) {
+    // the same fp64 expressions as form_adam_params, one plane per thread (fp64
+    // division is slow; a single thread forming all 59 would delay every CTA)
+    if (threadIdx.x < kPlanes) {
+      const double bc1 = 1.0 - ::pow(h.beta1, double(*t_dev));
+      s_adam.step[threadIdx.x] = float(double(h.lr[threadIdx.x]) / bc1);
+    } else if (threadIdx.x == kPlanes) {
+      const double bc2 = 1.0 - ::pow(h.beta2, double(*t_dev));
+      s_adam.b1 = float(h.beta1);
+      s_adam.c1 = float(1.0 - h.beta1);
+      s_adam.b2 = float(h.beta2);
+      s_adam.c2 = float(1.0 - h.beta2);
+      s_adam.eps = float(h.eps);
+      s_adam.inv_sqrt_bc2 = float(1.0 / ::sqrt(bc2));
+    }
+    __syncthreads();
+  }
+  const AdamParams& a = kDevT ? s_adam : a_in;
   __shared__ float s_geo[11][kFusedBlock];
   __shared__ float s_Y[16][kFusedBlock];
   __shared__ float s_gc[3][kFusedBlock];
@@ -407,23 +429,38 @@ gs_status project_bwd_launch(gs_dims dims, const float* params, const gs_camera*
   return launch_status();
 }
 
-template <bool kAccIn>
-gs_status fused_launch(gs_dims dims, float* params, const gs_camera* cam, const gs_proj* proj, const float* grad2d,
-                       const float* grads_in, float* m, float* v, const gs::AdamParams& a, cudaStream_t stream) {
+// The dynamic shared-memory opt-in of all four fused variants, set together on the
+// first call of any of them (an eager step before a CUDA graph capture has then set
+// it for the variants the graph uses).
+bool fused_attrs_ready() {
   using namespace gs;
-  static bool attr_set = false;
+  static bool ok = false;
+  if (ok) return true;
+  ok = cudaFuncSetAttribute(k_project_bwd_adam<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                            int(fused_dyn_smem(false))) == cudaSuccess &&
+       cudaFuncSetAttribute(k_project_bwd_adam<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                            int(fused_dyn_smem(true))) == cudaSuccess &&
+       cudaFuncSetAttribute(k_project_bwd_adam<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                            int(fused_dyn_smem(false))) == cudaSuccess &&
+       cudaFuncSetAttribute(k_project_bwd_adam<true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                            int(fused_dyn_smem(true))) == cudaSuccess;
+  return ok;
+}
+
+template <bool kAccIn, bool kDevT>
+gs_status fused_launch(gs_dims dims, float* params, const gs_camera* cam, const gs_proj* proj, const float* grad2d,
+                       const float* grads_in, float* m, float* v, const gs::AdamParams& a, const gs::AdamHyper& h,
+                       const int64_t* t_dev, cudaStream_t stream) {
+  using namespace gs;
   const size_t smem = fused_dyn_smem(kAccIn);
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(k_project_bwd_adam<kAccIn>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) !=
-        cudaSuccess)
-      return GS_ERR_CUDA;
-    attr_set = true;
-  }
+  if (!fused_attrs_ready()) return GS_ERR_CUDA;
   const int blocks = grid_for(dims.n_pad / kFusedBlock, 1, kSmCount * 2);
-  k_project_bwd_adam<kAccIn><<<blocks, kFusedBlock, smem, stream>>>(params, dims.n, dims.n_pad, cam_dev(*cam),
-                                                                     proj->count, grad2d, grads_in, m, v, a);
+  k_project_bwd_adam<kAccIn, kDevT><<<blocks, kFusedBlock, smem, stream>>>(
+      params, dims.n, dims.n_pad, cam_dev(*cam), proj->count, grad2d, grads_in, m, v, a, h, t_dev);
   return launch_status();
 }
+
+__global__ void k_counter_add(int64_t* c, int64_t d) { *c += d; }
 
 }  // namespace
 
@@ -451,6 +488,37 @@ extern "C" gs_status gs_project_bwd_adam(gs_dims dims, float* params, const gs_c
     return GS_ERR_INVALID_ARG;
   AdamParams a;
   if (!make_adam_params(lr_plane, beta1, beta2, eps, t, a)) return GS_ERR_INVALID_ARG;
-  return grads_in ? fused_launch<true>(dims, params, cam, proj, grad2d, grads_in, m, v, a, stream)
-                  : fused_launch<false>(dims, params, cam, proj, grad2d, nullptr, m, v, a, stream);
+  const AdamHyper h{};
+  return grads_in ? fused_launch<true, false>(dims, params, cam, proj, grad2d, grads_in, m, v, a, h, nullptr, stream)
+                  : fused_launch<false, false>(dims, params, cam, proj, grad2d, nullptr, m, v, a, h, nullptr, stream);
+}
+
+extern "C" gs_status gs_project_bwd_adam_tdev(gs_dims dims, float* params, const gs_camera* cam, const gs_proj* proj,
+                                              const float* grad2d, const float* grads_in, float* m, float* v,
+                                              const float lr_plane[GS_N_PLANES], double beta1, double beta2,
+                                              double eps, const int64_t* t_dev, uint32_t* dev_status,
+                                              cudaStream_t stream) {
+  using namespace gs;
+  if (!dims_ok(dims) || !camera_ok(cam) || !params || !proj || !proj->count || !grad2d || !m || !v || !lr_plane ||
+      !t_dev || !dev_status)
+    return GS_ERR_INVALID_ARG;
+  if (!aligned(params, 16) || !aligned(grad2d, 16) || !aligned(m, 16) || !aligned(v, 16) || !aligned(t_dev, 8) ||
+      (grads_in && !aligned(grads_in, 16)))
+    return GS_ERR_INVALID_ARG;
+  if (!adam_hyper_ok(beta1, beta2, eps)) return GS_ERR_INVALID_ARG;
+  AdamHyper h;
+  for (int k = 0; k < kPlanes; ++k) h.lr[k] = lr_plane[k];
+  h.beta1 = beta1;
+  h.beta2 = beta2;
+  h.eps = eps;
+  const AdamParams a{};
+  return grads_in ? fused_launch<true, true>(dims, params, cam, proj, grad2d, grads_in, m, v, a, h, t_dev, stream)
+                  : fused_launch<false, true>(dims, params, cam, proj, grad2d, nullptr, m, v, a, h, t_dev, stream);
+}
+
+extern "C" gs_status gs_step_counter_add(int64_t* counter, int64_t delta, cudaStream_t stream) {
+  using namespace gs;
+  if (!counter || !aligned(counter, 8)) return GS_ERR_INVALID_ARG;
+  k_counter_add<<<1, 1, 0, stream>>>(counter, delta);
+  return launch_status();
 }

@@ -15,7 +15,8 @@ import numpy as np
 import math
 
 from . import (BinBuffers, ProjBuffers, N_GRAD2D, SSIM_MAPS, adam_step, bin_sort, project, project_bwd,
-               project_bwd_accumulate, project_bwd_adam, render_bwd, render_fwd, ssim_bwd, ssim_fwd, status_str)
+               project_bwd_accumulate, project_bwd_adam, project_bwd_adam_tdev, render_bwd, render_fwd,
+               ssim_bwd, ssim_fwd, status_str, step_counter_add)
 
 
 def batch_adam_hyper(batch: int, lr_plane, beta1: float, beta2: float, eps: float):
@@ -188,6 +189,37 @@ class Trainer:
             s = self.batch_ssim.cpu().numpy().astype(np.float64)
             v += self.dssim * float((1.0 - s).mean())
         return v
+
+    # CUDA graphs --------------------------------------------------------------------
+    def capture_step(self, cam: dict, target):
+        """A CUDA graph of one fused step for this camera against ``target`` (a device
+        tensor the caller keeps alive): the step counter advance, forward, loss
+        backward and the fused projection backward + Adam reading the step count
+        from device memory.  Replay it with ``replay``; eager and replayed steps may
+        be mixed (the device step count follows ``t``)."""
+        import torch
+        if not self.fused:
+            raise ValueError("graph capture runs the fused step")
+        if getattr(self, "t_dev", None) is None:
+            self.t_dev = torch.zeros(1, dtype=torch.int64, device=self.params.device)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            step_counter_add(self.t_dev, 1)
+            self.forward(cam)
+            self.loss_backward(cam, target)
+            project_bwd_adam_tdev(self.n, self.params, cam, self.proj, self.grad2d, self.m, self.v, self.lr_plane,
+                                  self.beta1, self.beta2, self.eps, self.t_dev, self.status)
+        return g
+
+    def replay(self, graph) -> None:
+        """One step from a graph of ``capture_step`` (on the current stream)."""
+        if int(self._t_dev_synced) != self.t:
+            self.t_dev.fill_(self.t)
+        graph.replay()
+        self.t += 1
+        self._t_dev_synced = self.t
+
+    _t_dev_synced = -1
 
     def step_staged(self, cam: dict, targets: HostTargets, slot: int, stream=None) -> None:
         """``step`` against the target uploaded into ``slot`` of ``targets``."""

@@ -304,6 +304,27 @@ gs_status gs_project_bwd_adam(gs_dims dims, float* params, const gs_camera* cam,
                               uint32_t* dev_status, cudaStream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * gs_project_bwd_adam_tdev -- gs_project_bwd_adam with the Adam step count read from
+ * device memory when the kernel runs, for steps replayed from a CUDA graph (whose
+ * kernel arguments are fixed at capture).  The bias corrections and per-plane step
+ * sizes are formed from it in fp64 inside the kernel, as gs_adam_step forms them on
+ * the host.  The pages' trace attributes idle GPU time to launch overhead between
+ * small kernels ("Scaling 3D Gaussian Splatting with Distributed Compute", trace
+ * section); a captured step removes the per-launch host work.
+ *   t_dev  1 int64 (device, 8-byte aligned, read): the step count, >= 1 when the
+ *          kernel runs (advance it with gs_step_counter_add inside the graph).
+ *   Other arguments and errors as gs_project_bwd_adam (lr_plane, beta1, beta2 and
+ *   eps are captured by value). */
+gs_status gs_project_bwd_adam_tdev(gs_dims dims, float* params, const gs_camera* cam, const gs_proj* proj,
+                                   const float* grad2d, const float* grads_in, float* m, float* v,
+                                   const float lr_plane[GS_N_PLANES], double beta1, double beta2, double eps,
+                                   const int64_t* t_dev, uint32_t* dev_status, cudaStream_t stream);
+
+/* gs_step_counter_add -- *counter += delta on the stream (counter: 1 device int64,
+ * 8-byte aligned).  Errors: GS_ERR_INVALID_ARG for a null or misaligned counter. */
+gs_status gs_step_counter_add(int64_t* counter, int64_t delta, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------
  * gs_bin_sort_noalloc -- gs_bin_sort for callers that must not allocate device
  * memory (for example code that runs where cudaMalloc is not allowed or not
  * wanted after start-up: host callbacks, a render loop with all memory reserved

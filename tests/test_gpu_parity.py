@@ -526,6 +526,60 @@ def test_batch_of_one_is_the_single_view_step(case):
     assert close.mean() > 0.999, close.mean()
 
 
+def test_device_step_count_equals_host_step_count(case):
+    """gs_project_bwd_adam_tdev forms lr / (1 - beta1^t) and 1 / sqrt(1 - beta2^t)
+    from a step count in device memory in fp64, as gs_project_bwd_adam does on the
+    host: on identical seeded 2D gradients over three steps (t = 1, 2, 3) the
+    parameters and moments agree to an ulp."""
+    P, cam, n = case["P"], case["cam"], case["n"]
+    n_pad = P.shape[1]
+    W, H = cam["width"], cam["height"]
+    lr = gi.lr_planes()
+    a = gs.Trainer(P, n, W, H, capacity=1 << 20, lr_plane=lr)
+    b = gs.Trainer(P, n, W, H, capacity=1 << 20, lr_plane=lr)
+    st = _status()
+    t_dev = torch.zeros(1, dtype=torch.int64, device=DEV)
+    for t in range(1, 4):
+        g2 = torch.from_numpy(gi.random_grad2d(200 + t, n, n_pad)).to(DEV)
+        gs.project(n, a.params, cam, a.proj, st)
+        gs.project_bwd_adam(n, a.params, cam, a.proj, g2, a.m, a.v, lr, 0.9, 0.999, 1e-15, t, st)
+        gs.project(n, b.params, cam, b.proj, st)
+        gs.step_counter_add(t_dev, 1)
+        gs.project_bwd_adam_tdev(n, b.params, cam, b.proj, g2, b.m, b.v, lr, 0.9, 0.999, 1e-15, t_dev, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0 and int(t_dev.item()) == 3
+    for x, y in ((a.params, b.params), (a.m, b.m), (a.v, b.v)):
+        x, y = x.cpu().numpy().astype(np.float64), y.cpu().numpy().astype(np.float64)
+        assert np.all(np.abs(x - y) <= 2.5e-7 * np.abs(x) + 1e-30)
+
+
+def test_graph_replayed_steps_match_eager_steps(case):
+    """Steps captured as CUDA graphs (camera, target and hyperparameters fixed at
+    capture, the step count advanced and read on the device) replay the eager steps:
+    four steps over three views after one eager step give the same losses (each
+    step's loss depends on all parameters the earlier steps moved)."""
+    P, n = case["P"], case["n"]
+    cams = _batch_cams(case)
+    W, H = cams[0]["width"], cams[0]["height"]
+    tg = [torch.from_numpy(gi.offset_target(oracle.render(oracle.project(P, n, c, 32), W, H)["image"],
+                                            seed=80 + k)).to(DEV) for k, c in enumerate(cams)]
+    a = gs.Trainer(P, n, W, H, capacity=1 << 20, lr_plane=gi.lr_planes())
+    b = gs.Trainer(P, n, W, H, capacity=1 << 20, lr_plane=gi.lr_planes())
+    a.step(cams[0], tg[0])
+    b.step(cams[0], tg[0])
+    graphs = [b.capture_step(c, t) for c, t in zip(cams, tg)]
+    order = [1, 2, 0, 1]
+    la, lb = [], []
+    for k in order:
+        a.step(cams[k], tg[k])
+        la.append(float(a.loss.item()))
+        b.replay(graphs[k])
+        lb.append(float(b.loss.item()))
+    assert a.check_status() == 0 and b.check_status() == 0
+    assert b.t == a.t == 5 and int(b.t_dev.item()) == 5
+    np.testing.assert_allclose(lb, la, rtol=1e-5)
+
+
 # ----------------------------------------------------------------------------- edge cases
 
 def test_empty_scene_all_culled():
