@@ -195,24 +195,25 @@ def stage_bytes(N, n_pad, V, K, P, passes, dssim=False):
         "bin_sort": 8 * N + 100 * V + (8 + 16 * passes + 112) * K,
         # records once per tile, image + T + n_contrib written
         "render_fwd": 48 * K + 20 * P,
-        # grad2d cleared, records once per tile, image/target/T/n_contrib read (and
-        # the D-SSIM image gradient when that term is on)
-        "render_bwd": 36 * n_pad + 48 * K + (44 if dssim else 32) * P,
+        # grad2d (12 floats per Gaussian) cleared, records once per tile,
+        # image/target/T/n_contrib read (and the D-SSIM image gradient when that term is on)
+        "render_bwd": 48 * n_pad + 48 * K + (44 if dssim else 32) * P,
         # D-SSIM: image + target read, 15 maps (3 partials, 2 means per channel)
         # written; the maps, image and target read again, the image gradient written
         "ssim": 180 * P,
-        # all: count + 59 gradient planes written; visible: 59 params + 9 grad2d read
-        "project_bwd": 240 * N + 272 * V,
+        # all: count + 59 gradient planes written; visible: 59 params + the 48-byte
+        # grad2d slot read
+        "project_bwd": 240 * N + 284 * V,
         # p, g, m, v read; p, m, v written
         "adam": 59 * n_pad * 28,
     }
 
 
-# Bytes the fused projection backward + Adam actually moves: count, 9 grad2d of the
+# Bytes the fused projection backward + Adam actually moves: count, the 48-byte grad2d slot of the
 # visible, p, m, v read and written for every parameter (the gradient planes are
 # never written).  The step roofline still charges rows a5 + a6 their own bytes.
 def fused_bytes(N, n_pad, V):
-    return 4 * N + 36 * V + 59 * n_pad * 24
+    return 4 * N + 48 * V + 59 * n_pad * 24
 
 
 # Rows of the step each measured stage covers.

@@ -25,6 +25,23 @@ N_PLANES = 59
 TILE = 16
 REC_FLOATS = 12
 N_GRAD2D = 9
+GRAD2D_STRIDE = 12  # floats per Gaussian in the interleaved grad2d buffer
+
+
+def grad2d_planes(grad2d, n: int) -> np.ndarray:
+    """The nine 2D partials of Gaussians [0, n) as (9, n) planes, from the interleaved
+    (n_pad, 12) buffer gs_render_bwd writes (host copy)."""
+    g = grad2d.detach().cpu().numpy() if hasattr(grad2d, "detach") else np.asarray(grad2d)
+    return np.ascontiguousarray(g.reshape(-1, GRAD2D_STRIDE)[:n, :N_GRAD2D].T)
+
+
+def grad2d_interleaved(planes: np.ndarray) -> np.ndarray:
+    """(9, n_pad) planes -> the interleaved (n_pad, 12) layout the projection
+    backward reads (host arrays)."""
+    planes = np.asarray(planes, np.float32)
+    out = np.zeros((planes.shape[1], GRAD2D_STRIDE), np.float32)
+    out[:, :N_GRAD2D] = planes.T
+    return out
 SSIM_MAPS = 15  # planes of gs_ssim_fwd's maps: 3 partials and 2 local means per channel
 
 GS_OK = 0

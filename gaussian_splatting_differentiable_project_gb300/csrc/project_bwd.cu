@@ -53,8 +53,14 @@ __device__ __forceinline__ bool chain_rule(const float* P, int64_t n, int64_t n_
   if (i < n && count[i] > 0u) project_geo<kReadOnly>(P, n_pad, i, cam, g);
   if (!g.visible) return false;
   float gq2[9];
-#pragma unroll
-  for (int q = 0; q < 9; ++q) gq2[q] = __ldg(g2 + int64_t(q) * n_pad + i);
+  {
+    // interleaved: the nine partials of Gaussian i at 12 i + 0..8 (three float4)
+    const float4* g4 = reinterpret_cast<const float4*>(g2) + 3 * i;
+    const float4 x = __ldg(g4), y = __ldg(g4 + 1), z = __ldg(g4 + 2);
+    gq2[0] = x.x, gq2[1] = x.y, gq2[2] = x.z, gq2[3] = x.w;
+    gq2[4] = y.x, gq2[5] = y.y, gq2[6] = y.z, gq2[7] = y.w;
+    gq2[8] = z.x;
+  }
   const float gmx = gq2[0], gmy = gq2[1], gA = gq2[2], gB = gq2[3], gC = gq2[4], go = gq2[5];
 
   // ---- colour: SH coefficients and the view direction

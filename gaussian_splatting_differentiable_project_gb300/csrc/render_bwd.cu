@@ -6,7 +6,9 @@
 // division by (1 - alpha) and carrying the normalised colour of everything
 // behind it.  Per entry each lane holds nine partials; a warp that has any
 // contribution reduces them with a shuffle reduce-scatter (14 shuffles instead
-// of 45 for nine butterflies) and nine lanes issue one global atomic each.
+// of 45 for nine butterflies) and nine lanes add the sums, in one atomic
+// instruction, to the Gaussian's interleaved 12-float slot of grad2d (two 32-byte
+// sectors instead of nine planes' lines).
 #include "api_util.h"
 #include "raster_common.cuh"
 
@@ -132,7 +134,6 @@ __global__ void __launch_bounds__(kRasterThreads)
     if (nb > 1) st.issue(nb - 2, 1);
   }
   float acc0 = bg0, acc1 = bg1, acc2 = bg2;
-  float* gp = grad2d;
   for (int u = 0; u < nb; ++u) {
     const int b = nb - 1 - u;
     const int slot = u & 1;
@@ -151,52 +152,50 @@ __global__ void __launch_bounds__(kRasterThreads)
         mask &= ~(1u << hb);
         const int j = j0 + hb;
         const uint32_t pos = pos0 + uint32_t(j);
-        float v[9];
-        bool contrib = false;
+        // Every lane evaluates the entry; skip and clamp decisions become predicates
+        // and a non-contributing lane carries alpha = 0, which leaves its state
+        // unchanged and its partials zero (the warp stays converged).
         const float4 ra = R[j].a;
         const float4 rb = R[j].b;
         const float4 rc = R[j].c;
-        if (pos < nc) {
-          const float dx = __fsub_rn(px, ra.x), dy = __fsub_rn(py, ra.y);
-          const float power = conic_power(dx, dy, ra.z, ra.w, rb.x);
-          if (!(power > 0.0f) && !(power < kPowerSkip)) {
-            const float e = gs_expf_core(power);
-            const float vv = __fmul_rn(rb.y, e);
-            const bool clamped = !(vv < kAlphaMax);
-            const float alpha = clamped ? kAlphaMax : vv;
-            if (!(alpha < kAlphaMin)) {
-              contrib = true;
-              const float Ti = __fdividef(T, 1.0f - alpha);
-              const float wgt = alpha * Ti;
-              v[6] = g0 * wgt;
-              v[7] = g1 * wgt;
-              v[8] = g2 * wgt;
-              const float dLda = Ti * (g0 * (rb.z - acc0) + g1 * (rb.w - acc1) + g2 * (rc.x - acc2));
-              acc0 = alpha * rb.z + (1.0f - alpha) * acc0;
-              acc1 = alpha * rb.w + (1.0f - alpha) * acc1;
-              acc2 = alpha * rc.x + (1.0f - alpha) * acc2;
-              T = Ti;
-              const float dLdp = clamped ? 0.0f : dLda * alpha;
-              v[5] = clamped ? 0.0f : dLda * e;
-              // power = ca dx^2 + cb dx dy + cc dy^2 with (ca, cb, cc) = (-A/2, -B, -C/2)
-              v[0] = -dLdp * (2.0f * ra.z * dx + ra.w * dy);  // d/d mean x (dx = px - mx)
-              v[1] = -dLdp * (ra.w * dx + 2.0f * rb.x * dy);  // d/d mean y
-              v[2] = -0.5f * dLdp * dx * dx;                  // d/dA
-              v[3] = -dLdp * dx * dy;                         // d/dB
-              v[4] = -0.5f * dLdp * dy * dy;                  // d/dC
-            }
-          }
-        }
-        if (!contrib) {
-  #pragma unroll
-          for (int q = 0; q < 9; ++q) v[q] = 0.0f;
-        }
+        const float dx = __fsub_rn(px, ra.x), dy = __fsub_rn(py, ra.y);
+        const float power = conic_power(dx, dy, ra.z, ra.w, rb.x);
+        const bool in_range = (pos < nc) && !(power > 0.0f) && !(power < kPowerSkip);
+        const float e = gs_expf_core(in_range ? power : 0.0f);
+        const float vv = __fmul_rn(rb.y, e);
+        const bool clamped = !(vv < kAlphaMax);
+        const float alpha_raw = clamped ? kAlphaMax : vv;
+        const bool contrib = in_range && !(alpha_raw < kAlphaMin);
+        const float alpha = contrib ? alpha_raw : 0.0f;
+        const float Ti = __fdividef(T, 1.0f - alpha);
+        const float wgt = alpha * Ti;
+        float v[9];
+        v[6] = g0 * wgt;
+        v[7] = g1 * wgt;
+        v[8] = g2 * wgt;
+        const float dLda = Ti * (g0 * (rb.z - acc0) + g1 * (rb.w - acc1) + g2 * (rc.x - acc2));
+        acc0 = alpha * rb.z + (1.0f - alpha) * acc0;
+        acc1 = alpha * rb.w + (1.0f - alpha) * acc1;
+        acc2 = alpha * rc.x + (1.0f - alpha) * acc2;
+        T = contrib ? Ti : T;
+        const bool lin = contrib && !clamped;
+        const float dLdp = lin ? dLda * alpha : 0.0f;
+        v[5] = lin ? dLda * e : 0.0f;
+        // power = ca dx^2 + cb dx dy + cc dy^2 with (ca, cb, cc) = (-A/2, -B, -C/2)
+        v[0] = -dLdp * (2.0f * ra.z * dx + ra.w * dy);  // d/d mean x (dx = px - mx)
+        v[1] = -dLdp * (ra.w * dx + 2.0f * rb.x * dy);  // d/d mean y
+        v[2] = -0.5f * dLdp * dx * dx;                  // d/dA
+        v[3] = -dLdp * dx * dy;                         // d/dB
+        v[4] = -0.5f * dLdp * dy * dy;                  // d/dC
         if (__any_sync(0xffffffffu, contrib)) {
           float s8, s9;
           warp_reduce9(v, &s8, &s9);
+          // one atomic instruction: lanes 0, 4, ..., 28 add partials 0..7, lane 1
+          // partial 8, all into the Gaussian's 12-float slot
           const uint32_t gid = __float_as_uint(rc.y);
-          if ((lane & 3) == 0) atomicAdd(gp + int64_t(lane >> 2) * n_pad + gid, s8);
-          if (lane == 1) atomicAdd(gp + int64_t(8) * n_pad + gid, s9);
+          const bool nine = lane == 1;
+          if (((lane & 3) == 0) || nine)
+            atomicAdd(grad2d + int64_t(gid) * GS_GRAD2D_STRIDE + (nine ? 8 : (lane >> 2)), nine ? s9 : s8);
         }
       }
     }
@@ -227,7 +226,7 @@ extern "C" gs_status gs_render_bwd(gs_dims dims, const gs_camera* cam, const gs_
   if (!bins->rec || !bins->ranges || !bins->n_isect || capacity_K == 0) return GS_ERR_INVALID_ARG;
   if (!aligned(bins->rec, 16) || !aligned(bins->ranges, 8) || !aligned(grad2d, 16)) return GS_ERR_INVALID_ARG;
   if (!(l1_weight >= 0.0f) || !std::isfinite(l1_weight)) return GS_ERR_INVALID_ARG;
-  const int64_t n4 = int64_t(GS_N_GRAD2D) * dims.n_pad / 4;
+  const int64_t n4 = int64_t(GS_GRAD2D_STRIDE) * dims.n_pad / 4;
   k_zero4<<<grid_for(n4, 256, kSmCount * 8), 256, 0, stream>>>(reinterpret_cast<float4*>(grad2d), n4, loss_out);
   const int TX = (cam->width + kTile - 1) / kTile;
   const int64_t tiles = n_tiles(cam);

@@ -14,7 +14,7 @@ import numpy as np
 
 import math
 
-from . import (BinBuffers, ProjBuffers, N_GRAD2D, SSIM_MAPS, adam_step, bin_sort, project, project_bwd,
+from . import (BinBuffers, ProjBuffers, GRAD2D_STRIDE, SSIM_MAPS, adam_step, bin_sort, project, project_bwd,
                project_bwd_accumulate, project_bwd_adam, project_bwd_adam_tdev, render_bwd, render_fwd,
                ssim_bwd, ssim_fwd, status_str, step_counter_add)
 
@@ -83,7 +83,7 @@ class Trainer:
         self.m = torch.zeros_like(self.params)
         self.v = torch.zeros_like(self.params)
         self.grads = torch.empty_like(self.params)
-        self.grad2d = torch.empty((N_GRAD2D, self.n_pad), dtype=torch.float32, device=device)
+        self.grad2d = torch.empty((self.n_pad, GRAD2D_STRIDE), dtype=torch.float32, device=device)
         self.proj = ProjBuffers(self.n_pad, device)
         self.bins = BinBuffers(self.n, capacity, width, height, device)
         self.image = torch.empty((3, height, width), dtype=torch.float32, device=device)

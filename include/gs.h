@@ -60,7 +60,8 @@ extern "C" {
 #define GS_N_PLANES 59
 #define GS_TILE 16          /* tile edge in pixels */
 #define GS_REC_FLOATS 12    /* projected record: 48 bytes */
-#define GS_N_GRAD2D 9       /* 2D gradient planes */
+#define GS_N_GRAD2D 9       /* 2D partials per Gaussian */
+#define GS_GRAD2D_STRIDE 12 /* floats per Gaussian in grad2d (interleaved, 3 unused) */
 
 typedef enum gs_status {
   GS_OK = 0,
@@ -212,8 +213,11 @@ gs_status gs_render_fwd(const gs_camera* cam, const gs_bins* bins, uint32_t capa
  *   target      3 x H x W fp32 (read).
  *   l1_weight   weight of the L1 term (1 for the L1 objective, 1 - lambda with D-SSIM).
  *   dLdC_extra  3 x H x W fp32 added to the loss gradient, or null.
- *   grad2d      9 x n_pad fp32 (write; zeroed by this call first), planes
- *               (d mx, d my, d A, d B, d C, d opacity, d r, d g, d b).
+ *   grad2d      GS_GRAD2D_STRIDE x n_pad fp32, interleaved (write; zeroed by this
+ *               call first): Gaussian i's partials at 12 i + (d mx, d my, d A, d B,
+ *               d C, d opacity, d r, d g, d b), 12 i + 9..11 unused.  A warp's nine
+ *               sums for one Gaussian land in two 32-byte sectors instead of nine
+ *               planes' lines.
  *   loss_out    1 fp32 (write; zeroed first).
  * Errors: as gs_render_fwd, plus a negative or non-finite l1_weight. */
 gs_status gs_render_bwd(gs_dims dims, const gs_camera* cam, const gs_bins* bins, uint32_t capacity_K,
@@ -250,7 +254,8 @@ gs_status gs_ssim_bwd(int32_t width, int32_t height, const float* image, const f
  * -> logit; colour -> SH coefficients and view direction -> mu.  Clamped colour
  * channels and clamped Jacobian abscissae pass zero gradient; radius and rect are
  * constants.  Culled Gaussians and padding get zero gradients.
- *   params 59 x n_pad (read); proj from gs_project (read); grad2d 9 x n_pad (read);
+ *   params 59 x n_pad (read); proj from gs_project (read); grad2d as written by
+ *   gs_render_bwd (read, 16-byte aligned);
  *   grads  59 x n_pad fp32 (write, every entry).
  * Errors: as gs_project. */
 gs_status gs_project_bwd(gs_dims dims, const float* params, const gs_camera* cam, const gs_proj* proj,

@@ -122,4 +122,5 @@ def test_binding_constants_match_the_header():
     assert int(defs["GS_TILE"]) == gs.TILE
     assert int(defs["GS_REC_FLOATS"]) == gs.REC_FLOATS
     assert int(defs["GS_N_GRAD2D"]) == gs.N_GRAD2D
+    assert int(defs["GS_GRAD2D_STRIDE"]) == gs.GRAD2D_STRIDE
     assert int(defs["GS_SSIM_MAPS"]) == gs.SSIM_MAPS

@@ -145,7 +145,7 @@ def _check_block(tr, ref, cam, tx0, ty0, nt, backward=True):
     torch.cuda.synchronize()
     sel = inside[idx]
     assert sel.sum() > 50
-    got = tr.grad2d.cpu().numpy()[:, idx[sel]]
+    got = gs.grad2d_planes(tr.grad2d, tr.n_pad)[:, idx[sel]]
     _grad_close(got, rb["grad2d"][:, sel], what="grad2d (block)")
 
 
@@ -158,8 +158,8 @@ def _check_fused_sample(tr, P, n, cam, idx):
     gs.project(n, tr.params, cam, tr.proj, tr.status)
     tr.m.zero_()
     tr.v.zero_()
-    gs.project_bwd_adam(n, tr.params, cam, tr.proj, torch.from_numpy(g2).to(DEV), tr.m, tr.v, lr, 0.9, 0.999, 1e-15,
-                        1, tr.status)
+    gs.project_bwd_adam(n, tr.params, cam, tr.proj, torch.from_numpy(gs.grad2d_interleaved(g2)).to(DEV), tr.m, tr.v,
+                        lr, 0.9, 0.999, 1e-15, 1, tr.status)
     torch.cuda.synchronize()
     Ps = np.ascontiguousarray(P[:, idx])
     gref = oracle.project_bwd(Ps, len(idx), cam, g2[:, idx], prec=32)
@@ -216,7 +216,7 @@ def test_iso1m_512_full_parity():
     gs.render_bwd(n, tr.n_pad, cam, tr.bins, tr.bg, tr.image, torch.from_numpy(target).to(DEV), tr.T_final,
                   tr.n_contrib, tr.grad2d, tr.loss, tr.status)
     torch.cuda.synchronize()
-    _grad_close(tr.grad2d.cpu().numpy()[:, :n], rb["grad2d"], what="grad2d")
+    _grad_close(gs.grad2d_planes(tr.grad2d, n), rb["grad2d"], what="grad2d")
     assert abs(float(tr.loss.item()) - rb["loss"]) <= 1e-5 * rb["loss"]
     _check_fused_sample(tr, P, n, cam, np.random.default_rng(1).choice(n, 50_000, replace=False))
     assert tr.check_status() == 0

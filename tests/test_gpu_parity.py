@@ -209,11 +209,11 @@ def test_render_bwd_parity(case):
     tr.backward(cam, tgt)
     torch.cuda.synchronize()
     assert tr.check_status() == 0
-    g2 = tr.grad2d.cpu().numpy()[:, :n]
+    g2 = gs.grad2d_planes(tr.grad2d, n)
     _grad_close(g2, rd["grad2d"], what="grad2d")
     assert abs(float(tr.loss.item()) - rd["loss"]) <= 1e-5 * rd["loss"]
     # padding gets no gradient
-    assert not tr.grad2d[:, n:].any()
+    assert not tr.grad2d[n:].any()
 
 
 def test_project_bwd_parity(case):
@@ -221,7 +221,7 @@ def test_project_bwd_parity(case):
     tr, P, cam, n = case["tr"], case["P"], case["cam"], case["n"]
     g2 = gi.random_grad2d(11, n, P.shape[1])
     ref = oracle.project_bwd(P, n, cam, g2[:, :n], prec=32)
-    g2d = torch.from_numpy(g2).to(DEV)
+    g2d = torch.from_numpy(gs.grad2d_interleaved(g2)).to(DEV)
     st = _status()
     gs.project(n, tr.params, cam, tr.proj, st)
     gs.project_bwd(n, tr.params, cam, tr.proj, g2d, tr.grads, st)
@@ -268,7 +268,7 @@ def test_whole_step_end_to_end(case, fused):
     tr.step(cam, torch.from_numpy(target).to(DEV))
     torch.cuda.synchronize()
     assert tr.check_status() == 0
-    _grad_close(tr.grad2d.cpu().numpy()[:, :n], ref["render"]["grad2d"], what="grad2d")
+    _grad_close(gs.grad2d_planes(tr.grad2d, n), ref["render"]["grad2d"], what="grad2d")
     gref = ref["grads"][:, :n]
     if not fused:
         _grad_close(tr.grads.cpu().numpy()[:, :n], gref, rtol=2e-4, floor=2e-6, what="param grads")
@@ -299,7 +299,7 @@ def test_fused_project_bwd_adam_equals_separate_calls(case):
     b = gs.Trainer(P, n, W, H, capacity=1 << 20, lr_plane=lr, fused=True)
     st = _status()
     for t in range(1, 4):
-        g2 = torch.from_numpy(gi.random_grad2d(100 + t, n, n_pad)).to(DEV)
+        g2 = torch.from_numpy(gs.grad2d_interleaved(gi.random_grad2d(100 + t, n, n_pad))).to(DEV)
         gs.project(n, a.params, cam, a.proj, st)
         gs.project_bwd(n, a.params, cam, a.proj, g2, a.grads, st)
         gs.adam_step(n, a.params, a.grads, a.m, a.v, lr, 0.9, 0.999, 1e-15, t)
@@ -400,7 +400,7 @@ def test_whole_step_with_dssim_end_to_end(case, fused):
     assert tr.check_status() == 0
     assert abs(tr.total_loss() - ref["render"]["loss"]) <= 1e-5 * abs(ref["render"]["loss"])
     assert abs(float(tr.ssim_val.item()) - ref["render"]["ssim"]) <= 1e-5
-    _grad_close(tr.grad2d.cpu().numpy()[:, :n], ref["render"]["grad2d"], what="grad2d")
+    _grad_close(gs.grad2d_planes(tr.grad2d, n), ref["render"]["grad2d"], what="grad2d")
     gref = ref["grads"][:, :n]
     if not fused:
         _grad_close(tr.grads.cpu().numpy()[:, :n], gref, rtol=2e-4, floor=2e-6, what="param grads")
@@ -431,7 +431,7 @@ def test_render_bwd_extra_image_gradient(case):
     torch.cuda.synchronize()
     assert int(st.item()) == 0
     assert float(tr.loss.item()) == 0.0
-    _grad_close(tr.grad2d.cpu().numpy()[:, :n], rd["grad2d"], what="grad2d")
+    _grad_close(gs.grad2d_planes(tr.grad2d, n), rd["grad2d"], what="grad2d")
 
 
 def test_staged_host_targets_feed_the_right_step(case):
@@ -540,7 +540,7 @@ def test_device_step_count_equals_host_step_count(case):
     st = _status()
     t_dev = torch.zeros(1, dtype=torch.int64, device=DEV)
     for t in range(1, 4):
-        g2 = torch.from_numpy(gi.random_grad2d(200 + t, n, n_pad)).to(DEV)
+        g2 = torch.from_numpy(gs.grad2d_interleaved(gi.random_grad2d(200 + t, n, n_pad))).to(DEV)
         gs.project(n, a.params, cam, a.proj, st)
         gs.project_bwd_adam(n, a.params, cam, a.proj, g2, a.m, a.v, lr, 0.9, 0.999, 1e-15, t, st)
         gs.project(n, b.params, cam, b.proj, st)
@@ -661,4 +661,4 @@ def test_large_gaussian_spanning_many_tiles():
     tgt = torch.from_numpy(gi.offset_target(oracle.render(ref, 200, 120)["image"], 2)).to(DEV)
     tr.backward(cam, tgt)
     torch.cuda.synchronize()
-    _grad_close(tr.grad2d.cpu().numpy()[:, :n], rd["grad2d"], what="grad2d")
+    _grad_close(gs.grad2d_planes(tr.grad2d, n), rd["grad2d"], what="grad2d")
