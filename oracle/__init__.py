@@ -303,3 +303,6 @@ def step(params, n: int, cam: dict, target, m, v, t: int, lr_plane, beta1=0.9, b
     gfull[:, :n] = grads
     p1, m1, v1 = adam(params.astype(np.float64), gfull, m, v, lr_plane, beta1, beta2, eps, t)
     return {"proj": pr, "render": rd, "grads": gfull, "params": p1, "m": m1, "v": v1}
+
+
+from . import densify  # noqa: E402,F401  (adaptive density control)

@@ -686,3 +686,168 @@ def test_batch_first_step_moves_by_sqrt_batch_lr():
     expect = P.astype(np.float64) - 2.0 * lr * np.sign(g)
     assert big.sum() > 50
     np.testing.assert_allclose(r["params"][big], expect[big], rtol=0, atol=1e-11)  # a flip moves by >= 2.5e-4
+
+
+# ----------------------------------------------------------------------------- density control
+
+def _dscene(n=8, seed=0):
+    rng = np.random.default_rng(seed)
+    means = rng.uniform(-0.5, 0.5, (n, 3))
+    ls = np.full((n, 3), -5.0)  # scale 0.0067: below 0.01 x extent 1
+    q = rng.normal(size=(n, 4))
+    q /= np.linalg.norm(q, axis=1, keepdims=True)
+    P, _ = _scene(means, ls, quats=q, logits=np.zeros(n))
+    return P
+
+
+def test_densify_thresholds_are_the_stated_ones():
+    """fp32 thresholds formed in fp64: sigmoid(logit_prune) = 0.005, exp(log scale) =
+    0.01 x extent, the reset logit is that of 2 x 0.005, and the split shrink is 1.6."""
+    th = oracle.densify.thresholds(extent=3.3)
+    # fp32 rounding of a logit near -5 moves the sigmoid by at most ~3e-9
+    assert abs(1.0 / (1.0 + math.exp(-float(th["logit_prune"]))) - 0.005) < 5e-9
+    assert abs(math.exp(float(th["log_grow_scale"])) - 0.033) < 1e-8
+    assert abs(math.exp(float(th["log_prune_scale"])) - 0.33) < 1e-7
+    assert abs(1.0 / (1.0 + math.exp(-float(th["logit_reset"]))) - 0.01) < 5e-9
+    assert abs(math.exp(float(th["log_shrink"])) - 1.6) < 1e-6
+    assert th["grad"] == np.float32(2e-4)
+
+
+def test_densify_decisions_on_constructed_gaussians():
+    D = oracle.densify
+    th = D.thresholds(extent=1.0)
+    P = _dscene()
+    n = 8
+    acc = np.zeros(n, np.float32)
+    cnt = np.zeros(n, np.int64)
+    P[10, 0] = -6.0                              # sigmoid 0.0025 < 0.005: prune
+    acc[1], cnt[1] = 9e-4, 3                      # mean 3e-4 > 2e-4, small: clone
+    acc[2], cnt[2] = 9e-4, 3
+    P[3:6, 2] = [-4.0, -2.0, -4.0]                # max scale e^-2 = 0.135 > 0.01: split
+    acc[3], cnt[3] = 3e-4, 3                      # mean 1e-4: keep
+    P[10, 4] = float(th["logit_prune"])           # exactly at the threshold: not below, keep
+    acc[5], cnt[5] = np.float32(2e-4), 1          # mean equals the threshold (strict >): keep
+    acc[6], cnt[6] = 6e-4, 2                      # mean 3e-4 and max log-scale exactly at the
+    P[3:6, 6] = [float(th["log_grow_scale"]), -5.0, -5.0]  # clone threshold (<=): clone
+    P[10, 7] = -5.3                               # sigmoid 0.00497 < 0.005: prune
+    action, offset, n_out = D.plan(P, n, acc, cnt, th)
+    assert action.tolist() == [D.PRUNE, D.CLONE, D.SPLIT, D.KEEP, D.KEEP, D.KEEP, D.CLONE, D.PRUNE]
+    assert offset.tolist() == [0, 0, 2, 4, 5, 6, 7, 9]
+    assert n_out == 9
+    # the optional large-Gaussian prune also removes Gaussian 2: its largest log-scale
+    # -2 exceeds ln(0.1 x extent) = -2.303
+    a2, _, _ = D.plan(P, n, acc, cnt, th, prune_big=True)
+    assert a2[2] == D.PRUNE and (a2 == D.PRUNE).sum() == 3
+
+
+def test_split_children_follow_the_rotated_axes():
+    """With xi = (e_a, e_b) the children sit at mu + s_a r_a and mu + s_b r_b, where r_k
+    is column k of the rotation (scipy's, from the same quaternion) and s_k the scale;
+    children's log-scales are shrunk by ln 1.6, every other plane is copied and their
+    Adam moments start at zero."""
+    Rot = pytest.importorskip("scipy.spatial.transform").Rotation
+    D = oracle.densify
+    th = D.thresholds()
+    P = _dscene(n=4, seed=3)
+    P[3:6, :4] = np.array([[-1.0, -1.5, -2.0]] * 4).T
+    n = 4
+    acc = np.full(n, 1e-3, np.float32)
+    cnt = np.ones(n, np.int64)
+    action, offset, n_out = D.plan(P, n, acc, cnt, th)
+    assert (action == D.SPLIT).all() and n_out == 8
+    randn = np.zeros((n, 6), np.float32)
+    for i in range(n):
+        randn[i, i % 3] = 1.0              # child 0 along axis i % 3
+        randn[i, 3 + (i + 1) % 3] = -2.0   # child 1 along axis (i + 1) % 3, twice, reversed
+    m = np.random.default_rng(0).normal(size=(59, P.shape[1])).astype(np.float32)
+    v = np.abs(m)
+    out_p, out_m, out_v = D.apply(P, m, v, n, action, offset, n_out, randn, th)
+    for i in range(n):
+        q = P[6:10, i].astype(np.float64)
+        rot = Rot.from_quat([q[1], q[2], q[3], q[0]]).as_matrix()
+        s = np.exp(P[3:6, i].astype(np.float64))
+        a, b = i % 3, (i + 1) % 3
+        np.testing.assert_allclose(out_p[0:3, 2 * i], P[0:3, i] + s[a] * rot[:, a], rtol=0, atol=1e-6)
+        np.testing.assert_allclose(out_p[0:3, 2 * i + 1], P[0:3, i] - 2.0 * s[b] * rot[:, b], rtol=0, atol=1e-6)
+        for k in (0, 1):
+            np.testing.assert_array_equal(out_p[3:6, 2 * i + k], (P[3:6, i] - np.float32(np.log(1.6))))
+            np.testing.assert_array_equal(out_p[6:, 2 * i + k], P[6:, i])
+    assert not out_m[:, :8].any() and not out_v[:, :8].any()
+    assert not out_p[:, 8:].any()
+
+
+def test_clone_keeps_the_original_moments_and_copies_it():
+    D = oracle.densify
+    th = D.thresholds()
+    P = _dscene(n=3, seed=4)
+    n = 3
+    acc = np.array([1e-3, 0.0, 1e-3], np.float32)
+    cnt = np.array([2, 0, 2])
+    action, offset, n_out = D.plan(P, n, acc, cnt, th)
+    assert action.tolist() == [D.CLONE, D.KEEP, D.CLONE] and offset.tolist() == [0, 2, 3] and n_out == 5
+    rng = np.random.default_rng(1)
+    m = rng.normal(size=P.shape).astype(np.float32)
+    v = np.abs(rng.normal(size=P.shape)).astype(np.float32)
+    out_p, out_m, out_v = D.apply(P, m, v, n, action, offset, n_out, np.zeros((n, 6), np.float32), th)
+    for src, dst in ((0, 0), (1, 2), (2, 3)):
+        np.testing.assert_array_equal(out_p[:, dst], P[:, src])
+        np.testing.assert_array_equal(out_m[:, dst], m[:, src])
+        np.testing.assert_array_equal(out_v[:, dst], v[:, src])
+    for src, dst in ((0, 1), (2, 4)):
+        np.testing.assert_array_equal(out_p[:, dst], P[:, src])
+        assert not out_m[:, dst].any() and not out_v[:, dst].any()
+
+
+def test_densify_count_identity_and_offsets():
+    """N_out = N - pruned - split + cloned + 2 split, offsets strictly increase over
+    the Gaussians that produce output, and every output column is written once."""
+    D = oracle.densify
+    th = D.thresholds(extent=3.3)
+    cfg = gi.CONFIGS["tiny"]
+    P = gi.scene_for(cfg).copy()
+    n = cfg.n
+    P[10, :n:40] = -7.0  # some transparent Gaussians to prune
+    rng = np.random.default_rng(7)
+    acc = rng.exponential(3e-4, n).astype(np.float32)
+    cnt = rng.integers(0, 4, n)
+    action, offset, n_out = D.plan(P, n, acc, cnt, th, prune_big=True)
+    c = np.bincount(action, minlength=4)
+    assert min(c) > 0
+    assert n_out == n - c[D.PRUNE] - c[D.SPLIT] + c[D.CLONE] + 2 * c[D.SPLIT]
+    live = action != D.PRUNE
+    assert np.all(np.diff(offset[live].astype(np.int64)) > 0)
+    out_p, _, _ = D.apply(P, P, P, n, action, offset, n_out, rng.normal(size=(n, 6)).astype(np.float32), th)
+    assert out_p.shape[1] % 256 == 0 and out_p.shape[1] >= n_out
+    written = np.zeros(out_p.shape[1], bool)
+    for i in np.nonzero(live)[0]:
+        written[offset[i]:offset[i] + (1 if action[i] == D.KEEP else 2)] = True
+    assert written[:n_out].all() and not written[n_out:].any()
+
+
+def test_opacity_reset_clamps_to_twice_the_prune_opacity():
+    D = oracle.densify
+    th = D.thresholds()
+    P = _dscene(n=4, seed=5)
+    P[10, :4] = [-6.0, -4.0, 0.0, 3.0]
+    m = np.ones_like(P)
+    v = np.ones_like(P)
+    D.opacity_reset(P, m, v, 4, th)
+    sig = 1.0 / (1.0 + np.exp(-P[10, :4].astype(np.float64)))
+    np.testing.assert_allclose(sig, np.minimum([0.0024726, 0.0179862, 0.5, 0.9525741], 0.01), rtol=1e-5)
+    assert not m[10, :4].any() and not v[10, :4].any() and m[9, 0] == 1.0
+
+
+def test_accumulate_is_the_ndc_scaled_norm():
+    """A gradient of (2a / W, 2b / H) on the projected mean is (a, b) in NDC units:
+    the accumulator gains sqrt(a^2 + b^2) for visible Gaussians and nothing else."""
+    D = oracle.densify
+    W, H = 64, 48
+    g = np.zeros((9, 3), np.float32)
+    g[0] = [2 * 3.0 / W, 2 * 0.5 / W, 1.0]
+    g[1] = [2 * 4.0 / H, 2 * 1.2 / H, 1.0]
+    acc = np.zeros(3, np.float32)
+    cnt = np.zeros(3, np.int64)
+    D.accumulate(g, np.array([True, True, False]), W, H, acc, cnt)
+    D.accumulate(g, np.array([True, False, False]), W, H, acc, cnt)
+    np.testing.assert_allclose(acc, [10.0, 1.3, 0.0], rtol=1e-6)
+    assert cnt.tolist() == [2, 1, 0]
