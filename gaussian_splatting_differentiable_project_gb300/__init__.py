@@ -77,6 +77,15 @@ class GsProj(ctypes.Structure):
                 ("rect", ctypes.c_void_p), ("count", ctypes.c_void_p)]
 
 
+class GsDensifyCfg(ctypes.Structure):
+    _fields_ = [("grad_threshold", ctypes.c_float), ("logit_prune", ctypes.c_float),
+                ("log_grow_scale", ctypes.c_float), ("log_prune_scale", ctypes.c_float),
+                ("prune_big", ctypes.c_int32)]
+
+
+DENSIFY_PRUNE, DENSIFY_KEEP, DENSIFY_CLONE, DENSIFY_SPLIT = 0, 1, 2, 3
+
+
 class GsBins(ctypes.Structure):
     _fields_ = [("keys", ctypes.c_void_p), ("ids", ctypes.c_void_p), ("rec", ctypes.c_void_p),
                 ("ranges", ctypes.c_void_p), ("n_isect", ctypes.c_void_p)]
@@ -133,6 +142,16 @@ def load(build_if_missing: bool = True):
         lib.gs_project_bwd_adam_tdev.restype = st
         lib.gs_step_counter_add.argtypes = [P, ctypes.c_int64, P]
         lib.gs_step_counter_add.restype = st
+        lib.gs_densify_accumulate.argtypes = [GsDims, P, P, ctypes.c_int32, ctypes.c_int32, P, P, P]
+        lib.gs_densify_accumulate.restype = st
+        lib.gs_densify_workspace_bytes.argtypes = [GsDims]
+        lib.gs_densify_workspace_bytes.restype = ctypes.c_size_t
+        lib.gs_densify_plan.argtypes = [GsDims, P, P, P, ctypes.POINTER(GsDensifyCfg), P, P, P, P, ctypes.c_size_t, P]
+        lib.gs_densify_plan.restype = st
+        lib.gs_densify_apply.argtypes = [GsDims, ctypes.c_int64, P, P, P, P, P, P, P, ctypes.c_float, P, P, P, P, P]
+        lib.gs_densify_apply.restype = st
+        lib.gs_opacity_reset.argtypes = [GsDims, P, P, P, ctypes.c_float, P]
+        lib.gs_opacity_reset.restype = st
         lib.gs_ssim_fwd.argtypes = [ctypes.c_int32, ctypes.c_int32, P, P, ctypes.c_float, P, P, P]
         lib.gs_ssim_fwd.restype = st
         lib.gs_ssim_bwd.argtypes = [ctypes.c_int32, ctypes.c_int32, P, P, P, P, P]
@@ -345,6 +364,49 @@ def project_bwd_adam_tdev(n: int, params, cam: dict, proj: ProjBuffers, grad2d, 
 
 def step_counter_add(counter, delta: int = 1, stream=None) -> None:
     _check(load().gs_step_counter_add(_p(counter), int(delta), _stream(stream)), "gs_step_counter_add")
+
+
+def densify_thresholds(extent: float, grow_grad2d: float = 2e-4, grow_scale3d: float = 0.01,
+                       prune_opa: float = 0.005, prune_scale3d: float = 0.1, split_shrink: float = 1.6,
+                       prune_big: bool = False):
+    """The density-control thresholds of the cited 3DGS method, formed in fp64 and
+    rounded to fp32 once: (the plan's configuration, ln split_shrink, the opacity-reset
+    logit of 2 x prune_opa)."""
+    import math
+    cfg = GsDensifyCfg(float(grow_grad2d), math.log(prune_opa / (1.0 - prune_opa)),
+                       math.log(grow_scale3d * extent), math.log(prune_scale3d * extent), int(bool(prune_big)))
+    reset = 2.0 * prune_opa
+    return cfg, float(np.float32(math.log(split_shrink))), float(np.float32(math.log(reset / (1.0 - reset))))
+
+
+def densify_accumulate(n: int, n_pad: int, count, grad2d, width: int, height: int, grad_acc, vis_cnt,
+                       stream=None) -> None:
+    _check(load().gs_densify_accumulate(dims(n, n_pad), _p(count), _p(grad2d), int(width), int(height),
+                                        _p(grad_acc), _p(vis_cnt), _stream(stream)), "gs_densify_accumulate")
+
+
+def densify_plan(n: int, params, grad_acc, vis_cnt, cfg: GsDensifyCfg, action, offset, n_out, workspace,
+                 stream=None) -> None:
+    _check(load().gs_densify_plan(dims(n, params.shape[1]), _p(params), _p(grad_acc), _p(vis_cnt),
+                                  ctypes.byref(cfg), _p(action), _p(offset), _p(n_out), _p(workspace),
+                                  workspace.numel() * workspace.element_size(), _stream(stream)), "gs_densify_plan")
+
+
+def densify_workspace_bytes(n: int, n_pad: int) -> int:
+    return int(load().gs_densify_workspace_bytes(dims(n, n_pad)))
+
+
+def densify_apply(n: int, params, m, v, action, offset, n_out, randn, log_shrink: float, params_dst, m_dst, v_dst,
+                  dev_status, stream=None) -> None:
+    _check(load().gs_densify_apply(dims(n, params.shape[1]), int(params_dst.shape[1]), _p(params), _p(m), _p(v),
+                                   _p(action), _p(offset), _p(n_out), _p(randn), float(log_shrink),
+                                   _p(params_dst), _p(m_dst), _p(v_dst), _p(dev_status), _stream(stream)),
+           "gs_densify_apply")
+
+
+def opacity_reset(n: int, params, m, v, logit_max: float, stream=None) -> None:
+    _check(load().gs_opacity_reset(dims(n, params.shape[1]), _p(params), _p(m), _p(v), float(logit_max),
+                                   _stream(stream)), "gs_opacity_reset")
 
 
 def util_expf(x, y, stream=None) -> None:

@@ -14,9 +14,10 @@ import numpy as np
 
 import math
 
-from . import (BinBuffers, ProjBuffers, GRAD2D_STRIDE, SSIM_MAPS, adam_step, bin_sort, project, project_bwd,
-               project_bwd_accumulate, project_bwd_adam, project_bwd_adam_tdev, render_bwd, render_fwd,
-               ssim_bwd, ssim_fwd, status_str, step_counter_add)
+from . import (BinBuffers, ProjBuffers, GRAD2D_STRIDE, SSIM_MAPS, adam_step, bin_sort, densify_accumulate,
+               densify_apply, densify_plan, densify_thresholds, densify_workspace_bytes, opacity_reset, project,
+               project_bwd, project_bwd_accumulate, project_bwd_adam, project_bwd_adam_tdev, render_bwd,
+               render_fwd, ssim_bwd, ssim_fwd, status_str, step_counter_add)
 
 
 def batch_adam_hyper(batch: int, lr_plane, beta1: float, beta2: float, eps: float):
@@ -104,6 +105,9 @@ class Trainer:
             self.dLdC = torch.empty((3, height, width), dtype=torch.float32, device=device)
             self.ssim_val = torch.zeros(1, dtype=torch.float32, device=device)
         self.t = 0
+        self.capacity = int(capacity)
+        self.device = device
+        self.density = None
 
     # the stages ------------------------------------------------------------------
     def forward(self, cam: dict, stream=None) -> None:
@@ -129,6 +133,7 @@ class Trainer:
 
     def backward(self, cam: dict, target, stream=None) -> None:
         self.loss_backward(cam, target, stream)
+        self.accumulate_density(cam, stream)
         project_bwd(self.n, self.params, cam, self.proj, self.grad2d, self.grads, self.status, stream)
 
     def optimizer_step(self, stream=None) -> None:
@@ -146,6 +151,7 @@ class Trainer:
             self.optimizer_step(stream)
             return
         self.loss_backward(cam, target, stream)
+        self.accumulate_density(cam, stream)
         self.t += 1
         project_bwd_adam(self.n, self.params, cam, self.proj, self.grad2d, self.m, self.v, self.lr_plane, self.beta1,
                          self.beta2, self.eps, self.t, self.status, stream)
@@ -171,6 +177,7 @@ class Trainer:
             self.forward(cam, stream)
             self.loss_backward(cam, target, stream, weight=1.0 / B, loss_out=self.batch_losses[k:k + 1],
                                ssim_out=self.batch_ssim[k:k + 1] if self.dssim > 0.0 else None)
+            self.accumulate_density(cam, stream)
             if self.fused and k == B - 1:
                 project_bwd_adam(self.n, self.params, cam, self.proj, self.grad2d, self.m, self.v, lr_b, b1, b2,
                                  eps_b, self.t, self.status, stream, grads_in=self.grads if B > 1 else None)
@@ -189,6 +196,64 @@ class Trainer:
             s = self.batch_ssim.cpu().numpy().astype(np.float64)
             v += self.dssim * float((1.0 - s).mean())
         return v
+
+    # adaptive density control ---------------------------------------------------------
+    def enable_density_control(self, extent: float, prune_big: bool = False, **thresholds) -> None:
+        """Accumulate each visible Gaussian's NDC-scaled 2D mean-gradient norm after
+        every step's loss backward (for refine) with the cited method's thresholds,
+        ``extent`` being the scene's extent (the cameras' radius x 1.1 there)."""
+        import torch
+        cfg, log_shrink, logit_reset = densify_thresholds(extent, prune_big=prune_big, **thresholds)
+        self.density = {"cfg": cfg, "log_shrink": log_shrink, "logit_reset": logit_reset}
+        self.grad_acc = torch.zeros(self.n_pad, dtype=torch.float32, device=self.device)
+        self.vis_cnt = torch.zeros(self.n_pad, dtype=torch.int32, device=self.device)
+
+    def accumulate_density(self, cam: dict, stream=None) -> None:
+        if self.density is not None:
+            densify_accumulate(self.n, self.n_pad, self.proj.count, self.grad2d, cam["width"], cam["height"],
+                               self.grad_acc, self.vis_cnt, stream)
+
+    def refine(self, randn=None, seed: int = 0) -> dict:
+        """Clone, split and prune by the accumulated gradients (synchronises to read
+        the new count), rebuild the parameter, moment and per-Gaussian buffers at the
+        new size, and clear the accumulators.  ``randn``: (n, 6) fp32 normals for the
+        split children (drawn from ``seed`` when not given).  Returns the counts."""
+        import torch
+        if self.density is None:
+            raise RuntimeError("enable_density_control first")
+        n, dev = self.n, self.device
+        action = torch.empty(max(n, 1), dtype=torch.uint8, device=dev)
+        offset = torch.empty(max(n, 1), dtype=torch.int32, device=dev)
+        n_out = torch.zeros(1, dtype=torch.int32, device=dev)
+        ws = torch.empty(densify_workspace_bytes(n, self.n_pad), dtype=torch.uint8, device=dev)
+        densify_plan(n, self.params, self.grad_acc, self.vis_cnt, self.density["cfg"], action, offset, n_out, ws)
+        n_new = int(n_out.item())
+        n_pad_new = max(256, -(-n_new // 256) * 256)
+        if randn is None:
+            gen = torch.Generator(device=dev)
+            gen.manual_seed(int(seed))
+            randn = torch.randn((max(n, 1), 6), generator=gen, device=dev, dtype=torch.float32)
+        P = torch.empty((self.params.shape[0], n_pad_new), dtype=torch.float32, device=dev)
+        M = torch.empty_like(P)
+        V = torch.empty_like(P)
+        densify_apply(n, self.params, self.m, self.v, action, offset, n_out, randn, self.density["log_shrink"], P, M,
+                      V, self.status)
+        counts = torch.bincount(action[:n].to(torch.int64), minlength=4).tolist() if n else [0, 0, 0, 0]
+        self.params, self.m, self.v = P, M, V
+        self.n, self.n_pad = n_new, n_pad_new
+        self.grads = torch.empty_like(P)
+        self.grad2d = torch.empty((n_pad_new, GRAD2D_STRIDE), dtype=torch.float32, device=dev)
+        self.proj = ProjBuffers(n_pad_new, dev)
+        self.bins = BinBuffers(n_new, self.capacity, self.width, self.height, dev)
+        self.grad_acc = torch.zeros(n_pad_new, dtype=torch.float32, device=dev)
+        self.vis_cnt = torch.zeros(n_pad_new, dtype=torch.int32, device=dev)
+        return {"n": n_new, "pruned": counts[0], "kept": counts[1], "cloned": counts[2], "split": counts[3]}
+
+    def reset_opacity(self, stream=None) -> None:
+        """Clamp opacities to 2 x the prune opacity and zero their Adam moments."""
+        if self.density is None:
+            raise RuntimeError("enable_density_control first")
+        opacity_reset(self.n, self.params, self.m, self.v, self.density["logit_reset"], stream)
 
     # CUDA graphs --------------------------------------------------------------------
     def capture_step(self, cam: dict, target):

@@ -330,6 +330,72 @@ gs_status gs_project_bwd_adam_tdev(gs_dims dims, float* params, const gs_camera*
 gs_status gs_step_counter_add(int64_t* counter, int64_t delta, cudaStream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * Adaptive density control.  "Scaling 3D Gaussian Splatting with Distributed
+ * Compute": adaptive density control clones, splits and prunes Gaussians every
+ * hundred steps (memory-wall section), from 2D position gradients accumulated over the
+ * steps (step walkthrough), starting at step 500 (trace section).  Thresholds and
+ * the split rule are the cited 3DGS method's; the caller forms each threshold in
+ * fp64 and the kernels compare in fp32:
+ *   grow if acc / max(cnt, 1) > grad_threshold (2e-4, the NDC-scaled 2D gradient);
+ *   clone if the largest log-scale <= log_grow_scale (ln(0.01 x scene extent)), else
+ *   split into two children at mu + R(q) diag(exp s) xi_k with log-scales - log_shrink
+ *   (ln 1.6); prune (first) if the opacity logit < logit_prune (ln(0.005 / 0.995)) or,
+ *   with prune_big, the largest log-scale > log_prune_scale (ln(0.1 x extent)). */
+typedef struct gs_densify_cfg {
+  float grad_threshold;
+  float logit_prune;
+  float log_grow_scale;
+  float log_prune_scale;
+  int32_t prune_big;
+} gs_densify_cfg;
+
+#define GS_DENSIFY_PRUNE 0
+#define GS_DENSIFY_KEEP 1
+#define GS_DENSIFY_CLONE 2
+#define GS_DENSIFY_SPLIT 3
+
+/* gs_densify_accumulate -- for each Gaussian i < n with count[i] > 0 (visible in
+ * this view): grad_acc[i] += |(d mx W/2, d my H/2)| from grad2d (gs_render_bwd's
+ * interleaved layout), vis_cnt[i] += 1.  fp32: the two products, their squares,
+ * the sum and the square root each rounded once.
+ *   count (gs_proj.count), grad2d (read); grad_acc n fp32, vis_cnt n uint32 (read
+ *   and write; the caller zeroes them after each refinement).
+ * Errors: GS_ERR_INVALID_ARG for bad dims, sizes or pointers. */
+gs_status gs_densify_accumulate(gs_dims dims, const uint32_t* count, const float* grad2d, int32_t width,
+                                int32_t height, float* grad_acc, uint32_t* vis_cnt, cudaStream_t stream);
+
+/* gs_densify_plan -- per Gaussian i < n its action (GS_DENSIFY_*) and the offset of
+ * its outputs in the new arrays (exclusive scan of 0, 1, 2, 2 outputs for prune,
+ * keep, clone, split, in index order); *n_out = the new count (device).
+ *   params 59 x n_pad (read); action n uint8, offset n uint32, n_out 1 uint32
+ *   (write); workspace >= gs_densify_workspace_bytes(dims), 4-byte aligned.
+ * Errors: GS_ERR_INVALID_ARG for bad dims, pointers or a small workspace. */
+size_t gs_densify_workspace_bytes(gs_dims dims);
+gs_status gs_densify_plan(gs_dims dims, const float* params, const float* grad_acc, const uint32_t* vis_cnt,
+                          const gs_densify_cfg* cfg, uint8_t* action, uint32_t* offset, uint32_t* n_out,
+                          void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* gs_densify_apply -- the new parameter and Adam moment planes (59 x n_pad_dst each)
+ * from a plan.  A kept Gaussian and a clone's original keep their moments; a clone's
+ * copy and a split's two children start with zero moments; the children's means are
+ * mu + R(q) diag(exp s) xi_k with xi = randn[6 i + 3 k .. + 2] (inputs: the method's
+ * random draws), their log-scales s - log_shrink, every other plane copied.
+ * Columns [n_out, n_pad_dst) are cleared.
+ *   n_pad_dst: a multiple of 256 >= *n_out (else GS_ERR_CAPACITY on the device and
+ *   nothing is written); the destination arrays must not overlap the sources.
+ * Errors: GS_ERR_INVALID_ARG for bad dims, pointers, n_pad_dst or log_shrink. */
+gs_status gs_densify_apply(gs_dims src, int64_t n_pad_dst, const float* params, const float* m, const float* v,
+                           const uint8_t* action, const uint32_t* offset, const uint32_t* n_out, const float* randn,
+                           float log_shrink, float* params_dst, float* m_dst, float* v_dst, uint32_t* dev_status,
+                           cudaStream_t stream);
+
+/* gs_opacity_reset -- opacity logit <- min(logit, logit_max) (the method resets
+ * opacities to at most 2 x 0.005 periodically) and the opacity plane's Adam moments
+ * zeroed, for Gaussians i < n.  Errors: GS_ERR_INVALID_ARG for bad dims, pointers or
+ * a non-finite logit_max. */
+gs_status gs_opacity_reset(gs_dims dims, float* params, float* m, float* v, float logit_max, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------
  * gs_bin_sort_noalloc -- gs_bin_sort for callers that must not allocate device
  * memory (for example code that runs where cudaMalloc is not allowed or not
  * wanted after start-up: host callbacks, a render loop with all memory reserved
