@@ -508,22 +508,30 @@ def test_batch_step_matches_oracle(case, fused):
 
 
 def test_batch_of_one_is_the_single_view_step(case):
-    """step_batch with one view runs the same calls as step: the same parameters to
-    within the atomics' summation order."""
+    """step_batch with one view runs the same calls as step: the same loss, and the
+    same parameters wherever the gradient's sign is certain (elsewhere the first Adam
+    step, lr sign(g), follows the atomics' summation order)."""
     P, cam, n = case["P"], case["cam"], case["n"]
     W, H = cam["width"], cam["height"]
-    tgt = torch.from_numpy(_target_for(case)).to(DEV)
+    target = _target_for(case)
+    tgt = torch.from_numpy(target).to(DEV)
     a = gs.Trainer(P, n, W, H, capacity=1 << 20, lr_plane=gi.lr_planes())
     b = gs.Trainer(P, n, W, H, capacity=1 << 20, lr_plane=gi.lr_planes())
     a.step(cam, tgt)
     b.step_batch([cam], [tgt])
     torch.cuda.synchronize()
     assert abs(b.batch_loss() - float(a.loss.item())) <= 1e-6 * float(a.loss.item())
-    x, y = a.params.cpu().numpy().astype(np.float64), b.params.cpu().numpy().astype(np.float64)
-    moved = np.abs(x - P.astype(np.float64)) > 0
-    assert moved.mean() > 0.2
-    close = np.abs(x - y) <= 1e-6 * np.abs(x) + 1e-7
-    assert close.mean() > 0.999, close.mean()
+    z = np.zeros((59, P.shape[1]))
+    gref = oracle.step(P, n, cam, target, z, z, 1, gi.lr_planes())["grads"][:, :n]
+    gscale = np.zeros((59, 1))
+    for lo, hi in GROUPS_59:
+        gscale[lo:hi] = np.abs(gref[lo:hi]).max()
+    defined = np.abs(gref) > 1e-3 * gscale
+    assert defined.mean() > 0.2
+    x = a.params.cpu().numpy()[:, :n].astype(np.float64)
+    y = b.params.cpu().numpy()[:, :n].astype(np.float64)
+    bad = (np.abs(x - y) > 1e-6 * np.abs(x) + 1e-7) & defined
+    assert not bad.any(), bad.sum()
 
 
 def test_device_step_count_equals_host_step_count(case):
