@@ -199,18 +199,35 @@ __global__ void __launch_bounds__(kScanThreads)
   const uint32_t V = *vcount;
   uint64_t round_base = block_prefix[blockIdx.x];
   const int64_t base = int64_t(blockIdx.x) * kScanBlock;
+  // the gathers of round r + 1 (index, then that Gaussian's count and rect) are in
+  // flight while round r is scanned and written out
+  uint32_t g_next = 0, c_next = 0;
+  uint2 rc_next = make_uint2(0u, 0u);
+  {
+    const int64_t i = base + threadIdx.x;
+    if (i < V) {
+      g_next = sorted_ids[i];
+      c_next = count[g_next];
+      rc_next = rect[g_next];
+    }
+  }
 #pragma unroll 1
   for (int r = 0; r < kScanItems; ++r) {
-    const int64_t i = base + int64_t(r) * kScanThreads + threadIdx.x;
-    uint32_t c = 0, g = 0, tx0 = 0, ty0 = 0, w = 1;
-    if (i < V) {
-      g = sorted_ids[i];
-      c = count[g];
-      const uint2 rc = rect[g];
-      tx0 = rc.x & 0xFFFFu;
-      ty0 = rc.x >> 16;
-      w = (rc.y & 0xFFFFu) - tx0 + 1u;
+    const uint32_t g = g_next, c = c_next;
+    const uint2 rc = rc_next;
+    {
+      const int64_t i = base + int64_t(r + 1) * kScanThreads + threadIdx.x;
+      g_next = 0;
+      c_next = 0;
+      rc_next = make_uint2(0u, 0u);
+      if (r + 1 < kScanItems && i < V) {
+        g_next = sorted_ids[i];
+        c_next = count[g_next];
+        rc_next = rect[g_next];
+      }
     }
+    const uint32_t tx0 = rc.x & 0xFFFFu, ty0 = rc.x >> 16;
+    const uint32_t w = c ? (rc.y & 0xFFFFu) - tx0 + 1u : 1u;
     uint32_t total;
     const uint32_t off = block_excl_scan_256(c, s_warp, &total);  // also orders s_hist clear
 #pragma unroll 1
