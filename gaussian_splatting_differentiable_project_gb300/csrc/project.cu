@@ -27,27 +27,50 @@ __device__ __forceinline__ float skip_radius(float lam, float o) {
   return r <= 128.0f ? r : __int_as_float(0x7f7fffff);
 }
 
-__global__ void __launch_bounds__(256, 2)
+constexpr int kProjGroup = 256;                                        // Gaussians per CTA group
+constexpr size_t kProjSmem = size_t(kPlanes) * kProjGroup * sizeof(float);  // 59 planes: 60416 bytes
+
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst));
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(src) : "memory");
+}
+
+// One CTA takes groups of 256 consecutive Gaussians.  The group's 59 parameter
+// planes (60 KB) are first copied into shared memory with cp.async, all of them in
+// flight at once, so one thread per Gaussian then projects from shared memory
+// without the two dependent rounds of global loads (geometry, then SH for the
+// visible) that bound it before.  The frozen operation sequence is unchanged.
+__global__ void __launch_bounds__(kProjGroup, 2)
     k_project(const float* __restrict__ P, int64_t n, int64_t n_pad, CamDev cam, float4* __restrict__ rec,
               float* __restrict__ depth, int32_t* __restrict__ radius, uint2* __restrict__ rect,
               uint32_t* __restrict__ count, uint32_t* __restrict__ dev_status) {
-  const int64_t stride = int64_t(gridDim.x) * blockDim.x;
-  for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n_pad; i += stride) {
+  extern __shared__ __align__(16) float s_p[];  // [kPlanes][kProjGroup]
+  const int tid = threadIdx.x;
+  for (int64_t b0 = int64_t(blockIdx.x) * kProjGroup; b0 < n_pad; b0 += int64_t(gridDim.x) * kProjGroup) {
+    constexpr int kRow4 = kProjGroup / 4;
+    for (int e = tid; e < kPlanes * kRow4; e += kProjGroup) {
+      const int pl = e / kRow4, q = (e % kRow4) * 4;
+      cp_async16(s_p + pl * kProjGroup + q, P + int64_t(pl) * n_pad + b0 + q);
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+    __syncthreads();
+    const int64_t i = b0 + tid;
     Geo g;
     g.visible = false;
     g.nonfinite = false;
-    if (i < n) project_geo(P, n_pad, i, cam, g);
+    if (i < n) project_geo<false>(s_p, kProjGroup, tid, cam, g);
     bool vis = g.visible;
     bool nonfin = g.nonfinite;
     float o = 0.0f, rgb[3] = {0.0f, 0.0f, 0.0f};
     if (vis) {
-      o = opacity_of(ldp(P, n_pad, 10, i));
+      o = opacity_of(s_p[10 * kProjGroup + tid]);
       float d[3], len;
       view_dir(g.mux, g.muy, g.muz, cam, d, &len);
       float Y[16];
       sh_basis(d[0], d[1], d[2], Y);
       bool cl[3];
-      sh_colour(P, n_pad, i, Y, rgb, cl, &nonfin);
+      sh_colour<false>(s_p, kProjGroup, tid, Y, rgb, cl, &nonfin);
       if (nonfin) vis = false;
     }
     if (nonfin) raise_status(dev_status, GS_ERR_NONFINITE);
@@ -65,6 +88,7 @@ __global__ void __launch_bounds__(256, 2)
       rect[i] = make_uint2(0u, 0u);
       count[i] = 0u;
     }
+    __syncthreads();  // the group's planes are read before the next group is staged
   }
 }
 
@@ -77,10 +101,15 @@ extern "C" gs_status gs_project(gs_dims dims, const float* params, const gs_came
   if (!proj.rec || !proj.depth || !proj.radius || !proj.rect || !proj.count) return GS_ERR_INVALID_ARG;
   if (!aligned(params, 16) || !aligned(proj.rec, 16) || !aligned(proj.rect, 8)) return GS_ERR_INVALID_ARG;
   if (dims.n == 0 && dims.n_pad == 0) return GS_OK;
-  const int threads = 256;
-  const int blocks = grid_for(dims.n_pad, threads, kSmCount * 64);
-  k_project<<<blocks, threads, 0, stream>>>(params, dims.n, dims.n_pad, cam_dev(*cam),
-                                            reinterpret_cast<float4*>(proj.rec), proj.depth, proj.radius,
-                                            reinterpret_cast<uint2*>(proj.rect), proj.count, dev_status);
+  static bool attr_set = false;
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(k_project, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kProjSmem)) != cudaSuccess)
+      return GS_ERR_CUDA;
+    attr_set = true;
+  }
+  const int blocks = grid_for(dims.n_pad / kProjGroup, 1, kSmCount * 2);
+  k_project<<<blocks, kProjGroup, kProjSmem, stream>>>(params, dims.n, dims.n_pad, cam_dev(*cam),
+                                                      reinterpret_cast<float4*>(proj.rec), proj.depth, proj.radius,
+                                                      reinterpret_cast<uint2*>(proj.rect), proj.count, dev_status);
   return launch_status();
 }

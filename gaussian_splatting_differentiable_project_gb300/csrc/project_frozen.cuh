@@ -76,7 +76,8 @@ struct Geo {
 };
 
 // Parameter load.  kReadOnly uses the read-only data path; kernels that also write
-// the parameter planes (the fused projection backward + Adam) use plain loads.
+// the parameter planes (the fused projection backward + Adam) or read them from
+// shared memory (the staged projection) use plain loads.
 template <bool kReadOnly = true>
 __device__ __forceinline__ float ldp(const float* P, int64_t n_pad, int plane, int64_t i) {
   if (kReadOnly) return __ldg(P + int64_t(plane) * n_pad + i);
@@ -244,13 +245,14 @@ __device__ __forceinline__ void view_dir(float mux, float muy, float muz, const 
 
 // Colour: max(0, sum_k Y_k sh_k + 0.5) per channel, with the clamp flags; sets
 // *nonfinite if any SH coefficient is NaN/Inf.
+template <bool kReadOnly = true>
 __device__ __forceinline__ void sh_colour(const float* __restrict__ P, int64_t n_pad, int64_t i,
                                           const float Y[16], float rgb[3], bool clamped[3], bool* nonfinite) {
   float acc[3];
   bool fin = true;
 #pragma unroll
   for (int ch = 0; ch < 3; ++ch) {
-    const float sh = ldp(P, n_pad, 11 + ch, i);
+    const float sh = ldp<kReadOnly>(P, n_pad, 11 + ch, i);
     fin = fin && isfinite(sh);
     acc[ch] = __fmul_rn(Y[0], sh);
   }
@@ -258,7 +260,7 @@ __device__ __forceinline__ void sh_colour(const float* __restrict__ P, int64_t n
   for (int k = 1; k < 16; ++k) {
 #pragma unroll
     for (int ch = 0; ch < 3; ++ch) {
-      const float sh = ldp(P, n_pad, 11 + 3 * k + ch, i);
+      const float sh = ldp<kReadOnly>(P, n_pad, 11 + 3 * k + ch, i);
       fin = fin && isfinite(sh);
       acc[ch] = __fmaf_rn(Y[k], sh, acc[ch]);
     }
