@@ -306,7 +306,16 @@ __global__ void __launch_bounds__(kSortThreads)
   for (int it = 0; it < kSortItems; ++it) {
     const uint32_t idx = wbase + uint32_t(it) * 32 + uint32_t(lane);
     const uint32_t d = (idx < K) ? (key[it] >> shift) & 0xFFu : 256u;
-    const uint32_t peers = __match_any_sync(0xffffffffu, d);
+    // lanes holding the same digit: eight ballots, one per digit bit, narrow the
+    // warp to this lane's digit class (the out-of-range marker 256 forms its own
+    // class through the ninth bit)
+    uint32_t peers = __ballot_sync(0xffffffffu, d >> 8);
+    peers = (d >> 8) ? peers : ~peers;
+#pragma unroll
+    for (int bit = 0; bit < 8; ++bit) {
+      const uint32_t b = __ballot_sync(0xffffffffu, (d >> bit) & 1u);
+      peers &= ((d >> bit) & 1u) ? b : ~b;
+    }
     const int leader = __ffs(peers) - 1;
     uint32_t old = 0;
     if (d < 256u && lane == leader) {
