@@ -477,6 +477,8 @@ def run_gb300(args, cfg, ws, rank, local):
     tr.raise_on_status()
     stage_ms = ({name: float(np.mean([ev[s][i].elapsed_time(ev[s][i + 1]) for s in range(K)]))
                  for i, name in enumerate(STAGES)} if B == 1 and not graphs else None)
+    # per-step device time (first to last stage event of each step)
+    step_ms = ([ev[s][0].elapsed_time(ev[s][len(STAGES)]) for s in range(K)] if stage_ms is not None else None)
     value = whole_job_rate(ws, K, ms)
 
     # ---------------------------------------------------------------- e2e leg
@@ -592,6 +594,8 @@ def run_gb300(args, cfg, ws, rank, local):
         "views_per_s": value * B,
         "roofline": roof,
         "step_roofline_frac": t_star / (ms / K / 1e3),
+        "step_ms_median": float(np.median(step_ms)) if step_ms else None,
+        "step_ms_p90": float(np.percentile(step_ms, 90)) if step_ms else None,
         "stages_ms": stage_ms, "stages": per_stage,
         "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches_per_step * K,
         "clocks": clk, "setup_s": setup_s,
