@@ -4,20 +4,22 @@
 // It is produced by two onesweep radix sorts that move fewer bytes than one sort of
 // the 64-bit keys:
 //   1. the visible Gaussians, compacted in index order, sorted stably by their 32-bit
-//      depth bits (4 passes over V elements);
+//      depth bits less the smallest visible depth bits (4 passes over V elements);
 //   2. one (tile, index) pair per intersection, emitted in that depth order, sorted
 //      stably by tile (ceil(tile bits / 8) passes over K elements).
 // Within a tile the pairs keep the depth order with ties by index, which is the order
 // of the 64-bit keys; the keys themselves are written in the final gather.
 //
 // Kernels, in stream order:
-//   k_bs_prep          per 4096 Gaussians: the visible count and the sum of tile
-//                      counts; clears histograms, tickets, look-back words and the
-//                      tile ranges (the workspace needs no initialisation)
-//   k_bs_scan_sums x2  one block each: exclusive scan of the visible counts -> V; sum
-//                      of the tile counts -> K = n_isect (capacity check)
-//   k_bs_compact       visible Gaussians in index order -> (depth bits, index); digit
-//                      histograms of the depth passes
+//   k_bs_prep          per 4096 Gaussians: the visible count, the sum of tile counts
+//                      and the smallest visible depth bits; clears histograms,
+//                      tickets, look-back words and the tile ranges (the workspace
+//                      needs no initialisation)
+//   k_bs_scan_sums x2  one block each: exclusive scan of the visible counts -> V and
+//                      the smallest depth bits; sum of the tile counts -> K = n_isect
+//                      (capacity check)
+//   k_bs_compact       visible Gaussians in index order -> (depth bits - smallest,
+//                      index); digit histograms of the depth passes
 //   k_bs_onesweep x4   depth passes
 //   k_bs_sorted_sums   per 4096 depth-sorted Gaussians: sum of tile counts
 //   k_bs_scan_sums     one block: exclusive scan of those sums
@@ -28,9 +30,10 @@
 //   k_bs_ranges_gather per intersection: tile [start, end), the 64-bit key (the depth
 //                      is in the record's last slot) and the 48-byte record gathered
 // A onesweep pass: CTAs take 4096-key partitions in ticket order, rank their keys
-// stably by digit (match_any per warp, per-warp histograms), publish per-digit
+// stably by digit (nine ballots per warp, per-warp histograms), publish per-digit
 // aggregates and look back over earlier partitions (bounded wait), then scatter
-// through shared memory so each digit's run leaves contiguously.
+// through shared memory so each digit's run leaves contiguously.  A pass whose
+// histogram puts every key at digit 0 is the identity and only copies.
 #include "api_util.h"
 #include "binsort_layout.h"
 #include "block_scan.cuh"
@@ -66,10 +69,11 @@ __device__ __forceinline__ uint64_t block_sum_256(uint64_t v, uint64_t* s_warp /
 
 // ------------------------------------------------------------------ kernels
 __global__ void __launch_bounds__(kScanThreads)
-    k_bs_prep(const uint32_t* __restrict__ count, int64_t n, int64_t n_blocks, uint64_t* __restrict__ block_vis,
-              uint64_t* __restrict__ block_cnt, uint4* __restrict__ zero, int64_t zero_vec,
-              uint2* __restrict__ ranges, int64_t tiles) {
+    k_bs_prep(const uint32_t* __restrict__ count, const float* __restrict__ depth, int64_t n, int64_t n_blocks,
+              uint64_t* __restrict__ block_vis, uint64_t* __restrict__ block_cnt, uint64_t* __restrict__ block_min,
+              uint4* __restrict__ zero, int64_t zero_vec, uint2* __restrict__ ranges, int64_t tiles) {
   __shared__ uint64_t s_w[8];
+  __shared__ uint32_t s_min[8];
   // clearing (every block takes a grid-strided share)
   const int64_t gstride = int64_t(gridDim.x) * blockDim.x;
   const int64_t gid = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -78,35 +82,56 @@ __global__ void __launch_bounds__(kScanThreads)
   if (blockIdx.x >= n_blocks) return;
   const int64_t base = int64_t(blockIdx.x) * kScanBlock;
   uint64_t s = 0;
-  uint32_t v = 0;
+  uint32_t v = 0, mn = ~0u;
 #pragma unroll 4
   for (int it = 0; it < kScanItems; ++it) {
     const int64_t i = base + int64_t(it) * kScanThreads + threadIdx.x;
     const uint32_t c = (i < n) ? count[i] : 0u;
     s += c;
     v += (c > 0u);
+    if (c > 0u) mn = min(mn, __float_as_uint(depth[i]));
   }
-  const uint64_t tv = block_sum_256(v, s_w);
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+  if ((threadIdx.x & 31) == 0) s_min[threadIdx.x >> 5] = mn;
+  const uint64_t tv = block_sum_256(v, s_w);  // its barriers order s_min
   const uint64_t ts = block_sum_256(s, s_w);
   if (threadIdx.x == 0) {
+    for (int w = 0; w < 8; ++w) mn = min(mn, s_min[w]);
     block_vis[blockIdx.x] = tv;
     block_cnt[blockIdx.x] = ts;
+    block_min[blockIdx.x] = mn;
   }
 }
 
 // One block: exclusive scan of n_blocks 64-bit sums in place; the total goes to
 // *total (clamped to 32 bits) when total is not null, with GS_ERR_CAPACITY raised if
-// it exceeds cap.
+// it exceeds cap.  With block_min not null, the smallest of its n_blocks entries
+// goes to *min_out as well.
 __global__ void __launch_bounds__(1024)
     k_bs_scan_sums(uint64_t* __restrict__ block_sums, int64_t n_blocks, uint32_t* __restrict__ total, uint64_t cap,
-                   uint32_t* __restrict__ dev_status) {
+                   uint32_t* __restrict__ dev_status, const uint64_t* __restrict__ block_min = nullptr,
+                   uint32_t* __restrict__ min_out = nullptr) {
   __shared__ uint64_t s_part[1024];
+  __shared__ uint32_t s_min[32];
   const int t = threadIdx.x;
   const int64_t per = (n_blocks + 1023) / 1024;
   const int64_t b0 = int64_t(t) * per, b1 = min(n_blocks, b0 + per);
   uint64_t s = 0;
   for (int64_t b = b0; b < b1; ++b) s += block_sums[b];
   s_part[t] = s;
+  if (block_min) {
+    uint32_t mn = ~0u;
+    for (int64_t b = b0; b < b1; ++b) mn = min(mn, uint32_t(block_min[b]));
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+    if ((t & 31) == 0) s_min[t >> 5] = mn;
+    __syncthreads();
+    if (t == 0) {
+      for (int w = 0; w < 32; ++w) mn = min(mn, s_min[w]);
+      *min_out = mn;
+    }
+  }
   __syncthreads();
   // Hillis-Steele inclusive scan over 1024 partial sums
   for (int o = 1; o < 1024; o <<= 1) {
@@ -128,16 +153,20 @@ __global__ void __launch_bounds__(1024)
   }
 }
 
-// Visible Gaussians (count > 0) in index order -> (depth bits, index) at their
-// compacted positions; histograms of the four 8-bit digits of the depth bits.
+// Visible Gaussians (count > 0) in index order -> (depth bits - smallest visible depth
+// bits, index) at their compacted positions; histograms of the four 8-bit digits of
+// those keys.  Positive fp32 depths order like their bits, and subtracting the
+// smallest keeps that order; a scene whose depths lie within a factor of about four
+// then has keys below 2^24, and the last depth pass finds every digit 0.
 __global__ void __launch_bounds__(kScanThreads)
     k_bs_compact(const uint32_t* __restrict__ count, const float* __restrict__ depth, int64_t n,
-                 const uint64_t* __restrict__ block_prefix, uint32_t* __restrict__ dk, uint32_t* __restrict__ dv,
-                 uint32_t* __restrict__ hist) {
+                 const uint64_t* __restrict__ block_prefix, const uint32_t* __restrict__ key_min,
+                 uint32_t* __restrict__ dk, uint32_t* __restrict__ dv, uint32_t* __restrict__ hist) {
   __shared__ uint32_t s_warp[8];
   __shared__ uint32_t s_hist[kDepthPasses * 256];
   for (int k = threadIdx.x; k < kDepthPasses * 256; k += kScanThreads) s_hist[k] = 0;
   uint64_t pos = block_prefix[blockIdx.x];
+  const uint32_t kmin = *key_min;
   const int64_t base = int64_t(blockIdx.x) * kScanBlock;
 #pragma unroll 1
   for (int r = 0; r < kScanItems; ++r) {
@@ -146,7 +175,7 @@ __global__ void __launch_bounds__(kScanThreads)
     uint32_t total;
     const uint32_t off = block_excl_scan_256(f ? 1u : 0u, s_warp, &total);  // also orders s_hist clear
     if (f) {
-      const uint32_t key = __float_as_uint(depth[i]);
+      const uint32_t key = __float_as_uint(depth[i]) - kmin;
       dk[pos + off] = key;
       dv[pos + off] = uint32_t(i);
 #pragma unroll
@@ -178,7 +207,11 @@ __global__ void __launch_bounds__(kScanThreads)
   if (threadIdx.x == 0) block_sums[blockIdx.x] = t;
 }
 
-constexpr int kEmitStage = 4096;  // pairs staged in shared memory per write-out chunk
+// Pairs staged in shared memory per write-out chunk.  A round of 256 Gaussians
+// averages about 800 pairs, and 2048 keeps a block at 20 KB of shared memory; with
+// at most 32 registers a thread, eight blocks fit on an SM and 4M Gaussians (977
+// blocks) run in one wave.
+constexpr int kEmitStage = 2048;
 
 // Emission: a block owns depth-sorted positions [block * 4096, +4096) and the
 // contiguous output range [block_prefix, block_prefix + block total).  It walks them
@@ -186,7 +219,7 @@ constexpr int kEmitStage = 4096;  // pairs staged in shared memory per write-out
 // gives each Gaussian's offset, and the round's (tile, index) pairs are staged through
 // shared memory so that they leave in contiguous, coalesced runs.  The digit
 // histograms of every tile pass are accumulated on the way out.
-__global__ void __launch_bounds__(kScanThreads)
+__global__ void __launch_bounds__(kScanThreads, 8)
     k_bs_emit(const uint32_t* __restrict__ sorted_ids, const uint32_t* __restrict__ vcount,
               const uint32_t* __restrict__ count, const uint2* __restrict__ rect,
               const uint64_t* __restrict__ block_prefix, uint32_t* __restrict__ tk, uint32_t* __restrict__ tv,
@@ -235,10 +268,19 @@ __global__ void __launch_bounds__(kScanThreads)
       // this thread's pairs k in [0, c) whose round offset off + k lies in the chunk
       const uint32_t lo = (c0 > off) ? c0 - off : 0u;
       const uint32_t hi = min(c, (c0 + kEmitStage > off) ? c0 + kEmitStage - off : 0u);
-      for (uint32_t k = lo; k < hi; ++k) {
-        const uint32_t ty = ty0 + k / w, tx = tx0 + k % w;
-        s_key[off + k - c0] = ty * uint32_t(TX) + tx;
-        s_id[off + k - c0] = g;
+      if (lo < hi) {
+        // pair k is tile (tx0 + k % w, ty0 + k / w): one division, then row-major steps
+        uint32_t ky = lo / w, kx = lo - ky * w;
+        uint32_t t = (ty0 + ky) * uint32_t(TX) + tx0 + kx;
+        for (uint32_t k = lo; k < hi; ++k) {
+          s_key[off + k - c0] = t;
+          s_id[off + k - c0] = g;
+          ++t;
+          if (++kx == w) {
+            kx = 0;
+            t += uint32_t(TX) - w;
+          }
+        }
       }
       __syncthreads();
       const uint32_t m = min(uint32_t(kEmitStage), total - c0);
@@ -276,6 +318,15 @@ __global__ void __launch_bounds__(kSortThreads)
   __shared__ uint32_t s_part;
 
   const uint32_t K = min(*n_ptr, cap);
+  if (hist[0] == K) {
+    // every key has digit 0 here: the stable pass is the identity, so copy
+    const uint32_t lo = blockIdx.x * uint32_t(kPart), hi = min(K, lo + uint32_t(kPart));
+    for (uint32_t i = lo + threadIdx.x; i < hi; i += kSortThreads) {
+      kout[i] = kin[i];
+      vout[i] = vin[i];
+    }
+    return;
+  }
   if (threadIdx.x == 0) s_part = atomicAdd(ticket, 1u);
   for (int k = threadIdx.x; k < kSortWarps * 256; k += kSortThreads) s_whist[k] = 0;
   __syncthreads();
@@ -447,19 +498,21 @@ extern "C" gs_status gs_bin_sort(gs_dims dims, const gs_proj* proj, const gs_cam
   // 1. per-block visible counts and tile-count sums + clearing
   const int clear_blocks = kSmCount * 4;
   const int b1 = int(L.n_blocks > clear_blocks ? L.n_blocks : clear_blocks);
-  k_bs_prep<<<b1, kScanThreads, 0, stream>>>(proj->count, dims.n, L.n_blocks, block_vis, block_cnt,
-                                              reinterpret_cast<uint4*>(ws + L.zero_begin), int64_t(L.zero_bytes / 16),
-                                              reinterpret_cast<uint2*>(bins.ranges), tiles);
-  // 2. V (and the compaction offsets); K (capacity check)
-  k_bs_scan_sums<<<1, 1024, 0, stream>>>(block_vis, L.n_blocks, vcount, ~0ull, dev_status);
+  // (block_sums is free until step 5 and holds the per-block smallest depth bits)
+  k_bs_prep<<<b1, kScanThreads, 0, stream>>>(proj->count, proj->depth, dims.n, L.n_blocks, block_vis, block_cnt,
+                                              block_sums, reinterpret_cast<uint4*>(ws + L.zero_begin),
+                                              int64_t(L.zero_bytes / 16), reinterpret_cast<uint2*>(bins.ranges),
+                                              tiles);
+  // 2. V (and the compaction offsets), the smallest visible depth bits; K (capacity check)
+  k_bs_scan_sums<<<1, 1024, 0, stream>>>(block_vis, L.n_blocks, vcount, ~0ull, dev_status, block_sums, vcount + 1);
   k_bs_scan_sums<<<1, 1024, 0, stream>>>(block_cnt, L.n_blocks, bins.n_isect, capacity_K, dev_status);
   // 3. compaction + depth digit histograms, 4. depth passes (even: ends in A)
   uint32_t* dkA = reinterpret_cast<uint32_t*>(ws + L.dkA());
   uint32_t* dvA = reinterpret_cast<uint32_t*>(ws + L.dvA);
   uint32_t* dkB = reinterpret_cast<uint32_t*>(ws + L.dkB(dims.n));
   uint32_t* dvB = reinterpret_cast<uint32_t*>(ws + L.dvB(dims.n));
-  k_bs_compact<<<int(L.n_blocks), kScanThreads, 0, stream>>>(proj->count, proj->depth, dims.n, block_vis, dkA, dvA,
-                                                             hist);
+  k_bs_compact<<<int(L.n_blocks), kScanThreads, 0, stream>>>(proj->count, proj->depth, dims.n, block_vis,
+                                                             vcount + 1, dkA, dvA, hist);
   {
     uint32_t *ka = dkA, *va = dvA, *kb = dkB, *vb = dvB;
     for (int p = 0; p < kDepthPasses; ++p) {

@@ -179,6 +179,48 @@ def test_bin_sort_deterministic(case):
     assert torch.equal(tr.image, img0)
 
 
+def _depth_scene(depths, seed):
+    """The tiny scene with its means moved to the given camera depths, inside the
+    field of view, for the camera at (0, 0, 3) looking at the origin."""
+    cfg = gi.CONFIGS["tiny"]
+    n = len(depths)
+    P = gi.scene_for(cfg, n=n, seed=seed).copy()
+    cam = gi.camera((0.0, 0.0, 3.0), 128, 128)
+    rng = np.random.default_rng(seed)
+    xy = rng.uniform(-0.4, 0.4, (n, 2)) * depths[:, None]
+    c = np.stack([xy[:, 0], xy[:, 1], depths], 1)
+    R = cam["R"].astype(np.float64)
+    t = cam["t"].astype(np.float64)
+    P[0:3, :n] = ((c - t) @ R).T.astype(np.float32)  # world = R^T (c - t)
+    P[3:6, :n] = np.log(0.004 * depths)[None, :].astype(np.float32)  # a few pixels wide at any depth
+    return P, n, cam
+
+
+@pytest.mark.parametrize("span", ["wide", "narrow"])
+def test_bin_sort_depth_ranges(span):
+    """Depths over four decades make every depth digit vary; depths within a few
+    ulps of 3 leave the upper three digits constant, so those passes are identities.
+    Both must give the oracle's keys and ids."""
+    rng = np.random.default_rng(5)
+    if span == "wide":
+        d = np.exp(rng.uniform(np.log(0.05), np.log(500.0), 3000))
+    else:
+        d = 3.0 + rng.integers(-40, 40, 3000) * 2.4e-7  # +-40 ulps of 3
+    P, n, cam = _depth_scene(d, 6)
+    ref = oracle.project(P, n, cam, 32)
+    vis = ref["count"] > 0
+    assert vis.sum() > 2000
+    bits = ref["depth"][vis].view(np.uint32).astype(np.int64)
+    spread = int(bits.max() - bits.min())
+    assert spread >= (1 << 24) if span == "wide" else spread < (1 << 8)
+    tr = _gpu_forward(P, n, cam)
+    tl = oracle.tile_lists(ref, cam["width"], cam["height"])
+    K = tr.n_isect()
+    assert K == tl["K"] and tr.check_status() == 0
+    np.testing.assert_array_equal(tr.bins.keys.cpu().numpy()[:K].view(np.uint64), tl["keys"])
+    np.testing.assert_array_equal(_u32(tr.bins.ids)[:K], tl["ids"])
+
+
 # ----------------------------------------------------------------------------- forward
 
 def test_render_fwd_parity(case):
