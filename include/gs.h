@@ -281,7 +281,9 @@ gs_status gs_project_bwd_accumulate(gs_dims dims, const float* params, const gs_
  *   p -= (lr[plane] / (1 - beta1^t)) m / (sqrt(v) / sqrt(1 - beta2^t) + eps)
  * The hyperparameters arrive in fp64; 1 - beta, the bias corrections and the
  * per-plane step sizes are formed on the host in fp64 and rounded to fp32 once
- * (so that, e.g., 1 - 0.999 is not taken from an fp32 0.999).
+ * (so that, e.g., 1 - 0.999 is not taken from an fp32 0.999).  The square root and
+ * the division of the update are the hardware approximations (relative error of
+ * order 2^-22), which move p by about 1e-6 of the step size.
  *   params, m, v: 59 x n_pad fp32 (read and write, 16-byte aligned);
  *   grads 59 x n_pad (read); lr_plane: 59 floats (host); t >= 1 the step count.
  * Errors: GS_ERR_INVALID_ARG for null/misaligned pointers, bad sizes, t < 1 or
