@@ -156,7 +156,7 @@ __global__ void __launch_bounds__(kRasterThreads)
     // 32 entries at a time, from the top: cull against the warp's block with one
     // ballot, then walk the set bits from the highest down.
     for (int j0 = ((jmax - 1) >> 5) << 5; j0 >= 0 && jmax > 0; j0 -= 32) {
-      uint32_t mask = warp_cull(R, j0, jmax, bx0, bx1, by0, by1);
+      uint32_t mask = warp_cull_ellipse(R, j0, jmax, bx0, bx1, by0, by1);
       while (mask) {
         const int hb = 31 - __clz(mask);
         mask &= ~(1u << hb);
