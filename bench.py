@@ -8,9 +8,9 @@ and synthetic and resident on the GPU before the timed region; parameters, Adam
 state and targets (22.5 GB) exceed L2 many times over, so no flush is needed.
 
 One JSON line is printed (rank 0).  Besides the device-timed value it carries:
-  e2e           the same steps through the public API with each step's target
-                copied from pinned host memory (on a copy stream, overlapping the
-                previous step) and its loss read back;
+  e2e           the same steps (from the same model state) through the public API
+                with each step's target copied from pinned host memory (on a copy
+                stream, overlapping the previous step) and its loss read back;
   roofline      for the kernel with the largest share of step time;
   cpu_baseline  the CPU oracle timed on this host on a bounded sample;
   stages_ms     per-stage device time per step (CUDA events on the stream);
@@ -450,6 +450,10 @@ def run_gb300(args, cfg, ws, rank, local):
                 graphs[v] = tr.capture_step(cams[v], targets[v])
         torch.cuda.synchronize()
 
+    # the model state the timed steps start from: the end-to-end leg restarts from it,
+    # so that both legs time the same steps (training changes the per-step work)
+    snap = (tr.params.clone(), tr.m.clone(), tr.v.clone(), tr.t) if not args.no_e2e else None
+
     # ---------------------------------------------------------------- timed region
     K = args.steps
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(STAGES) + 1)] for _ in range(K)]
@@ -485,6 +489,11 @@ def run_gb300(args, cfg, ws, rank, local):
     e2e = None
     if not args.no_e2e:
         graphs.clear()  # they read the device-resident targets freed below
+        tr.params.copy_(snap[0])
+        tr.m.copy_(snap[1])
+        tr.v.copy_(snap[2])
+        tr.t = snap[3]
+        del snap
         host_t = torch.empty_like(targets, device="cpu").pin_memory()
         host_t.copy_(targets)
         del targets
