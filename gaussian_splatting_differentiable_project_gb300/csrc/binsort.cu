@@ -394,24 +394,37 @@ __global__ void __launch_bounds__(kSortThreads)
   const uint32_t gstart = block_excl_scan_256(hist[d], s_warp, nullptr);
   const uint32_t lstart = block_excl_scan_256(tot, s_warp, nullptr);
 
+  // Look back in windows of kLookWindow predecessors: their words are loaded
+  // together, then walked from the nearest, adding aggregates up to the first
+  // inclusive prefix; a word not yet published is re-read (bounded) until it is.
   uint32_t excl = 0;
   if (part > 0) {
     int64_t j = int64_t(part) - 1;
     int spins = 0;
-    for (;;) {
-      const uint32_t w = ld_relaxed(look + size_t(j) * 256 + d);
-      const uint32_t f = w & ~kCountMask;
-      if (f == 0u) {
-        if (++spins > kSpinLimit) {
-          raise_status(dev_status, GS_ERR_TIMEOUT);
-          break;
+    bool done = false;
+    while (!done) {
+      uint32_t w[kLookWindow];
+#pragma unroll
+      for (int k = 0; k < kLookWindow; ++k)
+        w[k] = (j - k >= 0) ? ld_relaxed(look + size_t(j - k) * 256 + d) : kFlagInc;
+#pragma unroll
+      for (int k = 0; k < kLookWindow; ++k) {
+        if (!done) {
+          uint32_t v = w[k];
+          while ((v & ~kCountMask) == 0u) {
+            if (++spins > kSpinLimit) {
+              raise_status(dev_status, GS_ERR_TIMEOUT);
+              v = kFlagInc;
+              break;
+            }
+            __nanosleep(32);
+            v = ld_relaxed(look + size_t(j - k) * 256 + d);
+          }
+          excl += v & kCountMask;
+          if ((v & ~kCountMask) == kFlagInc || j - k == 0) done = true;
         }
-        __nanosleep(32);
-        continue;
       }
-      excl += w & kCountMask;
-      if (f == kFlagInc || j == 0) break;
-      --j;
+      j -= kLookWindow;
     }
     st_relaxed(mine, kFlagInc | (excl + tot));
   }

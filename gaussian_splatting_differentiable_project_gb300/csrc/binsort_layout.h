@@ -21,6 +21,7 @@ constexpr uint32_t kFlagAgg = 1u << 30;
 constexpr uint32_t kFlagInc = 2u << 30;
 constexpr uint32_t kCountMask = (1u << 30) - 1u;
 constexpr int kSpinLimit = 1 << 22;
+constexpr int kLookWindow = 4;  // predecessors read at once in a look-back
 constexpr size_t kSortSmem = size_t(kPart) * 8 + size_t(kSortWarps) * 256 * 4;  // 40 KB
 
 constexpr size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
