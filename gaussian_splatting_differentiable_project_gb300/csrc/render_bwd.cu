@@ -130,7 +130,7 @@ __global__ void __launch_bounds__(kRasterThreads)
   n_max = min(n_max, end - start);
   if (n_max == 0) return;
 
-  BatchStager st{srec + start, n_max, s_rec[0], s_rec[1], s_bar};
+  BatchStager<kBatch> st{srec + start, n_max, &s_rec[0][0], s_bar};
   const int nb = int((n_max + kBatch - 1) / kBatch);
   if (threadIdx.x == 0) {
     mbar_init(&s_bar[0], 1);

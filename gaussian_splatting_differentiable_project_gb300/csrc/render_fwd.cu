@@ -1,7 +1,7 @@
 // gs_render_fwd: per-tile front-to-back alpha compositing.
 //
 // One CTA per 8x8 quarter of a 16x16 tile, one thread per pixel.  The tile's
-// sorted records are staged into shared memory in batches of 64 (3 KB) by
+// sorted records are staged into shared memory in batches of 96 (4.5 KB) by
 // cp.async.bulk with two mbarrier-tracked buffers, so the next batch streams in
 // while the current one is composited; every thread reads the same record
 // (shared-memory broadcast).  A pixel stops at its transmittance threshold; the
@@ -15,7 +15,7 @@ __global__ void __launch_bounds__(kRasterThreads)
     k_render_fwd(const Rec* __restrict__ srec, const uint2* __restrict__ ranges, const uint32_t* __restrict__ n_isect,
                  uint32_t cap, int W, int H, int TX, float bg0, float bg1, float bg2, float* __restrict__ image,
                  float* __restrict__ T_final, uint32_t* __restrict__ n_contrib, uint32_t* __restrict__ dev_status) {
-  __shared__ __align__(128) Rec s_rec[2][kBatch];
+  __shared__ __align__(128) Rec s_rec[2][kBatchFwd];
   __shared__ __align__(8) uint64_t s_bar[2];
 
   const int tile = tile_of_block();
@@ -36,8 +36,8 @@ __global__ void __launch_bounds__(kRasterThreads)
   bool done = !inside;
 
   if (n > 0) {
-    BatchStager st{srec + start, n, s_rec[0], s_rec[1], s_bar};
-    const int nb = int((n + kBatch - 1) / kBatch);
+    BatchStager<kBatchFwd> st{srec + start, n, &s_rec[0][0], s_bar};
+    const int nb = int((n + kBatchFwd - 1) / kBatchFwd);
     if (threadIdx.x == 0) {
       mbar_init(&s_bar[0], 1);
       mbar_init(&s_bar[1], 1);
@@ -54,7 +54,7 @@ __global__ void __launch_bounds__(kRasterThreads)
       mbar_wait(&s_bar[slot], uint32_t((b >> 1) & 1), dev_status);
       const Rec* R = st.buffer(slot);
       const int cnt = int(st.count(b));
-      const uint32_t pos0 = uint32_t(b) * kBatch;
+      const uint32_t pos0 = uint32_t(b) * kBatchFwd;
       // Warp-uniform walk over the batch: 32 entries at a time are culled against
       // the warp's 8x4 block by one ballot, then the warp steps through the set
       // bits in order; every lane takes its skip / stop decisions as predicates,
