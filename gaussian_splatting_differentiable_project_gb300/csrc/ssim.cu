@@ -6,6 +6,10 @@
 // a horizontal 11-tap pass writes the 42 staged rows x 32 columns, and a vertical pass
 // finishes in registers.  In each pass a thread produces 4 adjacent outputs from a
 // 14-value window held in registers, so a staged value is read once per 4 outputs.
+// Staging is by cp.async (4 bytes per value, zero-filled outside the image), so all of
+// a channel's loads are in flight together and hold no registers; the next channel's
+// staging is issued as soon as the horizontal pass has read the current one, and
+// lands while the vertical pass and the per-pixel work run.
 //
 // gs_ssim_fwd: the local means, variances and covariance, then per pixel the partial
 //   derivatives of S times dL/dS = -lambda / (3 H W):
@@ -57,19 +61,38 @@ inline SsimWindow ssim_window() {
   return w;
 }
 
-// Stage NQ planes of channel c (plane q at base[q] + c P) with the halo into
-// s[q][42][43]; values outside the image are 0, and shift[q] is subtracted from all.
+// 4-byte cp.async global -> shared; with `in` false nothing is read and the 4 bytes
+// are zero-filled (src must still be a valid address).
+__device__ __forceinline__ void cp_async4_zfill(float* dst, const float* src, bool in) {
+  const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst));
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(d), "l"(src), "r"(in ? 4 : 0) : "memory");
+}
+__device__ __forceinline__ void ssim_cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void ssim_cp_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
+// Issue the staging of NQ planes of channel c (plane q at base[q] + c P) with the
+// halo into s[q][42][43], values outside the image 0; one commit group.
 template <int NQ>
-__device__ __forceinline__ void ssim_stage(float (*s)[kSsimIn][kSsimInStride], const float* const* base, int W,
-                                           int H, int64_t P, int c, int ox, int oy, const float* shift) {
+__device__ __forceinline__ void ssim_stage(float (*s)[kSsimIn][kSsimInStride], const float* const (&base)[NQ], int W,
+                                           int H, int64_t P, int c, int ox, int oy) {
+  // element k = threadIdx.x + 256 i of the 42 x 42 block: (row, column) stepped by
+  // (6, 4) per i, with a carry, instead of a division per element
+  int r = threadIdx.x / kSsimIn, col = threadIdx.x - r * kSsimIn;
   for (int k = threadIdx.x; k < kSsimIn * kSsimIn; k += kSsimThreads) {
-    const int r = k / kSsimIn, col = k - r * kSsimIn;
     const int gy = oy - kSsimHalo + r, gx = ox - kSsimHalo + col;
     const bool in = gx >= 0 && gx < W && gy >= 0 && gy < H;
-    const int64_t e = int64_t(c) * P + int64_t(gy) * W + gx;
+    const int64_t e = in ? int64_t(c) * P + int64_t(gy) * W + gx : 0;
 #pragma unroll
-    for (int q = 0; q < NQ; ++q) s[q][r][col] = (in ? base[q][e] : 0.0f) - shift[q];
+    for (int q = 0; q < NQ; ++q) cp_async4_zfill(&s[q][r][col], base[q] + e, in);
+    static_assert(kSsimThreads == 6 * kSsimIn + 4, "row / column step of the staging loop");
+    col += 4;
+    r += 6;
+    if (col >= kSsimIn) {
+      col -= kSsimIn;
+      r += 1;
+    }
   }
+  ssim_cp_commit();
 }
 
 // out[j] += sum_t g[t] v[j + t] for the 4 outputs of a group.
@@ -81,7 +104,8 @@ __device__ __forceinline__ void ssim_tap4(float (&out)[kSsimGroup], const float 
       if (k - j >= 0 && k - j < 11) out[j] = fmaf(w.g[k - j], v[k], out[j]);
 }
 
-__global__ void __launch_bounds__(kSsimThreads)
+// Four CTAs per SM (at most 64 registers a thread; it needs 51 so, 73 unbounded).
+__global__ void __launch_bounds__(kSsimThreads, 4)
     k_ssim_fwd(const float* __restrict__ x, const float* __restrict__ y, int W, int H, SsimWindow w, float dLdS,
                float inv3P, float* __restrict__ maps, float* __restrict__ ssim_out) {
   __shared__ float s_in[2][kSsimIn][kSsimInStride];
@@ -92,19 +116,21 @@ __global__ void __launch_bounds__(kSsimThreads)
   const int vcol = threadIdx.x % kSsimTile, vrow = (threadIdx.x / kSsimTile) * kSsimGroup;
   const int64_t centre = int64_t(min(oy + kSsimTile / 2, H - 1)) * W + min(ox + kSsimTile / 2, W - 1);
   float ssum = 0.0f;
+  const float* const planes[2] = {x, y};
+  ssim_stage<2>(s_in, planes, W, H, P, 0, ox, oy);
   for (int c = 0; c < 3; ++c) {
     const float shift[2] = {x[c * P + centre], y[c * P + centre]};
-    const float* planes[2] = {x, y};
-    ssim_stage<2>(s_in, planes, W, H, P, c, ox, oy, shift);
-    __syncthreads();
-    // horizontal: moments of the shifted values (x, y, x^2, y^2, x y) along rows
+    ssim_cp_wait_all();
+    __syncthreads();  // channel c staged for every thread; the previous vertical pass done with s_h
+    // horizontal: moments of the shifted values (x, y, x^2, y^2, x y) along rows; the
+    // shift is taken here (outside the image: 0 - shift)
     for (int i = threadIdx.x; i < kSsimHItems; i += kSsimThreads) {
       const int r = i % kSsimIn, c0 = (i / kSsimIn) * kSsimGroup;
       float a[kSsimWin], b[kSsimWin], aa[kSsimWin], bb[kSsimWin], ab[kSsimWin];
 #pragma unroll
       for (int k = 0; k < kSsimWin; ++k) {
-        a[k] = s_in[0][r][c0 + k];
-        b[k] = s_in[1][r][c0 + k];
+        a[k] = s_in[0][r][c0 + k] - shift[0];
+        b[k] = s_in[1][r][c0 + k] - shift[1];
         aa[k] = a[k] * a[k];
         bb[k] = b[k] * b[k];
         ab[k] = a[k] * b[k];
@@ -120,7 +146,8 @@ __global__ void __launch_bounds__(kSsimThreads)
 #pragma unroll
         for (int j = 0; j < kSsimGroup; ++j) s_h[q][r][c0 + j] = m[q][j];
     }
-    __syncthreads();
+    __syncthreads();  // s_in read by every thread: the next channel may land there
+    if (c + 1 < 3) ssim_stage<2>(s_in, planes, W, H, P, c + 1, ox, oy);
     // vertical: 4 rows of one column per thread
     float m[5][kSsimGroup] = {};
 #pragma unroll
@@ -152,12 +179,11 @@ __global__ void __launch_bounds__(kSsimThreads)
       maps[(12 + c) * P + e] = my;
       ssum += S;
     }
-    __syncthreads();
   }
 #pragma unroll
   for (int o = 16; o >= 1; o >>= 1) ssum += __shfl_xor_sync(0xffffffffu, ssum, o);
   if ((threadIdx.x & 31) == 0) s_red[threadIdx.x >> 5] = ssum;
-  __syncthreads();
+  __syncthreads();  // (s_red is not s_h: no conflict with the last vertical pass)
   if (threadIdx.x == 0) {
     float t = 0.f;
     for (int k = 0; k < kSsimThreads / 32; ++k) t += s_red[k];
@@ -168,44 +194,43 @@ __global__ void __launch_bounds__(kSsimThreads)
 __global__ void __launch_bounds__(kSsimThreads)
     k_ssim_bwd(const float* __restrict__ x, const float* __restrict__ y, int W, int H, SsimWindow w,
                const float* __restrict__ maps, float* __restrict__ dLdx) {
-  __shared__ float s_in[3][kSsimIn][kSsimInStride];
+  // the five maps of a channel (a, b, c, mu_x, mu_y) staged raw (36 KB, dynamic shared
+  // memory); A is formed as the horizontal pass reads them (zero outside the image,
+  // where every map is 0)
+  extern __shared__ __align__(16) float ssim_dyn[];
+  float(*s_in)[kSsimIn][kSsimInStride] = reinterpret_cast<float(*)[kSsimIn][kSsimInStride]>(ssim_dyn);
   __shared__ float s_h[3][kSsimIn][kSsimHStride];
   const int ox = blockIdx.x * kSsimTile, oy = blockIdx.y * kSsimTile;
   const int64_t P = int64_t(W) * H;
   const int vcol = threadIdx.x % kSsimTile, vrow = (threadIdx.x / kSsimTile) * kSsimGroup;
   const int64_t centre = int64_t(min(oy + kSsimTile / 2, H - 1)) * W + min(ox + kSsimTile / 2, W - 1);
+  const float* const planes[5] = {maps, maps + 3 * P, maps + 6 * P, maps + 9 * P, maps + 12 * P};
+  ssim_stage<5>(s_in, planes, W, H, P, 0, ox, oy);
   for (int c = 0; c < 3; ++c) {
     const float sx = x[c * P + centre], sy = y[c * P + centre];
-    // stage A (about the shift), b and c of this channel with the halo; zero outside
-    for (int k = threadIdx.x; k < kSsimIn * kSsimIn; k += kSsimThreads) {
-      const int r = k / kSsimIn, col = k - r * kSsimIn;
-      const int gy = oy - kSsimHalo + r, gx = ox - kSsimHalo + col;
-      float va = 0.f, vb = 0.f, vc = 0.f;
-      if (gx >= 0 && gx < W && gy >= 0 && gy < H) {
-        const int64_t e = int64_t(c) * P + int64_t(gy) * W + gx;
-        vb = maps[3 * P + e];
-        vc = maps[6 * P + e];
-        va = maps[e] - 2.f * (maps[9 * P + e] - sx) * vb - (maps[12 * P + e] - sy) * vc;
-      }
-      s_in[0][r][col] = va;
-      s_in[1][r][col] = vb;
-      s_in[2][r][col] = vc;
-    }
-    __syncthreads();
+    ssim_cp_wait_all();
+    __syncthreads();  // channel c staged for every thread; the previous vertical pass done with s_h
     for (int i = threadIdx.x; i < kSsimHItems; i += kSsimThreads) {
       const int r = i % kSsimIn, c0 = (i / kSsimIn) * kSsimGroup;
+      float va[kSsimWin], vb[kSsimWin], vc[kSsimWin];
 #pragma unroll
-      for (int q = 0; q < 3; ++q) {
-        float v[kSsimWin];
-#pragma unroll
-        for (int k = 0; k < kSsimWin; ++k) v[k] = s_in[q][r][c0 + k];
-        float o[kSsimGroup] = {};
-        ssim_tap4(o, v, w);
-#pragma unroll
-        for (int j = 0; j < kSsimGroup; ++j) s_h[q][r][c0 + j] = o[j];
+      for (int k = 0; k < kSsimWin; ++k) {
+        vb[k] = s_in[1][r][c0 + k];
+        vc[k] = s_in[2][r][c0 + k];
+        // A about the shift
+        va[k] = s_in[0][r][c0 + k] - 2.f * (s_in[3][r][c0 + k] - sx) * vb[k] - (s_in[4][r][c0 + k] - sy) * vc[k];
       }
+      float o[3][kSsimGroup] = {};
+      ssim_tap4(o[0], va, w);
+      ssim_tap4(o[1], vb, w);
+      ssim_tap4(o[2], vc, w);
+#pragma unroll
+      for (int q = 0; q < 3; ++q)
+#pragma unroll
+        for (int j = 0; j < kSsimGroup; ++j) s_h[q][r][c0 + j] = o[q][j];
     }
-    __syncthreads();
+    __syncthreads();  // s_in read by every thread: the next channel may land there
+    if (c + 1 < 3) ssim_stage<5>(s_in, planes, W, H, P, c + 1, ox, oy);
     float g[3][kSsimGroup] = {};
 #pragma unroll
     for (int q = 0; q < 3; ++q) {
@@ -221,11 +246,22 @@ __global__ void __launch_bounds__(kSsimThreads)
       const int64_t e = int64_t(c) * P + int64_t(py) * W + px;
       dLdx[e] = g[0][j] + 2.f * (x[e] - sx) * g[1][j] + (y[e] - sy) * g[2][j];
     }
-    __syncthreads();
   }
 }
 
 __global__ void k_zero1(float* p) { *p = 0.0f; }
+
+constexpr size_t kSsimBwdDyn = size_t(5) * kSsimIn * kSsimInStride * sizeof(float);  // 36120 bytes
+
+// The backward's dynamic shared-memory opt-in (its 52 KB in all exceed the 48 KB
+// default), set on the first call (an eager step before a CUDA graph capture sets it).
+bool ssim_bwd_attr_ready() {
+  static bool ok = false;
+  if (!ok)
+    ok = cudaFuncSetAttribute(k_ssim_bwd, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSsimBwdDyn)) ==
+         cudaSuccess;
+  return ok;
+}
 
 }  // namespace gs
 
@@ -247,7 +283,8 @@ extern "C" gs_status gs_ssim_bwd(int32_t width, int32_t height, const float* ima
                                  const float* maps, float* dLdC, cudaStream_t stream) {
   using namespace gs;
   if (width <= 0 || height <= 0 || !image || !target || !maps || !dLdC) return GS_ERR_INVALID_ARG;
+  if (!ssim_bwd_attr_ready()) return GS_ERR_CUDA;
   const dim3 grid((width + kSsimTile - 1) / kSsimTile, (height + kSsimTile - 1) / kSsimTile);
-  k_ssim_bwd<<<grid, kSsimThreads, 0, stream>>>(image, target, width, height, ssim_window(), maps, dLdC);
+  k_ssim_bwd<<<grid, kSsimThreads, kSsimBwdDyn, stream>>>(image, target, width, height, ssim_window(), maps, dLdC);
   return launch_status();
 }
