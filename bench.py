@@ -5,7 +5,10 @@ Workload (default): 4M-Gaussian blob isosurface at 2048x2048 with 448 orbit view
 SH degree 3, fp32; step s trains view s mod 448 against that view's target image
 (a render of the same surface sampled with another seed).  Every input is seeded
 and synthetic and resident on the GPU before the timed region; parameters, Adam
-state and targets (22.5 GB) exceed L2 many times over, so no flush is needed.
+state and targets (22.5 GB) exceed L2 many times over, so no flush is needed.  Before
+the warm-up the Gaussians are stored in Morton order of their means (a layout that
+changes a step's result only through the index that breaks ties between equal fp32
+depths; ``--order generated`` keeps the generator's order).
 
 One JSON line is printed (rank 0).  Besides the device-timed value it carries:
   e2e           the same steps (from the same model state) through the public API
@@ -64,6 +67,9 @@ def parse():
                          "headline is one view per step")
     ap.add_argument("--graph", action="store_true",
                     help="replay each view's step from a CUDA graph captured after the warm-up (one view per step)")
+    ap.add_argument("--order", choices=["morton", "generated"], default="morton",
+                    help="storage order of the Gaussians, set once before the warm-up: Morton order of the means "
+                         "(gs_spatial_order) or the order the scene generator wrote them in")
     ap.add_argument("--dssim", type=float, default=0.0,
                     help="D-SSIM weight lambda: the loss becomes (1 - lambda) L1 + lambda (1 - SSIM) (0 = L1)")
     return ap.parse_args()
@@ -379,6 +385,8 @@ def run_gb300(args, cfg, ws, rank, local):
     del rend, Ptd
 
     tr = gs.Trainer(Pd, n, W, H, capacity, gi.lr_planes(), device=dev, fused=not args.separate, dssim=args.dssim)
+    if args.order == "morton":
+        tr.reorder_spatially()
     STAGES = list(STAGES_SEPARATE if args.separate else STAGES_FUSED)
     if args.dssim > 0:
         STAGES.insert(STAGES.index("render_bwd"), "ssim")
@@ -598,7 +606,7 @@ def run_gb300(args, cfg, ws, rank, local):
         "dtype": "f32", "data": "synthetic",
         "config": dict(_config_dict(cfg), parallelism=f"replicas{ws}", capacity_K=capacity,
                        objective=(f"{1 - args.dssim:g} L1 + {args.dssim:g} (1 - SSIM)" if args.dssim > 0 else "L1"),
-                       K_mean=Kmean, visible_mean=Vmean, pairs_bwd_mean=Emean, batch=B,
+                       K_mean=Kmean, visible_mean=Vmean, pairs_bwd_mean=Emean, batch=B, storage_order=args.order,
                        cuda_graph=bool(graphs)),
         "views_per_s": value * B,
         "roofline": roof,

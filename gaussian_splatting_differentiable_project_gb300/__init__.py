@@ -158,6 +158,12 @@ def load(build_if_missing: bool = True):
         lib.gs_ssim_bwd.restype = st
         lib.gs_util_expf.argtypes = [P, P, ctypes.c_int64, P]
         lib.gs_util_expf.restype = st
+        lib.gs_spatial_order_workspace_bytes.argtypes = [GsDims]
+        lib.gs_spatial_order_workspace_bytes.restype = ctypes.c_size_t
+        lib.gs_spatial_order.argtypes = [GsDims, P, P, P, ctypes.c_size_t, P, P]
+        lib.gs_spatial_order.restype = st
+        lib.gs_permute_planes.argtypes = [GsDims, ctypes.c_int32, P, P, P, P]
+        lib.gs_permute_planes.restype = st
         lib.gs_status_str.argtypes = [ctypes.c_uint32]
         lib.gs_status_str.restype = ctypes.c_char_p
         lib.gs_version.restype = ctypes.c_char_p
@@ -390,6 +396,26 @@ def densify_plan(n: int, params, grad_acc, vis_cnt, cfg: GsDensifyCfg, action, o
     _check(load().gs_densify_plan(dims(n, params.shape[1]), _p(params), _p(grad_acc), _p(vis_cnt),
                                   ctypes.byref(cfg), _p(action), _p(offset), _p(n_out), _p(workspace),
                                   workspace.numel() * workspace.element_size(), _stream(stream)), "gs_densify_plan")
+
+
+def spatial_order_workspace_bytes(n: int, n_pad: int) -> int:
+    return int(load().gs_spatial_order_workspace_bytes(dims(n, n_pad)))
+
+
+def spatial_order(n: int, params, perm, workspace, dev_status, stream=None) -> None:
+    """perm[j] = index of the Gaussian stored at j in Morton order of the means."""
+    _check(load().gs_spatial_order(dims(n, params.shape[1]), _p(params), _p(perm), _p(workspace),
+                                   int(workspace.numel() * workspace.element_size()), _p(dev_status), _stream(stream)),
+           "gs_spatial_order")
+
+
+def permute_planes(n: int, perm, src, dst, stream=None) -> None:
+    """dst[:, j] = src[:, perm[j]] for j < n, padding copied (src, dst: planes x n_pad,
+    any 4-byte element type)."""
+    planes = 1 if src.dim() == 1 else int(src.shape[0])
+    n_pad = int(src.shape[-1])
+    _check(load().gs_permute_planes(dims(n, n_pad), planes, _p(perm), _p(src), _p(dst), _stream(stream)),
+           "gs_permute_planes")
 
 
 def densify_workspace_bytes(n: int, n_pad: int) -> int:

@@ -474,6 +474,121 @@ __global__ void __launch_bounds__(256)
   }
 }
 
+// ------------------------------------------------------------------ spatial order
+// A storage order of the Gaussians along a Morton (Z-order) curve of their means, so
+// that Gaussians near each other in space, which share tiles, sit near each other in
+// memory.  Per axis, q = floor((mu - lo) * (1023 / (hi - lo)) + 0.5) clamped to
+// [0, 1023], with lo, hi the axis's bounds over the Gaussians' finite means and every
+// operation an explicit IEEE fp32 one (reproducible off the GPU); the code interleaves
+// the three 10-bit q (x in bit 0, y in bit 1, z in bit 2) and the order is the stable
+// sort of the codes (ties by index).  A non-finite coordinate counts as lo.
+constexpr int kSoThreads = 256;
+
+// Float -> uint32 whose unsigned order is the float order (for atomic min / max).
+__device__ __forceinline__ uint32_t so_ordered(float f) {
+  const uint32_t u = __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float so_unordered(uint32_t u) {
+  return __uint_as_float((u & 0x80000000u) ? (u & 0x7FFFFFFFu) : ~u);
+}
+
+// ws words: [0, 3) ordered min per axis, [3, 6) ordered max, 6: n; the histograms,
+// tickets and look-back words of the four passes are cleared.
+__global__ void k_so_init(uint32_t* __restrict__ box, int64_t n, uint4* __restrict__ zero, int64_t zero_vec) {
+  const int64_t gid = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  for (int64_t k = gid; k < zero_vec; k += int64_t(gridDim.x) * blockDim.x) zero[k] = make_uint4(0u, 0u, 0u, 0u);
+  if (gid < 3) {
+    box[gid] = 0xFFFFFFFFu;
+    box[3 + gid] = 0u;
+  }
+  if (gid == 0) box[6] = uint32_t(n);
+}
+
+__global__ void __launch_bounds__(kSoThreads)
+    k_so_bbox(const float* __restrict__ params, int64_t n, int64_t n_pad, uint32_t* __restrict__ box) {
+  uint32_t lo[3] = {0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu}, hi[3] = {0u, 0u, 0u};
+  for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += int64_t(gridDim.x) * blockDim.x) {
+#pragma unroll
+    for (int a = 0; a < 3; ++a) {
+      const float v = params[a * n_pad + i];
+      if (isfinite(v)) {
+        lo[a] = min(lo[a], so_ordered(v));
+        hi[a] = max(hi[a], so_ordered(v));
+      }
+    }
+  }
+#pragma unroll
+  for (int a = 0; a < 3; ++a) {
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+      lo[a] = min(lo[a], __shfl_xor_sync(0xffffffffu, lo[a], o));
+      hi[a] = max(hi[a], __shfl_xor_sync(0xffffffffu, hi[a], o));
+    }
+    if ((threadIdx.x & 31) == 0) {
+      atomicMin(&box[a], lo[a]);
+      atomicMax(&box[3 + a], hi[a]);
+    }
+  }
+}
+
+__device__ __forceinline__ uint32_t so_spread10(uint32_t x) {
+  x &= 0x3FFu;
+  x = (x | (x << 16)) & 0x030000FFu;
+  x = (x | (x << 8)) & 0x0300F00Fu;
+  x = (x | (x << 4)) & 0x030C30C3u;
+  x = (x | (x << 2)) & 0x09249249u;
+  return x;
+}
+
+__global__ void __launch_bounds__(kSoThreads)
+    k_so_codes(const float* __restrict__ params, int64_t n, int64_t n_pad, const uint32_t* __restrict__ box,
+               uint32_t* __restrict__ keys, uint32_t* __restrict__ vals, uint32_t* __restrict__ hist) {
+  __shared__ uint32_t s_hist[4 * 256];
+  for (int k = threadIdx.x; k < 4 * 256; k += kSoThreads) s_hist[k] = 0;
+  float lo[3], sc[3];
+#pragma unroll
+  for (int a = 0; a < 3; ++a) {
+    const bool any = box[a] <= box[3 + a];
+    lo[a] = any ? so_unordered(box[a]) : 0.0f;
+    const float ext = any ? __fsub_rn(so_unordered(box[3 + a]), lo[a]) : 0.0f;
+    sc[a] = ext > 0.0f ? __fdiv_rn(1023.0f, ext) : 0.0f;
+  }
+  __syncthreads();
+  for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += int64_t(gridDim.x) * blockDim.x) {
+    uint32_t code = 0;
+#pragma unroll
+    for (int a = 0; a < 3; ++a) {
+      const float v = params[a * n_pad + i];
+      const float t = isfinite(v) ? __fadd_rn(__fmul_rn(__fsub_rn(v, lo[a]), sc[a]), 0.5f) : 0.0f;
+      const uint32_t q = uint32_t(fminf(fmaxf(floorf(t), 0.0f), 1023.0f));
+      code |= so_spread10(q) << a;
+    }
+    keys[i] = code;
+    vals[i] = uint32_t(i);
+#pragma unroll
+    for (int p = 0; p < 4; ++p) atomicAdd(&s_hist[p * 256 + ((code >> (8 * p)) & 0xFFu)], 1u);
+  }
+  __syncthreads();
+  for (int k = threadIdx.x; k < 4 * 256; k += kSoThreads) {
+    const uint32_t v = s_hist[k];
+    if (v) atomicAdd(&hist[k], v);
+  }
+}
+
+// dst[p][i] = src[p][perm[i]] for i < n, p < planes (32-bit elements); dst[p][i] =
+// src[p][i] for the padding n <= i < n_pad.
+__global__ void __launch_bounds__(256)
+    k_permute_planes(const uint32_t* __restrict__ perm, int64_t n, int64_t n_pad, int planes,
+                     const uint32_t* __restrict__ src, uint32_t* __restrict__ dst) {
+  const int64_t total = int64_t(planes) * n_pad;
+  for (int64_t k = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; k < total; k += int64_t(gridDim.x) * blockDim.x) {
+    const int64_t p = k / n_pad, i = k - p * n_pad;
+    const int64_t from = i < n ? int64_t(perm[i]) : i;
+    dst[k] = src[p * n_pad + from];
+  }
+}
+
 }  // namespace gs
 
 extern "C" size_t gs_bin_sort_workspace_bytes(gs_dims dims, uint32_t capacity_K, int32_t width, int32_t height) {
@@ -576,3 +691,90 @@ extern "C" gs_status gs_bin_sort(gs_dims dims, const gs_proj* proj, const gs_cam
   return launch_status();
 }
 
+
+namespace {
+// Workspace of gs_spatial_order: keys A and B, values B (the values A are the caller's
+// perm), the box and count words, then histograms, tickets and look-back words of four
+// passes (cleared by k_so_init).
+struct SoLayout {
+  size_t kA, kB, vB, box, hist, tickets, look, total;
+  int64_t parts;
+};
+SoLayout so_layout(int64_t n) {
+  using namespace gs;
+  SoLayout L{};
+  L.parts = (n + kPart - 1) / kPart;
+  if (L.parts < 1) L.parts = 1;
+  size_t off = 0;
+  L.kA = off;
+  off += align256(size_t(n) * 4);
+  L.kB = off;
+  off += align256(size_t(n) * 4);
+  L.vB = off;
+  off += align256(size_t(n) * 4);
+  L.box = off;
+  off += 256;
+  L.hist = off;
+  off += align256(size_t(4) * 256 * 4);
+  L.tickets = off;
+  off += 256;
+  L.look = off;
+  off += align256(size_t(4) * size_t(L.parts) * 256 * 4);
+  L.total = off;
+  return L;
+}
+}  // namespace
+
+extern "C" size_t gs_spatial_order_workspace_bytes(gs_dims dims) {
+  if (dims.n < 0) return 0;
+  return so_layout(dims.n).total;
+}
+
+extern "C" gs_status gs_spatial_order(gs_dims dims, const float* params, uint32_t* perm, void* workspace,
+                                      size_t workspace_bytes, uint32_t* dev_status, cudaStream_t stream) {
+  using namespace gs;
+  if (!dims_ok(dims) || !params || !perm || !workspace || !dev_status) return GS_ERR_INVALID_ARG;
+  if (!aligned(workspace, 256) || !aligned(perm, 4)) return GS_ERR_INVALID_ARG;
+  const SoLayout L = so_layout(dims.n);
+  if (workspace_bytes < L.total) return GS_ERR_INVALID_ARG;
+  if (dims.n == 0) return GS_OK;
+  char* ws = static_cast<char*>(workspace);
+  uint32_t* kA = reinterpret_cast<uint32_t*>(ws + L.kA);
+  uint32_t* kB = reinterpret_cast<uint32_t*>(ws + L.kB);
+  uint32_t* vB = reinterpret_cast<uint32_t*>(ws + L.vB);
+  uint32_t* box = reinterpret_cast<uint32_t*>(ws + L.box);
+  uint32_t* hist = reinterpret_cast<uint32_t*>(ws + L.hist);
+  uint32_t* tickets = reinterpret_cast<uint32_t*>(ws + L.tickets);
+  uint32_t* look = reinterpret_cast<uint32_t*>(ws + L.look);
+  const int64_t zero_vec = int64_t(L.total - L.hist) / 16;
+  k_so_init<<<kSmCount * 4, 256, 0, stream>>>(box, dims.n, reinterpret_cast<uint4*>(ws + L.hist), zero_vec);
+  const int g = grid_for(dims.n, kSoThreads, kSmCount * 8);
+  k_so_bbox<<<g, kSoThreads, 0, stream>>>(params, dims.n, dims.n_pad, box);
+  k_so_codes<<<g, kSoThreads, 0, stream>>>(params, dims.n, dims.n_pad, box, kA, perm, hist);
+  // four stable 8-bit passes over the 30-bit codes; an even count ends in (kA, perm)
+  uint32_t *ka = kA, *va = perm, *kb = kB, *vb = vB;
+  for (int p = 0; p < 4; ++p) {
+    k_bs_onesweep<<<int(L.parts), kSortThreads, kSortSmem, stream>>>(ka, va, kb, vb, box + 6, uint32_t(dims.n), 8 * p,
+                                                                    hist + 256 * p, look + size_t(p) * L.parts * 256,
+                                                                    tickets + p, dev_status);
+    uint32_t* t = ka;
+    ka = kb;
+    kb = t;
+    t = va;
+    va = vb;
+    vb = t;
+  }
+  return launch_status();
+}
+
+extern "C" gs_status gs_permute_planes(gs_dims dims, int32_t planes, const uint32_t* perm, const void* src, void* dst,
+                                       cudaStream_t stream) {
+  using namespace gs;
+  if (!dims_ok(dims) || planes <= 0 || !perm || !src || !dst || src == dst) return GS_ERR_INVALID_ARG;
+  if (!aligned(src, 4) || !aligned(dst, 4)) return GS_ERR_INVALID_ARG;
+  const int64_t total = int64_t(planes) * dims.n_pad;
+  if (total == 0) return GS_OK;
+  k_permute_planes<<<grid_for(total, 256, kSmCount * 16), 256, 0, stream>>>(
+      perm, dims.n, dims.n_pad, planes, static_cast<const uint32_t*>(src), static_cast<uint32_t*>(dst));
+  return launch_status();
+}

@@ -15,9 +15,10 @@ import numpy as np
 import math
 
 from . import (BinBuffers, ProjBuffers, GRAD2D_STRIDE, SSIM_MAPS, adam_step, bin_sort, densify_accumulate,
-               densify_apply, densify_plan, densify_thresholds, densify_workspace_bytes, opacity_reset, project,
-               project_bwd, project_bwd_accumulate, project_bwd_adam, project_bwd_adam_tdev, render_bwd,
-               render_fwd, ssim_bwd, ssim_fwd, status_str, step_counter_add)
+               densify_apply, densify_plan, densify_thresholds, densify_workspace_bytes, opacity_reset,
+               permute_planes, project, project_bwd, project_bwd_accumulate, project_bwd_adam,
+               project_bwd_adam_tdev, render_bwd, render_fwd, spatial_order, spatial_order_workspace_bytes,
+               ssim_bwd, ssim_fwd, status_str, step_counter_add)
 
 
 def batch_adam_hyper(batch: int, lr_plane, beta1: float, beta2: float, eps: float):
@@ -248,6 +249,27 @@ class Trainer:
         self.grad_acc = torch.zeros(n_pad_new, dtype=torch.float32, device=dev)
         self.vis_cnt = torch.zeros(n_pad_new, dtype=torch.int32, device=dev)
         return {"n": n_new, "pruned": counts[0], "kept": counts[1], "cloned": counts[2], "split": counts[3]}
+
+    def reorder_spatially(self, stream=None):
+        """Store the Gaussians in Morton order of their means (``gs_spatial_order``):
+        the parameters, the Adam moments and any density accumulators are permuted
+        together, so training continues unchanged but for the index that breaks ties
+        between equal fp32 depths.  Gaussians near each other in space then sit near each other in memory,
+        which the record gather and the backward's gradient atomics feel on scenes
+        larger than L2.  Returns perm (perm[j] = the index before of the Gaussian now at
+        j).  CUDA graphs captured before refer to the old buffers: capture again."""
+        import torch
+        n, dev = self.n, self.device
+        perm = torch.empty(max(n, 1), dtype=torch.int32, device=dev)
+        ws = torch.empty(max(spatial_order_workspace_bytes(n, self.n_pad), 256), dtype=torch.uint8, device=dev)
+        spatial_order(n, self.params, perm, ws, self.status, stream)
+        names = ["params", "m", "v"] + (["grad_acc", "vis_cnt"] if self.density is not None else [])
+        for name in names:
+            src = getattr(self, name)
+            dst = torch.empty_like(src)
+            permute_planes(n, perm, src, dst, stream)
+            setattr(self, name, dst)
+        return perm[:n]
 
     def reset_opacity(self, stream=None) -> None:
         """Clamp opacities to 2 x the prune opacity and zero their Adam moments."""

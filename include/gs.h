@@ -423,6 +423,37 @@ gs_status gs_bin_sort_noalloc(gs_dims dims, const gs_proj* proj, const gs_camera
                               gs_bins bins, uint32_t* dev_status, cudaStream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * gs_spatial_order -- a storage order of the Gaussians along a Morton (Z-order)
+ * curve of their means, for locality: Gaussians near each other in space share
+ * tiles, and stored near each other the binning's record gather and the backward's
+ * gradient atomics find their lines in L2.  Not a step of the method (the pages give
+ * no storage order); a layout applied once, before training and after each density
+ * refinement.  A step's result depends on the order only through the index that
+ * breaks ties between equal fp32 depths in a tile.
+ *   Code of Gaussian i: per axis q = floor((mu - lo) * (1023 / (hi - lo)) + 0.5)
+ *   clamped to [0, 1023], each operation in IEEE fp32 in that order, lo and hi the
+ *   axis's smallest and largest finite mean (a non-finite coordinate counts as lo;
+ *   hi = lo gives q = 0); the 30-bit code interleaves the three q, x in bit 0.
+ *   perm: n uint32 (device, written): perm[j] = the index of the Gaussian placed at
+ *   j, i.e. the stable sort of the codes (ties by index).
+ *   workspace: gs_spatial_order_workspace_bytes(dims) bytes, 256-byte aligned.
+ * Errors: GS_ERR_INVALID_ARG for bad dims, null or misaligned pointers, a short
+ * workspace; a look-back wait that runs out raises GS_ERR_TIMEOUT in dev_status. */
+size_t gs_spatial_order_workspace_bytes(gs_dims dims);
+gs_status gs_spatial_order(gs_dims dims, const float* params, uint32_t* perm, void* workspace, size_t workspace_bytes,
+                           uint32_t* dev_status, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * gs_permute_planes -- applies a storage order to `planes` planes of 32-bit values
+ * (parameters, Adam moments, per-Gaussian accumulators):
+ *   dst[p n_pad + j] = src[p n_pad + perm[j]] for j < n; the padding j >= n copied.
+ *   src, dst distinct device buffers of planes x n_pad elements, 4-byte aligned;
+ *   perm as gs_spatial_order writes it (every entry < n).
+ * Errors: GS_ERR_INVALID_ARG for bad dims, planes <= 0, null or aliasing buffers. */
+gs_status gs_permute_planes(gs_dims dims, int32_t planes, const uint32_t* perm, const void* src, void* dst,
+                            cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------
  * gs_util_expf -- the library's fp32 exponential (Cody-Waite reduction, degree-7
  * Taylor polynomial, 2^k scaling; the one every compositing decision uses), on n
  * device floats, so that callers can check it against another implementation.

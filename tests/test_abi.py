@@ -90,6 +90,17 @@ def test_argument_errors_are_returned_without_a_gpu():
         r = lib.gs_render_bwd(gs.dims(10, 256), ctypes.byref(cam), ctypes.byref(bins), 1000, bg, p, p, p, p, w, None,
                               p, p, p, None)
         assert r == gs.GS_ERR_INVALID_ARG, w
+    # spatial order: null perm, short or misaligned workspace; permutation: no planes,
+    # aliasing buffers
+    need = lib.gs_spatial_order_workspace_bytes(gs.dims(1000, 1024))
+    assert need >= 3 * 1000 * 4
+    ws = ctypes.c_void_p(256)
+    assert lib.gs_spatial_order(gs.dims(1000, 1024), p, None, ws, need, p, None) == gs.GS_ERR_INVALID_ARG
+    assert lib.gs_spatial_order(gs.dims(1000, 1024), p, p, ws, need - 1, p, None) == gs.GS_ERR_INVALID_ARG
+    assert lib.gs_spatial_order(gs.dims(1000, 1024), p, p, ctypes.c_void_p(272), need, p, None) == \
+        gs.GS_ERR_INVALID_ARG
+    assert lib.gs_permute_planes(gs.dims(1000, 1024), 0, p, p, ctypes.c_void_p(32), None) == gs.GS_ERR_INVALID_ARG
+    assert lib.gs_permute_planes(gs.dims(1000, 1024), 59, p, p, p, None) == gs.GS_ERR_INVALID_ARG
 
 
 def test_product_package_has_no_oracle_or_cpu_path():
