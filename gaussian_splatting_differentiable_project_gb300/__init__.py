@@ -29,15 +29,16 @@ GRAD2D_STRIDE = 12  # floats per Gaussian in the interleaved grad2d buffer
 
 
 def grad2d_planes(grad2d, n: int) -> np.ndarray:
-    """The nine 2D partials of Gaussians [0, n) as (9, n) planes, from the interleaved
-    (n_pad, 12) buffer gs_render_bwd writes (host copy)."""
+    """The nine sums of Gaussians [0, n) as (9, n) planes, from the interleaved
+    (n_pad, 12) buffer gs_render_bwd writes (host copy): the five moments of
+    dL/dpower (S1..S5, see gs.h) and the opacity and colour partials."""
     g = grad2d.detach().cpu().numpy() if hasattr(grad2d, "detach") else np.asarray(grad2d)
     return np.ascontiguousarray(g.reshape(-1, GRAD2D_STRIDE)[:n, :N_GRAD2D].T)
 
 
 def grad2d_interleaved(planes: np.ndarray) -> np.ndarray:
-    """(9, n_pad) planes -> the interleaved (n_pad, 12) layout the projection
-    backward reads (host arrays)."""
+    """(9, n_pad) planes (moments S1..S5, then opacity and colour partials) -> the
+    interleaved (n_pad, 12) layout the projection backward reads (host arrays)."""
     planes = np.asarray(planes, np.float32)
     out = np.zeros((planes.shape[1], GRAD2D_STRIDE), np.float32)
     out[:, :N_GRAD2D] = planes.T
@@ -142,7 +143,7 @@ def load(build_if_missing: bool = True):
         lib.gs_project_bwd_adam_tdev.restype = st
         lib.gs_step_counter_add.argtypes = [P, ctypes.c_int64, P]
         lib.gs_step_counter_add.restype = st
-        lib.gs_densify_accumulate.argtypes = [GsDims, P, P, ctypes.c_int32, ctypes.c_int32, P, P, P]
+        lib.gs_densify_accumulate.argtypes = [GsDims, P, P, P, ctypes.c_int32, ctypes.c_int32, P, P, P]
         lib.gs_densify_accumulate.restype = st
         lib.gs_densify_workspace_bytes.argtypes = [GsDims]
         lib.gs_densify_workspace_bytes.restype = ctypes.c_size_t
@@ -385,10 +386,13 @@ def densify_thresholds(extent: float, grow_grad2d: float = 2e-4, grow_scale3d: f
     return cfg, float(np.float32(math.log(split_shrink))), float(np.float32(math.log(reset / (1.0 - reset))))
 
 
-def densify_accumulate(n: int, n_pad: int, count, grad2d, width: int, height: int, grad_acc, vis_cnt,
+def densify_accumulate(n: int, n_pad: int, proj: "ProjBuffers", grad2d, width: int, height: int, grad_acc, vis_cnt,
                        stream=None) -> None:
-    _check(load().gs_densify_accumulate(dims(n, n_pad), _p(count), _p(grad2d), int(width), int(height),
-                                        _p(grad_acc), _p(vis_cnt), _stream(stream)), "gs_densify_accumulate")
+    """grad_acc += the NDC-scaled norm of each visible Gaussian's mean2d gradient, formed
+    from grad2d's moments and the conic of its record in ``proj``; vis_cnt += 1."""
+    _check(load().gs_densify_accumulate(dims(n, n_pad), _p(proj.count), _p(proj.rec), _p(grad2d), int(width),
+                                        int(height), _p(grad_acc), _p(vis_cnt), _stream(stream)),
+           "gs_densify_accumulate")
 
 
 def densify_plan(n: int, params, grad_acc, vis_cnt, cfg: GsDensifyCfg, action, offset, n_out, workspace,

@@ -4,7 +4,9 @@
 // the steps (step walkthrough), starting at step 500 (trace section); thresholds and
 // the split rule of the cited 3DGS method.
 //
-//   gs_densify_accumulate  per visible Gaussian: acc += |(g_mx W/2, g_my H/2)|, cnt += 1
+//   gs_densify_accumulate  per visible Gaussian: acc += |(g_mx W/2, g_my H/2)|, cnt += 1,
+//                          the mean gradient formed from grad2d's moments and the
+//                          conic of the Gaussian's record
 //   gs_densify_plan        per Gaussian an action (prune / keep / clone / split) and the
 //                          offset of its outputs (block scan + one-block scan of the
 //                          block sums); the new count
@@ -27,13 +29,19 @@ constexpr int kDenBlock = kDenThreads * kDenItems;  // Gaussians per plan block
 constexpr uint8_t kPrune = 0, kKeep = 1, kClone = 2, kSplit = 3;
 
 __global__ void __launch_bounds__(256)
-    k_densify_accum(const uint32_t* __restrict__ count, const float4* __restrict__ grad2d, int64_t n, float half_w,
-                    float half_h, float* __restrict__ acc, uint32_t* __restrict__ cnt) {
+    k_densify_accum(const uint32_t* __restrict__ count, const float4* __restrict__ rec,
+                    const float4* __restrict__ grad2d, int64_t n, float half_w, float half_h,
+                    float* __restrict__ acc, uint32_t* __restrict__ cnt) {
   const int64_t stride = int64_t(gridDim.x) * blockDim.x;
   for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride) {
     if (count[i] == 0u) continue;
-    const float4 g = grad2d[3 * i];  // (d mx, d my, d A, d B) of the 12-float slot
-    const float gx = __fmul_rn(g.x, half_w), gy = __fmul_rn(g.y, half_h);
+    const float4 s = grad2d[3 * i];  // (S1, S2, S3, S4) of the 12-float slot
+    const float4 ra = rec[3 * i];    // (mx, my, -A/2, -B)
+    const float cc = reinterpret_cast<const float*>(rec)[12 * i + 4];  // -C/2
+    const float A = -2.0f * ra.z, B = -ra.w, C = -2.0f * cc;      // exact
+    const float dmx = __fadd_rn(__fmul_rn(A, s.x), __fmul_rn(B, s.y));
+    const float dmy = __fadd_rn(__fmul_rn(B, s.x), __fmul_rn(C, s.y));
+    const float gx = __fmul_rn(dmx, half_w), gy = __fmul_rn(dmy, half_h);
     acc[i] = __fadd_rn(acc[i], __fsqrt_rn(__fadd_rn(__fmul_rn(gx, gx), __fmul_rn(gy, gy))));
     cnt[i] += 1u;
   }
@@ -205,16 +213,17 @@ inline int64_t densify_blocks(int64_t n) {
 
 }  // namespace gs
 
-extern "C" gs_status gs_densify_accumulate(gs_dims dims, const uint32_t* count, const float* grad2d, int32_t width,
-                                           int32_t height, float* grad_acc, uint32_t* vis_cnt, cudaStream_t stream) {
+extern "C" gs_status gs_densify_accumulate(gs_dims dims, const uint32_t* count, const float* rec, const float* grad2d,
+                                           int32_t width, int32_t height, float* grad_acc, uint32_t* vis_cnt,
+                                           cudaStream_t stream) {
   using namespace gs;
-  if (!dims_ok(dims) || !count || !grad2d || !grad_acc || !vis_cnt || width <= 0 || height <= 0)
+  if (!dims_ok(dims) || !count || !rec || !grad2d || !grad_acc || !vis_cnt || width <= 0 || height <= 0)
     return GS_ERR_INVALID_ARG;
-  if (!aligned(grad2d, 16)) return GS_ERR_INVALID_ARG;
+  if (!aligned(grad2d, 16) || !aligned(rec, 16)) return GS_ERR_INVALID_ARG;
   if (dims.n == 0) return GS_OK;
   k_densify_accum<<<grid_for(dims.n, 256, kSmCount * 16), 256, 0, stream>>>(
-      count, reinterpret_cast<const float4*>(grad2d), dims.n, 0.5f * float(width), 0.5f * float(height), grad_acc,
-      vis_cnt);
+      count, reinterpret_cast<const float4*>(rec), reinterpret_cast<const float4*>(grad2d), dims.n,
+      0.5f * float(width), 0.5f * float(height), grad_acc, vis_cnt);
   return launch_status();
 }
 

@@ -61,7 +61,11 @@ __device__ __forceinline__ bool chain_rule(const float* P, int64_t n, int64_t n_
     gq2[4] = y.x, gq2[5] = y.y, gq2[6] = y.z, gq2[7] = y.w;
     gq2[8] = z.x;
   }
-  const float gmx = gq2[0], gmy = gq2[1], gA = gq2[2], gB = gq2[3], gC = gq2[4], go = gq2[5];
+  // slots 0..4 hold the moments S1..S5 of q = dL/dpower over the pixel offsets;
+  // with the conic: dL/dmx = A S1 + B S2, dL/dmy = B S1 + C S2, dL/dA = -S3/2,
+  // dL/dB = -S4, dL/dC = -S5/2
+  const float gmx = g.A * gq2[0] + g.B * gq2[1], gmy = g.B * gq2[0] + g.C * gq2[1];
+  const float gA = -0.5f * gq2[2], gB = -gq2[3], gC = -0.5f * gq2[4], go = gq2[5];
 
   // ---- colour: SH coefficients and the view direction
   float d[3], len;

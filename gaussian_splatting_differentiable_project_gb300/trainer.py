@@ -211,7 +211,7 @@ class Trainer:
 
     def accumulate_density(self, cam: dict, stream=None) -> None:
         if self.density is not None:
-            densify_accumulate(self.n, self.n_pad, self.proj.count, self.grad2d, cam["width"], cam["height"],
+            densify_accumulate(self.n, self.n_pad, self.proj, self.grad2d, cam["width"], cam["height"],
                                self.grad_acc, self.vis_cnt, stream)
 
     def refine(self, randn=None, seed: int = 0) -> dict:

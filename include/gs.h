@@ -206,18 +206,24 @@ gs_status gs_render_fwd(const gs_camera* cam, const gs_bins* bins, uint32_t capa
  * term's gradient from gs_ssim_bwd); loss_out = l1_weight mean |C - C*| over the
  * 3 H W values.  Each pixel walks its composited entries in reverse, recovering T
  * by division by (1 - alpha), and produces per entry the partials of the loss with
- * respect to mean2d (x, y), the conic (A, B, C), opacity and colour (r, g, b);
+ * respect to opacity and colour (r, g, b) and, for mean2d and the conic, the five
+ * moments of q = dL/dpower over the pixel offset (dx, dy) = (px - mx, py - my);
  * partials of a warp are summed by shuffles and added to grad2d with global
- * atomics (summation order is not fixed).
+ * atomics (summation order is not fixed).  The conic is the Gaussian's own, so its
+ * products are applied once to the sums, by the consumers: with power =
+ * -(A dx^2 + C dy^2)/2 - B dx dy and S1..S5 the sums of q dx, q dy, q dx^2, q dx dy,
+ * q dy^2,  dL/dmx = A S1 + B S2,  dL/dmy = B S1 + C S2,  dL/dA = -S3/2,
+ * dL/dB = -S4,  dL/dC = -S5/2.
  *   image, T_final, n_contrib: outputs of gs_render_fwd (read).
  *   target      3 x H x W fp32 (read).
  *   l1_weight   weight of the L1 term (1 for the L1 objective, 1 - lambda with D-SSIM).
  *   dLdC_extra  3 x H x W fp32 added to the loss gradient, or null.
  *   grad2d      GS_GRAD2D_STRIDE x n_pad fp32, interleaved (write; zeroed by this
- *               call first): Gaussian i's partials at 12 i + (d mx, d my, d A, d B,
- *               d C, d opacity, d r, d g, d b), 12 i + 9..11 unused.  A warp's nine
- *               sums for one Gaussian land in two 32-byte sectors instead of nine
- *               planes' lines.
+ *               call first): Gaussian i's sums at 12 i + (S1, S2, S3, S4, S5,
+ *               d opacity, d r, d g, d b), 12 i + 9..11 unused.  A warp's nine sums
+ *               for one Gaussian land in two 32-byte sectors instead of nine planes'
+ *               lines.  gs_project_bwd (and the calls built on it) and
+ *               gs_densify_accumulate read this layout.
  *   loss_out    1 fp32 (write; zeroed first).
  * Errors: as gs_render_fwd, plus a negative or non-finite l1_weight. */
 gs_status gs_render_bwd(gs_dims dims, const gs_camera* cam, const gs_bins* bins, uint32_t capacity_K,
@@ -357,14 +363,18 @@ typedef struct gs_densify_cfg {
 #define GS_DENSIFY_SPLIT 3
 
 /* gs_densify_accumulate -- for each Gaussian i < n with count[i] > 0 (visible in
- * this view): grad_acc[i] += |(d mx W/2, d my H/2)| from grad2d (gs_render_bwd's
- * interleaved layout), vis_cnt[i] += 1.  fp32: the two products, their squares,
- * the sum and the square root each rounded once.
- *   count (gs_proj.count), grad2d (read); grad_acc n fp32, vis_cnt n uint32 (read
- *   and write; the caller zeroes them after each refinement).
+ * this view): grad_acc[i] += |(d mx W/2, d my H/2)|, vis_cnt[i] += 1, with the mean
+ * gradient formed from grad2d's sums (gs_render_bwd's layout) and the conic of the
+ * Gaussian's record: d mx = A S1 + B S2, d my = B S1 + C S2 (A = -2 rec[2],
+ * B = -rec[3], C = -2 rec[4]).  fp32: each product, sum, square and the square root
+ * rounded once, in that order.
+ *   count, rec (gs_proj.count, gs_proj.rec), grad2d (read); grad_acc n fp32,
+ *   vis_cnt n uint32 (read and write; the caller zeroes them after each
+ *   refinement).
  * Errors: GS_ERR_INVALID_ARG for bad dims, sizes or pointers. */
-gs_status gs_densify_accumulate(gs_dims dims, const uint32_t* count, const float* grad2d, int32_t width,
-                                int32_t height, float* grad_acc, uint32_t* vis_cnt, cudaStream_t stream);
+gs_status gs_densify_accumulate(gs_dims dims, const uint32_t* count, const float* rec, const float* grad2d,
+                                int32_t width, int32_t height, float* grad_acc, uint32_t* vis_cnt,
+                                cudaStream_t stream);
 
 /* gs_densify_plan -- per Gaussian i < n its action (GS_DENSIFY_*) and the offset of
  * its outputs in the new arrays (exclusive scan of 0, 1, 2, 2 outputs for prune,

@@ -29,20 +29,27 @@ def _scene(n):
 
 @pytest.mark.parametrize("n", [4096, 3000])
 def test_accumulate_matches_oracle(n):
+    """Seeded sums in grad2d's layout on the GPU; the oracle accumulates the mean
+    gradients they define (the header's formula with the Gaussian's conic, each fp32
+    product and sum rounded once, as stated there)."""
     P, cam = _scene(n)
     W, H = cam["width"], cam["height"]
     tr = gs.Trainer(P, n, W, H, capacity=1 << 20, lr_plane=gi.lr_planes())
     tr.enable_density_control(3.3)
     pr = oracle.project(P, n, cam, 32)
-    tgt = gi.offset_target(oracle.render(pr, W, H)["image"], seed=2)
-    g2 = oracle.render(pr, W, H, target=tgt)["grad2d"].astype(np.float32)
     tr.forward(cam)
-    tr.grad2d.copy_(torch.from_numpy(gs.grad2d_interleaved(np.pad(g2, ((0, 0), (0, tr.n_pad - n))))))
+    S = gi.random_grad2d(5, n, tr.n_pad)
+    tr.grad2d.copy_(torch.from_numpy(gs.grad2d_interleaved(S)))
+    vis = pr["count"] > 0
+    A, B, C = (np.where(vis, pr["conic"][:, k], 0).astype(np.float32) for k in range(3))
+    g2 = np.zeros((9, n), np.float32)
+    g2[0] = (A * S[0, :n]).astype(np.float32) + (B * S[1, :n]).astype(np.float32)
+    g2[1] = (B * S[0, :n]).astype(np.float32) + (C * S[1, :n]).astype(np.float32)
     acc = np.zeros(n, np.float32)
     cnt = np.zeros(n, np.int64)
     for _ in range(2):
-        gs.densify_accumulate(n, tr.n_pad, tr.proj.count, tr.grad2d, W, H, tr.grad_acc, tr.vis_cnt)
-        D.accumulate(g2, pr["count"] > 0, W, H, acc, cnt)
+        gs.densify_accumulate(n, tr.n_pad, tr.proj, tr.grad2d, W, H, tr.grad_acc, tr.vis_cnt)
+        D.accumulate(g2, vis, W, H, acc, cnt)
     torch.cuda.synchronize()
     np.testing.assert_array_equal(tr.vis_cnt.cpu().numpy()[:n], cnt)
     np.testing.assert_array_equal(tr.grad_acc.cpu().numpy()[:n].view(np.uint32), acc.view(np.uint32))

@@ -18,6 +18,7 @@ import pytest
 
 import gs_inputs as gi
 import oracle
+from _grad2d import moments_to_partials
 
 pytestmark = pytest.mark.gpu
 
@@ -145,13 +146,14 @@ def _check_block(tr, ref, cam, tx0, ty0, nt, backward=True):
     torch.cuda.synchronize()
     sel = inside[idx]
     assert sel.sum() > 50
-    got = gs.grad2d_planes(tr.grad2d, tr.n_pad)[:, idx[sel]]
+    got = moments_to_partials(gs.grad2d_planes(tr.grad2d, tr.n_pad)[:, idx[sel]], ref["conic"][idx[sel]])
     _grad_close(got, rb["grad2d"][:, sel], what="grad2d (block)")
 
 
 def _check_fused_sample(tr, P, n, cam, idx):
-    """Fused projection backward + Adam (t = 1) on seeded 2D gradients, against the
-    oracle's projection backward and Adam for sampled Gaussians."""
+    """Fused projection backward + Adam (t = 1) on seeded 2D sums, against the
+    oracle's projection backward (fed the partials they define) and Adam for sampled
+    Gaussians."""
     n_pad = P.shape[1]
     g2 = gi.random_grad2d(21, n, n_pad)
     lr = gi.lr_planes()
@@ -162,7 +164,8 @@ def _check_fused_sample(tr, P, n, cam, idx):
                         lr, 0.9, 0.999, 1e-15, 1, tr.status)
     torch.cuda.synchronize()
     Ps = np.ascontiguousarray(P[:, idx])
-    gref = oracle.project_bwd(Ps, len(idx), cam, g2[:, idx], prec=32)
+    conic = oracle.project(Ps, len(idx), cam, 32)["conic"]
+    gref = oracle.project_bwd(Ps, len(idx), cam, moments_to_partials(g2[:, idx], conic), prec=32)
     pr, mr, vr = oracle.adam(Ps.astype(np.float64), gref, np.zeros_like(gref), np.zeros_like(gref), lr, 0.9, 0.999,
                              1e-15, 1)
     m = tr.m.cpu().numpy()[:, idx]
@@ -216,7 +219,7 @@ def test_iso1m_512_full_parity():
     gs.render_bwd(n, tr.n_pad, cam, tr.bins, tr.bg, tr.image, torch.from_numpy(target).to(DEV), tr.T_final,
                   tr.n_contrib, tr.grad2d, tr.loss, tr.status)
     torch.cuda.synchronize()
-    _grad_close(gs.grad2d_planes(tr.grad2d, n), rb["grad2d"], what="grad2d")
+    _grad_close(moments_to_partials(gs.grad2d_planes(tr.grad2d, n), ref["conic"]), rb["grad2d"], what="grad2d")
     assert abs(float(tr.loss.item()) - rb["loss"]) <= 1e-5 * rb["loss"]
     _check_fused_sample(tr, P, n, cam, np.random.default_rng(1).choice(n, 50_000, replace=False))
     assert tr.check_status() == 0

@@ -20,6 +20,7 @@ import pytest
 
 import gs_inputs as gi
 import oracle
+from _grad2d import moments_to_partials
 
 pytestmark = pytest.mark.gpu
 
@@ -40,6 +41,11 @@ def _status():
 
 def _u32(t):
     return t.cpu().numpy().view(np.uint32)
+
+
+def _partials(tr, n, conic):
+    """The GPU's grad2d of Gaussians [0, n) as the nine 2D partials (header layout)."""
+    return moments_to_partials(gs.grad2d_planes(tr.grad2d, n), conic[:n])
 
 
 GROUPS_59 = [(0, 3), (3, 10), (10, 11), (11, 59)]
@@ -251,18 +257,18 @@ def test_render_bwd_parity(case):
     tr.backward(cam, tgt)
     torch.cuda.synchronize()
     assert tr.check_status() == 0
-    g2 = gs.grad2d_planes(tr.grad2d, n)
-    _grad_close(g2, rd["grad2d"], what="grad2d")
+    _grad_close(_partials(tr, n, ref["conic"]), rd["grad2d"], what="grad2d")
     assert abs(float(tr.loss.item()) - rd["loss"]) <= 1e-5 * rd["loss"]
     # padding gets no gradient
     assert not tr.grad2d[n:].any()
 
 
 def test_project_bwd_parity(case):
-    """Seeded stand-in 2D gradients fed to both sides isolate the chain rule."""
+    """Seeded stand-in 2D sums fed to both sides isolate the chain rule (the oracle
+    gets them as the partials the header's layout defines)."""
     tr, P, cam, n = case["tr"], case["P"], case["cam"], case["n"]
     g2 = gi.random_grad2d(11, n, P.shape[1])
-    ref = oracle.project_bwd(P, n, cam, g2[:, :n], prec=32)
+    ref = oracle.project_bwd(P, n, cam, moments_to_partials(g2[:, :n], case["ref_proj"]["conic"][:n]), prec=32)
     g2d = torch.from_numpy(gs.grad2d_interleaved(g2)).to(DEV)
     st = _status()
     gs.project(n, tr.params, cam, tr.proj, st)
@@ -310,7 +316,7 @@ def test_whole_step_end_to_end(case, fused):
     tr.step(cam, torch.from_numpy(target).to(DEV))
     torch.cuda.synchronize()
     assert tr.check_status() == 0
-    _grad_close(gs.grad2d_planes(tr.grad2d, n), ref["render"]["grad2d"], what="grad2d")
+    _grad_close(_partials(tr, n, case["ref_proj"]["conic"]), ref["render"]["grad2d"], what="grad2d")
     gref = ref["grads"][:, :n]
     if not fused:
         _grad_close(tr.grads.cpu().numpy()[:, :n], gref, rtol=2e-4, floor=2e-6, what="param grads")
@@ -442,7 +448,7 @@ def test_whole_step_with_dssim_end_to_end(case, fused):
     assert tr.check_status() == 0
     assert abs(tr.total_loss() - ref["render"]["loss"]) <= 1e-5 * abs(ref["render"]["loss"])
     assert abs(float(tr.ssim_val.item()) - ref["render"]["ssim"]) <= 1e-5
-    _grad_close(gs.grad2d_planes(tr.grad2d, n), ref["render"]["grad2d"], what="grad2d")
+    _grad_close(_partials(tr, n, case["ref_proj"]["conic"]), ref["render"]["grad2d"], what="grad2d")
     gref = ref["grads"][:, :n]
     if not fused:
         _grad_close(tr.grads.cpu().numpy()[:, :n], gref, rtol=2e-4, floor=2e-6, what="param grads")
@@ -473,7 +479,7 @@ def test_render_bwd_extra_image_gradient(case):
     torch.cuda.synchronize()
     assert int(st.item()) == 0
     assert float(tr.loss.item()) == 0.0
-    _grad_close(gs.grad2d_planes(tr.grad2d, n), rd["grad2d"], what="grad2d")
+    _grad_close(_partials(tr, n, ref["conic"]), rd["grad2d"], what="grad2d")
 
 
 def test_staged_host_targets_feed_the_right_step(case):
@@ -711,4 +717,4 @@ def test_large_gaussian_spanning_many_tiles():
     tgt = torch.from_numpy(gi.offset_target(oracle.render(ref, 200, 120)["image"], 2)).to(DEV)
     tr.backward(cam, tgt)
     torch.cuda.synchronize()
-    _grad_close(gs.grad2d_planes(tr.grad2d, n), rd["grad2d"], what="grad2d")
+    _grad_close(_partials(tr, n, ref["conic"]), rd["grad2d"], what="grad2d")
