@@ -187,10 +187,13 @@ __global__ void __launch_bounds__(kRasterThreads)
         v[6] = g0 * wgt;
         v[7] = g1 * wgt;
         v[8] = g2 * wgt;
-        const float dLda = Ti * (g0 * (rb.z - acc0) + g1 * (rb.w - acc1) + g2 * (rc.x - acc2));
-        acc0 = alpha * rb.z + (1.0f - alpha) * acc0;
-        acc1 = alpha * rb.w + (1.0f - alpha) * acc1;
-        acc2 = alpha * rc.x + (1.0f - alpha) * acc2;
+        // colour of the entry minus the normalised colour behind it; the carried colour
+        // then moves toward the entry's by alpha (acc + alpha (c - acc))
+        const float d0 = rb.z - acc0, d1 = rb.w - acc1, d2 = rc.x - acc2;
+        const float dLda = Ti * (g0 * d0 + g1 * d1 + g2 * d2);
+        acc0 = fmaf(alpha, d0, acc0);
+        acc1 = fmaf(alpha, d1, acc1);
+        acc2 = fmaf(alpha, d2, acc2);
         T = contrib ? Ti : T;
         const bool lin = contrib && !clamped;
         const float dLdp = lin ? dLda * alpha : 0.0f;
