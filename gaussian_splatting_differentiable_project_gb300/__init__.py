@@ -159,6 +159,12 @@ def load(build_if_missing: bool = True):
         lib.gs_ssim_bwd.restype = st
         lib.gs_util_expf.argtypes = [P, P, ctypes.c_int64, P]
         lib.gs_util_expf.restype = st
+        lib.gs_util_lookback_probe_bytes.argtypes = []
+        lib.gs_util_lookback_probe_bytes.restype = ctypes.c_size_t
+        lib.gs_util_lookback_probe.argtypes = [ctypes.c_int32, P, ctypes.c_size_t, P, P]
+        lib.gs_util_lookback_probe.restype = st
+        lib.gs_util_mbarrier_probe.argtypes = [ctypes.c_int32, P, P]
+        lib.gs_util_mbarrier_probe.restype = st
         lib.gs_spatial_order_workspace_bytes.argtypes = [GsDims]
         lib.gs_spatial_order_workspace_bytes.restype = ctypes.c_size_t
         lib.gs_spatial_order.argtypes = [GsDims, P, P, P, ctypes.c_size_t, P, P]

@@ -309,7 +309,7 @@ __global__ void __launch_bounds__(kSortThreads)
     k_bs_onesweep(const uint32_t* __restrict__ kin, const uint32_t* __restrict__ vin, uint32_t* __restrict__ kout,
                   uint32_t* __restrict__ vout, const uint32_t* __restrict__ n_ptr, uint32_t cap, int shift,
                   const uint32_t* __restrict__ hist, uint32_t* __restrict__ look, uint32_t* __restrict__ ticket,
-                  uint32_t* __restrict__ dev_status) {
+                  uint32_t* __restrict__ dev_status, int spin_limit = kSpinLimit) {
   extern __shared__ __align__(16) unsigned char smem[];
   uint32_t* s_keys = reinterpret_cast<uint32_t*>(smem);
   uint32_t* s_vals = s_keys + kPart;
@@ -412,7 +412,7 @@ __global__ void __launch_bounds__(kSortThreads)
         if (!done) {
           uint32_t v = w[k];
           while ((v & ~kCountMask) == 0u) {
-            if (++spins > kSpinLimit) {
+            if (++spins > spin_limit) {
               raise_status(dev_status, GS_ERR_TIMEOUT);
               v = kFlagInc;
               break;
@@ -776,5 +776,55 @@ extern "C" gs_status gs_permute_planes(gs_dims dims, int32_t planes, const uint3
   if (total == 0) return GS_OK;
   k_permute_planes<<<grid_for(total, 256, kSmCount * 16), 256, 0, stream>>>(
       perm, dims.n, dims.n_pad, planes, static_cast<const uint32_t*>(src), static_cast<uint32_t*>(dst));
+  return launch_status();
+}
+
+// ------------------------------------------------------------------ wait probe
+// A onesweep pass whose first partition never runs: its look-back word is never
+// published, so the one CTA (partition 1) waits on it until spin_limit runs out, raises
+// GS_ERR_TIMEOUT and finishes its scatter (in bounds: with nothing added from the
+// look-back each key lands inside its digit's range).  Scratch: keys and values in and
+// out for two partitions, the histogram, the count, the ticket and two partitions'
+// look-back words.
+namespace {
+constexpr size_t kProbeKeys = 2 * size_t(gs::kPart);
+constexpr size_t kProbeBytes = (4 * kProbeKeys + 256 + 2 + 2 * 256) * sizeof(uint32_t);
+
+__global__ void k_probe_init(uint32_t* __restrict__ w) {
+  uint32_t* kin = w;
+  uint32_t* vin = kin + kProbeKeys;
+  uint32_t* hist = vin + 3 * kProbeKeys;  // after kout, vout
+  uint32_t* n = hist + 256;
+  uint32_t* ticket = n + 1;
+  uint32_t* look = ticket + 1;
+  for (uint32_t i = threadIdx.x; i < kProbeKeys; i += blockDim.x) {
+    kin[i] = i & 255u;
+    vin[i] = i;
+  }
+  for (uint32_t d = threadIdx.x; d < 256; d += blockDim.x) hist[d] = uint32_t(kProbeKeys / 256);
+  for (uint32_t k = threadIdx.x; k < 2 * 256; k += blockDim.x) look[k] = 0u;
+  if (threadIdx.x == 0) {
+    *n = uint32_t(kProbeKeys);
+    *ticket = 1u;  // partition 0 is never taken
+  }
+}
+}  // namespace
+
+extern "C" size_t gs_util_lookback_probe_bytes(void) { return kProbeBytes; }
+
+extern "C" gs_status gs_util_lookback_probe(int32_t spin_limit, void* scratch, size_t scratch_bytes,
+                                            uint32_t* dev_status, cudaStream_t stream) {
+  using namespace gs;
+  if (spin_limit <= 0 || !scratch || scratch_bytes < kProbeBytes || !dev_status || !aligned(scratch, 16))
+    return GS_ERR_INVALID_ARG;
+  uint32_t* w = static_cast<uint32_t*>(scratch);
+  uint32_t *kin = w, *vin = kin + kProbeKeys, *kout = vin + kProbeKeys, *vout = kout + kProbeKeys;
+  uint32_t* hist = vout + kProbeKeys;
+  uint32_t* n = hist + 256;
+  uint32_t* ticket = n + 1;
+  uint32_t* look = ticket + 1;
+  k_probe_init<<<1, 256, 0, stream>>>(w);
+  k_bs_onesweep<<<1, kSortThreads, kSortSmem, stream>>>(kin, vin, kout, vout, n, uint32_t(kProbeKeys), 0, hist, look,
+                                                        ticket, dev_status, spin_limit);
   return launch_status();
 }

@@ -138,8 +138,9 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 
 // Wait for phase `parity` of the barrier with an iteration limit; false (and the
 // TIMEOUT status bit) if the limit ran out.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* dev_status) {
-  for (int it = 0; it < kWaitLimit; ++it) {
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* dev_status,
+                                          int limit = kWaitLimit) {
+  for (int it = 0; it < limit; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
   }
   raise_status(dev_status, GS_ERR_TIMEOUT);

@@ -129,3 +129,25 @@ extern "C" gs_status gs_render_fwd(const gs_camera* cam, const gs_bins* bins, ui
       capacity_K, cam->width, cam->height, TX, bg[0], bg[1], bg[2], image, T_final, n_contrib, dev_status);
   return launch_status();
 }
+
+// ------------------------------------------------------------------ wait probe
+// The rasterisers' bounded mbarrier wait on a barrier nothing arrives at: phase 0 never
+// completes, the wait gives up after wait_limit tries, raises GS_ERR_TIMEOUT and returns.
+namespace {
+__global__ void k_mbar_probe(int limit, uint32_t* __restrict__ dev_status) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    gs::mbar_init(&bar, 1);
+    gs::fence_mbar_init();
+  }
+  __syncthreads();
+  gs::mbar_wait(&bar, 0u, dev_status, limit);
+}
+}  // namespace
+
+extern "C" gs_status gs_util_mbarrier_probe(int32_t wait_limit, uint32_t* dev_status, cudaStream_t stream) {
+  using namespace gs;
+  if (wait_limit <= 0 || !dev_status) return GS_ERR_INVALID_ARG;
+  k_mbar_probe<<<1, 32, 0, stream>>>(wait_limit, dev_status);
+  return launch_status();
+}

@@ -470,6 +470,22 @@ gs_status gs_permute_planes(gs_dims dims, int32_t planes, const uint32_t* perm, 
  * Errors: GS_ERR_INVALID_ARG for null pointers or n < 0. */
 gs_status gs_util_expf(const float* x, float* y, int64_t n, cudaStream_t stream);
 
+/* ---------------------------------------------------------------------------
+ * gs_util_lookback_probe / gs_util_mbarrier_probe -- make the library's two bounded
+ * waits run out, so that callers and tests can see the failure path without a GPU
+ * fault or hang.  gs_util_lookback_probe runs one onesweep pass whose first partition
+ * never runs: the one CTA's look-back waits on a word nothing publishes for spin_limit
+ * tries (the binning's passes use 2^22), raises GS_ERR_TIMEOUT in dev_status and
+ * finishes in bounds.  gs_util_mbarrier_probe waits on an mbarrier nothing arrives at
+ * for wait_limit tries (the rasterisers use 2^24), raises GS_ERR_TIMEOUT and returns.
+ *   scratch: gs_util_lookback_probe_bytes() device bytes, 16-byte aligned.
+ * Errors: GS_ERR_INVALID_ARG for a limit <= 0, null pointers, short or misaligned
+ * scratch. */
+size_t gs_util_lookback_probe_bytes(void);
+gs_status gs_util_lookback_probe(int32_t spin_limit, void* scratch, size_t scratch_bytes, uint32_t* dev_status,
+                                 cudaStream_t stream);
+gs_status gs_util_mbarrier_probe(int32_t wait_limit, uint32_t* dev_status, cudaStream_t stream);
+
 /* Static description of a status value (several bits: the lowest set one). */
 const char* gs_status_str(uint32_t status);
 

@@ -101,6 +101,12 @@ def test_argument_errors_are_returned_without_a_gpu():
         gs.GS_ERR_INVALID_ARG
     assert lib.gs_permute_planes(gs.dims(1000, 1024), 0, p, p, ctypes.c_void_p(32), None) == gs.GS_ERR_INVALID_ARG
     assert lib.gs_permute_planes(gs.dims(1000, 1024), 59, p, p, p, None) == gs.GS_ERR_INVALID_ARG
+    # wait probes: a non-positive limit, short scratch
+    nb = lib.gs_util_lookback_probe_bytes()
+    assert nb > 0
+    assert lib.gs_util_lookback_probe(0, p, nb, p, None) == gs.GS_ERR_INVALID_ARG
+    assert lib.gs_util_lookback_probe(100, p, nb - 1, p, None) == gs.GS_ERR_INVALID_ARG
+    assert lib.gs_util_mbarrier_probe(-1, p, None) == gs.GS_ERR_INVALID_ARG
 
 
 def test_product_package_has_no_oracle_or_cpu_path():

@@ -718,3 +718,30 @@ def test_large_gaussian_spanning_many_tiles():
     tr.backward(cam, tgt)
     torch.cuda.synchronize()
     _grad_close(_partials(tr, n, ref["conic"]), rd["grad2d"], what="grad2d")
+
+
+# ----------------------------------------------------------------------------- bounded waits
+
+@pytest.mark.parametrize("which", ["lookback", "mbarrier"])
+def test_bounded_wait_runs_out_and_the_context_stays_usable(which):
+    """A wait on a flag nothing sets (a look-back word never published, an mbarrier
+    nothing arrives at) gives up after its limit: GS_ERR_TIMEOUT in the status word, the
+    kernel returns, and the next calls on the device run normally."""
+    lib = gs.load()
+    st = _status()
+    s = torch.cuda.current_stream().cuda_stream
+    if which == "lookback":
+        scratch = torch.empty(lib.gs_util_lookback_probe_bytes(), dtype=torch.uint8, device=DEV)
+        r = lib.gs_util_lookback_probe(2000, scratch.data_ptr(), scratch.numel(), st.data_ptr(), s)
+    else:
+        r = lib.gs_util_mbarrier_probe(2000, st.data_ptr(), s)
+    assert r == gs.GS_OK
+    torch.cuda.synchronize()
+    assert int(st.item()) & gs.GS_ERR_TIMEOUT
+    # the context is usable: a forward pass runs and matches the oracle
+    cfg, P, n = _scene("tiny")
+    cam = _cam_for(cfg)
+    tr = _gpu_forward(P, n, cam)
+    rd = oracle.render(oracle.project(P, n, cam, 32), cam["width"], cam["height"])
+    assert tr.check_status() == 0
+    np.testing.assert_array_equal(tr.image.cpu().numpy().view(np.uint32), rd["image"].view(np.uint32))
