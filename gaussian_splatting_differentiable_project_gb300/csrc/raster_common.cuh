@@ -31,6 +31,22 @@ __device__ __forceinline__ void pixel_of_thread(int TX, int& px, int& py) {
   py = ty * kTile + (q >> 1) * 8 + warp * 4 + (lane >> 3);
 }
 
+// The backward runs one warp (one 8x4 block) per CTA, eight CTAs per tile: a warp whose
+// pixels need fewer entries than its neighbour's then finishes and frees its slot,
+// instead of waiting at every batch barrier for the other warp of a two-warp CTA
+// (0.987x of the backward's time against two-warp CTAs).
+constexpr int kBwdThreads = 32;
+constexpr int kBwdCtasPerTile = 8;
+
+__device__ __forceinline__ int bwd_tile_of_block() { return int(blockIdx.x) / kBwdCtasPerTile; }
+
+// Origin (top-left pixel) of the backward CTA's 8x4 block.
+__device__ __forceinline__ void bwd_block_origin(int TX, int& bx, int& by) {
+  const int tile = bwd_tile_of_block(), q = int(blockIdx.x) % kBwdCtasPerTile;
+  bx = (tile % TX) * kTile + (q & 1) * 8;
+  by = (tile / TX) * kTile + (q >> 1) * 4;
+}
+
 // Pixel-centre bounds of this warp's 8x4 block.
 __device__ __forceinline__ void warp_block_bounds(int TX, float& x0, float& x1, float& y0, float& y1) {
   const int tile = tile_of_block(), q = int(blockIdx.x) % kCtasPerTile;

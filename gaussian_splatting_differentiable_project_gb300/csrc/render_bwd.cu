@@ -1,7 +1,8 @@
 // gs_render_bwd: L1 loss gradient and the compositing backward.
 //
-// One CTA per 8x8 quarter tile, one thread per pixel, the tile's records staged in
-// reverse batches by cp.async.bulk (as in the forward).  Each pixel walks its composited
+// One warp per CTA, one 8x4 block of a 16x16 tile (eight CTAs per tile), one thread per
+// pixel, the tile's records staged in reverse batches by cp.async.bulk (as in the
+// forward).  Each pixel walks its composited
 // entries back to front, recovering the transmittance before each entry by
 // division by (1 - alpha) and carrying the normalised colour of everything
 // behind it.  Per entry each lane holds nine partials: the opacity and colour
@@ -62,7 +63,7 @@ __device__ __forceinline__ void warp_reduce9(const float v[9], float* out8, floa
   *out9 = z;
 }
 
-__global__ void __launch_bounds__(kRasterThreads)
+__global__ void __launch_bounds__(kBwdThreads)
     k_render_bwd(const Rec* __restrict__ srec, const uint2* __restrict__ ranges, const uint32_t* __restrict__ n_isect,
                  uint32_t cap, int W, int H, int TX, float bg0, float bg1, float bg2, const float* __restrict__ image,
                  const float* __restrict__ target, const float* __restrict__ T_final,
@@ -71,17 +72,16 @@ __global__ void __launch_bounds__(kRasterThreads)
                  uint32_t* __restrict__ dev_status) {
   __shared__ __align__(128) Rec s_rec[2][kBatch];
   __shared__ __align__(8) uint64_t s_bar[2];
-  __shared__ float s_red[kRasterThreads / 32];
-  __shared__ uint32_t s_max[kRasterThreads / 32];
 
-  const int tile = tile_of_block();
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int pxi, pyi;
-  pixel_of_thread(TX, pxi, pyi);
+  const int tile = bwd_tile_of_block();
+  const int lane = threadIdx.x & 31;
+  int obx, oby;
+  bwd_block_origin(TX, obx, oby);
+  const int pxi = obx + (lane & 7), pyi = oby + (lane >> 3);
   const bool inside = pxi < W && pyi < H;
   const float px = float(pxi) + 0.5f, py = float(pyi) + 0.5f;
-  float bx0, bx1, by0, by1;
-  warp_block_bounds(TX, bx0, bx1, by0, by1);
+  const float bx0 = float(obx) + 0.5f, bx1 = float(obx) + 7.5f;
+  const float by0 = float(oby) + 0.5f, by1 = float(oby) + 3.5f;
 
   // per-pixel loss gradient
   float g0 = 0.0f, g1 = 0.0f, g2 = 0.0f, T = 1.0f, lsum = 0.0f;
@@ -105,7 +105,7 @@ __global__ void __launch_bounds__(kRasterThreads)
     T = T_final[pix];
     nc = n_contrib[pix];
   }
-  // CTA loss partial and the largest n_contrib
+  // the warp's loss partial and its largest n_contrib
   float ls = lsum;
   uint32_t mx = nc;
 #pragma unroll
@@ -114,19 +114,8 @@ __global__ void __launch_bounds__(kRasterThreads)
     mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
   }
   const uint32_t warp_max = mx;
-  if (lane == 0) {
-    s_red[warp] = ls;
-    s_max[warp] = mx;
-  }
-  __syncthreads();
-  uint32_t n_max = 0;
-  if (threadIdx.x == 0) {
-    float t = 0.0f;
-    for (int w = 0; w < kRasterThreads / 32; ++w) t += s_red[w];
-    atomicAdd(loss, t * (l1w * inv3P));
-  }
-#pragma unroll
-  for (int w = 0; w < kRasterThreads / 32; ++w) n_max = max(n_max, s_max[w]);
+  if (lane == 0) atomicAdd(loss, ls * (l1w * inv3P));
+  uint32_t n_max = warp_max;
 
   const uint32_t K = min(*n_isect, cap);
   const uint2 rg = ranges[tile];
@@ -260,7 +249,7 @@ extern "C" gs_status gs_render_bwd(gs_dims dims, const gs_camera* cam, const gs_
   const int TX = (cam->width + kTile - 1) / kTile;
   const int64_t tiles = n_tiles(cam);
   const float inv3P = float(1.0 / (3.0 * double(cam->width) * double(cam->height)));
-  k_render_bwd<<<int(tiles * kCtasPerTile), kRasterThreads, 0, stream>>>(
+  k_render_bwd<<<int(tiles * kBwdCtasPerTile), kBwdThreads, 0, stream>>>(
       reinterpret_cast<const Rec*>(bins->rec), reinterpret_cast<const uint2*>(bins->ranges), bins->n_isect,
       capacity_K, cam->width, cam->height, TX, bg[0], bg[1], bg[2], image, target, T_final, n_contrib, grad2d,
       dims.n_pad, loss_out, inv3P, l1_weight, dLdC_extra, dev_status);
