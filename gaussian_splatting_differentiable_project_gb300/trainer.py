@@ -313,6 +313,28 @@ class Trainer:
         self.step(cam, targets.get(slot, stream), stream)
         targets.release(slot, stream)
 
+    # checkpoint ----------------------------------------------------------------------
+    def save(self, path) -> None:
+        """Write the state a run resumes from to one ``.npz`` file (host copies;
+        synchronises): the parameter and Adam moment planes, the Adam step count and
+        the Gaussian count."""
+        np.savez(path, params=self.params.cpu().numpy(), m=self.m.cpu().numpy(), v=self.v.cpu().numpy(),
+                 t=np.int64(self.t), n=np.int64(self.n))
+
+    @classmethod
+    def load(cls, path, width: int, height: int, capacity: int, lr_plane, **kwargs) -> "Trainer":
+        """A trainer resumed from ``save``'s file.  Image size, capacity, learning rates
+        and the other constructor options are the caller's, as for a new trainer;
+        density control, if wanted, is enabled again (its accumulators start at zero,
+        as after a refinement)."""
+        import torch
+        with np.load(path) as z:
+            tr = cls(z["params"], int(z["n"]), width, height, capacity, lr_plane, **kwargs)
+            tr.m.copy_(torch.from_numpy(z["m"]))
+            tr.v.copy_(torch.from_numpy(z["v"]))
+            tr.t = int(z["t"])
+        return tr
+
     # host-side reads (synchronise) -----------------------------------------------
     def total_loss(self) -> float:
         """(1 - lambda) L1 + lambda (1 - SSIM) of the last step (L1 alone for lambda = 0)."""
