@@ -607,7 +607,8 @@ def run_gb300(args, cfg, ws, rank, local):
         "config": dict(_config_dict(cfg), parallelism=f"replicas{ws}", capacity_K=capacity,
                        objective=(f"{1 - args.dssim:g} L1 + {args.dssim:g} (1 - SSIM)" if args.dssim > 0 else "L1"),
                        K_mean=Kmean, visible_mean=Vmean, pairs_bwd_mean=Emean,
-                       entries_per_pixel=Emean / float(W * H), batch=B, storage_order=args.order,
+                       entries_per_pixel=Emean / float(W * H), batch=B, storage_order=args.order, seed=args.seed,
+                       gpu=torch.cuda.get_device_name(dev),
                        cuda_graph=bool(graphs)),
         "views_per_s": value * B,
         "roofline": roof,
