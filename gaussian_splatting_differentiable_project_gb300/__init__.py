@@ -7,9 +7,18 @@ current CUDA stream.  There is no CPU path: if the library is missing or no GPU 
 present, the calls raise.
 
 Entry points (same names as the C ABI, without the ``gs_`` prefix):
-``project``, ``bin_sort``, ``render_fwd``, ``render_bwd``, ``project_bwd``,
-``adam_step``, the fused ``project_bwd_adam``, plus ``bin_sort_noalloc``,
-``util_expf`` and ``bin_sort_workspace_bytes``.
+- the step: ``project``, ``bin_sort``, ``render_fwd``, ``render_bwd``,
+  ``project_bwd``, ``adam_step``, and the fused ``project_bwd_adam``;
+- the D-SSIM term: ``ssim_fwd``, ``ssim_bwd``;
+- batches and graphs: ``project_bwd_accumulate``, ``project_bwd_adam_tdev``,
+  ``step_counter_add``;
+- density control: ``densify_accumulate``, ``densify_plan``, ``densify_apply``,
+  ``opacity_reset``;
+- storage order: ``spatial_order``, ``permute_planes``;
+- sizes and utilities: ``bin_sort_workspace_bytes``, ``densify_workspace_bytes``,
+  ``spatial_order_workspace_bytes``, ``bin_sort_noalloc``, ``util_expf``.
+Tensor arguments must be dense CUDA tensors; anything else raises ``GsError``
+before a call is made.
 """
 from __future__ import annotations
 
@@ -194,7 +203,57 @@ def _stream(stream=None):
 
 
 def _p(t) -> ctypes.c_void_p:
+    """The device address of a dense CUDA tensor.  The library reads and writes every
+    buffer as a dense array in device memory, so a host tensor (whose address a kernel
+    cannot dereference) or a strided view (which it would misread) is refused here,
+    before anything is enqueued."""
+    if not t.is_cuda:
+        raise GsError(f"expected a CUDA tensor, got one on {t.device} with shape {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise GsError(f"expected a contiguous tensor, got shape {tuple(t.shape)} with strides {t.stride()}")
     return ctypes.c_void_p(t.data_ptr())
+
+
+# element kinds of _buf: fp32, any 4-byte integer (int32 or uint32 buffers), int64,
+# bytes, or any 4-byte type
+_KINDS = {
+    "f32": ("fp32", lambda t: t.dtype == _torch().float32),
+    "i32": ("a 4-byte integer type", lambda t: t.element_size() == 4 and not t.is_floating_point()),
+    "i64": ("int64", lambda t: t.dtype == _torch().int64),
+    "u8": ("uint8", lambda t: t.dtype == _torch().uint8),
+    "any4": ("a 4-byte type", lambda t: t.element_size() == 4),
+}
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _buf(t, count: int, kind: str, what: str) -> ctypes.c_void_p:
+    """``_p`` for a buffer the library reads or writes ``count`` elements of: its type
+    and size are checked first (a short buffer would be overrun on the device)."""
+    name, ok = _KINDS[kind]
+    if not ok(t):
+        raise GsError(f"{what}: expected {name}, got {t.dtype}")
+    if t.numel() < count:
+        raise GsError(f"{what}: needs {count} elements, got {t.numel()} (shape {tuple(t.shape)})")
+    return _p(t)
+
+
+def _planes(t, n_pad: int, what: str, planes: int = N_PLANES) -> ctypes.c_void_p:
+    return _buf(t, planes * n_pad, "f32", what)
+
+
+def _check_proj(proj, n_pad: int) -> None:
+    if proj.depth.numel() < n_pad:
+        raise GsError(f"projection buffers hold {proj.depth.numel()} Gaussians, need {n_pad}")
+
+
+def _check_bins(bins, cam: GsCamera) -> None:
+    if bins.ranges.shape[0] < n_tiles(cam.width, cam.height):
+        raise GsError(f"bin buffers hold ranges for {bins.ranges.shape[0]} tiles, the view has "
+                      f"{n_tiles(cam.width, cam.height)}")
 
 
 def camera(cam: dict) -> GsCamera:
@@ -262,8 +321,10 @@ class BinBuffers:
 
 def project(n: int, params, cam: dict, proj: ProjBuffers, dev_status, stream=None) -> None:
     cc = camera(cam)
-    _check(load().gs_project(dims(n, params.shape[1]), _p(params), ctypes.byref(cc), proj.c(), _p(dev_status),
-                             _stream(stream)), "gs_project")
+    n_pad = int(params.shape[1])
+    _check_proj(proj, n_pad)
+    _check(load().gs_project(dims(n, n_pad), _planes(params, n_pad, "params"), ctypes.byref(cc), proj.c(),
+                             _buf(dev_status, 1, "i32", "dev_status"), _stream(stream)), "gs_project")
 
 
 def bin_sort_workspace_bytes(n: int, capacity: int, width: int, height: int) -> int:
@@ -272,10 +333,12 @@ def bin_sort_workspace_bytes(n: int, capacity: int, width: int, height: int) -> 
 
 def bin_sort(n: int, n_pad: int, proj: ProjBuffers, cam: dict, bins: BinBuffers, dev_status, stream=None) -> None:
     cc = camera(cam)
+    _check_proj(proj, n_pad)
+    _check_bins(bins, cc)
     pc = proj.c()
     _check(load().gs_bin_sort(dims(n, n_pad), ctypes.byref(pc), ctypes.byref(cc), bins.capacity, bins.c(),
-                              ctypes.c_void_p(bins.ws_ptr()), bins.ws_bytes, _p(dev_status), _stream(stream)),
-           "gs_bin_sort")
+                              ctypes.c_void_p(bins.ws_ptr()), bins.ws_bytes, _buf(dev_status, 1, "i32", "dev_status"),
+                              _stream(stream)), "gs_bin_sort")
 
 
 def bin_sort_noalloc(n: int, n_pad: int, proj: ProjBuffers, cam: dict, bins: BinBuffers, dev_status,
@@ -283,9 +346,19 @@ def bin_sort_noalloc(n: int, n_pad: int, proj: ProjBuffers, cam: dict, bins: Bin
     """gs_bin_sort with the library's fixed scratch instead of bins.workspace (for
     callers that may not allocate device memory; see include/gs.h for the limits)."""
     cc = camera(cam)
+    _check_proj(proj, n_pad)
+    _check_bins(bins, cc)
     pc = proj.c()
     _check(load().gs_bin_sort_noalloc(dims(n, n_pad), ctypes.byref(pc), ctypes.byref(cc), bins.capacity, bins.c(),
-                                      _p(dev_status), _stream(stream)), "gs_bin_sort_noalloc")
+                                      _buf(dev_status, 1, "i32", "dev_status"), _stream(stream)),
+           "gs_bin_sort_noalloc")
+
+
+def _lr(lr_plane):
+    lr = [float(x) for x in np.asarray(lr_plane, np.float64).reshape(-1)]
+    if len(lr) != N_PLANES:
+        raise GsError(f"lr_plane: needs {N_PLANES} learning rates, got {len(lr)}")
+    return (ctypes.c_float * N_PLANES)(*lr)
 
 
 def _bg(bg):
@@ -294,58 +367,81 @@ def _bg(bg):
 
 def render_fwd(cam: dict, bins: BinBuffers, bg, image, T_final, n_contrib, dev_status, stream=None) -> None:
     cc = camera(cam)
+    _check_bins(bins, cc)
     bc = bins.c()
-    _check(load().gs_render_fwd(ctypes.byref(cc), ctypes.byref(bc), bins.capacity, _bg(bg), _p(image), _p(T_final),
-                                _p(n_contrib), _p(dev_status), _stream(stream)), "gs_render_fwd")
+    P = cc.width * cc.height
+    _check(load().gs_render_fwd(ctypes.byref(cc), ctypes.byref(bc), bins.capacity, _bg(bg),
+                                _buf(image, 3 * P, "f32", "image"), _buf(T_final, P, "f32", "T_final"),
+                                _buf(n_contrib, P, "i32", "n_contrib"), _buf(dev_status, 1, "i32", "dev_status"),
+                                _stream(stream)), "gs_render_fwd")
 
 
 def render_bwd(n: int, n_pad: int, cam: dict, bins: BinBuffers, bg, image, target, T_final, n_contrib, grad2d,
                loss, dev_status, stream=None, l1_weight: float = 1.0, dLdC_extra=None) -> None:
     cc = camera(cam)
+    _check_bins(bins, cc)
     bc = bins.c()
-    extra = _p(dLdC_extra) if dLdC_extra is not None else None
+    P = cc.width * cc.height
+    extra = _buf(dLdC_extra, 3 * P, "f32", "dLdC_extra") if dLdC_extra is not None else None
     _check(load().gs_render_bwd(dims(n, n_pad), ctypes.byref(cc), ctypes.byref(bc), bins.capacity, _bg(bg),
-                                _p(image), _p(target), _p(T_final), _p(n_contrib), float(l1_weight), extra,
-                                _p(grad2d), _p(loss), _p(dev_status), _stream(stream)), "gs_render_bwd")
+                                _buf(image, 3 * P, "f32", "image"), _buf(target, 3 * P, "f32", "target"),
+                                _buf(T_final, P, "f32", "T_final"), _buf(n_contrib, P, "i32", "n_contrib"),
+                                float(l1_weight), extra, _planes(grad2d, n_pad, "grad2d", GRAD2D_STRIDE),
+                                _buf(loss, 1, "f32", "loss"), _buf(dev_status, 1, "i32", "dev_status"),
+                                _stream(stream)), "gs_render_bwd")
 
 
 def ssim_fwd(image, target, lam: float, maps, ssim_out, stream=None) -> None:
     """Mean SSIM of image (3 x H x W) against target into ssim_out, and the partial
     derivatives of lam (1 - SSIM) and local means into maps (SSIM_MAPS x H x W)."""
     _, H, W = image.shape
-    _check(load().gs_ssim_fwd(W, H, _p(image), _p(target), float(lam), _p(maps), _p(ssim_out), _stream(stream)),
-           "gs_ssim_fwd")
+    P = H * W
+    _check(load().gs_ssim_fwd(W, H, _buf(image, 3 * P, "f32", "image"), _buf(target, 3 * P, "f32", "target"),
+                              float(lam), _buf(maps, SSIM_MAPS * P, "f32", "maps"),
+                              _buf(ssim_out, 1, "f32", "ssim_out"), _stream(stream)), "gs_ssim_fwd")
 
 
 def ssim_bwd(image, target, maps, dLdC, stream=None) -> None:
     """d[lam (1 - SSIM)] / d image into dLdC (3 x H x W), from ssim_fwd's maps."""
     _, H, W = image.shape
-    _check(load().gs_ssim_bwd(W, H, _p(image), _p(target), _p(maps), _p(dLdC), _stream(stream)), "gs_ssim_bwd")
+    P = H * W
+    _check(load().gs_ssim_bwd(W, H, _buf(image, 3 * P, "f32", "image"), _buf(target, 3 * P, "f32", "target"),
+                              _buf(maps, SSIM_MAPS * P, "f32", "maps"), _buf(dLdC, 3 * P, "f32", "dLdC"),
+                              _stream(stream)), "gs_ssim_bwd")
 
 
 def project_bwd(n: int, params, cam: dict, proj: ProjBuffers, grad2d, grads, dev_status, stream=None) -> None:
     cc = camera(cam)
+    n_pad = int(params.shape[1])
+    _check_proj(proj, n_pad)
     pc = proj.c()
-    _check(load().gs_project_bwd(dims(n, params.shape[1]), _p(params), ctypes.byref(cc), ctypes.byref(pc),
-                                 _p(grad2d), _p(grads), _p(dev_status), _stream(stream)), "gs_project_bwd")
+    _check(load().gs_project_bwd(dims(n, n_pad), _planes(params, n_pad, "params"), ctypes.byref(cc),
+                                 ctypes.byref(pc), _planes(grad2d, n_pad, "grad2d", GRAD2D_STRIDE),
+                                 _planes(grads, n_pad, "grads"), _buf(dev_status, 1, "i32", "dev_status"),
+                                 _stream(stream)), "gs_project_bwd")
 
 
 def project_bwd_accumulate(n: int, params, cam: dict, proj: ProjBuffers, grad2d, grads, dev_status,
                            stream=None) -> None:
     """grads += the chain rule of this view's grad2d (a later view of a batch)."""
     cc = camera(cam)
+    n_pad = int(params.shape[1])
+    _check_proj(proj, n_pad)
     pc = proj.c()
-    _check(load().gs_project_bwd_accumulate(dims(n, params.shape[1]), _p(params), ctypes.byref(cc),
-                                            ctypes.byref(pc), _p(grad2d), _p(grads), _p(dev_status),
+    _check(load().gs_project_bwd_accumulate(dims(n, n_pad), _planes(params, n_pad, "params"), ctypes.byref(cc),
+                                            ctypes.byref(pc), _planes(grad2d, n_pad, "grad2d", GRAD2D_STRIDE),
+                                            _planes(grads, n_pad, "grads"), _buf(dev_status, 1, "i32", "dev_status"),
                                             _stream(stream)), "gs_project_bwd_accumulate")
 
 
 def adam_step(n: int, params, grads, m, v, lr_plane, beta1: float, beta2: float, eps: float, t: int,
               stream=None) -> None:
     """Adam step number ``t`` (>= 1); bias corrections are formed inside the call."""
-    lr = (ctypes.c_float * N_PLANES)(*[float(x) for x in lr_plane])
-    _check(load().gs_adam_step(dims(n, params.shape[1]), _p(params), _p(grads), _p(m), _p(v), lr, float(beta1),
-                               float(beta2), float(eps), int(t), _stream(stream)), "gs_adam_step")
+    lr = _lr(lr_plane)
+    n_pad = int(params.shape[1])
+    _check(load().gs_adam_step(dims(n, n_pad), _planes(params, n_pad, "params"), _planes(grads, n_pad, "grads"),
+                               _planes(m, n_pad, "m"), _planes(v, n_pad, "v"), lr, float(beta1), float(beta2),
+                               float(eps), int(t), _stream(stream)), "gs_adam_step")
 
 
 def project_bwd_adam(n: int, params, cam: dict, proj: ProjBuffers, grad2d, m, v, lr_plane, beta1: float,
@@ -353,12 +449,16 @@ def project_bwd_adam(n: int, params, cam: dict, proj: ProjBuffers, grad2d, m, v,
     """Projection backward and Adam step ``t`` in one pass (no gradient planes);
     ``grads_in``: gradients accumulated by earlier views of a batch, or None."""
     cc = camera(cam)
+    n_pad = int(params.shape[1])
+    _check_proj(proj, n_pad)
     pc = proj.c()
-    lr = (ctypes.c_float * N_PLANES)(*[float(x) for x in lr_plane])
-    gin = _p(grads_in) if grads_in is not None else None
-    _check(load().gs_project_bwd_adam(dims(n, params.shape[1]), _p(params), ctypes.byref(cc), ctypes.byref(pc),
-                                      _p(grad2d), gin, _p(m), _p(v), lr, float(beta1), float(beta2), float(eps),
-                                      int(t), _p(dev_status), _stream(stream)), "gs_project_bwd_adam")
+    lr = _lr(lr_plane)
+    gin = _planes(grads_in, n_pad, "grads_in") if grads_in is not None else None
+    _check(load().gs_project_bwd_adam(dims(n, n_pad), _planes(params, n_pad, "params"), ctypes.byref(cc),
+                                      ctypes.byref(pc), _planes(grad2d, n_pad, "grad2d", GRAD2D_STRIDE), gin,
+                                      _planes(m, n_pad, "m"), _planes(v, n_pad, "v"), lr, float(beta1),
+                                      float(beta2), float(eps), int(t), _buf(dev_status, 1, "i32", "dev_status"),
+                                      _stream(stream)), "gs_project_bwd_adam")
 
 
 def project_bwd_adam_tdev(n: int, params, cam: dict, proj: ProjBuffers, grad2d, m, v, lr_plane, beta1: float,
@@ -366,17 +466,22 @@ def project_bwd_adam_tdev(n: int, params, cam: dict, proj: ProjBuffers, grad2d, 
     """project_bwd_adam with the step count read from the device int64 ``t_dev`` when
     the kernel runs (for CUDA graph capture)."""
     cc = camera(cam)
+    n_pad = int(params.shape[1])
+    _check_proj(proj, n_pad)
     pc = proj.c()
-    lr = (ctypes.c_float * N_PLANES)(*[float(x) for x in lr_plane])
-    gin = _p(grads_in) if grads_in is not None else None
-    _check(load().gs_project_bwd_adam_tdev(dims(n, params.shape[1]), _p(params), ctypes.byref(cc),
-                                           ctypes.byref(pc), _p(grad2d), gin, _p(m), _p(v), lr, float(beta1),
-                                           float(beta2), float(eps), _p(t_dev), _p(dev_status), _stream(stream)),
+    lr = _lr(lr_plane)
+    gin = _planes(grads_in, n_pad, "grads_in") if grads_in is not None else None
+    _check(load().gs_project_bwd_adam_tdev(dims(n, n_pad), _planes(params, n_pad, "params"), ctypes.byref(cc),
+                                           ctypes.byref(pc), _planes(grad2d, n_pad, "grad2d", GRAD2D_STRIDE), gin,
+                                           _planes(m, n_pad, "m"), _planes(v, n_pad, "v"), lr, float(beta1),
+                                           float(beta2), float(eps), _buf(t_dev, 1, "i64", "t_dev"),
+                                           _buf(dev_status, 1, "i32", "dev_status"), _stream(stream)),
            "gs_project_bwd_adam_tdev")
 
 
 def step_counter_add(counter, delta: int = 1, stream=None) -> None:
-    _check(load().gs_step_counter_add(_p(counter), int(delta), _stream(stream)), "gs_step_counter_add")
+    _check(load().gs_step_counter_add(_buf(counter, 1, "i64", "counter"), int(delta), _stream(stream)),
+           "gs_step_counter_add")
 
 
 def densify_thresholds(extent: float, grow_grad2d: float = 2e-4, grow_scale3d: float = 0.01,
@@ -396,15 +501,20 @@ def densify_accumulate(n: int, n_pad: int, proj: "ProjBuffers", grad2d, width: i
                        stream=None) -> None:
     """grad_acc += the NDC-scaled norm of each visible Gaussian's mean2d gradient, formed
     from grad2d's moments and the conic of its record in ``proj``; vis_cnt += 1."""
-    _check(load().gs_densify_accumulate(dims(n, n_pad), _p(proj.count), _p(proj.rec), _p(grad2d), int(width),
-                                        int(height), _p(grad_acc), _p(vis_cnt), _stream(stream)),
-           "gs_densify_accumulate")
+    _check_proj(proj, n_pad)
+    _check(load().gs_densify_accumulate(dims(n, n_pad), _p(proj.count), _p(proj.rec),
+                                        _planes(grad2d, n_pad, "grad2d", GRAD2D_STRIDE), int(width), int(height),
+                                        _buf(grad_acc, n, "f32", "grad_acc"), _buf(vis_cnt, n, "i32", "vis_cnt"),
+                                        _stream(stream)), "gs_densify_accumulate")
 
 
 def densify_plan(n: int, params, grad_acc, vis_cnt, cfg: GsDensifyCfg, action, offset, n_out, workspace,
                  stream=None) -> None:
-    _check(load().gs_densify_plan(dims(n, params.shape[1]), _p(params), _p(grad_acc), _p(vis_cnt),
-                                  ctypes.byref(cfg), _p(action), _p(offset), _p(n_out), _p(workspace),
+    n_pad = int(params.shape[1])
+    _check(load().gs_densify_plan(dims(n, n_pad), _planes(params, n_pad, "params"),
+                                  _buf(grad_acc, n, "f32", "grad_acc"), _buf(vis_cnt, n, "i32", "vis_cnt"),
+                                  ctypes.byref(cfg), _buf(action, n, "u8", "action"), _buf(offset, n, "i32", "offset"),
+                                  _buf(n_out, 1, "i32", "n_out"), _p(workspace),
                                   workspace.numel() * workspace.element_size(), _stream(stream)), "gs_densify_plan")
 
 
@@ -414,9 +524,10 @@ def spatial_order_workspace_bytes(n: int, n_pad: int) -> int:
 
 def spatial_order(n: int, params, perm, workspace, dev_status, stream=None) -> None:
     """perm[j] = index of the Gaussian stored at j in Morton order of the means."""
-    _check(load().gs_spatial_order(dims(n, params.shape[1]), _p(params), _p(perm), _p(workspace),
-                                   int(workspace.numel() * workspace.element_size()), _p(dev_status), _stream(stream)),
-           "gs_spatial_order")
+    n_pad = int(params.shape[1])
+    _check(load().gs_spatial_order(dims(n, n_pad), _planes(params, n_pad, "params"), _buf(perm, n, "i32", "perm"),
+                                   _p(workspace), int(workspace.numel() * workspace.element_size()),
+                                   _buf(dev_status, 1, "i32", "dev_status"), _stream(stream)), "gs_spatial_order")
 
 
 def permute_planes(n: int, perm, src, dst, stream=None) -> None:
@@ -424,8 +535,9 @@ def permute_planes(n: int, perm, src, dst, stream=None) -> None:
     any 4-byte element type)."""
     planes = 1 if src.dim() == 1 else int(src.shape[0])
     n_pad = int(src.shape[-1])
-    _check(load().gs_permute_planes(dims(n, n_pad), planes, _p(perm), _p(src), _p(dst), _stream(stream)),
-           "gs_permute_planes")
+    _check(load().gs_permute_planes(dims(n, n_pad), planes, _buf(perm, n, "i32", "perm"),
+                                    _buf(src, planes * n_pad, "any4", "src"), _buf(dst, planes * n_pad, "any4", "dst"),
+                                    _stream(stream)), "gs_permute_planes")
 
 
 def densify_workspace_bytes(n: int, n_pad: int) -> int:
@@ -434,19 +546,25 @@ def densify_workspace_bytes(n: int, n_pad: int) -> int:
 
 def densify_apply(n: int, params, m, v, action, offset, n_out, randn, log_shrink: float, params_dst, m_dst, v_dst,
                   dev_status, stream=None) -> None:
-    _check(load().gs_densify_apply(dims(n, params.shape[1]), int(params_dst.shape[1]), _p(params), _p(m), _p(v),
-                                   _p(action), _p(offset), _p(n_out), _p(randn), float(log_shrink),
-                                   _p(params_dst), _p(m_dst), _p(v_dst), _p(dev_status), _stream(stream)),
-           "gs_densify_apply")
+    n_pad, n_pad_dst = int(params.shape[1]), int(params_dst.shape[1])
+    _check(load().gs_densify_apply(dims(n, n_pad), n_pad_dst, _planes(params, n_pad, "params"),
+                                   _planes(m, n_pad, "m"), _planes(v, n_pad, "v"), _buf(action, n, "u8", "action"),
+                                   _buf(offset, n, "i32", "offset"), _buf(n_out, 1, "i32", "n_out"),
+                                   _buf(randn, 6 * n, "f32", "randn"), float(log_shrink),
+                                   _planes(params_dst, n_pad_dst, "params_dst"), _planes(m_dst, n_pad_dst, "m_dst"),
+                                   _planes(v_dst, n_pad_dst, "v_dst"), _buf(dev_status, 1, "i32", "dev_status"),
+                                   _stream(stream)), "gs_densify_apply")
 
 
 def opacity_reset(n: int, params, m, v, logit_max: float, stream=None) -> None:
-    _check(load().gs_opacity_reset(dims(n, params.shape[1]), _p(params), _p(m), _p(v), float(logit_max),
-                                   _stream(stream)), "gs_opacity_reset")
+    n_pad = int(params.shape[1])
+    _check(load().gs_opacity_reset(dims(n, n_pad), _planes(params, n_pad, "params"), _planes(m, n_pad, "m"),
+                                   _planes(v, n_pad, "v"), float(logit_max), _stream(stream)), "gs_opacity_reset")
 
 
 def util_expf(x, y, stream=None) -> None:
-    _check(load().gs_util_expf(_p(x), _p(y), x.numel(), _stream(stream)), "gs_util_expf")
+    _check(load().gs_util_expf(_buf(x, 0, "f32", "x"), _buf(y, x.numel(), "f32", "y"), x.numel(), _stream(stream)),
+           "gs_util_expf")
 
 
 def version() -> str:

@@ -141,3 +141,160 @@ def test_binding_constants_match_the_header():
     assert int(defs["GS_N_GRAD2D"]) == gs.N_GRAD2D
     assert int(defs["GS_GRAD2D_STRIDE"]) == gs.GRAD2D_STRIDE
     assert int(defs["GS_SSIM_MAPS"]) == gs.SSIM_MAPS
+
+
+def test_binding_refuses_host_and_strided_tensors():
+    """Every buffer crosses the boundary as a device address of a dense array: the
+    binding refuses a host tensor (a kernel cannot dereference its address) and a
+    strided view (it would be misread) before the library is called."""
+    torch = pytest.importorskip("torch")
+    import gaussian_splatting_differentiable_project_gb300 as gs
+    cam = {"R": [1, 0, 0, 0, 1, 0, 0, 0, 1], "t": [0, 0, 3], "fx": 100, "fy": 100, "cx": 64, "cy": 64,
+           "width": 128, "height": 128, "campos": [0, 0, -3]}
+    params = torch.zeros((gs.N_PLANES, 256))
+    with pytest.raises(gs.GsError, match="CUDA tensor"):
+        gs.project(10, params, cam, gs.ProjBuffers(256, "cpu"), torch.zeros(1, dtype=torch.int32))
+    with pytest.raises(gs.GsError, match="CUDA tensor"):
+        gs.util_expf(torch.zeros(8), torch.zeros(8))
+    strided = torch.zeros((4, 8)).t()
+
+    class _OnDevice:
+        """A strided view that claims to live on the device (no GPU here)."""
+        is_cuda = True
+        shape = strided.shape
+
+        def is_contiguous(self):
+            return strided.is_contiguous()
+
+        def stride(self):
+            return strided.stride()
+
+    with pytest.raises(gs.GsError, match="contiguous"):
+        gs._p(_OnDevice())
+
+
+def test_binding_checks_buffer_types_and_sizes(monkeypatch):
+    """A buffer of the wrong type or too small for the call's sizes is refused before
+    the library is called (a short buffer would be overrun on the device).  Host
+    tensors stand in for device ones here: the address step (whose device check the
+    test above covers), the stream and the library are replaced by stubs, so nothing is
+    dereferenced and nothing is launched; a call whose buffers all pass reaches the
+    stub library and returns."""
+    torch = pytest.importorskip("torch")
+    import numpy as np
+    import gaussian_splatting_differentiable_project_gb300 as gs
+    W, H, n, n_pad = 64, 48, 100, 256
+    cam = {"R": [1, 0, 0, 0, 1, 0, 0, 0, 1], "t": [0, 0, 3], "fx": 60, "fy": 60, "cx": 32, "cy": 24,
+           "width": W, "height": H, "campos": [0, 0, -3]}
+    st = torch.zeros(1, dtype=torch.int32)
+    proj = gs.ProjBuffers(n_pad, "cpu")
+    bins = gs.BinBuffers(n, 4096, W, H, "cpu")
+
+    calls = []
+
+    class _StubLib:
+        def __getattr__(self, name):
+            return lambda *a: calls.append(name) or 0
+
+    monkeypatch.setattr(gs, "_p", lambda t: ctypes.c_void_p(16))
+    monkeypatch.setattr(gs, "_stream", lambda stream=None: None)
+    monkeypatch.setattr(gs, "load", lambda *a, **k: _StubLib())
+
+    def refused(match, fn, *a, **k):
+        before = len(calls)
+        with pytest.raises(gs.GsError, match=match):
+            fn(*a, **k)
+        assert len(calls) == before
+
+    params = torch.zeros((gs.N_PLANES, n_pad))
+    img, T, nc = torch.zeros((3, H, W)), torch.zeros((H, W)), torch.zeros((H, W), dtype=torch.int32)
+    g2 = torch.zeros((n_pad, gs.GRAD2D_STRIDE))
+    lr = np.full(gs.N_PLANES, 1e-3)
+    i32 = lambda k: torch.zeros(k, dtype=torch.int32)  # noqa: E731
+
+    # every buffer right: the stub library is reached
+    gs.project(n, params, cam, proj, st)
+    gs.render_fwd(cam, bins, (0, 0, 0), img, T, nc, st)
+    gs.render_bwd(n, n_pad, cam, bins, (0, 0, 0), img, img, T, nc, g2, torch.zeros(1), st, dLdC_extra=img)
+    gs.adam_step(n, params, params, params, params, lr, 0.9, 0.999, 1e-15, 1)
+    gs.permute_planes(n, i32(n), params, params)
+    assert calls == ["gs_project", "gs_render_fwd", "gs_render_bwd", "gs_adam_step", "gs_permute_planes"]
+    u8 = torch.zeros(n, dtype=torch.uint8)
+    i64 = torch.zeros(1, dtype=torch.int64)
+    cfg = gs.densify_thresholds(3.0)[0]
+    gs.bin_sort(n, n_pad, proj, cam, bins, st)
+    gs.bin_sort_noalloc(n, n_pad, proj, cam, bins, st)
+    gs.ssim_fwd(img, img, 0.2, torch.zeros((gs.SSIM_MAPS, H, W)), torch.zeros(1))
+    gs.ssim_bwd(img, img, torch.zeros((gs.SSIM_MAPS, H, W)), img)
+    gs.project_bwd(n, params, cam, proj, g2, params, st)
+    gs.project_bwd_accumulate(n, params, cam, proj, g2, params, st)
+    gs.project_bwd_adam(n, params, cam, proj, g2, params, params, lr, 0.9, 0.999, 1e-15, 1, st, grads_in=params)
+    gs.project_bwd_adam_tdev(n, params, cam, proj, g2, params, params, lr, 0.9, 0.999, 1e-15, i64, st)
+    gs.step_counter_add(i64, 1)
+    gs.densify_accumulate(n, n_pad, proj, g2, W, H, torch.zeros(n), i32(n))
+    gs.densify_plan(n, params, torch.zeros(n), i32(n), cfg, u8, i32(n), i32(1), torch.zeros(16, dtype=torch.uint8))
+    gs.densify_apply(n, params, params, params, u8, i32(n), i32(1), torch.zeros((n, 6)), 0.47, params, params, params,
+                     st)
+    gs.opacity_reset(n, params, params, params, -4.6)
+    gs.spatial_order(n, params, i32(n), torch.zeros(16, dtype=torch.uint8), st)
+    gs.util_expf(torch.zeros(8), torch.zeros(8))
+    assert len(calls) == 20
+
+    refused("params: expected fp32", gs.project, n, params.double(), cam, proj, st)
+    refused("params: needs", gs.project, n, params[:58].contiguous(), cam, proj, st)
+    refused("dev_status: expected a 4-byte integer", gs.project, n, params, cam, proj, st.long())
+    refused("projection buffers hold", gs.project, n, torch.zeros((gs.N_PLANES, 512)), cam, proj, st)
+    refused("tiles", gs.bin_sort, n, n_pad, proj, dict(cam, width=2 * W), bins, st)
+    refused("image: needs", gs.render_fwd, cam, bins, (0, 0, 0), torch.zeros((3, H, W - 1)), T, nc, st)
+    refused("n_contrib: expected", gs.render_fwd, cam, bins, (0, 0, 0), img, T, nc.float(), st)
+    refused("grad2d: needs", gs.render_bwd, n, n_pad, cam, bins, (0, 0, 0), img, img, T, nc,
+            torch.zeros((n_pad, gs.N_GRAD2D)), torch.zeros(1), st)
+    refused("dLdC_extra: needs", gs.render_bwd, n, n_pad, cam, bins, (0, 0, 0), img, img, T, nc, g2,
+            torch.zeros(1), st, dLdC_extra=torch.zeros((2, H, W)))
+    refused("maps: needs", gs.ssim_fwd, img, img, 0.2, torch.zeros((gs.SSIM_MAPS - 1, H, W)), torch.zeros(1))
+    refused("lr_plane", gs.adam_step, n, params, params, params, params, lr[:-1], 0.9, 0.999, 1e-15, 1)
+    refused("v: needs", gs.adam_step, n, params, params, params, params[:, :128].contiguous(), lr, 0.9, 0.999,
+            1e-15, 1)
+    refused("t_dev: expected int64", gs.project_bwd_adam_tdev, n, params, cam, proj, g2, params, params, lr, 0.9,
+            0.999, 1e-15, i32(1), st)
+    refused("perm: needs", gs.permute_planes, n, i32(n - 1), params, params)
+    refused("dst: expected a 4-byte", gs.permute_planes, n, i32(n), params, params.double())
+    refused("randn: needs", gs.densify_apply, n, params, params, params, torch.zeros(n, dtype=torch.uint8), i32(n),
+            i32(1), torch.zeros((n, 5)), 0.47, params, params, params, st)
+    refused("action: expected uint8", gs.densify_plan, n, params, torch.zeros(n), i32(n),
+            gs.densify_thresholds(3.0)[0], i32(n), i32(n), i32(1), torch.zeros(16, dtype=torch.uint8))
+
+
+@pytest.mark.parametrize("fused,dssim", [(True, 0.0), (False, 0.2)])
+def test_trainer_buffers_pass_the_binding_checks(monkeypatch, fused, dssim):
+    """Every call the trainer makes (steps, batch steps, density control, storage order)
+    hands the binding buffers of the right type and size: run against the stub library
+    of the test above, on host tensors."""
+    torch = pytest.importorskip("torch")
+    import numpy as np
+    import gaussian_splatting_differentiable_project_gb300 as gs
+    W, H, n, n_pad = 64, 48, 300, 512
+    cam = {"R": [1, 0, 0, 0, 1, 0, 0, 0, 1], "t": [0, 0, 3], "fx": 60, "fy": 60, "cx": 32, "cy": 24,
+           "width": W, "height": H, "campos": [0, 0, -3]}
+    tr = gs.Trainer(np.zeros((gs.N_PLANES, n_pad), np.float32), n, W, H, capacity=4096,
+                    lr_plane=np.full(gs.N_PLANES, 1e-3), device="cpu", fused=fused, dssim=dssim)
+    calls = []
+
+    class _StubLib:
+        def __getattr__(self, name):
+            return lambda *a: calls.append(name) or 0
+
+    monkeypatch.setattr(gs, "_p", lambda t: ctypes.c_void_p(16))
+    monkeypatch.setattr(gs, "_stream", lambda stream=None: None)
+    monkeypatch.setattr(gs, "load", lambda *a, **k: _StubLib())
+    target = torch.zeros((3, H, W))
+    tr.step(cam, target)
+    tr.step_batch([cam, cam, cam], [target] * 3)
+    tr.enable_density_control(3.0)
+    tr.step(cam, target)
+    tr.reorder_spatially()
+    tr.reset_opacity()
+    stats = tr.refine(randn=torch.zeros((n, 6)))
+    assert stats["n"] == 0 and tr.n_pad == 256
+    assert "gs_render_bwd" in calls and "gs_densify_apply" in calls and "gs_permute_planes" in calls
+    assert ("gs_project_bwd_adam" in calls) == fused and ("gs_ssim_fwd" in calls) == (dssim > 0)
