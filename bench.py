@@ -574,8 +574,13 @@ def run_gb300(args, cfg, ws, rank, local):
         moved = fused_bytes(n, n_pad, Vmean) if name == "project_bwd_adam" else sum(byt[r] for r in rows)
         fl = sum(flops.get(r, 0.0) for r in rows)
         bound = "alu" if fl / (peak_fp32 * 1e12) > moved / (peak_bw * 1e9) else "hbm"
+        t_own = max(moved / (peak_bw * 1e9), fl / (peak_fp32 * 1e12))
         per_stage[name] = {"ms": stage_ms[name], "bound": bound, "rows": rows,
-                           "gbs": moved / t_meas / 1e9, "tflops": fl / t_meas / 1e12, "frac": t_rows / t_meas}
+                           "gbs": moved / t_meas / 1e9, "tflops": fl / t_meas / 1e12, "frac": t_own / t_meas}
+        if len(rows) > 1:
+            # the fused stage against the rows it replaces (their gradient planes
+            # included), as the step roofline charges it
+            per_stage[name]["frac_rows"] = t_rows / t_meas
     roof = None  # batch and graph steps have no per-stage events
     if stage_ms is not None:
         dom = max(STAGES, key=lambda s: stage_ms[s])
