@@ -282,13 +282,17 @@ class OracleSample:
                      f"touch them (binning, compositing forward and backward; scaled x{self.TY / band_rows:g}), "
                      f"summed to one full step")
 
-    def seconds(self) -> float:
+    def seconds(self, count_used: bool = False) -> float:
+        """One sampled step, scaled to a full step.  With count_used the band's render
+        also counts each pixel's composited entries (kept as ``composited_per_pixel``)."""
         o = self.oracle
         t0 = time.perf_counter()
         o.project(self.sub, self.n_sub, self.cam, 32)
         t1 = time.perf_counter()
-        o.render(self.band_proj, self.W, self.rows * 16, target=self.band_target)
+        rd = o.render(self.band_proj, self.W, self.rows * 16, target=self.band_target, count_used=count_used)
         t2 = time.perf_counter()
+        if count_used:
+            self.composited_per_pixel = float(rd["n_used"].mean())
         o.project_bwd(self.sub, self.n_sub, self.cam, self.g2, 32)
         t3 = time.perf_counter()
         o.adam(self.sub[:, : self.n_sub].astype(np.float64), self.z + 1e-6, self.z, self.z, gi.lr_planes(),
@@ -663,9 +667,12 @@ def _peak_src(key):
 def cpu_baseline(cfg, P, cam, tr, W, H):
     rows = max(1, (-(-H // 16)) // 16)
     smp = OracleSample(P, cfg.n, cam, frac_g=8, band_rows=rows)
-    sec = smp.seconds()
+    sec = smp.seconds(count_used=True)
+    r0 = (smp.TY - rows) // 2
     return {"value": 1.0 / sec, "unit": "steps/s", "cores": smp.oracle.threads(), "kind": "oracle",
-            "sample": smp.desc, "seconds_per_step": sec}
+            "sample": smp.desc, "seconds_per_step": sec,
+            "composited_per_pixel": {"value": smp.composited_per_pixel,
+                                     "over": f"tile rows {r0}-{r0 + rows - 1} of view 0, model before training"}}
 
 
 def main():

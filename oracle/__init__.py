@@ -89,7 +89,7 @@ def _load():
             lib.or_tile_lists_f32.restype = i64
             for name in ("or_render_f32", "or_render_f64"):
                 getattr(lib, name).argtypes = [i64, P, P, ctypes.c_int, ctypes.c_int, P, P, P, P, P, P, P,
-                                               ctypes.c_double, P]
+                                               ctypes.c_double, P, P]
             lib.or_project_bwd.argtypes = [P, i64, i64, ctypes.POINTER(OrCamera), ctypes.c_int, P, P]
             lib.or_ssim.argtypes = [ctypes.c_int, ctypes.c_int, P, P, ctypes.c_double, P]
             lib.or_ssim.restype = ctypes.c_double
@@ -140,6 +140,8 @@ def project(params: np.ndarray, n: int, cam: dict, prec: int = 32) -> dict:
     fp64 (for the pins)."""
     params = _c(params, np.float32)
     n_pad = params.shape[1]
+    if params.shape[0] != N_PLANES or not 0 <= n <= n_pad:
+        raise ValueError(f"project: params {params.shape} cannot hold {n} Gaussians")
     dt = np.float32 if prec == 32 else np.float64
     proj16 = np.zeros((n, 16), dt)
     iproj6 = np.zeros((n, 6), np.int32)
@@ -172,12 +174,13 @@ def tile_lists(proj: dict, width: int, height: int, cap: int | None = None) -> d
 
 
 def render(proj: dict, width: int, height: int, bg=(0.0, 0.0, 0.0), target=None, prec: int = 32,
-           l1_weight: float = 1.0, dLdC_extra=None) -> dict:
+           l1_weight: float = 1.0, dLdC_extra=None, count_used: bool = False) -> dict:
     """Front-to-back compositing of every pixel over its tile's list; with a
     target, also the loss l1_weight * mean |C - C*| (over 3 P values) and the
     per-Gaussian 2D gradients (9 x n fp64: d mx, d my, d A, d B, d C, d o, d r, d g,
     d b) from the suffix-sum backward, with dLdC_extra (3 x H x W fp64) added to the
-    loss gradient if given."""
+    loss gradient if given.  With count_used, also each pixel's number of composited
+    entries (alpha >= 1/255, before the transmittance stop) as "n_used"."""
     n = proj["proj16"].shape[0]
     dt = np.float32 if prec == 32 else np.float64
     P = width * height
@@ -193,9 +196,13 @@ def render(proj: dict, width: int, height: int, bg=(0.0, 0.0, 0.0), target=None,
         loss = np.zeros(1, np.float64)
     f = _load().or_render_f32 if prec == 32 else _load().or_render_f64
     extra = None if dLdC_extra is None else _c(dLdC_extra, np.float64).reshape(3, height, width)
+    n_used = np.zeros((height, width), np.uint32) if count_used else None
     f(n, _ptr(_c(proj["proj16"], dt)), _ptr(proj["iproj6"]), width, height, _ptr(bg_a), _ptr(tgt),
-      _ptr(image), _ptr(T_final), _ptr(n_contrib), _ptr(grad2d), _ptr(loss), float(l1_weight), _ptr(extra))
+      _ptr(image), _ptr(T_final), _ptr(n_contrib), _ptr(grad2d), _ptr(loss), float(l1_weight), _ptr(extra),
+      _ptr(n_used))
     out = {"image": image, "T_final": T_final, "n_contrib": n_contrib}
+    if count_used:
+        out["n_used"] = n_used
     if target is not None:
         out["grad2d"] = grad2d
         out["loss"] = float(loss[0])
@@ -207,6 +214,8 @@ def project_bwd(params: np.ndarray, n: int, cam: dict, grad2d: np.ndarray, prec:
     """Chain rule from the nine 2D gradients to the 59 parameter gradients (fp64);
     decisions (culling, clamps) are taken in precision ``prec``."""
     params = _c(params, np.float32)
+    if params.shape[0] != N_PLANES or not 0 <= n <= params.shape[1]:
+        raise ValueError(f"project_bwd: params {params.shape} cannot hold {n} Gaussians")
     g2 = _c(grad2d, np.float64).reshape(9, n)
     grads = np.zeros((N_PLANES, n), np.float64)
     cam_c = camera(cam)

@@ -471,14 +471,14 @@ struct Contrib {
 
 // Front-to-back compositing of one pixel in S precision.  Returns colour, final
 // transmittance, the count of entries iterated up to the last composited one,
-// and (optionally) the entries composited.
+// and (optionally) the entries composited and how many there were.
 template <class S>
 void render_pixel_fwd(const std::vector<Splat<S>>& sp, const std::vector<int32_t>& L, S px, S py,
                       const S bg[3], S out[3], S* T_out, uint32_t* n_contrib,
-                      std::vector<Contrib>* contribs) {
+                      std::vector<Contrib>* contribs, uint32_t* n_used = nullptr) {
   S T = S(1);
   S Cc[3] = {0, 0, 0};
-  uint32_t last = 0;
+  uint32_t last = 0, used = 0;
   const S one_255 = S(1) / S(255);
   for (size_t j = 0; j < L.size(); ++j) {
     const Splat<S>& g = sp[L[j]];
@@ -498,11 +498,13 @@ void render_pixel_fwd(const std::vector<Splat<S>>& sp, const std::vector<int32_t
     for (int ch = 0; ch < 3; ++ch) Cc[ch] = fma_(g.rgb[ch], wgt, Cc[ch]);
     T = Tn;
     last = uint32_t(j + 1);
+    ++used;
     if (contribs) contribs->push_back({int32_t(j), clamped});
   }
   for (int ch = 0; ch < 3; ++ch) out[ch] = fma_(T, bg[ch], Cc[ch]);
   *T_out = T;
   *n_contrib = last;
+  if (n_used) *n_used = used;
 }
 
 // Per-pixel backward with explicit suffix sums, all values in fp64.  The
@@ -585,10 +587,12 @@ std::vector<Splat<S>> splats_from(int64_t n, const S* proj16, const int32_t* ipr
 // Forward (and optionally backward) over all tiles.
 // The loss is l1_weight * mean |C - C*|; its gradient dL/dC = l1_weight sign(C - C*)
 // / (3P) plus dLdC_extra (another loss term's gradient, e.g. D-SSIM), if given.
+// n_used, if given, receives each pixel's count of composited entries.
 template <class S>
 void render_all(int64_t n, const S* proj16, const int32_t* iproj6, int W, int H, const S* bg_in,
                 const S* target, S* image, S* T_final, uint32_t* n_contrib, double* grad2d,
-                double* loss, double l1_weight = 1.0, const double* dLdC_extra = nullptr) {
+                double* loss, double l1_weight = 1.0, const double* dLdC_extra = nullptr,
+                uint32_t* n_used = nullptr) {
   const int TX = (W + kTile - 1) / kTile, TY = (H + kTile - 1) / kTile;
   std::vector<Splat<S>> sp = splats_from<S>(n, proj16, iproj6);
   auto lists = build_tile_lists<S>(sp, TX, TY);
@@ -610,13 +614,14 @@ void render_all(int64_t n, const S* proj16, const int32_t* iproj6, int W, int H,
         for (int xx = tx * kTile; xx < std::min(W, tx * kTile + kTile); ++xx) {
           const S px = S(xx) + S(0.5), py = S(yy) + S(0.5);
           S out[3], T;
-          uint32_t nc;
+          uint32_t nc, nu;
           cs.clear();
-          render_pixel_fwd<S>(sp, L, px, py, bg, out, &T, &nc, backward ? &cs : nullptr);
+          render_pixel_fwd<S>(sp, L, px, py, bg, out, &T, &nc, backward ? &cs : nullptr, &nu);
           const int64_t pix = int64_t(yy) * W + xx;
           for (int ch = 0; ch < 3; ++ch) image[ch * P + pix] = out[ch];
           T_final[pix] = T;
           n_contrib[pix] = nc;
+          if (n_used) n_used[pix] = nu;
           if (backward) {
             double dLdC[3];
             for (int ch = 0; ch < 3; ++ch) {
@@ -993,19 +998,20 @@ int64_t or_tile_lists_f32(int64_t n, const float* proj16, const int32_t* iproj6,
 }
 
 // Render forward (and backward if target and grad2d are non-null).
-// grad2d is 9 x n: (d mx, d my, d A, d B, d C, d o, d r, d g, d b).
+// grad2d is 9 x n: (d mx, d my, d A, d B, d C, d o, d r, d g, d b).  n_used (null, or
+// H x W) receives each pixel's count of composited entries.
 void or_render_f32(int64_t n, const float* proj16, const int32_t* iproj6, int W, int H, const float* bg,
                    const float* target, float* image, float* T_final, uint32_t* n_contrib,
-                   double* grad2d, double* loss, double l1_weight, const double* dLdC_extra) {
+                   double* grad2d, double* loss, double l1_weight, const double* dLdC_extra, uint32_t* n_used) {
   render_all<float>(n, proj16, iproj6, W, H, bg, target, image, T_final, n_contrib, grad2d, loss, l1_weight,
-                    dLdC_extra);
+                    dLdC_extra, n_used);
 }
 void or_render_f64(int64_t n, const double* proj16, const int32_t* iproj6, int W, int H,
                    const double* bg, const double* target, double* image, double* T_final,
                    uint32_t* n_contrib, double* grad2d, double* loss, double l1_weight,
-                   const double* dLdC_extra) {
+                   const double* dLdC_extra, uint32_t* n_used) {
   render_all<double>(n, proj16, iproj6, W, H, bg, target, image, T_final, n_contrib, grad2d, loss, l1_weight,
-                     dLdC_extra);
+                     dLdC_extra, n_used);
 }
 
 // Projection backward: grad2d (9 x n, fp64) -> grads (59 x n, fp64).  prec selects

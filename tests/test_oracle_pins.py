@@ -300,13 +300,14 @@ def test_stacked_gaussians_transmittance_closed_form(prec):
     P, n, cam = _on_pixel_scene(k, o, rgb)
     pr = oracle.project(P, n, cam, prec)
     assert np.allclose(pr["mean2d"], 16.5, atol=1e-4)
-    rd = oracle.render(pr, 32, 32, prec=prec)
+    rd = oracle.render(pr, 32, 32, prec=prec, count_used=True)
     o = 1.0 / (1.0 + math.exp(-float(P[10, 0])))   # the opacity the fp32 logit holds
     rgb = np.array([0.5 + float(P[11 + c, 0]) * 0.5 / math.sqrt(math.pi) for c in range(3)])
     j_stop = next(j for j in range(1, k + 1) if (1 - o) ** j < 1e-4)
     comp = j_stop - 1
     tol = 1e-12 if prec == 64 else 2e-6
     assert rd["n_contrib"][16, 16] == comp
+    assert rd["n_used"][16, 16] == comp             # every entry before the stop composites
     np.testing.assert_allclose(rd["T_final"][16, 16], (1 - o) ** comp, rtol=tol * 10)
     np.testing.assert_allclose(rd["image"][:, 16, 16], rgb * (1 - (1 - o) ** comp), rtol=tol * 10)
 
@@ -320,7 +321,7 @@ def test_single_gaussian_alpha_falloff_closed_form():
     P, n = _scene(np.zeros((1, 3)), math.log(sig), logits=[math.log(o / (1 - o))],
                   sh=np.tile(np.array([[[(1.0 - 0.5) * 2 * math.sqrt(math.pi)] * 3] + [[0.0] * 3] * 15]), (1, 1, 1)))
     pr = oracle.project(P, n, cam, 64)
-    rd = oracle.render(pr, W, H, prec=64)
+    rd = oracle.render(pr, W, H, prec=64, count_used=True)
     sig = math.exp(float(P[3, 0]))                  # values the fp32 planes hold
     o = 1.0 / (1.0 + math.exp(-float(P[10, 0])))
     rgb0 = 0.5 + float(P[11, 0]) * 0.5 / math.sqrt(math.pi)
@@ -335,6 +336,10 @@ def test_single_gaussian_alpha_falloff_closed_form():
     a[~inside] = 0.0
     np.testing.assert_allclose(rd["image"][0], rgb0 * a, atol=1e-12)
     np.testing.assert_allclose(rd["T_final"], 1 - a, atol=1e-12)
+    # one composited entry exactly where alpha reaches 1/255 (none on the level itself)
+    edge = np.abs(o * np.exp(-((xs - W / 2) ** 2 + (ys - H / 2) ** 2) / (2 * s2)) * 255 - 1) < 1e-9
+    assert not edge.any()
+    np.testing.assert_array_equal(rd["n_used"], (a > 0).astype(np.uint32))
 
 
 def test_alpha_sum_and_colour_bounds():
@@ -344,9 +349,15 @@ def test_alpha_sum_and_colour_bounds():
     P = gi.scene_for(cfg)
     cam = gi.cameras_for(cfg)[0]
     pr = oracle.project(P, cfg.n, cam, 32)
-    rd = oracle.render(pr, 128, 128)
+    rd = oracle.render(pr, 128, 128, count_used=True)
     T = rd["T_final"].astype(np.float64)
     assert T.max() <= 1.0 and T.min() >= 1e-4 * (1 - 1e-6)
+    # composited entries: at most those iterated, the last iterated one among them, and
+    # each takes at least 1/255 of the remaining transmittance
+    nu, nc = rd["n_used"].astype(np.int64), rd["n_contrib"].astype(np.int64)
+    assert np.all(nu <= nc) and np.array_equal(nu == 0, nc == 0)
+    assert np.all(T <= (1 - 1 / 255) ** nu * (1 + 1e-5))
+    assert nu.max() > 1
     cmax = pr["rgb"][pr["visible"]].max()
     assert np.all(rd["image"] <= cmax * (1 - T)[None] * (1 + 1e-5) + 1e-6)
     assert np.all(rd["image"] >= 0)
