@@ -183,7 +183,6 @@ def render(proj: dict, width: int, height: int, bg=(0.0, 0.0, 0.0), target=None,
     entries (alpha >= 1/255, before the transmittance stop) as "n_used"."""
     n = proj["proj16"].shape[0]
     dt = np.float32 if prec == 32 else np.float64
-    P = width * height
     image = np.zeros((3, height, width), dt)
     T_final = np.zeros((height, width), dt)
     n_contrib = np.zeros((height, width), np.uint32)
@@ -206,7 +205,6 @@ def render(proj: dict, width: int, height: int, bg=(0.0, 0.0, 0.0), target=None,
     if target is not None:
         out["grad2d"] = grad2d
         out["loss"] = float(loss[0])
-    del P
     return out
 
 
