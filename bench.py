@@ -228,10 +228,25 @@ STAGE_ROWS = {"project": ["project"], "bin_sort": ["bin_sort"], "render_fwd": ["
               "project_bwd_adam": ["project_bwd", "adam"], "ssim": ["ssim"]}
 
 
-# FP32 operations per iterated (pixel, entry) pair, counting an FMA as 2 and the
-# exponential as the 11 operations of its Cody-Waite + degree-7 evaluation.
-FLOP_FWD_PAIR = 41
-FLOP_BWD_PAIR = 75
+# Algorithmic operations per iterated (pixel, entry) pair of the compositing rule as
+# the method states it (per-pair partials of the mean and the conic), FMA = 2, the
+# exponential and the reciprocal 1 each, FP32 compares, min and selects 1 each:
+# forward 26 + exp = 27: offset 2; power -1/2 (A dx^2 + C dy^2) - B dx dy 9 (dx^2, dy^2,
+#   A dx^2 + C dy^2, -1/2, dx dy, the last FMA); the skip test 1; power log2(e) 1;
+#   o e^power 1; the 0.99 clamp 1; the 1/255 test 1; T (1 - alpha) 2; the stop test 1;
+#   alpha T 1; three colour FMAs 6.
+# backward 64 + exp + reciprocal = 66: the forward's evaluation up to the 1/255 test 16;
+#   T recovered as T / (1 - alpha) 2; alpha T 1; three colour partials 3; dL/dalpha
+#   (three colour differences from the carried colour, their dot product with dL/dC,
+#   times T) 9; the carried colour's update 3 FMAs 6; dL/dpower and dL/do with their two
+#   clamp selects 4; the mean partials (A dx + B dy, B dx + C dy, times dL/dpower) 8; the
+#   conic partials (dx^2, dx dy, dy^2 reused, their factors, times dL/dpower) 6; the
+#   nine partials added to the Gaussian's sums 9.
+# The achieved rate is these figures over the measured time.  This implementation's
+# exact exponential (two multiplies, a rounding and nine FMAs: 21 by this count) costs
+# more than the 1 counted here; its moment form of the partials costs less.
+FLOP_FWD_PAIR = 27
+FLOP_BWD_PAIR = 66
 # FP32 operations per pixel of the D-SSIM forward and backward over 3 channels.  Per
 # channel, forward: horizontal pass 158 (42 staged rows per 32 output rows; per 4
 # outputs 42 products and 5 moments x 44 FMAs), vertical 110, SSIM partials 35;
