@@ -208,8 +208,9 @@ gs_status gs_render_fwd(const gs_camera* cam, const gs_bins* bins, uint32_t capa
  * by division by (1 - alpha), and produces per entry the partials of the loss with
  * respect to opacity and colour (r, g, b) and, for mean2d and the conic, the five
  * moments of q = dL/dpower over the pixel offset (dx, dy) = (px - mx, py - my);
- * partials of a warp are summed by shuffles and added to grad2d with global
- * atomics (summation order is not fixed).  The conic is the Gaussian's own, so its
+ * a warp's partials for one entry are added to grad2d with global atomics, lane by
+ * lane when few lanes contribute and after a shuffle reduction otherwise (summation
+ * order is not fixed).  The conic is the Gaussian's own, so its
  * products are applied once to the sums, by the consumers: with power =
  * -(A dx^2 + C dy^2)/2 - B dx dy and S1..S5 the sums of q dx, q dy, q dx^2, q dx dy,
  * q dy^2,  dL/dmx = A S1 + B S2,  dL/dmy = B S1 + C S2,  dL/dA = -S3/2,
