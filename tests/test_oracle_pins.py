@@ -420,12 +420,32 @@ def _fd_scene(n=6, seed=11, W=32, H=32):
     return P, n, cam
 
 
-def test_render_backward_matches_finite_differences():
+def _clamped_pixels(pr, i, W=32, H=32):
+    """Pixels where Gaussian i alone reaches the 0.99 opacity clamp (o e^power >= 0.99)."""
+    ys, xs = np.mgrid[0:H, 0:W] + 0.5
+    mx, my = pr["mean2d"][i]
+    A, B, C = pr["conic"][i]
+    dx, dy = xs - mx, ys - my
+    power = -0.5 * (A * dx * dx + C * dy * dy) - B * dx * dy
+    return int((pr["opacity"][i] * np.exp(power) >= 0.99).sum())
+
+
+@pytest.mark.parametrize("hot", [None, 2])
+def test_render_backward_matches_finite_differences(hot):
     """The suffix-sum backward equals central differences (fp64) of the L1 loss with
     respect to each projected quantity (mean2d, conic, opacity, colour), with
-    tile rects held fixed and every residual sign far from zero."""
+    tile rects held fixed and every residual sign far from zero.  With ``hot``, that
+    Gaussian is nearly opaque (logit 12) and about 12 px wide: its alpha sits at the
+    0.99 clamp over a disc of pixels, where alpha no longer depends on its opacity or
+    its power."""
     P, n, cam = _fd_scene()
+    if hot is not None:
+        P = P.copy()
+        P[10, hot] = 12.0
+        P[3:6, hot] += 3.0
     pr = oracle.project(P, n, cam, 64)
+    if hot is not None:
+        assert _clamped_pixels(pr, hot) >= 20
     base = oracle.render(pr, 32, 32, prec=64)
     tgt = gi.offset_target(base["image"], seed=3)
     rd = oracle.render(pr, 32, 32, target=tgt, prec=64)
