@@ -470,14 +470,49 @@ def test_render_backward_matches_finite_differences(hot):
             assert abs(fd - g2[q, i]) <= 1e-6 * abs(fd) + 1e-10, (i, q, fd, g2[q, i])
 
 
-def test_project_backward_matches_finite_differences():
-    """The projection chain rule equals central differences (fp64) of a random
-    linear functional of the nine projected outputs with respect to all 59
-    parameters of each Gaussian (SH, quaternion normalisation, scales, mean)."""
-    P, n, cam = _fd_scene(n=4, seed=2)
-    w = np.random.default_rng(4).normal(size=(9, n))
+def _beyond_clamp_scene(W=64, H=64, sig=0.9):
+    """Two isotropic Gaussians at depth 3 whose camera-space abscissa x / z (first) or
+    ordinate y / z (second) is twice 1.3 x the half field of view, so the EWA
+    Jacobian takes the clamped value; wide enough that their footprints still reach
+    the image."""
+    cam = _cam(W, H)
+    z = 3.0
+    limx = 1.3 * (0.5 * W) / float(cam["fx"])
+    limy = 1.3 * (0.5 * H) / float(cam["fy"])
+    c = np.array([[2 * limx * z, 0.0, z], [0.0, -2 * limy * z, z]])
+    R = cam["R"].astype(np.float64)
+    t = cam["t"].astype(np.float64)
+    means = (c - t) @ R                              # world = R^T (c - t)
+    P, n = _scene(means, math.log(sig), logits=[1.0, -0.5])
+    return P, n, cam, limx, limy
+
+
+def test_projection_jacobian_clamp_closed_form():
+    """Beyond 1.3 x the half field of view the EWA Jacobian uses the clamped
+    abscissa (cited method): for an isotropic Gaussian of scale s at (x, 0, z) with
+    x / z past the limit L, J J^T = (f / z)^2 [[1 + L^2, 0], [0, 1]], so
+    Sigma_2 = s^2 (f / z)^2 diag(1 + L^2, 1) + 0.3 I; likewise along y.  The mean
+    itself projects unclamped."""
+    P, n, cam, limx, limy = _beyond_clamp_scene()
     pr = oracle.project(P, n, cam, 64)
     assert pr["visible"].all()
+    s = np.exp(P[3, :n].astype(np.float64))
+    fx, fy = float(cam["fx"]), float(cam["fy"])
+    z = (P[:3, :n].T.astype(np.float64) @ cam["R"].astype(np.float64).T + cam["t"].astype(np.float64))[:, 2]
+    a = (s * fx / z) ** 2
+    b = (s * fy / z) ** 2
+    np.testing.assert_allclose(pr["cov2d"][0], [a[0] * (1 + limx ** 2) + 0.3, 0.0, b[0] + 0.3], rtol=1e-9, atol=1e-9)
+    np.testing.assert_allclose(pr["cov2d"][1], [a[1] + 0.3, 0.0, b[1] * (1 + limy ** 2) + 0.3], rtol=1e-9, atol=1e-9)
+    # the means as the fp32 planes hold them, in camera space
+    c = P[:3, :n].T.astype(np.float64) @ cam["R"].astype(np.float64).T + cam["t"].astype(np.float64)
+    assert c[0, 0] / c[0, 2] > 1.9 * limx and c[1, 1] / c[1, 2] < -1.9 * limy
+    np.testing.assert_allclose(pr["mean2d"][:, 0], fx * c[:, 0] / c[:, 2] + float(cam["cx"]), rtol=1e-12)
+    np.testing.assert_allclose(pr["mean2d"][:, 1], fy * c[:, 1] / c[:, 2] + float(cam["cy"]), rtol=1e-12, atol=1e-12)
+
+
+def _project_bwd_fd(P, n, cam, w):
+    """Central differences (fp64) of sum(w * the nine projected outputs) against the
+    analytic chain rule, for all 59 parameters of each Gaussian."""
     an = oracle.project_bwd(P, n, cam, w, prec=64)
 
     def func(Pm):
@@ -494,6 +529,23 @@ def test_project_backward_matches_finite_differences():
             he = (float(Pp[pl, i]) - float(Pm_[pl, i])) / 2
             fd = (func(Pp) - func(Pm_)) / (2 * he)
             assert abs(fd - an[pl, i]) <= 2e-5 * abs(fd) + 1e-7 * np.abs(an[:, i]).max() + 1e-9, (i, pl, fd, an[pl, i])
+
+
+def test_project_backward_matches_finite_differences():
+    """The projection chain rule equals central differences (fp64) of a random
+    linear functional of the nine projected outputs with respect to all 59
+    parameters of each Gaussian (SH, quaternion normalisation, scales, mean)."""
+    P, n, cam = _fd_scene(n=4, seed=2)
+    assert oracle.project(P, n, cam, 64)["visible"].all()
+    _project_bwd_fd(P, n, cam, np.random.default_rng(4).normal(size=(9, n)))
+
+
+def test_project_backward_through_the_jacobian_clamp():
+    """Past the clamp the Jacobian no longer follows the mean's abscissa, so that
+    path passes no gradient; central differences of the clamped forward agree."""
+    P, n, cam, _, _ = _beyond_clamp_scene()
+    assert oracle.project(P, n, cam, 64)["visible"].all()
+    _project_bwd_fd(P, n, cam, np.random.default_rng(6).normal(size=(9, n)))
 
 
 def test_whole_step_gradient_matches_finite_differences():
