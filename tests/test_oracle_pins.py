@@ -274,6 +274,57 @@ def test_tile_lists_brute_force():
     assert tl["K"] == int(pr["count"].astype(np.int64).sum())
 
 
+def test_colour_along_the_view_axis_closed_form():
+    """A Gaussian at the origin seen from (0, 0, 3): the view direction runs from the
+    camera to the mean, d = (0, 0, -1).  On the axis only the m = 0 harmonics are
+    nonzero, Y_l0 = sqrt((2l + 1) / 4 pi) P_l(d_z) with P_l(-1) = (-1)^l, at indices
+    l^2 + l = 0, 2, 6, 12; so rgb = max(0, 0.5 + sum of those Y_k sh_k) per channel
+    (the degree-1 terms sqrt(3 / 4 pi) (-y, z, -x) give -k1 at index 2 and 0 at 1 and
+    3), and a channel below zero is clamped and passes no gradient; the others take
+    d rgb / d sh_k = Y_k."""
+    cam = _cam(32, 32)
+    k1 = math.sqrt(3 / (4 * math.pi))
+    y0 = 0.5 / math.sqrt(math.pi)
+    sh = np.zeros((1, 16, 3))
+    sh[0, 0] = [0.2, -0.4, 0.1]
+    sh[0, 2] = [0.3, -0.3, 2.0]                     # blue: 0.5 + 0.1 y0 - 2 k1 < 0
+    sh[0, 1] = sh[0, 3] = [5.0, -5.0, 5.0]          # Y_1 = Y_3 = 0 along d
+    sh[0, 6] = [0.1, 0.2, 0.1]
+    sh[0, 12] = [-0.05, 0.1, -0.05]
+    P, n = _scene(np.zeros((1, 3)), math.log(0.05), sh=sh)
+    pr = oracle.project(P, n, cam, 64)
+    Y = np.zeros(16)
+    for l in range(4):
+        Y[l * l + l] = math.sqrt((2 * l + 1) / (4 * math.pi)) * (-1) ** l
+    assert Y[0] == pytest.approx(y0) and Y[2] == pytest.approx(-k1)
+    coef = P[11:11 + 48, 0].astype(np.float64).reshape(16, 3)   # as the fp32 planes hold them
+    want = np.maximum(0.0, 0.5 + Y @ coef)
+    assert want[2] == 0.0 and want[:2].min() > 0
+    np.testing.assert_allclose(pr["rgb"][0], want, rtol=1e-12, atol=1e-15)
+    for ch in range(3):
+        w = np.zeros((9, 1))
+        w[6 + ch] = 1.0                             # d rgb[ch] / d params
+        g = oracle.project_bwd(P, n, cam, w, prec=64)[:, 0]
+        got = g[11 + ch::3][:16]
+        if ch == 2:
+            assert not got.any()
+        else:
+            np.testing.assert_allclose(got, Y, atol=1e-12)
+
+
+def test_loss_is_the_mean_absolute_residual():
+    """The loss is l1_weight x the mean of |C - C*| over the 3 H W values (the
+    configs' L1 objective), whatever the weight."""
+    P, n, cam = _fd_scene()
+    pr = oracle.project(P, n, cam, 64)
+    img = oracle.render(pr, 32, 32, prec=64)["image"]
+    tgt = gi.offset_target(img, seed=3)
+    for wgt in (1.0, 0.3):
+        rd = oracle.render(pr, 32, 32, target=tgt, prec=64, l1_weight=wgt)
+        want = wgt * np.abs(img - tgt.astype(np.float64)).sum() / (3 * 32 * 32)
+        assert rd["loss"] == pytest.approx(want, rel=1e-12)
+
+
 # ----------------------------------------------------------------------------- compositing
 
 def _on_pixel_scene(k, opacity, rgb, W=32, H=32, sigma=0.05):
