@@ -200,6 +200,10 @@ def test_projection_ewa_matches_finite_difference_of_perspective():
         got = np.array([[pr["cov2d"][i, 0] - 0.3, pr["cov2d"][i, 1]], [pr["cov2d"][i, 1], pr["cov2d"][i, 2] - 0.3]])
         np.testing.assert_allclose(got, cov, rtol=1e-6, atol=1e-8 * np.abs(cov).max())
         np.testing.assert_allclose(pr["mean2d"][i], pinhole(means[i]), rtol=1e-12)
+        # the conic (A, B, C) is the inverse of the full 2D covariance (low-pass included)
+        S2 = got + 0.3 * np.eye(2)
+        A, B, C = pr["conic"][i]
+        np.testing.assert_allclose(np.array([[A, B], [B, C]]) @ S2, np.eye(2), atol=1e-9)
 
 
 def test_projection_invariant_under_joint_rotation():
@@ -481,14 +485,15 @@ def _clamped_pixels(pr, i, W=32, H=32):
     return int((pr["opacity"][i] * np.exp(power) >= 0.99).sum())
 
 
-@pytest.mark.parametrize("hot", [None, 2])
-def test_render_backward_matches_finite_differences(hot):
+@pytest.mark.parametrize("hot,bg", [(None, (0.0, 0.0, 0.0)), (2, (0.0, 0.0, 0.0)), (None, (0.3, 0.6, 0.1))])
+def test_render_backward_matches_finite_differences(hot, bg):
     """The suffix-sum backward equals central differences (fp64) of the L1 loss with
     respect to each projected quantity (mean2d, conic, opacity, colour), with
     tile rects held fixed and every residual sign far from zero.  With ``hot``, that
     Gaussian is nearly opaque (logit 12) and about 12 px wide: its alpha sits at the
     0.99 clamp over a disc of pixels, where alpha no longer depends on its opacity or
-    its power."""
+    its power.  With a coloured background, what shows through (T_final bg) depends
+    on every entry's alpha too."""
     P, n, cam = _fd_scene()
     if hot is not None:
         P = P.copy()
@@ -497,9 +502,9 @@ def test_render_backward_matches_finite_differences(hot):
     pr = oracle.project(P, n, cam, 64)
     if hot is not None:
         assert _clamped_pixels(pr, hot) >= 20
-    base = oracle.render(pr, 32, 32, prec=64)
+    base = oracle.render(pr, 32, 32, bg=bg, prec=64)
     tgt = gi.offset_target(base["image"], seed=3)
-    rd = oracle.render(pr, 32, 32, target=tgt, prec=64)
+    rd = oracle.render(pr, 32, 32, bg=bg, target=tgt, prec=64)
     g2 = rd["grad2d"]
     assert np.abs(g2).max() > 0
     cols = [0, 1, 2, 3, 4, 5, 6, 7, 8]
@@ -514,7 +519,7 @@ def test_render_backward_matches_finite_differences(hot):
                 p2 = dict(pr)
                 p2["proj16"] = pr["proj16"].copy()
                 p2["proj16"][i, col] = x0 + sgn * h
-                r = oracle.render(p2, 32, 32, target=tgt, prec=64)
+                r = oracle.render(p2, 32, 32, bg=bg, target=tgt, prec=64)
                 np.testing.assert_array_equal(r["n_contrib"], rd["n_contrib"])
                 vals.append(r["loss"])
             fd = (vals[0] - vals[1]) / (2 * h)
