@@ -397,6 +397,37 @@ def test_single_gaussian_alpha_falloff_closed_form():
     np.testing.assert_array_equal(rd["n_used"], (a > 0).astype(np.uint32))
 
 
+def test_anisotropic_footprint_is_the_gaussian_of_the_2d_covariance():
+    """One rotated, elongated Gaussian: each pixel's alpha is o exp(-d^T Sigma_2^-1 d / 2)
+    with Sigma_2 the projected 2D covariance (fixed by the EWA pin) inverted here by
+    numpy, capped at 0.99, zero below 1/255 and outside the tile rect; the image is
+    rgb alpha on black."""
+    W = H = 48
+    cam = _cam(W, H)
+    Rot = pytest.importorskip("scipy.spatial.transform").Rotation
+    q = Rot.from_euler("xyz", [0.4, -0.3, 0.7]).as_quat()          # (x, y, z, w)
+    sh = np.zeros((1, 16, 3))
+    sh[0, 0] = [0.8, 0.2, -0.3]
+    P, n = _scene(np.zeros((1, 3)), np.array([[math.log(0.15), math.log(0.04), math.log(0.08)]]),
+                  quats=np.array([[q[3], q[0], q[1], q[2]]]), logits=[1.5], sh=sh)
+    pr = oracle.project(P, n, cam, 64)
+    rd = oracle.render(pr, W, H, prec=64)
+    a, b, c = pr["cov2d"][0]
+    assert abs(b) > 0.2 * math.sqrt(a * c)                          # clearly anisotropic, tilted
+    Sinv = np.linalg.inv(np.array([[a, b], [b, c]]))
+    ys, xs = np.mgrid[0:H, 0:W] + 0.5
+    d = np.stack([xs - pr["mean2d"][0, 0], ys - pr["mean2d"][0, 1]], -1)
+    alpha = float(pr["opacity"][0]) * np.exp(-0.5 * np.einsum("...i,ij,...j->...", d, Sinv, d))
+    alpha = np.minimum(alpha, 0.99)
+    alpha[alpha < 1 / 255] = 0.0
+    tx0, ty0, tx1, ty1 = pr["rect"][0]
+    tile_x, tile_y = np.floor((xs - 0.5) / 16), np.floor((ys - 0.5) / 16)
+    alpha[~((tile_x >= tx0) & (tile_x <= tx1) & (tile_y >= ty0) & (tile_y <= ty1))] = 0.0
+    assert (alpha > 0).sum() > 50
+    np.testing.assert_allclose(rd["image"], pr["rgb"][0][:, None, None] * alpha[None], atol=1e-12)
+    np.testing.assert_allclose(rd["T_final"], 1.0 - alpha, atol=1e-12)
+
+
 def test_alpha_sum_and_colour_bounds():
     """Accumulated alpha 1 - T lies in [0, 1 - 1e-4]; each channel is at most
     max colour x (1 - T) with a black background."""
