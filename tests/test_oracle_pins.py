@@ -793,6 +793,30 @@ def test_whole_step_gradient_with_dssim_matches_finite_differences():
             assert abs(fd - an[pl, i]) <= 2e-4 * abs(fd) + 2e-7 * np.abs(an).max(), (i, pl, fd, an[pl, i])
 
 
+def test_step_composes_the_objective():
+    """The whole step with lambda in {0, 0.2}: its loss is (1 - lambda) mean |C - C*| +
+    lambda (1 - SSIM(C, C*)) of its own render, and its parameter gradients are those
+    of the composition the test above checks against finite differences (render
+    backward with weight 1 - lambda plus the SSIM image gradient, then the projection
+    backward), up to the fp32 decisions and image the step uses."""
+    P, n, cam = _fd_scene(n=3, seed=9)
+    pr = oracle.project(P, n, cam, 64)
+    img = oracle.render(pr, 32, 32, prec=64)["image"]
+    tgt = gi.offset_target(img, seed=6)
+    z = np.zeros((59, P.shape[1]))
+    for lam in (0.0, 0.2):
+        r = oracle.step(P, n, cam, tgt, z, z, 1, gi.lr_planes(), dssim=lam)
+        c = r["render"]["image"].astype(np.float64)
+        want = (1 - lam) * np.abs(c - tgt).mean() + lam * (1 - oracle.ssim(c, tgt)[0])
+        assert r["render"]["loss"] == pytest.approx(want, rel=1e-9)
+        extra = oracle.ssim(img, tgt, lam)[1] if lam > 0 else None
+        rd = oracle.render(pr, 32, 32, target=tgt, prec=64, l1_weight=1 - lam, dLdC_extra=extra)
+        an = oracle.project_bwd(P, n, cam, rd["grad2d"], prec=64)
+        g = r["grads"][:, :n]
+        scale = np.abs(an).max(axis=1, keepdims=True)
+        assert np.all(np.abs(g - an) <= 1e-3 * np.abs(an) + 1e-4 * scale)
+
+
 # ----------------------------------------------------------------------------- batched step
 
 def test_batch_hyperparameters_follow_the_pages():
@@ -827,19 +851,20 @@ def test_batch_of_one_is_the_single_view_step():
         np.testing.assert_allclose(b[k], a[k], rtol=1e-15, atol=0)
 
 
-def test_batch_gradient_is_the_mean_of_view_gradients():
+@pytest.mark.parametrize("lam", [0.0, 0.2])
+def test_batch_gradient_is_the_mean_of_view_gradients(lam):
     """The batch loss is the mean of the view losses, so its gradient is the mean of
-    the single-view gradients (a dropped 1/BS or a missing view fails)."""
+    the single-view gradients (a dropped 1/BS or a missing view fails), with or
+    without the D-SSIM term."""
     P, n, cams, targets = _two_views()
     z = np.zeros((59, P.shape[1]))
-    g1 = oracle.step(P, n, cams[0], targets[0], z, z, 1, gi.lr_planes())["grads"]
-    g2 = oracle.step(P, n, cams[1], targets[1], z, z, 1, gi.lr_planes())["grads"]
-    r = oracle.step_batch(P, n, cams, targets, z, z, 1, gi.lr_planes())
+    s1 = oracle.step(P, n, cams[0], targets[0], z, z, 1, gi.lr_planes(), dssim=lam)
+    s2 = oracle.step(P, n, cams[1], targets[1], z, z, 1, gi.lr_planes(), dssim=lam)
+    g1, g2 = s1["grads"], s2["grads"]
+    r = oracle.step_batch(P, n, cams, targets, z, z, 1, gi.lr_planes(), dssim=lam)
     assert np.abs(g1 - g2).max() > 1e-3 * np.abs(g1).max()
-    np.testing.assert_allclose(r["grads"], 0.5 * (g1 + g2), rtol=1e-12, atol=1e-18)
-    l1 = oracle.step(P, n, cams[0], targets[0], z, z, 1, gi.lr_planes())["render"]["loss"]
-    l2 = oracle.step(P, n, cams[1], targets[1], z, z, 1, gi.lr_planes())["render"]["loss"]
-    assert abs(r["loss"] - 0.5 * (l1 + l2)) < 1e-12
+    np.testing.assert_allclose(r["grads"], 0.5 * (g1 + g2), rtol=1e-9, atol=1e-18)
+    assert abs(r["loss"] - 0.5 * (s1["render"]["loss"] + s2["render"]["loss"])) < 1e-12
 
 
 def test_batch_first_step_moves_by_sqrt_batch_lr():
