@@ -253,11 +253,17 @@ def test_projection_fp32_tracks_fp64():
 def test_tile_lists_brute_force():
     """Every tile's list equals, as a sequence, the Gaussians whose closed box
     [m - r, m + r]^2 overlaps the tile's half-open pixel square, sorted by
-    (fp32 depth, index): interval overlap, not the floor arithmetic of the rect."""
+    (fp32 depth, index): interval overlap, not the floor arithmetic of the rect.
+    Copies of a few Gaussians, placed before and after their originals, tie in depth
+    exactly: the lower index comes first."""
     cfg = gi.CONFIGS["tiny"]
-    P = gi.scene_for(cfg, n=600)
+    P = gi.scene_for(cfg, n=600).copy()
+    for src, dst in ((10, 400), (500, 20), (123, 124), (300, 7)):
+        P[:, dst] = P[:, src]
     cam = gi.camera((0.0, 0.0, 3.0), 72, 56)   # ragged tiles on both axes
     pr = oracle.project(P, 600, cam, 32)
+    vis0 = pr["count"] > 0
+    assert len(np.unique(pr["depth"][vis0])) <= vis0.sum() - 3
     tl = oracle.tile_lists(pr, 72, 56)
     m, r, z = pr["mean2d"].astype(np.float64), pr["radius"].astype(np.float64), pr["depth"]
     vis = pr["count"] > 0
