@@ -298,3 +298,36 @@ def test_trainer_buffers_pass_the_binding_checks(monkeypatch, fused, dssim):
     assert stats["n"] == 0 and tr.n_pad == 256
     assert "gs_render_bwd" in calls and "gs_densify_apply" in calls and "gs_permute_planes" in calls
     assert ("gs_project_bwd_adam" in calls) == fused and ("gs_ssim_fwd" in calls) == (dssim > 0)
+
+
+def test_size_and_camera_limits_are_refused_on_the_host():
+    """Sizes past the layout's limits and non-finite cameras are refused before
+    anything is enqueued: n outside [0, n_pad], n_pad above 2^31, images wider than
+    65,535 tiles, non-finite rotation or near plane; null or misaligned raster
+    buffers; a density destination whose stride is not a multiple of 256."""
+    import gaussian_splatting_differentiable_project_gb300 as gs
+    lib = gs.load()
+    p = ctypes.c_void_p(16)
+
+    def cam(**kw):
+        d = {"R": [1, 0, 0, 0, 1, 0, 0, 0, 1], "t": [0, 0, 3], "fx": 100, "fy": 100, "cx": 64, "cy": 64,
+             "width": 128, "height": 128, "campos": [0, 0, -3]}
+        d.update(kw)
+        return gs.camera(d)
+
+    c = cam()
+    pc = gs.GsProj(16, 16, 16, 16, 16)
+    bad = gs.GS_ERR_INVALID_ARG
+    assert lib.gs_project(gs.dims(300, 256), p, ctypes.byref(c), pc, p, None) == bad
+    assert lib.gs_project(gs.dims(-1, 256), p, ctypes.byref(c), pc, p, None) == bad
+    assert lib.gs_project(gs.dims(10, (1 << 31) + 256), p, ctypes.byref(c), pc, p, None) == bad
+    assert lib.gs_project(gs.dims(10, 256), p, ctypes.byref(cam(width=65535 * 16 + 1)), pc, p, None) == bad
+    assert lib.gs_project(gs.dims(10, 256), p, ctypes.byref(cam(R=[float("nan")] + [0] * 8)), pc, p, None) == bad
+    assert lib.gs_project(gs.dims(10, 256), p, ctypes.byref(cam(near_z=float("inf"))), pc, p, None) == bad
+    bg = (ctypes.c_float * 3)(0, 0, 0)
+    bins = gs.GsBins(16, 16, 16, 16, 16)
+    assert lib.gs_render_fwd(ctypes.byref(c), ctypes.byref(bins), 1000, bg, None, p, p, p, None) == bad
+    misaligned = gs.GsBins(16, 16, 20, 16, 16)
+    assert lib.gs_render_fwd(ctypes.byref(c), ctypes.byref(misaligned), 1000, bg, p, p, p, p, None) == bad
+    assert lib.gs_densify_apply(gs.dims(10, 256), 100, p, p, p, p, p, p, p, 0.47, p, p, p, p, None) == bad
+    assert lib.gs_opacity_reset(gs.dims(10, 256), p, None, p, -4.0, None) == bad
