@@ -636,6 +636,31 @@ def test_graph_replayed_steps_match_eager_steps(case):
     np.testing.assert_allclose(lb, la, rtol=1e-5)
 
 
+def test_render_on_a_coloured_background():
+    """Forward and backward on a coloured background against the oracle: image,
+    T_final and n_contrib bit for bit, the loss and the 2D gradients within tolerance.
+    What shows through (T_final bg) depends on every composited alpha, and the
+    backward's carried colour starts at the background."""
+    cfg = gi.CONFIGS["tiny"]
+    P = gi.scene_for(cfg)
+    n, W, H = cfg.n, cfg.width, cfg.height
+    cam = _cam_for(cfg)
+    bg = (0.3, 0.6, 0.1)
+    ref = oracle.project(P, n, cam, 32)
+    target = gi.offset_target(oracle.render(ref, W, H, bg=bg)["image"], seed=7)
+    rd = oracle.render(ref, W, H, bg=bg, target=target)
+    tr = gs.Trainer(P, n, W, H, capacity=1 << 20, lr_plane=gi.lr_planes(), bg=bg)
+    tr.forward(cam)
+    tr.loss_backward(cam, torch.from_numpy(target).to(DEV))
+    torch.cuda.synchronize()
+    assert tr.check_status() == 0
+    np.testing.assert_array_equal(_u32(tr.image), rd["image"].view(np.uint32))
+    np.testing.assert_array_equal(_u32(tr.T_final), rd["T_final"].view(np.uint32))
+    np.testing.assert_array_equal(_u32(tr.n_contrib), rd["n_contrib"])
+    assert abs(float(tr.loss.item()) - rd["loss"]) <= 1e-5 * rd["loss"]
+    _grad_close(_partials(tr, n, ref["conic"]), rd["grad2d"], what="grad2d (coloured background)")
+
+
 # ----------------------------------------------------------------------------- edge cases
 
 def test_empty_scene_all_culled():
