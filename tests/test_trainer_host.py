@@ -1,8 +1,9 @@
 """The trainer's host logic, without a GPU: checkpoints (save and load round-trip the
 parameter planes, the Adam moments, the step count and the Gaussian count bit for bit;
-the trainer only holds buffers until a step runs, so CPU tensors serve) and the Adam
-hyperparameters of a batch step."""
+the trainer only holds buffers until a step runs, so CPU tensors serve), the Adam
+hyperparameters of a batch step and the density-control thresholds."""
 import numpy as np
+import pytest
 import torch
 
 import gs_inputs as gi
@@ -45,3 +46,25 @@ def test_batch_hyperparameters_on_the_host():
     assert abs(b1) < 1e-15
     _, b1, b2, _ = batch_adam_hyper(16, lr, 0.9, 0.999, 1e-15)
     assert b1 == 0.0 and abs(b2 - 0.984) < 1e-15
+
+
+def test_density_thresholds_on_the_host():
+    """The density-control thresholds the binding hands the library, formed in fp64 and
+    rounded to fp32 once: grow above a mean 2D gradient of 2e-4; clone at most 0.01 x
+    the extent in scale (compared as a log-scale); prune below opacity 0.005 (as a
+    logit) or, optionally, above 0.1 x the extent; split children shrink by 1.6 (as a
+    log); the opacity reset clamps to twice the prune opacity (as a logit)."""
+    import math
+    import gaussian_splatting_differentiable_project_gb300 as gs
+    extent = 3.3
+    cfg, log_shrink, logit_reset = gs.densify_thresholds(extent, prune_big=True)
+    f32 = lambda x: float(np.float32(x))  # noqa: E731
+    assert f32(cfg.grad_threshold) == f32(2e-4)
+    assert f32(cfg.log_grow_scale) == f32(math.log(0.01 * extent))
+    assert f32(cfg.log_prune_scale) == f32(math.log(0.1 * extent))
+    assert f32(cfg.logit_prune) == f32(math.log(0.005 / 0.995))
+    assert cfg.prune_big == 1
+    assert log_shrink == f32(math.log(1.6))
+    assert logit_reset == f32(math.log(0.01 / 0.99))
+    # the logit threshold decides exactly where the sigmoid crosses 0.005
+    assert 1 / (1 + math.exp(-f32(cfg.logit_prune))) == pytest.approx(0.005, rel=1e-6)
