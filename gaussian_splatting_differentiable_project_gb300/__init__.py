@@ -35,6 +35,7 @@ TILE = 16
 REC_FLOATS = 12
 N_GRAD2D = 9
 GRAD2D_STRIDE = 12  # floats per Gaussian in the interleaved grad2d buffer
+SSIM_MAPS = 15  # planes of gs_ssim_fwd's maps: 3 partials and 2 local means per channel
 
 
 def grad2d_planes(grad2d, n: int) -> np.ndarray:
@@ -52,7 +53,7 @@ def grad2d_interleaved(planes: np.ndarray) -> np.ndarray:
     out = np.zeros((planes.shape[1], GRAD2D_STRIDE), np.float32)
     out[:, :N_GRAD2D] = planes.T
     return out
-SSIM_MAPS = 15  # planes of gs_ssim_fwd's maps: 3 partials and 2 local means per channel
+
 
 GS_OK = 0
 GS_ERR_INVALID_ARG = 1
