@@ -15,12 +15,12 @@ One JSON line is printed (rank 0).  Besides the device-timed value it carries:
                 with each step's target copied from pinned host memory (on a copy
                 stream, overlapping the previous step) and its loss read back;
   roofline      for the kernel with the largest share of step time;
-  cpu_baseline  the CPU oracle timed on this host on a bounded sample;
+  cpu_baseline  one whole, unsampled CPU oracle step timed on this host's cores;
   stages_ms     per-stage device time per step (CUDA events on the stream);
   clocks        SM clocks and throttle reasons sampled during the timed region.
 
 ``--impl reference`` times the CPU oracle instead (the reference arm of this
-build), each step a bounded sample of the same workload scaled to full steps.
+build): whole unsampled oracle steps over the same orbit views.
 Multi-GPU runs are independent replicas (the step does not shard).
 """
 from __future__ import annotations
@@ -254,66 +254,60 @@ FLOP_BWD_PAIR = 66
 FLOP_SSIM_PIX = 3 * (158 + 110 + 35 + 14 + 87 + 66 + 6)
 
 
-def fp32_peak_tflops(sm_mhz):
-    # 152 SMs x 128 FP32 lanes x 2 FLOP per FMA per clock
-    return 152 * 128 * 2 * sm_mhz * 1e6 / 1e12
+# Operations of an iterated pair that does not composite (the power is positive or
+# alpha falls below 1/255): the rule's evaluation up to the 1/255 test, offset 2, power
+# 9, skip test 1, power log2(e) 1, the exponential 1, o e^power 1, the 0.99 clamp 1,
+# the 1/255 test 1.
+FLOP_SKIP_PAIR = 17
+
+
+def composited_flops(per_pair: int, iterated: float, composited: float) -> float:
+    """Work of a rasteriser charging composited pairs the full per-pair count and the
+    other iterated pairs only their evaluation."""
+    return per_pair * composited + FLOP_SKIP_PAIR * max(0.0, iterated - composited)
+
+
+def fp32_peak_tflops(sm_mhz, sms):
+    # SMs x 128 FP32 lanes x 2 FLOP per FMA per clock
+    return sms * 128 * 2 * sm_mhz * 1e6 / 1e12
 
 
 # ----------------------------------------------------------------------------- CPU oracle leg
 
-class OracleSample:
-    """Full-step oracle time estimated from a bounded sample of one view's step.
+class OracleStep:
+    """Whole oracle steps, nothing sampled or scaled: per view, the projection of every
+    Gaussian, the tile lists and the compositing forward and backward of every pixel,
+    the projection backward of every Gaussian and Adam over every parameter, with the
+    parameters and moments carried from step to step.  The loss is L1 against a seeded
+    U(0, 1) target per view (the work of a step does not depend on the target's
+    values)."""
 
-    Per-Gaussian stages (projection, projection backward, Adam) run on every
-    frac_g-th Gaussian and are scaled by frac_g.  Binning and compositing (forward
-    and backward) run on a band of ``band_rows`` tile rows through the image centre,
-    given only the Gaussians whose tile rect meets the band, and are scaled by the
-    number of tile rows over band_rows."""
-
-    def __init__(self, P, n, cam, frac_g: int, band_rows: int):
+    def __init__(self, P, n, width, height, seed=0):
         import oracle
         oracle.build()
         self.oracle = oracle
-        W, H = int(cam["width"]), int(cam["height"])
-        self.TY = -(-H // 16)
-        self.frac_g, self.rows, self.W, self.cam = frac_g, band_rows, W, cam
-        sub = np.ascontiguousarray(P[:, : n : frac_g])
-        self.n_sub = sub.shape[1]
-        self.sub = np.zeros((59, gi.n_pad_of(self.n_sub)), np.float32)
-        self.sub[:, : self.n_sub] = sub
-        r0 = (self.TY - band_rows) // 2
-        band = dict(cam)
-        band["height"] = band_rows * 16
-        band["cy"] = np.float32(float(cam["cy"]) - 16 * r0)
-        pr = oracle.project(P, n, band, 32)
-        keep = np.nonzero(pr["count"] > 0)[0]
-        self.band_proj = {"proj16": np.ascontiguousarray(pr["proj16"][keep]),
-                          "iproj6": np.ascontiguousarray(pr["iproj6"][keep])}
-        self.band_target = np.full((3, band_rows * 16, W), 0.5, np.float32)
-        self.g2 = np.full((9, self.n_sub), 1e-6)
-        self.z = np.zeros((59, self.n_sub))
-        self.desc = (f"oracle on every {frac_g}th Gaussian (projection, projection backward, Adam; scaled "
-                     f"x{frac_g}) and on {band_rows} of {self.TY} tile rows of view 0 with the Gaussians that "
-                     f"touch them (binning, compositing forward and backward; scaled x{self.TY / band_rows:g}), "
-                     f"summed to one full step")
+        self.P = np.ascontiguousarray(P, np.float32)
+        self.n, self.W, self.H, self.seed = n, width, height, seed
+        self.m = np.zeros(self.P.shape, np.float64)
+        self.v = np.zeros(self.P.shape, np.float64)
+        self.t = 0
 
-    def seconds(self, count_used: bool = False) -> float:
-        """One sampled step, scaled to a full step.  With count_used the band's render
-        also counts each pixel's composited entries (kept as ``composited_per_pixel``)."""
-        o = self.oracle
+    def target(self, view: int) -> np.ndarray:
+        return gi.uniform_target(self.seed + 7919 * view, self.W, self.H)
+
+    def seconds(self, cam, target) -> float:
+        """One whole training step of the oracle for one view; returns its wall time."""
         t0 = time.perf_counter()
-        o.project(self.sub, self.n_sub, self.cam, 32)
-        t1 = time.perf_counter()
-        rd = o.render(self.band_proj, self.W, self.rows * 16, target=self.band_target, count_used=count_used)
-        t2 = time.perf_counter()
-        if count_used:
-            self.composited_per_pixel = float(rd["n_used"].mean())
-        o.project_bwd(self.sub, self.n_sub, self.cam, self.g2, 32)
-        t3 = time.perf_counter()
-        o.adam(self.sub[:, : self.n_sub].astype(np.float64), self.z + 1e-6, self.z, self.z, gi.lr_planes(),
-               0.9, 0.999, 1e-15, 1)
-        t4 = time.perf_counter()
-        return (t1 - t0 + t3 - t2 + t4 - t3) * self.frac_g + (t2 - t1) * self.TY / self.rows
+        r = self.oracle.step(self.P, self.n, cam, target, self.m, self.v, self.t + 1, gi.lr_planes())
+        self.P = r["params"].astype(np.float32)
+        self.m, self.v = r["m"], r["v"]
+        self.t += 1
+        return time.perf_counter() - t0
+
+    def desc(self, what: str) -> str:
+        return (f"{what}: whole oracle steps, every Gaussian and every pixel of the "
+                f"{self.W}x{self.H} view (projection, tile lists, compositing forward and backward, "
+                f"projection backward, Adam), nothing sampled or scaled; L1 against seeded U(0,1) targets")
 
 
 def _torch_dev():
@@ -325,26 +319,31 @@ def _torch_dev():
 
 
 def run_reference(args, cfg, rank):
-    """Reference arm: the CPU oracle, each step a bounded sample scaled to a full step."""
+    """Reference arm: the CPU oracle, whole unsampled steps over the orbit views in
+    order (the same views as the GPU arm's steps)."""
     if rank != 0:
         return
     cams = gi.cameras_for(cfg)
     P = gi.scene_for(cfg, seed=args.seed, device=_torch_dev() if cfg.n >= 1_000_000 else None)
-    smp = OracleSample(P, cfg.n, cams[0], frac_g=256, band_rows=1)
+    ost = OracleStep(P, cfg.n, cfg.width, cfg.height, seed=args.seed)
     per = []
     for s in range(args.warmup + args.steps):
-        sec = smp.seconds()
+        v = s % len(cams)
+        tgt = ost.target(v)
+        sec = ost.seconds(cams[v], tgt)
         if s >= args.warmup:
             per.append(sec)
-    val = 1.0 / float(np.mean(per))
+    val = len(per) / float(np.sum(per))
+    desc = ost.desc(f"{args.warmup} warm-up and {args.steps} timed steps, orbit views in order")
     line = {
         "impl": "reference", "metric": METRIC, "value": val, "unit": "steps/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 / val, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64 (fp32 decisions)", "data": "synthetic",
         "config": _config_dict(cfg),
-        "cpu_baseline": {"value": val, "unit": "steps/s", "cores": smp.oracle.threads(), "kind": "oracle",
-                         "sample": smp.desc},
+        "cpu_baseline": {"value": val, "unit": "steps/s", "cores": ost.oracle.threads(), "kind": "oracle",
+                         "sample": desc, "extrapolated": False},
         "e2e": {"value": val, "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "step_s": {"mean": float(np.mean(per)), "min": float(np.min(per)), "max": float(np.max(per))},
     }
     print(json.dumps(line), flush=True)
 
@@ -410,11 +409,17 @@ def run_gb300(args, cfg, ws, rank, local):
     if args.dssim > 0:
         STAGES.insert(STAGES.index("render_bwd"), "ssim")
     del Pd
-    # per-view work statistics (forward on the initial parameters)
-    E = []
+    # per-view work statistics (forward on the initial parameters): pairs iterated
+    # (sum of n_contrib) and pairs composited (the counting forward's n_used)
+    E, E_used = [], []
+    n_used = torch.empty_like(tr.n_contrib)
     for cam in cams:
-        tr.forward(cam)
+        gs.project(tr.n, tr.params, cam, tr.proj, tr.status)
+        gs.bin_sort(tr.n, tr.n_pad, tr.proj, cam, tr.bins, tr.status)
+        gs.render_fwd_counted(cam, tr.bins, tr.bg, tr.image, tr.T_final, tr.n_contrib, n_used, tr.status)
         E.append(int(tr.n_contrib.to(torch.int64).sum().item()))
+        E_used.append(int(n_used.to(torch.int64).sum().item()))
+    del n_used
     torch.cuda.synchronize()
     tr.raise_on_status()
     setup_s = time.time() - t_setup
@@ -568,12 +573,19 @@ def run_gb300(args, cfg, ws, rank, local):
     Kmean = float(np.mean([Ks[v] for v in views]))
     Vmean = float(np.mean([Vs[v] for v in views]))
     Emean = float(np.mean([E[v] for v in views]))
+    Eused = float(np.mean([E_used[v] for v in views]))
     Pix = W * H
     byt = stage_bytes(n, n_pad, Vmean, Kmean, Pix, passes, dssim=args.dssim > 0)
     peak_bw = _peak("hbm_gbs", 6800.0)
     sm_mhz = clk.get("sm_max_mhz") or 2070.0
-    peak_fp32 = fp32_peak_tflops(sm_mhz)
+    sms = gs.sm_count()
+    sms_torch = torch.cuda.get_device_properties(dev).multi_processor_count
+    peak_fp32 = fp32_peak_tflops(sm_mhz, sms)
     flops = {"render_fwd": FLOP_FWD_PAIR * Emean, "render_bwd": FLOP_BWD_PAIR * Emean, "ssim": FLOP_SSIM_PIX * Pix}
+    # the same rule charging a skipped pair (iterated, not composited) only its
+    # evaluation up to the 1/255 test
+    flops_comp = {"render_fwd": composited_flops(FLOP_FWD_PAIR, Emean, Eused),
+                  "render_bwd": composited_flops(FLOP_BWD_PAIR, Emean, Eused), "ssim": FLOP_SSIM_PIX * Pix}
     per_stage = {}
     t_star = 0.0
     row_t = {}
@@ -583,6 +595,9 @@ def run_gb300(args, cfg, ws, rank, local):
     for row in rows_all:
         row_t[row] = max(byt[row] / (peak_bw * 1e9), flops.get(row, 0.0) / (peak_fp32 * 1e12))
     t_star = sum(row_t.values())
+    # the same sum with the fused projection backward + Adam charged the bytes it moves
+    t_star_fused = (t_star - row_t["project_bwd"] - row_t["adam"]
+                    + fused_bytes(n, n_pad, Vmean) / (peak_bw * 1e9)) if not args.separate else None
     if B > 1:
         # a batch step: every row but Adam once per view, Adam once
         t_star = B * sum(t for r, t in row_t.items() if r != "adam") + row_t["adam"]
@@ -596,6 +611,10 @@ def run_gb300(args, cfg, ws, rank, local):
         t_own = max(moved / (peak_bw * 1e9), fl / (peak_fp32 * 1e12))
         per_stage[name] = {"ms": stage_ms[name], "bound": bound, "rows": rows,
                            "gbs": moved / t_meas / 1e9, "tflops": fl / t_meas / 1e12, "frac": t_own / t_meas}
+        fl_c = sum(flops_comp.get(r, 0.0) for r in rows)
+        if fl_c:
+            per_stage[name]["tflops_composited"] = fl_c / t_meas / 1e12
+            per_stage[name]["frac_composited"] = max(moved / (peak_bw * 1e9), fl_c / (peak_fp32 * 1e12)) / t_meas
         if len(rows) > 1:
             # the fused stage against the rows it replaces (their gradient planes
             # included), as the step roofline charges it
@@ -611,12 +630,18 @@ def run_gb300(args, cfg, ws, rank, local):
         else:
             roof = {"kernel": dom, "bound": "alu", "achieved": d["tflops"], "peak": peak_fp32, "unit": "TFLOP/s",
                     "frac": d["tflops"] / peak_fp32, "traffic": traffic,
-                    "peak_source": f"152 SMs x 128 FP32 lanes x 2 x {sm_mhz:.0f} MHz"}
+                    "peak_source": f"{sms} SMs (queried) x 128 FP32 lanes x 2 x {sm_mhz:.0f} MHz (max SM clock "
+                                   f"sampled during the timed region); MEASURED_PEAKS.json has no FP32 entry",
+                    "flop_per_pair": FLOP_FWD_PAIR if dom == "render_fwd" else FLOP_BWD_PAIR,
+                    "achieved_composited": d.get("tflops_composited"),
+                    "frac_composited": (d.get("tflops_composited") or 0.0) / peak_fp32,
+                    "flop_model_composited": f"{FLOP_SKIP_PAIR} FLOP per iterated pair that does not composite, "
+                                             f"the full count per composited pair"}
 
     cpu = None
     if not args.no_cpu_baseline and ws == 1:
         try:
-            cpu = cpu_baseline(cfg, P, cams[0], tr, W, H)
+            cpu = cpu_baseline(cfg, P, cams[0], W, H, args.seed)
         except Exception as exc:  # the baseline is reported, never required
             cpu = {"value": None, "unit": "steps/s", "kind": "oracle", "error": repr(exc)}
 
@@ -630,13 +655,17 @@ def run_gb300(args, cfg, ws, rank, local):
         "dtype": "f32", "data": "synthetic",
         "config": dict(_config_dict(cfg), parallelism=f"replicas{ws}", capacity_K=capacity,
                        objective=(f"{1 - args.dssim:g} L1 + {args.dssim:g} (1 - SSIM)" if args.dssim > 0 else "L1"),
-                       K_mean=Kmean, visible_mean=Vmean, pairs_bwd_mean=Emean,
-                       entries_per_pixel=Emean / float(W * H), batch=B, storage_order=args.order, seed=args.seed,
-                       gpu=torch.cuda.get_device_name(dev),
+                       K_mean=Kmean, visible_mean=Vmean, pairs_bwd_mean=Emean, pairs_composited_mean=Eused,
+                       entries_per_pixel=Emean / float(W * H), composited_per_pixel=Eused / float(W * H),
+                       visible_frac_all_views={"min": min(Vs) / n, "mean": float(np.mean(Vs)) / n,
+                                               "views": V_views},
+                       batch=B, storage_order=args.order, seed=args.seed,
+                       gpu=torch.cuda.get_device_name(dev), sm_count=sms, sm_count_torch=sms_torch,
                        cuda_graph=bool(graphs)),
         "views_per_s": value * B,
         "roofline": roof,
         "step_roofline_frac": t_star / (ms / K / 1e3),
+        "step_roofline_frac_fused_bytes": (t_star_fused / (ms / K / 1e3)) if (t_star_fused and B == 1) else None,
         "step_ms_median": float(np.median(step_ms)) if step_ms else None,
         "step_ms_p90": float(np.percentile(step_ms, 90)) if step_ms else None,
         "stages_ms": stage_ms, "stages": per_stage,
@@ -679,15 +708,12 @@ def _peak_src(key):
     return "of measured" if os.path.exists(os.path.join(ROOT, "MEASURED_PEAKS.json")) else "of fallback"
 
 
-def cpu_baseline(cfg, P, cam, tr, W, H):
-    rows = max(1, (-(-H // 16)) // 16)
-    smp = OracleSample(P, cfg.n, cam, frac_g=8, band_rows=rows)
-    sec = smp.seconds(count_used=True)
-    r0 = (smp.TY - rows) // 2
-    return {"value": 1.0 / sec, "unit": "steps/s", "cores": smp.oracle.threads(), "kind": "oracle",
-            "sample": smp.desc, "seconds_per_step": sec,
-            "composited_per_pixel": {"value": smp.composited_per_pixel,
-                                     "over": f"tile rows {r0}-{r0 + rows - 1} of view 0, model before training"}}
+def cpu_baseline(cfg, P, cam, W, H, seed):
+    """One whole oracle step of view 0 on this host's cores (unsampled)."""
+    ost = OracleStep(P, cfg.n, W, H, seed=seed)
+    sec = ost.seconds(cam, ost.target(0))
+    return {"value": 1.0 / sec, "unit": "steps/s", "cores": ost.oracle.threads(), "kind": "oracle",
+            "sample": ost.desc("one step of orbit view 0"), "seconds_per_step": sec, "extrapolated": False}
 
 
 def main():

@@ -9,6 +9,7 @@ present, the calls raise.
 Entry points (same names as the C ABI, without the ``gs_`` prefix):
 - the step: ``project``, ``bin_sort``, ``render_fwd``, ``render_bwd``,
   ``project_bwd``, ``adam_step``, and the fused ``project_bwd_adam``;
+  ``render_fwd_counted`` (the forward with per-pixel composited counts);
 - the D-SSIM term: ``ssim_fwd``, ``ssim_bwd``;
 - batches and graphs: ``project_bwd_accumulate``, ``project_bwd_adam_tdev``,
   ``step_counter_add``;
@@ -16,7 +17,8 @@ Entry points (same names as the C ABI, without the ``gs_`` prefix):
   ``opacity_reset``;
 - storage order: ``spatial_order``, ``permute_planes``;
 - sizes and utilities: ``bin_sort_workspace_bytes``, ``densify_workspace_bytes``,
-  ``spatial_order_workspace_bytes``, ``bin_sort_noalloc``, ``util_expf``.
+  ``spatial_order_workspace_bytes``, ``bin_sort_noalloc``, ``util_expf``,
+  ``sm_count``.
 Tensor arguments must be dense CUDA tensors; anything else raises ``GsError``
 before a call is made.
 """
@@ -132,6 +134,9 @@ def load(build_if_missing: bool = True):
         lib.gs_render_fwd.argtypes = [ctypes.POINTER(GsCamera), ctypes.POINTER(GsBins), ctypes.c_uint32,
                                       ctypes.POINTER(ctypes.c_float), P, P, P, P, P]
         lib.gs_render_fwd.restype = st
+        lib.gs_render_fwd_counted.argtypes = [ctypes.POINTER(GsCamera), ctypes.POINTER(GsBins), ctypes.c_uint32,
+                                              ctypes.POINTER(ctypes.c_float), P, P, P, P, P, P]
+        lib.gs_render_fwd_counted.restype = st
         lib.gs_render_bwd.argtypes = [GsDims, ctypes.POINTER(GsCamera), ctypes.POINTER(GsBins), ctypes.c_uint32,
                                       ctypes.POINTER(ctypes.c_float), P, P, P, P, ctypes.c_float, P, P, P, P, P]
         lib.gs_render_bwd.restype = st
@@ -184,6 +189,8 @@ def load(build_if_missing: bool = True):
         lib.gs_status_str.argtypes = [ctypes.c_uint32]
         lib.gs_status_str.restype = ctypes.c_char_p
         lib.gs_version.restype = ctypes.c_char_p
+        lib.gs_sm_count.argtypes = []
+        lib.gs_sm_count.restype = ctypes.c_int32
         _lib = lib
         return lib
 
@@ -375,6 +382,20 @@ def render_fwd(cam: dict, bins: BinBuffers, bg, image, T_final, n_contrib, dev_s
                                 _buf(image, 3 * P, "f32", "image"), _buf(T_final, P, "f32", "T_final"),
                                 _buf(n_contrib, P, "i32", "n_contrib"), _buf(dev_status, 1, "i32", "dev_status"),
                                 _stream(stream)), "gs_render_fwd")
+
+
+def render_fwd_counted(cam: dict, bins: BinBuffers, bg, image, T_final, n_contrib, n_used, dev_status,
+                       stream=None) -> None:
+    """render_fwd that also writes each pixel's number of composited entries."""
+    cc = camera(cam)
+    _check_bins(bins, cc)
+    bc = bins.c()
+    P = cc.width * cc.height
+    _check(load().gs_render_fwd_counted(ctypes.byref(cc), ctypes.byref(bc), bins.capacity, _bg(bg),
+                                        _buf(image, 3 * P, "f32", "image"), _buf(T_final, P, "f32", "T_final"),
+                                        _buf(n_contrib, P, "i32", "n_contrib"), _buf(n_used, P, "i32", "n_used"),
+                                        _buf(dev_status, 1, "i32", "dev_status"), _stream(stream)),
+           "gs_render_fwd_counted")
 
 
 def render_bwd(n: int, n_pad: int, cam: dict, bins: BinBuffers, bg, image, target, T_final, n_contrib, grad2d,
@@ -570,6 +591,11 @@ def util_expf(x, y, stream=None) -> None:
 
 def version() -> str:
     return load().gs_version().decode()
+
+
+def sm_count() -> int:
+    """The current device's SM count, as the library queried it for its grids."""
+    return int(load().gs_sm_count())
 
 
 from .trainer import HostTargets, Trainer  # noqa: E402  (re-export)

@@ -36,7 +36,7 @@ extern "C" gs_status gs_adam_step(gs_dims dims, float* params, const float* grad
   AdamParams a;
   if (!make_adam_params(lr_plane, beta1, beta2, eps, t, a)) return GS_ERR_INVALID_ARG;
   const int64_t n4 = int64_t(kPlanes) * dims.n_pad / 4;
-  const int blocks = grid_for(n4, 256, kSmCount * 16);
+  const int blocks = grid_for(n4, 256, sm_count() * 16);
   k_adam<<<blocks, 256, 0, stream>>>(reinterpret_cast<float4*>(params), reinterpret_cast<const float4*>(grads),
                                      reinterpret_cast<float4*>(m), reinterpret_cast<float4*>(v), n4, dims.n_pad / 4, a);
   return launch_status();

@@ -1,9 +1,32 @@
-// Small C-ABI utilities: status strings, version, and the library exponential
-// exposed for cross-checking.
+// Small C-ABI utilities: status strings, version, the device's SM count the grids
+// are sized from, and the library exponential exposed for cross-checking.
+#include <atomic>
+
 #include "api_util.h"
 #include "gs_common.cuh"
 
 namespace gs {
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_sm_count[kMaxDevices];  // 0 until queried
+}  // namespace
+
+int sm_count() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();  // leave no sticky error behind for launch_status
+    return 1;
+  }
+  int c = g_sm_count[dev].load(std::memory_order_relaxed);
+  if (c > 0) return c;
+  if (cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || c <= 0) {
+    cudaGetLastError();
+    return 1;
+  }
+  g_sm_count[dev].store(c, std::memory_order_relaxed);
+  return c;
+}
 
 __global__ void k_expf(const float* __restrict__ x, float* __restrict__ y, int64_t n) {
   const int64_t stride = int64_t(gridDim.x) * blockDim.x;
@@ -16,9 +39,11 @@ extern "C" gs_status gs_util_expf(const float* x, float* y, int64_t n, cudaStrea
   using namespace gs;
   if (n < 0 || (n > 0 && (!x || !y))) return GS_ERR_INVALID_ARG;
   if (n == 0) return GS_OK;
-  k_expf<<<grid_for(n, 256, kSmCount * 16), 256, 0, stream>>>(x, y, n);
+  k_expf<<<grid_for(n, 256, sm_count() * 16), 256, 0, stream>>>(x, y, n);
   return launch_status();
 }
+
+extern "C" int32_t gs_sm_count(void) { return gs::sm_count(); }
 
 extern "C" const char* gs_status_str(uint32_t status) {
   if (status == 0) return "ok";

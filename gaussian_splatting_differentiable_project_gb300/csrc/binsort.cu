@@ -624,7 +624,7 @@ extern "C" gs_status gs_bin_sort(gs_dims dims, const gs_proj* proj, const gs_cam
   const CamDev cd = cam_dev(*cam);
 
   // 1. per-block visible counts and tile-count sums + clearing
-  const int clear_blocks = kSmCount * 4;
+  const int clear_blocks = sm_count() * 4;
   const int b1 = int(L.n_blocks > clear_blocks ? L.n_blocks : clear_blocks);
   // (block_sums is free until step 5 and holds the per-block smallest depth bits)
   k_bs_prep<<<b1, kScanThreads, 0, stream>>>(proj->count, proj->depth, dims.n, L.n_blocks, block_vis, block_cnt,
@@ -683,7 +683,7 @@ extern "C" gs_status gs_bin_sort(gs_dims dims, const gs_proj* proj, const gs_cam
     vb = t;
   }
   // 8. ranges, 64-bit keys and the record gather
-  const int g = grid_for(capacity_K, 256, kSmCount * 16);
+  const int g = grid_for(capacity_K, 256, sm_count() * 16);
   k_bs_ranges_gather<<<g, 256, 0, stream>>>(ka, bins.ids, bins.n_isect, capacity_K,
                                             reinterpret_cast<const float4*>(proj->rec),
                                             reinterpret_cast<float4*>(bins.rec), bins.keys,
@@ -747,8 +747,8 @@ extern "C" gs_status gs_spatial_order(gs_dims dims, const float* params, uint32_
   uint32_t* tickets = reinterpret_cast<uint32_t*>(ws + L.tickets);
   uint32_t* look = reinterpret_cast<uint32_t*>(ws + L.look);
   const int64_t zero_vec = int64_t(L.total - L.hist) / 16;
-  k_so_init<<<kSmCount * 4, 256, 0, stream>>>(box, dims.n, reinterpret_cast<uint4*>(ws + L.hist), zero_vec);
-  const int g = grid_for(dims.n, kSoThreads, kSmCount * 8);
+  k_so_init<<<sm_count() * 4, 256, 0, stream>>>(box, dims.n, reinterpret_cast<uint4*>(ws + L.hist), zero_vec);
+  const int g = grid_for(dims.n, kSoThreads, sm_count() * 8);
   k_so_bbox<<<g, kSoThreads, 0, stream>>>(params, dims.n, dims.n_pad, box);
   k_so_codes<<<g, kSoThreads, 0, stream>>>(params, dims.n, dims.n_pad, box, kA, perm, hist);
   // four stable 8-bit passes over the 30-bit codes; an even count ends in (kA, perm)
@@ -774,7 +774,7 @@ extern "C" gs_status gs_permute_planes(gs_dims dims, int32_t planes, const uint3
   if (!aligned(src, 4) || !aligned(dst, 4)) return GS_ERR_INVALID_ARG;
   const int64_t total = int64_t(planes) * dims.n_pad;
   if (total == 0) return GS_OK;
-  k_permute_planes<<<grid_for(total, 256, kSmCount * 16), 256, 0, stream>>>(
+  k_permute_planes<<<grid_for(total, 256, sm_count() * 16), 256, 0, stream>>>(
       perm, dims.n, dims.n_pad, planes, static_cast<const uint32_t*>(src), static_cast<uint32_t*>(dst));
   return launch_status();
 }

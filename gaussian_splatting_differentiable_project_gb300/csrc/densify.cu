@@ -221,7 +221,7 @@ extern "C" gs_status gs_densify_accumulate(gs_dims dims, const uint32_t* count, 
     return GS_ERR_INVALID_ARG;
   if (!aligned(grad2d, 16) || !aligned(rec, 16)) return GS_ERR_INVALID_ARG;
   if (dims.n == 0) return GS_OK;
-  k_densify_accum<<<grid_for(dims.n, 256, kSmCount * 16), 256, 0, stream>>>(
+  k_densify_accum<<<grid_for(dims.n, 256, sm_count() * 16), 256, 0, stream>>>(
       count, reinterpret_cast<const float4*>(rec), reinterpret_cast<const float4*>(grad2d), dims.n,
       0.5f * float(width), 0.5f * float(height), grad_acc, vis_cnt);
   return launch_status();
@@ -260,7 +260,7 @@ extern "C" gs_status gs_densify_apply(gs_dims src, int64_t n_pad_dst, const floa
   if (n_pad_dst <= 0 || (n_pad_dst % 256) != 0 || n_pad_dst > (int64_t(1) << 31) || !std::isfinite(log_shrink))
     return GS_ERR_INVALID_ARG;
   const int64_t work = src.n > n_pad_dst ? src.n : n_pad_dst;
-  k_densify_apply<<<grid_for(work, 256, kSmCount * 16), 256, 0, stream>>>(
+  k_densify_apply<<<grid_for(work, 256, sm_count() * 16), 256, 0, stream>>>(
       params, m, v, src.n, src.n_pad, action, offset, n_out, randn, log_shrink, params_dst, m_dst, v_dst, n_pad_dst,
       dev_status);
   return launch_status();
@@ -271,7 +271,7 @@ extern "C" gs_status gs_opacity_reset(gs_dims dims, float* params, float* m, flo
   using namespace gs;
   if (!dims_ok(dims) || !params || !m || !v || !std::isfinite(logit_max)) return GS_ERR_INVALID_ARG;
   if (dims.n == 0) return GS_OK;
-  k_opacity_reset<<<grid_for(dims.n, 256, kSmCount * 16), 256, 0, stream>>>(params, m, v, dims.n, dims.n_pad,
+  k_opacity_reset<<<grid_for(dims.n, 256, sm_count() * 16), 256, 0, stream>>>(params, m, v, dims.n, dims.n_pad,
                                                                             logit_max);
   return launch_status();
 }

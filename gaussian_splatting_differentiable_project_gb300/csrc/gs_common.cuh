@@ -102,7 +102,10 @@ inline CamDev cam_dev(const gs_camera& c) {
 }
 
 // ------------------------------------------------------------------ misc
-constexpr int kSmCount = 152;
+// Streaming multiprocessors of the current device, queried once per device (api.cu);
+// grids of the streaming and persistent kernels are sized from it.  Every kernel so
+// sized loops over its work with a grid stride, so the count affects speed only.
+int sm_count();
 
 inline int grid_for(int64_t items, int threads, int max_blocks) {
   int64_t b = (items + threads - 1) / threads;

@@ -107,7 +107,7 @@ extern "C" gs_status gs_project(gs_dims dims, const float* params, const gs_came
       return GS_ERR_CUDA;
     attr_set = true;
   }
-  const int blocks = grid_for(dims.n_pad / kProjGroup, 1, kSmCount * 2);
+  const int blocks = grid_for(dims.n_pad / kProjGroup, 1, sm_count() * 2);
   k_project<<<blocks, kProjGroup, kProjSmem, stream>>>(params, dims.n, dims.n_pad, cam_dev(*cam),
                                                       reinterpret_cast<float4*>(proj.rec), proj.depth, proj.radius,
                                                       reinterpret_cast<uint2*>(proj.rect), proj.count, dev_status);

@@ -429,7 +429,7 @@ gs_status project_bwd_launch(gs_dims dims, const float* params, const gs_camera*
   if (!dims_ok(dims) || !camera_ok(cam) || !params || !proj || !proj->count || !grad2d || !grads || !dev_status)
     return GS_ERR_INVALID_ARG;
   if (!aligned(params, 16) || !aligned(grads, 16) || !aligned(grad2d, 16)) return GS_ERR_INVALID_ARG;
-  const int blocks = grid_for(dims.n_pad, 256, kSmCount * 64);
+  const int blocks = grid_for(dims.n_pad, 256, sm_count() * 64);
   if (acc)
     k_project_bwd<true><<<blocks, 256, 0, stream>>>(params, dims.n, dims.n_pad, cam_dev(*cam), proj->count, grad2d,
                                                     grads);
@@ -464,7 +464,7 @@ gs_status fused_launch(gs_dims dims, float* params, const gs_camera* cam, const 
   using namespace gs;
   const size_t smem = fused_dyn_smem(kAccIn);
   if (!fused_attrs_ready()) return GS_ERR_CUDA;
-  const int blocks = grid_for(dims.n_pad / kFusedBlock, 1, kSmCount * 2);
+  const int blocks = grid_for(dims.n_pad / kFusedBlock, 1, sm_count() * 2);
   k_project_bwd_adam<kAccIn, kDevT><<<blocks, kFusedBlock, smem, stream>>>(
       params, dims.n, dims.n_pad, cam_dev(*cam), proj->count, grad2d, grads_in, m, v, a, h, t_dev);
   return launch_status();

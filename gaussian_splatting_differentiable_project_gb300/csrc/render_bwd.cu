@@ -245,7 +245,7 @@ extern "C" gs_status gs_render_bwd(gs_dims dims, const gs_camera* cam, const gs_
   if (!aligned(bins->rec, 16) || !aligned(bins->ranges, 8) || !aligned(grad2d, 16)) return GS_ERR_INVALID_ARG;
   if (!(l1_weight >= 0.0f) || !std::isfinite(l1_weight)) return GS_ERR_INVALID_ARG;
   const int64_t n4 = int64_t(GS_GRAD2D_STRIDE) * dims.n_pad / 4;
-  k_zero4<<<grid_for(n4, 256, kSmCount * 8), 256, 0, stream>>>(reinterpret_cast<float4*>(grad2d), n4, loss_out);
+  k_zero4<<<grid_for(n4, 256, sm_count() * 8), 256, 0, stream>>>(reinterpret_cast<float4*>(grad2d), n4, loss_out);
   const int TX = (cam->width + kTile - 1) / kTile;
   const int64_t tiles = n_tiles(cam);
   const float inv3P = float(1.0 / (3.0 * double(cam->width) * double(cam->height)));

@@ -5,16 +5,20 @@
 // cp.async.bulk with two mbarrier-tracked buffers, so the next batch streams in
 // while the current one is composited; every thread reads the same record
 // (shared-memory broadcast).  A pixel stops at its transmittance threshold; the
-// CTA stops loading once __syncthreads_count reports no live pixel.
+// CTA stops loading once __syncthreads_count reports no live pixel.  The counting
+// instantiation (gs_render_fwd_counted) also writes each pixel's number of
+// composited entries; the training step runs the one without.
 #include "api_util.h"
 #include "raster_common.cuh"
 
 namespace gs {
 
+template <bool kCount>
 __global__ void __launch_bounds__(kRasterThreads)
     k_render_fwd(const Rec* __restrict__ srec, const uint2* __restrict__ ranges, const uint32_t* __restrict__ n_isect,
                  uint32_t cap, int W, int H, int TX, float bg0, float bg1, float bg2, float* __restrict__ image,
-                 float* __restrict__ T_final, uint32_t* __restrict__ n_contrib, uint32_t* __restrict__ dev_status) {
+                 float* __restrict__ T_final, uint32_t* __restrict__ n_contrib, uint32_t* __restrict__ n_used,
+                 uint32_t* __restrict__ dev_status) {
   __shared__ __align__(128) Rec s_rec[2][kBatchFwd];
   __shared__ __align__(8) uint64_t s_bar[2];
 
@@ -32,7 +36,7 @@ __global__ void __launch_bounds__(kRasterThreads)
   const uint32_t n = end - start;
 
   float T = 1.0f, C0 = 0.0f, C1 = 0.0f, C2 = 0.0f;
-  uint32_t last = 0;
+  uint32_t last = 0, used = 0;
   bool done = !inside;
 
   if (n > 0) {
@@ -83,6 +87,7 @@ __global__ void __launch_bounds__(kRasterThreads)
                   C2 = __fmaf_rn(R[j].c.x, w, C2);
                   T = Tn;
                   last = pos0 + uint32_t(j) + 1u;
+                  if (kCount) ++used;
                 }
               }
             }
@@ -110,24 +115,47 @@ __global__ void __launch_bounds__(kRasterThreads)
     image[2 * P + pix] = __fmaf_rn(T, bg2, C2);
     T_final[pix] = T;
     n_contrib[pix] = last;
+    if (kCount) n_used[pix] = used;
   }
 }
 
 }  // namespace gs
 
-extern "C" gs_status gs_render_fwd(const gs_camera* cam, const gs_bins* bins, uint32_t capacity_K, const float bg[3],
-                                   float* image, float* T_final, uint32_t* n_contrib, uint32_t* dev_status,
-                                   cudaStream_t stream) {
+namespace {
+gs_status render_fwd_launch(const gs_camera* cam, const gs_bins* bins, uint32_t capacity_K, const float bg[3],
+                            float* image, float* T_final, uint32_t* n_contrib, uint32_t* n_used, uint32_t* dev_status,
+                            cudaStream_t stream) {
   using namespace gs;
   if (!camera_ok(cam) || !bins || !bg || !image || !T_final || !n_contrib || !dev_status) return GS_ERR_INVALID_ARG;
   if (!bins->rec || !bins->ranges || !bins->n_isect || capacity_K == 0) return GS_ERR_INVALID_ARG;
   if (!aligned(bins->rec, 16) || !aligned(bins->ranges, 8)) return GS_ERR_INVALID_ARG;
   const int TX = (cam->width + kTile - 1) / kTile;
   const int64_t tiles = n_tiles(cam);
-  k_render_fwd<<<int(tiles * kCtasPerTile), kRasterThreads, 0, stream>>>(
-      reinterpret_cast<const Rec*>(bins->rec), reinterpret_cast<const uint2*>(bins->ranges), bins->n_isect,
-      capacity_K, cam->width, cam->height, TX, bg[0], bg[1], bg[2], image, T_final, n_contrib, dev_status);
+  const Rec* rec = reinterpret_cast<const Rec*>(bins->rec);
+  const uint2* ranges = reinterpret_cast<const uint2*>(bins->ranges);
+  if (n_used)
+    k_render_fwd<true><<<int(tiles * kCtasPerTile), kRasterThreads, 0, stream>>>(
+        rec, ranges, bins->n_isect, capacity_K, cam->width, cam->height, TX, bg[0], bg[1], bg[2], image, T_final,
+        n_contrib, n_used, dev_status);
+  else
+    k_render_fwd<false><<<int(tiles * kCtasPerTile), kRasterThreads, 0, stream>>>(
+        rec, ranges, bins->n_isect, capacity_K, cam->width, cam->height, TX, bg[0], bg[1], bg[2], image, T_final,
+        n_contrib, nullptr, dev_status);
   return launch_status();
+}
+}  // namespace
+
+extern "C" gs_status gs_render_fwd(const gs_camera* cam, const gs_bins* bins, uint32_t capacity_K, const float bg[3],
+                                   float* image, float* T_final, uint32_t* n_contrib, uint32_t* dev_status,
+                                   cudaStream_t stream) {
+  return render_fwd_launch(cam, bins, capacity_K, bg, image, T_final, n_contrib, nullptr, dev_status, stream);
+}
+
+extern "C" gs_status gs_render_fwd_counted(const gs_camera* cam, const gs_bins* bins, uint32_t capacity_K,
+                                           const float bg[3], float* image, float* T_final, uint32_t* n_contrib,
+                                           uint32_t* n_used, uint32_t* dev_status, cudaStream_t stream) {
+  if (!n_used) return GS_ERR_INVALID_ARG;
+  return render_fwd_launch(cam, bins, capacity_K, bg, image, T_final, n_contrib, n_used, dev_status, stream);
 }
 
 // ------------------------------------------------------------------ wait probe

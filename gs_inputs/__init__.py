@@ -329,6 +329,14 @@ def offset_target(image: np.ndarray, seed: int, lo: float = 0.05, hi: float = 0.
     return (image + sgn * mag).astype(image.dtype)
 
 
+def uniform_target(seed: int, width: int, height: int) -> np.ndarray:
+    """A seeded target image (3, height, width) fp32, U(0, 1) in every value: an L1
+    target that depends on no render, for checks where both sides render the same
+    image bit for bit (so they take every residual sign alike)."""
+    rng = np.random.default_rng(seed)
+    return rng.uniform(0.0, 1.0, (3, height, width)).astype(np.float32)
+
+
 def random_grad2d(seed: int, n: int, n_pad: int, scale: float = 1e-3) -> np.ndarray:
     """Seeded stand-in for the nine per-Gaussian 2D gradients (9, n_pad) fp32."""
     rng = np.random.default_rng(seed)

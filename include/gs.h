@@ -196,6 +196,17 @@ gs_status gs_render_fwd(const gs_camera* cam, const gs_bins* bins, uint32_t capa
                         float* image, float* T_final, uint32_t* n_contrib, uint32_t* dev_status,
                         cudaStream_t stream);
 
+/* gs_render_fwd_counted -- gs_render_fwd that also writes, per pixel, the number of
+ * entries it composited (alpha >= 1/255 and not stopped by the transmittance test):
+ *   n_used  H x W uint32 (write).
+ * The image, T_final and n_contrib are those of gs_render_fwd, bit for bit.  Not part
+ * of the training step: it measures how much of the iterated work composites (the
+ * mean number of Gaussians composited per pixel of a view).
+ * Errors: as gs_render_fwd, plus a null n_used. */
+gs_status gs_render_fwd_counted(const gs_camera* cam, const gs_bins* bins, uint32_t capacity_K, const float bg[3],
+                                float* image, float* T_final, uint32_t* n_contrib, uint32_t* n_used,
+                                uint32_t* dev_status, cudaStream_t stream);
+
 /* ---------------------------------------------------------------------------
  * gs_render_bwd -- loss gradient and the compositing backward.  "Scaling 3D
  * Gaussian Splatting with Distributed Compute", objective and gradient-descent
@@ -486,6 +497,12 @@ size_t gs_util_lookback_probe_bytes(void);
 gs_status gs_util_lookback_probe(int32_t spin_limit, void* scratch, size_t scratch_bytes, uint32_t* dev_status,
                                  cudaStream_t stream);
 gs_status gs_util_mbarrier_probe(int32_t wait_limit, uint32_t* dev_status, cudaStream_t stream);
+
+/* gs_sm_count -- the streaming multiprocessor count of the current device, which
+ * the library queries once per device and sizes the grids of its streaming and
+ * persistent kernels from (those kernels loop over their work with a grid stride, so
+ * the count changes speed, never results).  Returns 1 if no device can be queried. */
+int32_t gs_sm_count(void);
 
 /* Static description of a status value (several bits: the lowest set one). */
 const char* gs_status_str(uint32_t status);

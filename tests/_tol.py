@@ -1,0 +1,104 @@
+"""Tolerances of the GPU <-> oracle parity tests, in one place.
+
+* Integer, index and key outputs and the images: bit-exact (asserted by the tests
+  themselves).
+* Gradients (the nine 2D partials and the 59 parameter gradients): within 1e-4
+  relative with an absolute floor of 1e-6 x the largest magnitude of the same plane.
+  The stated 1e-6 floor is absolute at the tiny config, whose per-pixel loss gradient
+  is 1/(3*128*128); the floor keeps that proportion as images grow.
+  One exception: when every Gaussian of the scene is isotropic (equal log-scales on
+  the three axes, as the isosurface generators make them) the rotation leaves the
+  covariance unchanged, so the exact quaternion gradient is zero and both sides'
+  values are rounding noise of the covariance chain.  Those four planes then take
+  their floor from the largest gradient of the log-scale and quaternion planes
+  together, the chain whose noise they carry.
+* Adam: |p - p_ref| <= 1e-5 |p_ref| + ADAM_ABS, where the update is defined (below).
+"""
+import os
+
+import numpy as np
+
+RTOL = 1e-4
+FLOOR = 1e-6
+ADAM_RTOL = 1e-5
+ADAM_ABS = 1e-7
+QUAT = slice(6, 10)
+COV = slice(3, 10)
+
+
+def isotropic(P, n) -> bool:
+    """True if every Gaussian [0, n) of the (59, n_pad) planes has equal log-scales."""
+    ls = np.asarray(P[3:6, :n])
+    return bool(np.all(ls[0] == ls[1]) and np.all(ls[1] == ls[2]))
+
+
+def floors(ref, isotropic_scene=False):
+    """Per-plane absolute floors (rows x 1) for a (9 or 59, n) reference."""
+    ref = np.abs(np.asarray(ref, np.float64))
+    scale = ref.max(axis=1, keepdims=True) if ref.shape[1] else np.zeros((ref.shape[0], 1))
+    if ref.shape[0] == 59 and isotropic_scene:
+        scale[QUAT] = ref[COV].max()
+    return FLOOR * np.maximum(scale, 1e-30)
+
+
+def grad_excess(got, ref, isotropic_scene=False, rtol=RTOL):
+    """|got - ref| / tolerance, elementwise (<= 1 passes)."""
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    tol = rtol * np.abs(ref) + floors(ref, isotropic_scene)
+    return np.abs(got - ref) / tol
+
+
+def _log(what, ex):
+    """With GS_TOL_LOG set to a file path, append each check's worst excess per plane
+    (the measured error as a fraction of its tolerance) there."""
+    path = os.environ.get("GS_TOL_LOG")
+    if not path or not ex.size:
+        return
+    import inspect
+    test = next((f.function for f in inspect.stack() if f.function.startswith("test_")), "?")
+    worst = np.nanmax(ex, axis=1)
+    with open(path, "a") as f:
+        f.write(f"{test}\t{what}\t{float(np.nanmax(ex)):.4f}\t{' '.join(f'{w:.3f}' for w in worst)}\n")
+
+
+def grad_close(got, ref, isotropic_scene=False, what="", rtol=RTOL):
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    assert got.shape == ref.shape, (got.shape, ref.shape)
+    ex = grad_excess(got, ref, isotropic_scene, rtol)
+    _log(what, ex)
+    bad = ~(ex <= 1.0)
+    if bad.any():
+        pl, i = np.unravel_index(int(np.nanargmax(np.where(np.isnan(ex), np.inf, ex))), ref.shape)
+        per_plane = {int(p): round(float(np.nanmax(ex[p])), 3) for p in np.nonzero(bad.any(axis=1))[0]}
+        raise AssertionError(f"{what}: {int(bad.sum())} of {bad.size} outside tolerance; worst excess per plane "
+                             f"{per_plane}; worst plane {pl} index {i}: got {got[pl, i]!r} ref {ref[pl, i]!r}")
+    return float(ex.max()) if ex.size else 0.0
+
+
+def adam_defined(gref, isotropic_scene=False):
+    """Where an Adam update's direction is certain: at t = 1 an update is
+    lr sign(g), so entries whose oracle gradient lies within 1e-3 of its plane's
+    largest (the gradient tolerance, many times over) have no defined sign and are
+    left out of the end-to-end comparison.  (The stage test of Adam feeds both sides
+    identical inputs and compares every entry.)"""
+    g = np.abs(np.asarray(gref, np.float64))
+    scale = g.max(axis=1, keepdims=True)
+    if isotropic_scene:
+        scale[QUAT] = g[COV].max()
+    return g > 1e-3 * scale
+
+
+def adam_close(p, pref, defined=None, what="adam"):
+    p = np.asarray(p, np.float64)
+    pref = np.asarray(pref, np.float64)
+    bad = np.abs(p - pref) > ADAM_RTOL * np.abs(pref) + ADAM_ABS
+    if defined is not None:
+        bad &= defined
+    if os.environ.get("GS_TOL_LOG"):
+        ex = np.abs(p - pref) / (ADAM_RTOL * np.abs(pref) + ADAM_ABS)
+        if defined is not None:
+            ex = np.where(defined, ex, 0.0)
+        _log(what, ex.reshape(ex.shape[0], -1) if ex.ndim > 1 else ex[None])
+    assert not bad.any(), f"{what}: {int(bad.sum())} of {bad.size} outside 1e-5 |p| + 1e-7"

@@ -90,5 +90,19 @@ def test_tile_sort_passes(wh, passes):
 
 
 def test_fp32_peak():
-    # 152 SMs x 128 FP32 lanes x 2 FLOP per FMA x 2070 MHz
-    assert bench.fp32_peak_tflops(2070) == pytest.approx(80.54784)
+    # SMs (queried at run time) x 128 FP32 lanes x 2 FLOP per FMA x the SM clock:
+    # 152 SMs at 2070 MHz give 80.5 TFLOP/s
+    assert bench.fp32_peak_tflops(2070, 152) == pytest.approx(80.54784)
+    assert bench.fp32_peak_tflops(2070, 160) == pytest.approx(80.54784 * 160 / 152)
+
+
+def test_composited_flop_model():
+    """The second work figure: composited pairs the full per-pair count, the other
+    iterated pairs their evaluation up to the 1/255 test (17 operations: offset 2,
+    power 9, skip test 1, log2(e) 1, exponential 1, opacity product 1, clamp 1, the
+    1/255 test 1)."""
+    assert bench.FLOP_SKIP_PAIR == 2 + 9 + 1 + 1 + 1 + 1 + 1 + 1
+    assert bench.composited_flops(27, 100.0, 100.0) == 2700.0
+    assert bench.composited_flops(66, 100.0, 40.0) == 66 * 40 + 17 * 60
+    # every iterated pair costs at least its evaluation
+    assert bench.composited_flops(66, 100.0, 0.0) == 1700.0

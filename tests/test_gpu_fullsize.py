@@ -1,17 +1,20 @@
 """GPU <-> oracle parity at the configs' full sizes, in the launch configuration the
 bench uses (the library picks every launch shape from the sizes).
 
-* 1M Gaussians, 512x512: every stage against the oracle over the whole image.
-* 4M Gaussians, 2048x2048 (the bench's workload): the oracle on samples it can
+* 1M Gaussians at 512x512, 4M at 1024x1024 and 4M at 2048x2048 (the bench's
+  workload): the whole view.  Every Gaussian's projection, the key and id of every
+  intersection, every gathered record and every pixel's colour, T_final and
+  n_contrib bit-exact; every Gaussian's nine 2D gradients; and the fused projection
+  backward + Adam of every Gaussian (its first moment m = 0.1 g against the oracle's
+  gradient of the whole chain, the updated parameters against the oracle's Adam).
+* 18M Gaussians (turbulence isosurface), 2048x2048: the oracle on samples it can
   compute one by one (projection and the fused backward + Adam of sampled
-  Gaussians; compositing and its backward on a block of tiles, given every
-  Gaussian whose rect meets the block), and for the sort the properties that fix
-  its output uniquely at any size.
-* 18M Gaussians (turbulence isosurface), 2048x2048: the same sort properties,
-  sampled projection and a sampled tile block.
+  Gaussians; compositing and its backward on the tile block that the most rects
+  cover, given every Gaussian whose rect meets the block), and for the sort the
+  properties that fix its output uniquely at any size.
 
-Tolerances are those of test_gpu_parity.py: integer/key/index work and the
-images bit-exact, gradients 1e-4 relative with the group floor, Adam 1e-5.
+Tolerances are those of tests/_tol.py: integer/key/index work and the images
+bit-exact, gradients 1e-4 relative with the per-plane floor, Adam 1e-5.
 """
 import numpy as np
 import pytest
@@ -19,6 +22,7 @@ import pytest
 import gs_inputs as gi
 import oracle
 from _grad2d import moments_to_partials
+from _tol import adam_close, adam_defined, grad_close, isotropic
 
 pytestmark = pytest.mark.gpu
 
@@ -29,20 +33,6 @@ if not torch.cuda.is_available():
 import gaussian_splatting_differentiable_project_gb300 as gs  # noqa: E402
 
 DEV = "cuda"
-GROUPS_59 = [(0, 3), (3, 10), (10, 11), (11, 59)]
-GROUPS_9 = [(0, 2), (2, 5), (5, 6), (6, 9)]
-
-
-def _grad_close(got, ref, rtol=1e-4, floor=1e-6, what=""):
-    got = np.asarray(got, np.float64)
-    ref = np.asarray(ref, np.float64)
-    groups = GROUPS_59 if ref.shape[0] == 59 else GROUPS_9
-    scale = np.zeros((ref.shape[0], 1))
-    for a, b in groups:
-        scale[a:b] = max(np.abs(ref[a:b]).max(), 1e-30)
-    tol = rtol * np.abs(ref) + floor * scale
-    bad = np.abs(got - ref) > tol
-    assert not bad.any(), f"{what}: {bad.sum()} of {bad.size} outside tolerance"
 
 
 def _u32(t):
@@ -61,8 +51,11 @@ def _trainer_for(P, n, cam):
     return gs.Trainer(params, n, W, H, capacity=K + 4096, lr_plane=gi.lr_planes())
 
 
-def _check_projection(tr, P, n, cam, idx):
-    ref = oracle.project(np.ascontiguousarray(P[:, idx]), len(idx), cam, 32)
+def _check_projection(tr, P, n, cam, idx, ref=None):
+    """Projection of the Gaussians idx bit-exact against the oracle's (``ref``: the
+    oracle's projection of exactly those Gaussians, computed here if not given)."""
+    if ref is None:
+        ref = oracle.project(np.ascontiguousarray(P[:, idx]), len(idx), cam, 32)
     count = _u32(tr.proj.count)[idx]
     np.testing.assert_array_equal(count, ref["count"])
     vis = ref["count"] > 0
@@ -147,7 +140,7 @@ def _check_block(tr, ref, cam, tx0, ty0, nt, backward=True):
     sel = inside[idx]
     assert sel.sum() > 50
     got = moments_to_partials(gs.grad2d_planes(tr.grad2d, tr.n_pad)[:, idx[sel]], ref["conic"][idx[sel]])
-    _grad_close(got, rb["grad2d"][:, sel], what="grad2d (block)")
+    grad_close(got, rb["grad2d"][:, sel], what="grad2d (block)")
 
 
 def _check_fused_sample(tr, P, n, cam, idx):
@@ -169,14 +162,11 @@ def _check_fused_sample(tr, P, n, cam, idx):
     pr, mr, vr = oracle.adam(Ps.astype(np.float64), gref, np.zeros_like(gref), np.zeros_like(gref), lr, 0.9, 0.999,
                              1e-15, 1)
     m = tr.m.cpu().numpy()[:, idx]
-    _grad_close(m / 0.1, mr / 0.1, what="fused m = 0.1 g")
-    p = tr.params.cpu().numpy()[:, idx].astype(np.float64)
-    gscale = np.zeros((59, 1))
-    for a, b in GROUPS_59:
-        gscale[a:b] = np.abs(gref[a:b]).max()
-    defined = np.abs(gref) > 1e-3 * gscale
+    iso = isotropic(P, n)
+    grad_close(m / np.float64(np.float32(0.1)), gref, isotropic_scene=iso, what="fused m = 0.1 g")
+    defined = adam_defined(gref, iso)
     assert defined.mean() > 0.2
-    assert not ((np.abs(p - pr) > 1e-5 * np.abs(pr) + 1e-7) & defined).any()
+    adam_close(tr.params.cpu().numpy()[:, idx], pr, defined)
 
 
 def _densest_block(ref, TX, TY, nt):
@@ -193,59 +183,96 @@ def _densest_block(ref, TX, TY, nt):
     return min(max(0, tx - nt // 2), TX - nt), min(max(0, ty - nt // 2), TY - nt)
 
 
-# ----------------------------------------------------------------------------- 1M, 512x512
+# ----------------------------------------------------------------------------- whole views
 
-def test_iso1m_512_full_parity():
-    cfg = gi.CONFIGS["iso1m_512"]
+def _full_view_parity(name, view, seed):
+    cfg = gi.CONFIGS[name]
     P = gi.scene_for(cfg, device=DEV)
-    n = cfg.n
-    cam = gi.cameras_for(cfg)[5]
+    n, W, H = cfg.n, cfg.width, cfg.height
+    cam = gi.cameras_for(cfg)[view]
+    iso = isotropic(P, n)
+    assert iso
     tr = _trainer_for(P, n, cam)
     tr.forward(cam)
     torch.cuda.synchronize()
     assert tr.check_status() == 0
     ref = oracle.project(P, n, cam, 32)
-    assert _check_projection(tr, P, n, cam, np.arange(n)) > 0.9 * n
-    tl = oracle.tile_lists(ref, cfg.width, cfg.height)
+    assert _check_projection(tr, P, n, cam, np.arange(n), ref) > 0.9 * n
+    # binning: every key, id and range; every gathered record
+    tl = oracle.tile_lists(ref, W, H)
     K = tr.n_isect()
     assert K == tl["K"]
     np.testing.assert_array_equal(tr.bins.keys[:K].cpu().numpy().view(np.uint64), tl["keys"])
-    np.testing.assert_array_equal(_u32(tr.bins.ids)[:K], tl["ids"])
-    rd = oracle.render(ref, cfg.width, cfg.height)
-    np.testing.assert_array_equal(tr.image.cpu().numpy().view(np.uint32), rd["image"].view(np.uint32))
-    np.testing.assert_array_equal(_u32(tr.n_contrib), rd["n_contrib"])
-    target = gi.offset_target(rd["image"], seed=3)
-    rb = oracle.render(ref, cfg.width, cfg.height, target=target)
+    ids = _u32(tr.bins.ids)[:K]
+    np.testing.assert_array_equal(ids, tl["ids"])
+    rg = _u32(tr.bins.ranges)
+    nonempty = tl["ranges"][:, 1] > tl["ranges"][:, 0]
+    np.testing.assert_array_equal(rg[nonempty], tl["ranges"][nonempty])
+    assert np.all(rg[~nonempty] == 0)
+    del tl
+    gathered = tr.proj.rec[tr.bins.ids[:K].to(torch.int64)]
+    assert torch.equal(tr.bins.rec[:K].view(torch.int32), gathered.view(torch.int32))
+    del gathered
+    # compositing: every pixel; the backward: every Gaussian
+    target = gi.uniform_target(seed, W, H)
+    rb = oracle.render(ref, W, H, target=target)
+    np.testing.assert_array_equal(_u32(tr.image), rb["image"].view(np.uint32))
+    np.testing.assert_array_equal(_u32(tr.T_final), rb["T_final"].view(np.uint32))
+    np.testing.assert_array_equal(_u32(tr.n_contrib), rb["n_contrib"])
     gs.render_bwd(n, tr.n_pad, cam, tr.bins, tr.bg, tr.image, torch.from_numpy(target).to(DEV), tr.T_final,
                   tr.n_contrib, tr.grad2d, tr.loss, tr.status)
     torch.cuda.synchronize()
-    _grad_close(moments_to_partials(gs.grad2d_planes(tr.grad2d, n), ref["conic"]), rb["grad2d"], what="grad2d")
-    assert abs(float(tr.loss.item()) - rb["loss"]) <= 1e-5 * rb["loss"]
-    _check_fused_sample(tr, P, n, cam, np.random.default_rng(1).choice(n, 50_000, replace=False))
     assert tr.check_status() == 0
+    assert abs(float(tr.loss.item()) - rb["loss"]) <= 1e-5 * rb["loss"]
+    grad_close(moments_to_partials(gs.grad2d_planes(tr.grad2d, n), ref["conic"]), rb["grad2d"], what="grad2d")
+    # the fused projection backward + Adam (t = 1 from zero moments) of every Gaussian
+    lr = gi.lr_planes()
+    tr.m.zero_()
+    tr.v.zero_()
+    gs.project_bwd_adam(n, tr.params, cam, tr.proj, tr.grad2d, tr.m, tr.v, lr, 0.9, 0.999, 1e-15, 1, tr.status)
+    torch.cuda.synchronize()
+    assert tr.check_status() == 0
+    gref = oracle.project_bwd(P, n, cam, rb["grad2d"], 32)
+    del rb
+    grad_close(tr.m.cpu().numpy()[:, :n] / np.float64(np.float32(0.1)), gref, isotropic_scene=iso,
+               what="fused m = 0.1 g")
+    pr, _, _ = oracle.adam(P[:, :n].astype(np.float64), gref, np.zeros_like(gref), np.zeros_like(gref), lr, 0.9,
+                           0.999, 1e-15, 1)
+    defined = adam_defined(gref, iso)
+    assert defined.mean() > 0.2
+    adam_close(tr.params.cpu().numpy()[:, :n], pr, defined)
+    assert not tr.params[:, n:].any()
 
 
-# ----------------------------------------------------------------------------- 4M, 2048x2048
+def test_iso1m_512_full_parity():
+    """1M Gaussians, 512x512, orbit view 5."""
+    _full_view_parity("iso1m_512", 5, seed=3)
 
-def test_iso4m_2048_sampled_parity():
+
+def test_iso4m_1024_full_parity():
+    """4M Gaussians, 1024x1024 (the config with about 10-40 Gaussians per pixel),
+    orbit view 0."""
+    _full_view_parity("iso4m_1024", 0, seed=4)
+
+
+def test_iso4m_2048_full_parity():
+    """4M Gaussians, 2048x2048: the bench's workload, orbit view 0."""
+    _full_view_parity("iso4m_2048", 0, seed=5)
+
+
+def test_iso4m_2048_sort_properties_late_view():
+    """A second view of the bench's workload (orbit view 300) through the sort's
+    uniqueness properties and a sampled projection."""
     cfg = gi.CONFIGS["iso4m_2048"]
     P = gi.scene_for(cfg, device=DEV)
     n = cfg.n
-    cam = gi.cameras_for(cfg)[0]
+    cam = gi.cameras_for(cfg)[300]
     tr = _trainer_for(P, n, cam)
     tr.forward(cam)
     torch.cuda.synchronize()
     assert tr.check_status() == 0
-    rng = np.random.default_rng(2)
-    _check_projection(tr, P, n, cam, np.sort(rng.choice(n, 40_000, replace=False)))
-    TX, TY = cfg.width // 16, cfg.height // 16
-    _check_sort_properties(tr, n, TX)
-    ref = oracle.project(P, n, cam, 32)
-    tx0, ty0 = _densest_block(ref, TX, TY, 4)
-    _check_block(tr, ref, cam, tx0, ty0, 4)
-    _check_block(tr, ref, cam, TX // 2 - 2, TY // 2 - 2, 4, backward=False)
-    _check_fused_sample(tr, P, n, cam, np.sort(rng.choice(n, 40_000, replace=False)))
-    assert tr.check_status() == 0
+    _check_projection(tr, P, n, cam, np.sort(np.random.default_rng(2).choice(n, 40_000, replace=False)))
+    _check_sort_properties(tr, n, cfg.width // 16)
 
 
 # ----------------------------------------------------------------------------- 18M, 2048x2048
@@ -265,4 +292,6 @@ def test_turb18m_2048_sampled_parity():
     _check_sort_properties(tr, n, TX)
     ref = oracle.project(P, n, cam, 32)
     tx0, ty0 = _densest_block(ref, TX, TY, 3)
-    _check_block(tr, ref, cam, tx0, ty0, 3, backward=False)
+    _check_block(tr, ref, cam, tx0, ty0, 3)
+    _check_fused_sample(tr, P, n, cam, np.sort(rng.choice(n, 40_000, replace=False)))
+    assert tr.check_status() == 0
