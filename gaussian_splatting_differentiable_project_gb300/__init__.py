@@ -13,8 +13,9 @@ Entry points (same names as the C ABI, without the ``gs_`` prefix):
 - the D-SSIM term: ``ssim_fwd``, ``ssim_bwd``;
 - batches and graphs: ``project_bwd_accumulate``, ``project_bwd_adam_tdev``,
   ``step_counter_add``;
-- density control: ``densify_accumulate``, ``densify_plan``, ``densify_apply``,
-  ``opacity_reset``;
+- density control: ``densify_thresholds``, ``densify_accumulate``, ``densify_plan``,
+  ``densify_apply``, ``opacity_reset``;
+- the batch step's Adam hyperparameters: ``batch_hyper``;
 - storage order: ``spatial_order``, ``permute_planes``;
 - sizes and utilities: ``bin_sort_workspace_bytes``, ``densify_workspace_bytes``,
   ``spatial_order_workspace_bytes``, ``bin_sort_noalloc``, ``util_expf``,
@@ -189,6 +190,14 @@ def load(build_if_missing: bool = True):
         lib.gs_status_str.argtypes = [ctypes.c_uint32]
         lib.gs_status_str.restype = ctypes.c_char_p
         lib.gs_version.restype = ctypes.c_char_p
+        D = ctypes.POINTER(ctypes.c_double)
+        lib.gs_batch_hyper.argtypes = [ctypes.c_int32, D, ctypes.c_double, ctypes.c_double, ctypes.c_double, D, D, D,
+                                       D]
+        lib.gs_batch_hyper.restype = st
+        lib.gs_densify_thresholds.argtypes = [ctypes.c_double] * 6 + [ctypes.c_int32, ctypes.POINTER(GsDensifyCfg),
+                                                                      ctypes.POINTER(ctypes.c_float),
+                                                                      ctypes.POINTER(ctypes.c_float)]
+        lib.gs_densify_thresholds.restype = st
         lib.gs_sm_count.argtypes = []
         lib.gs_sm_count.restype = ctypes.c_int32
         _lib = lib
@@ -509,14 +518,30 @@ def step_counter_add(counter, delta: int = 1, stream=None) -> None:
 def densify_thresholds(extent: float, grow_grad2d: float = 2e-4, grow_scale3d: float = 0.01,
                        prune_opa: float = 0.005, prune_scale3d: float = 0.1, split_shrink: float = 1.6,
                        prune_big: bool = False):
-    """The density-control thresholds of the cited 3DGS method, formed in fp64 and
-    rounded to fp32 once: (the plan's configuration, ln split_shrink, the opacity-reset
-    logit of 2 x prune_opa)."""
-    import math
-    cfg = GsDensifyCfg(float(grow_grad2d), math.log(prune_opa / (1.0 - prune_opa)),
-                       math.log(grow_scale3d * extent), math.log(prune_scale3d * extent), int(bool(prune_big)))
-    reset = 2.0 * prune_opa
-    return cfg, float(np.float32(math.log(split_shrink))), float(np.float32(math.log(reset / (1.0 - reset))))
+    """The density-control thresholds (gs_densify_thresholds): (the plan's
+    configuration, ln split_shrink, the opacity-reset logit of 2 x prune_opa)."""
+    cfg = GsDensifyCfg()
+    shrink, reset = ctypes.c_float(), ctypes.c_float()
+    _check(load().gs_densify_thresholds(float(extent), float(grow_grad2d), float(grow_scale3d), float(prune_opa),
+                                        float(prune_scale3d), float(split_shrink), int(bool(prune_big)),
+                                        ctypes.byref(cfg), ctypes.byref(shrink), ctypes.byref(reset)),
+           "gs_densify_thresholds")
+    return cfg, float(shrink.value), float(reset.value)
+
+
+def batch_hyper(batch: int, lr_plane, beta1: float, beta2: float, eps: float):
+    """Adam hyperparameters of a step over ``batch`` views (gs_batch_hyper): (per-plane
+    learning rates, beta1, beta2, eps), fp64."""
+    lr = np.ascontiguousarray(np.asarray(lr_plane, np.float64).reshape(-1))
+    if lr.size != N_PLANES:
+        raise GsError(f"lr_plane: needs {N_PLANES} learning rates, got {lr.size}")
+    out = np.empty(N_PLANES, np.float64)
+    b1, b2, e = ctypes.c_double(), ctypes.c_double(), ctypes.c_double()
+    D = ctypes.POINTER(ctypes.c_double)
+    _check(load().gs_batch_hyper(int(batch), lr.ctypes.data_as(D), float(beta1), float(beta2), float(eps),
+                                 out.ctypes.data_as(D), ctypes.byref(b1), ctypes.byref(b2), ctypes.byref(e)),
+           "gs_batch_hyper")
+    return out, b1.value, b2.value, e.value
 
 
 def densify_accumulate(n: int, n_pad: int, proj: "ProjBuffers", grad2d, width: int, height: int, grad_acc, vis_cnt,

@@ -6,12 +6,18 @@
 
 // ---------------------------------------------------------------------------
 // gs_bin_sort_noalloc: the same binning for callers that may not allocate device
-// memory, e.g. code running inside a host callback or a real-time loop whose
-// memory is reserved up front, or a host that forbids device allocation after
-// start-up.  The sort's scratch lives in the file-scope array below, which every
-// GPU that uses this entry point holds until the process exits.  It is the only
-// object of this translation unit, so under lazy module loading (the CUDA default)
-// the module that carries it is loaded by the first call, not with the kernels.  Its size is the workspace of
+// memory, e.g. a real-time loop whose memory is all reserved at start-up, or an
+// application that embeds the library while its own allocator owns the GPU.  The
+// sort's scratch lives in the file-scope array below, which every GPU that loads
+// this module holds until the process exits.  It is the only object of this
+// translation unit.  Under lazy module loading (the CUDA default) the module that
+// carries it is loaded by the first call on a device, and that load is itself a
+// device allocation; with CUDA_MODULE_LOADING=EAGER every process that loads the
+// library holds the array on each GPU it uses.  Either way a caller makes one call
+// during start-up, before it stops allocating and before any stream capture.  The
+// array's device address is looked up once per device and kept: that assumes the
+// device's primary context, with no cudaDeviceReset after the first call (a reset
+// would leave the kept address stale).  Its size is the workspace of
 // n = GS_NOALLOC_MAX_N Gaussians, capacity_K = GS_NOALLOC_MAX_K intersections and
 // GS_NOALLOC_MAX_TILES tiles, which covers every smaller problem.
 namespace gs {

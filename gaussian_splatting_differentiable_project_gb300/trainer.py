@@ -12,24 +12,11 @@ from __future__ import annotations
 
 import numpy as np
 
-import math
-
-from . import (BinBuffers, ProjBuffers, GRAD2D_STRIDE, SSIM_MAPS, adam_step, bin_sort, densify_accumulate,
+from . import (BinBuffers, ProjBuffers, GRAD2D_STRIDE, SSIM_MAPS, adam_step, batch_hyper, bin_sort, densify_accumulate,
                densify_apply, densify_plan, densify_thresholds, densify_workspace_bytes, opacity_reset,
                permute_planes, project, project_bwd, project_bwd_accumulate, project_bwd_adam,
                project_bwd_adam_tdev, render_bwd, render_fwd, spatial_order, spatial_order_workspace_bytes,
                ssim_bwd, ssim_fwd, status_str, step_counter_add)
-
-
-def batch_adam_hyper(batch: int, lr_plane, beta1: float, beta2: float, eps: float):
-    """Adam hyperparameters of a step over ``batch`` views ("Scaling 3D Gaussian
-    Splatting with Distributed Compute", batch-size section): learning rates scale
-    with sqrt(batch), epsilon with 1 / sqrt(batch), and the momentum coefficients
-    follow the linearisation 1 - batch (1 - beta) of beta^batch, held at zero where
-    it would go negative (beta1 = 0.9 reaches zero at batch 10)."""
-    root = math.sqrt(batch)
-    lr = np.asarray(lr_plane, np.float64) * root
-    return lr, max(0.0, 1.0 - batch * (1.0 - beta1)), max(0.0, 1.0 - batch * (1.0 - beta2)), eps / root
 
 
 class HostTargets:
@@ -172,7 +159,7 @@ class Trainer:
             self.batch_losses = torch.zeros(B, dtype=torch.float32, device=self.params.device)
             if self.dssim > 0.0:
                 self.batch_ssim = torch.zeros(B, dtype=torch.float32, device=self.params.device)
-        lr_b, b1, b2, eps_b = batch_adam_hyper(B, self.lr_plane, self.beta1, self.beta2, self.eps)
+        lr_b, b1, b2, eps_b = batch_hyper(B, self.lr_plane, self.beta1, self.beta2, self.eps)
         self.t += 1
         for k, (cam, target) in enumerate(zip(cams, targets)):
             self.forward(cam, stream)

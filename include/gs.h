@@ -311,6 +311,21 @@ gs_status gs_adam_step(gs_dims dims, float* params, const float* grads, float* m
                        cudaStream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * gs_batch_hyper -- the Adam hyperparameters of a step over `batch` views ("Scaling 3D
+ * Gaussian Splatting with Distributed Compute", batch-size section): learning rates
+ * times sqrt(batch), epsilon divided by sqrt(batch), and each momentum coefficient
+ * 1 - batch (1 - beta), the linearisation of beta^batch (the page's formula did not
+ * survive extraction; under this reading beta1 = 0.9 reaches zero at batch 10, as the
+ * page states), held at zero beyond.  All in fp64; batch 1 returns the inputs.
+ * Host-only (no device work).
+ *   lr_plane: 59 doubles (host, read); lr_out: 59 doubles (host, write); the three
+ *   scalars written through their pointers.
+ * Errors: GS_ERR_INVALID_ARG for batch < 1, null pointers, betas outside [0, 1), a
+ * negative or non-finite eps or a non-finite learning rate. */
+gs_status gs_batch_hyper(int32_t batch, const double* lr_plane, double beta1, double beta2, double eps,
+                         double* lr_out, double* beta1_out, double* beta2_out, double* eps_out);
+
+/* ---------------------------------------------------------------------------
  * gs_project_bwd_adam -- gs_project_bwd followed by gs_adam_step in one pass, without
  * materialising the 59 gradient planes.  Same arithmetic as the two calls (each
  * thread derives its Gaussian's gradients in registers and applies the Adam element
@@ -354,13 +369,14 @@ gs_status gs_step_counter_add(int64_t* counter, int64_t delta, cudaStream_t stre
  * Compute": adaptive density control clones, splits and prunes Gaussians every
  * hundred steps (memory-wall section), from 2D position gradients accumulated over the
  * steps (step walkthrough), starting at step 500 (trace section).  Thresholds and
- * the split rule are the cited 3DGS method's; the caller forms each threshold in
- * fp64 and the kernels compare in fp32:
+ * the split rule are the cited 3DGS method's; each threshold is formed in fp64
+ * (gs_densify_thresholds) and the kernels compare in fp32:
  *   grow if acc / max(cnt, 1) > grad_threshold (2e-4, the NDC-scaled 2D gradient);
  *   clone if the largest log-scale <= log_grow_scale (ln(0.01 x scene extent)), else
  *   split into two children at mu + R(q) diag(exp s) xi_k with log-scales - log_shrink
  *   (ln 1.6); prune (first) if the opacity logit < logit_prune (ln(0.005 / 0.995)) or,
- *   with prune_big, the largest log-scale > log_prune_scale (ln(0.1 x extent)). */
+ *   with prune_big, the largest log-scale > log_prune_scale (ln(0.1 x extent)).
+ * gs_densify_thresholds (below) forms them. */
 typedef struct gs_densify_cfg {
   float grad_threshold;
   float logit_prune;
@@ -373,6 +389,18 @@ typedef struct gs_densify_cfg {
 #define GS_DENSIFY_KEEP 1
 #define GS_DENSIFY_CLONE 2
 #define GS_DENSIFY_SPLIT 3
+
+/* gs_densify_thresholds -- the configuration above, the split's log_shrink and the
+ * opacity reset's logit_max, formed in fp64 from the method's settings and rounded to
+ * fp32 once:  grad_threshold = grow_grad2d (2e-4);  logit_prune = logit(prune_opa)
+ * (prune_opa = 0.005);  log_grow_scale = ln(grow_scale3d x extent) (0.01);
+ * log_prune_scale = ln(prune_scale3d x extent) (0.1);  log_shrink = ln(split_shrink)
+ * (1.6);  logit_reset = logit(2 prune_opa).  Host-only (no device work).
+ * Errors: GS_ERR_INVALID_ARG for null outputs, a non-positive or non-finite extent,
+ * scale factor or shrink, or prune_opa outside (0, 0.5). */
+gs_status gs_densify_thresholds(double extent, double grow_grad2d, double grow_scale3d, double prune_opa,
+                                double prune_scale3d, double split_shrink, int32_t prune_big, gs_densify_cfg* cfg,
+                                float* log_shrink, float* logit_reset);
 
 /* gs_densify_accumulate -- for each Gaussian i < n with count[i] > 0 (visible in
  * this view): grad_acc[i] += |(d mx W/2, d my H/2)|, vis_cnt[i] += 1, with the mean
@@ -421,19 +449,23 @@ gs_status gs_opacity_reset(gs_dims dims, float* params, float* m, float* v, floa
 
 /* ---------------------------------------------------------------------------
  * gs_bin_sort_noalloc -- gs_bin_sort for callers that must not allocate device
- * memory (for example code that runs where cudaMalloc is not allowed or not
- * wanted after start-up: host callbacks, a render loop with all memory reserved
- * in advance, embedders whose allocator owns the GPU).  The paper has no
+ * memory (for example a render loop whose memory is all reserved in advance, or an
+ * embedding application whose own allocator owns the GPU).  The paper has no
  * counterpart; this is a library convenience.  Results are identical to
  * gs_bin_sort's.
- *   Scratch: a fixed array inside the library (68.5 MiB), held by every GPU
- *   that calls this entry point until the process exits.  It is used in place of the
- *   workspace argument; the caller still passes proj and bins.
+ *   Scratch: a fixed array inside the library (68.5 MiB), used in place of the
+ *   workspace argument; the caller still passes proj and bins.  Under lazy module
+ *   loading (the CUDA default) the array is placed on a device by the first call
+ *   there, and that placement is itself a device allocation; with
+ *   CUDA_MODULE_LOADING=EAGER every process that loads the library holds it on
+ *   each GPU it uses.  Either way it stays until the process exits.
  *   Limits: n <= GS_NOALLOC_MAX_N, capacity_K <= GS_NOALLOC_MAX_K, at most
  *   GS_NOALLOC_MAX_TILES tiles; larger sizes return GS_ERR_SCRATCH_LIMIT and
  *   nothing is enqueued.
- *   The first call on a device looks up the array's device address (with that
- *   device current); make that first call before any stream capture.
+ *   Set-up: the first call on a device looks up the array's device address (with
+ *   that device current) and keeps it.  Make one call during start-up, before the
+ *   caller stops allocating and before any stream capture.  The kept address
+ *   assumes the device's primary context and no cudaDeviceReset after that call.
  *   Every call on a device shares the one array: calls whose kernels overlap on
  *   the GPU (other streams, other host threads) race and corrupt each other.
  *   Serialise them.  Each call clears what must start at zero itself.

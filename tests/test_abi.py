@@ -238,7 +238,10 @@ def test_binding_checks_buffer_types_and_sizes(monkeypatch):
     gs.opacity_reset(n, params, params, params, -4.6)
     gs.spatial_order(n, params, i32(n), torch.zeros(16, dtype=torch.uint8), st)
     gs.util_expf(torch.zeros(8), torch.zeros(8))
-    assert len(calls) == 20
+    gs.render_fwd_counted(cam, bins, (0, 0, 0), img, T, nc, i32(W * H), st)
+    gs.batch_hyper(3, lr, 0.9, 0.999, 1e-15)
+    # the calls above plus the one inside densify_thresholds
+    assert len(calls) == 23 and calls.count("gs_densify_thresholds") == 1
 
     refused("params: expected fp32", gs.project, n, params.double(), cam, proj, st)
     refused("params: needs", gs.project, n, params[:58].contiguous(), cam, proj, st)
@@ -247,6 +250,8 @@ def test_binding_checks_buffer_types_and_sizes(monkeypatch):
     refused("tiles", gs.bin_sort, n, n_pad, proj, dict(cam, width=2 * W), bins, st)
     refused("image: needs", gs.render_fwd, cam, bins, (0, 0, 0), torch.zeros((3, H, W - 1)), T, nc, st)
     refused("n_contrib: expected", gs.render_fwd, cam, bins, (0, 0, 0), img, T, nc.float(), st)
+    refused("n_used: needs", gs.render_fwd_counted, cam, bins, (0, 0, 0), img, T, nc, i32(W * H - 1), st)
+    refused("lr_plane", gs.batch_hyper, 2, lr[:-1], 0.9, 0.999, 1e-15)
     refused("grad2d: needs", gs.render_bwd, n, n_pad, cam, bins, (0, 0, 0), img, img, T, nc,
             torch.zeros((n_pad, gs.N_GRAD2D)), torch.zeros(1), st)
     refused("dLdC_extra: needs", gs.render_bwd, n, n_pad, cam, bins, (0, 0, 0), img, img, T, nc, g2,

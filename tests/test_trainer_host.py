@@ -30,11 +30,13 @@ def test_save_load_round_trip(tmp_path):
 
 
 def test_batch_hyperparameters_on_the_host():
-    """The trainer's batch-step Adam hyperparameters follow the batch-size section of
+    """The library's batch-step Adam hyperparameters (gs_batch_hyper, a host call) follow
+    the batch-size section of
     "Scaling 3D Gaussian Splatting with Distributed Compute": learning rates times
     sqrt(B), epsilon over sqrt(B), beta -> 1 - B (1 - beta) with beta1 = 0.9 reaching
-    zero at B = 10 and held there beyond; one view leaves everything unchanged."""
-    from gaussian_splatting_differentiable_project_gb300.trainer import batch_adam_hyper
+    zero at B = 10 and held there beyond; one view leaves everything unchanged.  The
+    oracle's own statement of the rule agrees at every batch size."""
+    from gaussian_splatting_differentiable_project_gb300 import batch_hyper as batch_adam_hyper
     lr = gi.lr_planes()
     l1, b1, b2, e1 = batch_adam_hyper(1, lr, 0.9, 0.999, 1e-15)
     np.testing.assert_array_equal(l1, np.asarray(lr, np.float64))
@@ -46,11 +48,21 @@ def test_batch_hyperparameters_on_the_host():
     assert abs(b1) < 1e-15
     _, b1, b2, _ = batch_adam_hyper(16, lr, 0.9, 0.999, 1e-15)
     assert b1 == 0.0 and abs(b2 - 0.984) < 1e-15
+    import oracle
+    for B in (1, 2, 3, 7, 10, 11, 64):
+        got = batch_adam_hyper(B, lr, 0.9, 0.999, 1e-15)
+        want = oracle.batch_hyper(B, lr, 0.9, 0.999, 1e-15)
+        np.testing.assert_allclose(got[0], want[0], rtol=1e-15)
+        for a, b in zip(got[1:], want[1:]):
+            assert abs(a - b) <= 1e-15 * max(1.0, abs(b)), (B, got[1:], want[1:])
+    import gaussian_splatting_differentiable_project_gb300 as gs
+    with pytest.raises(gs.GsError):
+        batch_adam_hyper(0, lr, 0.9, 0.999, 1e-15)
 
 
 def test_density_thresholds_on_the_host():
-    """The density-control thresholds the binding hands the library, formed in fp64 and
-    rounded to fp32 once: grow above a mean 2D gradient of 2e-4; clone at most 0.01 x
+    """The density-control thresholds (gs_densify_thresholds, a host call), formed in
+    fp64 and rounded to fp32 once: grow above a mean 2D gradient of 2e-4; clone at most 0.01 x
     the extent in scale (compared as a log-scale); prune below opacity 0.005 (as a
     logit) or, optionally, above 0.1 x the extent; split children shrink by 1.6 (as a
     log); the opacity reset clamps to twice the prune opacity (as a logit)."""
@@ -68,3 +80,11 @@ def test_density_thresholds_on_the_host():
     assert logit_reset == f32(math.log(0.01 / 0.99))
     # the logit threshold decides exactly where the sigmoid crosses 0.005
     assert 1 / (1 + math.exp(-f32(cfg.logit_prune))) == pytest.approx(0.005, rel=1e-6)
+    # the oracle's own thresholds agree
+    import oracle
+    th = oracle.densify.thresholds(extent=extent)
+    for k in ("logit_prune", "log_grow_scale", "log_prune_scale"):
+        assert f32(getattr(cfg, k)) == f32(th[k]), k
+    assert log_shrink == f32(th["log_shrink"]) and logit_reset == f32(th["logit_reset"])
+    with pytest.raises(gs.GsError):
+        gs.densify_thresholds(-1.0)

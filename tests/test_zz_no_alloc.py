@@ -2,8 +2,8 @@
 device memory.
 
 Some callers cannot call cudaMalloc: code that runs where allocation is forbidden or
-would stall (host callbacks, a real-time loop whose memory is all reserved at start-up,
-an embedding application whose own allocator owns the GPU).  This entry point takes
+would stall (a real-time loop whose memory is all reserved at start-up, an embedding
+application whose own allocator owns the GPU).  This entry point takes
 its sort scratch from a fixed array inside the library instead of a caller-provided
 workspace.  Its results must equal gs_bin_sort's bit for bit (sort keys, ids, tile
 ranges and gathered records are integer/index work), on consecutive calls that reuse
