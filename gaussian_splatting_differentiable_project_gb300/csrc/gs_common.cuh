@@ -31,11 +31,18 @@ __device__ __forceinline__ void raise_status(uint32_t* dev_status, uint32_t bits
 }
 
 // ------------------------------------------------------------------ exponential
-// Cody-Waite: x = k ln2 + r, ln2 split into a 16-bit high part and the rest,
-// |r| <= ln2/2; e^r by its degree-7 Taylor polynomial in Horner form; times 2^k
-// built in the exponent field.  Valid for x in [-87, 88] (all results normal).
+// Cody-Waite: x = k ln2 + r, ln2 split into a 16-bit high part and the rest; e^r by
+// its degree-7 Taylor polynomial in Horner form; times 2^k in the exponent field.
+// k, the integer nearest to x log2(e), comes from one FMA against 1.5 * 2^23 (whose
+// ulp is 1, so the sum is rounded to an integer from the exact product) and one exact
+// subtraction: no float-to-integer conversions.  The low bits of that sum hold k
+// (1.5 * 2^23's low nine bits are zero), so shifting its bits up by 23 gives k << 23,
+// which added to the polynomial's bits scales it by 2^k exactly while the result is
+// normal: x in [-87, 88].
 __device__ __forceinline__ float gs_expf_core(float x) {
-  const float kf = rintf(__fmul_rn(x, 1.44269504088896341f));
+  const float kRound = 12582912.0f;  // 1.5 * 2^23
+  const float s = __fmaf_rn(x, 1.44269504088896341f, kRound);
+  const float kf = __fsub_rn(s, kRound);
   float r = __fmaf_rn(-kf, 0.693145751953125f, x);
   r = __fmaf_rn(-kf, 1.4286068203094173e-06f, r);
   float p = 1.0f / 5040.0f;
@@ -46,8 +53,7 @@ __device__ __forceinline__ float gs_expf_core(float x) {
   p = __fmaf_rn(p, r, 0.5f);
   p = __fmaf_rn(p, r, 1.0f);
   p = __fmaf_rn(p, r, 1.0f);
-  const int k = __float2int_rn(kf);
-  return __fmul_rn(p, __int_as_float((k + 127) << 23));
+  return __uint_as_float(__float_as_uint(p) + (__float_as_uint(s) << 23));
 }
 
 // Whole real line: NaN passes through, above 88 gives +inf, below -87 gives 0.

@@ -107,18 +107,23 @@ void parallel_for(int64_t n, const std::function<void(int64_t, int64_t)>& fn) {
 
 // --------------------------------------------------------------------------------
 // gs_expf: single-precision exponential from Cody and Waite's argument reduction
-// (x = k ln2 + r with ln2 split into a short high part and a low part, |r| <= ln2/2)
-// and the degree-7 Taylor polynomial of e^r in Horner form, scaled by 2^k through
-// the exponent field.  Truncation error r^8/8! <= 5.2e-9, below half an fp32 ulp.
-// Defined on [-87, 88] (results stay normal); below that it returns 0, above +inf.
+// (x = k ln2 + r with ln2 split into a short high part and a low part) and the
+// degree-7 Taylor polynomial of e^r in Horner form, scaled by 2^k through the
+// exponent field.  k is the integer nearest to x log2(e), rounded once from the exact
+// product: fma(x, log2 e, 1.5 2^23) lands on an integer (its ulp is 1), and
+// subtracting 1.5 2^23 again is exact.  Then |r| <= ln2/2 plus a rounding, and the
+// truncation error r^8/8! <= 5.3e-9 stays below half an fp32 ulp.  Defined on
+// [-87, 88], where every result is a normal number, so adding k to the exponent field
+// is the exact product with 2^k; below that it returns 0, above +inf.
 float gs_expf(float x) {
   if (!(x == x)) return x;
   if (x > 88.0f) return std::numeric_limits<float>::infinity();
   if (x < -87.0f) return 0.0f;
   const float kLog2e = 1.44269504088896341f;
+  const float kRound = 12582912.0f;               // 1.5 * 2^23
   const float kLn2Hi = 0.693145751953125f;       // 16 significant bits
   const float kLn2Lo = 1.4286068203094173e-06f;  // ln2 - kLn2Hi
-  float kf = std::rint(x * kLog2e);
+  const float kf = std::fma(x, kLog2e, kRound) - kRound;
   float r = std::fma(-kf, kLn2Hi, x);
   r = std::fma(-kf, kLn2Lo, r);
   float p = 1.0f / 5040.0f;
@@ -129,11 +134,13 @@ float gs_expf(float x) {
   p = std::fma(p, r, 0.5f);
   p = std::fma(p, r, 1.0f);
   p = std::fma(p, r, 1.0f);
-  int32_t k = int32_t(kf);
-  uint32_t bits = uint32_t(k + 127) << 23;  // 2^k, k in [-126, 127]
-  float two_k;
-  std::memcpy(&two_k, &bits, 4);
-  return p * two_k;
+  const int32_t k = int32_t(kf);
+  uint32_t bits;
+  std::memcpy(&bits, &p, 4);
+  bits += uint32_t(k) << 23;  // k in [-126, 127]; the result stays normal
+  float out;
+  std::memcpy(&out, &bits, 4);
+  return out;
 }
 
 template <class S> S ex(S x);

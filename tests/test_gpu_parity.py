@@ -16,7 +16,7 @@ import pytest
 import gs_inputs as gi
 import oracle
 from _grad2d import moments_to_partials
-from _tol import adam_close, adam_defined, grad_close, isotropic
+from _tol import DSSIM_FLOOR, adam_close, adam_defined, grad_close, isotropic
 
 pytestmark = pytest.mark.gpu
 
@@ -44,8 +44,8 @@ def _partials(tr, n, conic):
     return moments_to_partials(gs.grad2d_planes(tr.grad2d, n), conic[:n])
 
 
-def _grad_close(got, ref, what="", iso=False):
-    return grad_close(got, ref, isotropic_scene=iso, what=what)
+def _grad_close(got, ref, what="", iso=False, **kw):
+    return grad_close(got, ref, isotropic_scene=iso, what=what, **kw)
 
 
 def _scene(name, n=None, seed=0):
@@ -456,11 +456,12 @@ def test_whole_step_with_dssim_end_to_end(case, fused):
     assert abs(float(tr.ssim_val.item()) - ref["render"]["ssim"]) <= 1e-5
     _grad_close(_partials(tr, n, case["ref_proj"]["conic"]), ref["render"]["grad2d"], what="grad2d")
     gref = ref["grads"][:, :n]
+    # the parameter gradients inherit the SSIM image gradient's fp32 error (tests/_tol.py)
     if fused:
         _grad_close(tr.m.cpu().numpy()[:, :n] / np.float64(np.float32(0.1)), gref, what="fused m = 0.1 g",
-                    iso=case["iso"])
+                    iso=case["iso"], floor=DSSIM_FLOOR)
     else:
-        _grad_close(tr.grads.cpu().numpy()[:, :n], gref, what="param grads", iso=case["iso"])
+        _grad_close(tr.grads.cpu().numpy()[:, :n], gref, what="param grads", iso=case["iso"], floor=DSSIM_FLOOR)
     defined = adam_defined(gref, case["iso"])
     assert defined.mean() > 0.2
     adam_close(tr.params.cpu().numpy()[:, :n], ref["params"][:, :n], defined)
