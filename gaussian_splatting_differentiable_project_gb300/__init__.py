@@ -132,14 +132,17 @@ def load(build_if_missing: bool = True):
         lib.gs_bin_sort_noalloc.argtypes = [GsDims, ctypes.POINTER(GsProj), ctypes.POINTER(GsCamera),
                                             ctypes.c_uint32, GsBins, P, P]
         lib.gs_bin_sort_noalloc.restype = st
+        lib.gs_render_cmask_bytes.argtypes = [ctypes.c_uint32, ctypes.c_int32, ctypes.c_int32]
+        lib.gs_render_cmask_bytes.restype = ctypes.c_size_t
         lib.gs_render_fwd.argtypes = [ctypes.POINTER(GsCamera), ctypes.POINTER(GsBins), ctypes.c_uint32,
-                                      ctypes.POINTER(ctypes.c_float), P, P, P, P, P]
+                                      ctypes.POINTER(ctypes.c_float), P, P, P, P, ctypes.c_size_t, P, P]
         lib.gs_render_fwd.restype = st
         lib.gs_render_fwd_counted.argtypes = [ctypes.POINTER(GsCamera), ctypes.POINTER(GsBins), ctypes.c_uint32,
-                                              ctypes.POINTER(ctypes.c_float), P, P, P, P, P, P]
+                                              ctypes.POINTER(ctypes.c_float), P, P, P, P, P, ctypes.c_size_t, P, P]
         lib.gs_render_fwd_counted.restype = st
         lib.gs_render_bwd.argtypes = [GsDims, ctypes.POINTER(GsCamera), ctypes.POINTER(GsBins), ctypes.c_uint32,
-                                      ctypes.POINTER(ctypes.c_float), P, P, P, P, ctypes.c_float, P, P, P, P, P]
+                                      ctypes.POINTER(ctypes.c_float), P, P, P, P, P, ctypes.c_size_t, ctypes.c_float,
+                                      P, P, P, P, P]
         lib.gs_render_bwd.restype = st
         lib.gs_project_bwd.argtypes = [GsDims, P, ctypes.POINTER(GsCamera), ctypes.POINTER(GsProj), P, P, P, P]
         lib.gs_project_bwd.restype = st
@@ -324,6 +327,10 @@ class BinBuffers:
         ws = bin_sort_workspace_bytes(n, capacity, width, height)
         self.workspace = torch.empty(ws + 256, dtype=torch.uint8, device=device)
         self.ws_bytes = ws
+        # the forward's composited-entry masks for this capacity and tile grid (written by
+        # render_fwd, read by render_bwd)
+        self.cmask_bytes = render_cmask_bytes(capacity, width, height)
+        self.cmask = torch.empty(self.cmask_bytes // 4, dtype=torch.int32, device=device)
 
     def ws_ptr(self) -> int:
         p = self.workspace.data_ptr()
@@ -346,6 +353,15 @@ def project(n: int, params, cam: dict, proj: ProjBuffers, dev_status, stream=Non
 
 def bin_sort_workspace_bytes(n: int, capacity: int, width: int, height: int) -> int:
     return int(load().gs_bin_sort_workspace_bytes(dims(n, max(256, n)), int(capacity), int(width), int(height)))
+
+
+def render_cmask_bytes(capacity: int, width: int, height: int) -> int:
+    return int(load().gs_render_cmask_bytes(int(capacity), int(width), int(height)))
+
+
+def _check_cmask(bins, cc) -> ctypes.c_void_p:
+    need = render_cmask_bytes(bins.capacity, cc.width, cc.height)
+    return _buf(bins.cmask, need // 4, "i32", "bins.cmask")
 
 
 def bin_sort(n: int, n_pad: int, proj: ProjBuffers, cam: dict, bins: BinBuffers, dev_status, stream=None) -> None:
@@ -387,10 +403,11 @@ def render_fwd(cam: dict, bins: BinBuffers, bg, image, T_final, n_contrib, dev_s
     _check_bins(bins, cc)
     bc = bins.c()
     P = cc.width * cc.height
+    cm = _check_cmask(bins, cc)
     _check(load().gs_render_fwd(ctypes.byref(cc), ctypes.byref(bc), bins.capacity, _bg(bg),
                                 _buf(image, 3 * P, "f32", "image"), _buf(T_final, P, "f32", "T_final"),
-                                _buf(n_contrib, P, "i32", "n_contrib"), _buf(dev_status, 1, "i32", "dev_status"),
-                                _stream(stream)), "gs_render_fwd")
+                                _buf(n_contrib, P, "i32", "n_contrib"), cm, bins.cmask_bytes,
+                                _buf(dev_status, 1, "i32", "dev_status"), _stream(stream)), "gs_render_fwd")
 
 
 def render_fwd_counted(cam: dict, bins: BinBuffers, bg, image, T_final, n_contrib, n_used, dev_status,
@@ -400,11 +417,12 @@ def render_fwd_counted(cam: dict, bins: BinBuffers, bg, image, T_final, n_contri
     _check_bins(bins, cc)
     bc = bins.c()
     P = cc.width * cc.height
+    cm = _check_cmask(bins, cc)
     _check(load().gs_render_fwd_counted(ctypes.byref(cc), ctypes.byref(bc), bins.capacity, _bg(bg),
                                         _buf(image, 3 * P, "f32", "image"), _buf(T_final, P, "f32", "T_final"),
                                         _buf(n_contrib, P, "i32", "n_contrib"), _buf(n_used, P, "i32", "n_used"),
-                                        _buf(dev_status, 1, "i32", "dev_status"), _stream(stream)),
-           "gs_render_fwd_counted")
+                                        cm, bins.cmask_bytes, _buf(dev_status, 1, "i32", "dev_status"),
+                                        _stream(stream)), "gs_render_fwd_counted")
 
 
 def render_bwd(n: int, n_pad: int, cam: dict, bins: BinBuffers, bg, image, target, T_final, n_contrib, grad2d,
@@ -414,10 +432,12 @@ def render_bwd(n: int, n_pad: int, cam: dict, bins: BinBuffers, bg, image, targe
     bc = bins.c()
     P = cc.width * cc.height
     extra = _buf(dLdC_extra, 3 * P, "f32", "dLdC_extra") if dLdC_extra is not None else None
+    cm = _check_cmask(bins, cc)
     _check(load().gs_render_bwd(dims(n, n_pad), ctypes.byref(cc), ctypes.byref(bc), bins.capacity, _bg(bg),
                                 _buf(image, 3 * P, "f32", "image"), _buf(target, 3 * P, "f32", "target"),
                                 _buf(T_final, P, "f32", "T_final"), _buf(n_contrib, P, "i32", "n_contrib"),
-                                float(l1_weight), extra, _planes(grad2d, n_pad, "grad2d", GRAD2D_STRIDE),
+                                cm, bins.cmask_bytes, float(l1_weight), extra,
+                                _planes(grad2d, n_pad, "grad2d", GRAD2D_STRIDE),
                                 _buf(loss, 1, "f32", "loss"), _buf(dev_status, 1, "i32", "dev_status"),
                                 _stream(stream)), "gs_render_bwd")
 

@@ -31,6 +31,21 @@ __device__ __forceinline__ void pixel_of_thread(int TX, int& px, int& py) {
   py = ty * kTile + (q >> 1) * 8 + warp * 4 + (lane >> 3);
 }
 
+// ------------------------------------------------------------------ composited-entry masks
+// The forward records, for every 8x4 block of a tile and every 32-entry chunk of the
+// tile's list that the block's warp walks, each pixel's 32-bit mask of the entries it
+// composited (bit i: list position 32 c + i of chunk c, counted from the tile's first
+// entry).  The backward walks only those entries.  Chunk c of the tile whose list
+// starts at `start` is stored at chunk slot (start >> 5) + tile + c: consecutive tiles'
+// slots never overlap (the next list starts n entries later, and ceil(n / 32) <=
+// floor(n / 32) + 1), and every slot is below capacity_K / 32 + tiles + 1.
+constexpr int kBlocksPerTile = 8;  // 8x4 blocks of a 16x16 tile
+
+__device__ __forceinline__ size_t cmask_index(uint32_t start, int tile, uint32_t chunk_pos, int block, int lane) {
+  const size_t slot = size_t(start >> 5) + size_t(tile) + size_t(chunk_pos >> 5);
+  return (slot * kBlocksPerTile + size_t(block)) * 32 + size_t(lane);
+}
+
 // The backward runs one warp (one 8x4 block) per CTA, eight CTAs per tile: a warp whose
 // pixels need fewer entries than its neighbour's then finishes and frees its slot,
 // instead of waiting at every batch barrier for the other warp of a two-warp CTA

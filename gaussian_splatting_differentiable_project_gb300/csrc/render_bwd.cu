@@ -2,19 +2,21 @@
 //
 // One warp per CTA, one 8x4 block of a 16x16 tile (eight CTAs per tile), one thread per
 // pixel, the tile's records staged in reverse batches by cp.async.bulk (as in the
-// forward).  Each pixel walks its composited
-// entries back to front, recovering the transmittance before each entry by
-// division by (1 - alpha) and carrying the normalised colour of everything
-// behind it.  Per entry each lane holds nine partials: the opacity and colour
-// partials, and for the mean and the conic the five moments (q dx, q dy, q dx^2,
-// q dx dy, q dy^2) of q = dL/dpower.  The conic is the Gaussian's own, so the
-// projection backward applies it once to the summed moments instead of each lane
-// applying it per entry (10 fewer instructions per entry, 6% of the kernel).  A warp with at most
-// kDirectLanes contributing lanes adds them lane by lane with vector atomics; a
-// fuller warp reduces them with a shuffle reduce-scatter (14 shuffles instead of 45
-// for nine butterflies) and nine lanes add the sums in one atomic instruction.  Both
-// land in the Gaussian's interleaved 12-float slot of grad2d (two 32-byte sectors
-// instead of nine planes' lines).
+// forward).  The warp walks back to front only the entries that at least one of its
+// pixels composited, as the forward's per-chunk masks record them (the union of the
+// block's masks), so entries that every pixel skipped cost nothing and no pixel tests
+// whether an entry is in range.  At each entry a pixel that composited it recomputes
+// alpha in the forward's fp32 sequence (the same value and the same clamp decision),
+// recovers the transmittance before the entry by division by (1 - alpha) and carries
+// the normalised colour of everything behind it.  Its nine partials are the opacity and
+// colour partials and, for the mean and the conic, the five moments (q dx, q dy,
+// q dx^2, q dx dy, q dy^2) of q = dL/dpower; the conic is the Gaussian's own, so the
+// projection backward applies it once to the summed moments (10 fewer instructions per
+// entry).  A warp with at most kDirectLanes contributing lanes adds them lane by lane
+// with vector atomics; a fuller warp reduces them with a shuffle reduce-scatter (14
+// shuffles instead of 45 for nine butterflies) and nine lanes add the sums in one
+// atomic instruction.  Both land in the Gaussian's interleaved 12-float slot of grad2d
+// (two 32-byte sectors instead of nine planes' lines).
 #include "api_util.h"
 #include "raster_common.cuh"
 
@@ -67,21 +69,20 @@ __global__ void __launch_bounds__(kBwdThreads)
     k_render_bwd(const Rec* __restrict__ srec, const uint2* __restrict__ ranges, const uint32_t* __restrict__ n_isect,
                  uint32_t cap, int W, int H, int TX, float bg0, float bg1, float bg2, const float* __restrict__ image,
                  const float* __restrict__ target, const float* __restrict__ T_final,
-                 const uint32_t* __restrict__ n_contrib, float* __restrict__ grad2d, int64_t n_pad,
-                 float* __restrict__ loss, float inv3P, float l1w, const float* __restrict__ dLdC_extra,
-                 uint32_t* __restrict__ dev_status) {
+                 const uint32_t* __restrict__ n_contrib, const uint32_t* __restrict__ cmask,
+                 float* __restrict__ grad2d, int64_t n_pad, float* __restrict__ loss, float inv3P, float l1w,
+                 const float* __restrict__ dLdC_extra, uint32_t* __restrict__ dev_status) {
   __shared__ __align__(128) Rec s_rec[2][kBatch];
   __shared__ __align__(8) uint64_t s_bar[2];
 
   const int tile = bwd_tile_of_block();
+  const int block = int(blockIdx.x) % kBwdCtasPerTile;  // the 8x4 block within the tile
   const int lane = threadIdx.x & 31;
   int obx, oby;
   bwd_block_origin(TX, obx, oby);
   const int pxi = obx + (lane & 7), pyi = oby + (lane >> 3);
   const bool inside = pxi < W && pyi < H;
   const float px = float(pxi) + 0.5f, py = float(pyi) + 0.5f;
-  const float bx0 = float(obx) + 0.5f, bx1 = float(obx) + 7.5f;
-  const float by0 = float(oby) + 0.5f, by1 = float(oby) + 3.5f;
 
   // per-pixel loss gradient
   float g0 = 0.0f, g1 = 0.0f, g2 = 0.0f, T = 1.0f, lsum = 0.0f;
@@ -115,12 +116,11 @@ __global__ void __launch_bounds__(kBwdThreads)
   }
   const uint32_t warp_max = mx;
   if (lane == 0) atomicAdd(loss, ls * (l1w * inv3P));
-  uint32_t n_max = warp_max;
 
   const uint32_t K = min(*n_isect, cap);
   const uint2 rg = ranges[tile];
   const uint32_t start = min(rg.x, K), end = min(max(rg.y, rg.x), K);
-  n_max = min(n_max, end - start);
+  const uint32_t n_max = min(warp_max, end - start);
   if (n_max == 0) return;
 
   BatchStager<kBatch> st{srec + start, n_max, &s_rec[0][0], s_bar};
@@ -131,7 +131,7 @@ __global__ void __launch_bounds__(kBwdThreads)
     fence_mbar_init();
   }
   __syncthreads();
-  // batches are consumed last to first; use u counts consumption order
+  // batches are consumed last to first; u counts consumption order
   if (threadIdx.x == 0) {
     st.issue(nb - 1, 0);
     if (nb > 1) st.issue(nb - 2, 1);
@@ -146,30 +146,30 @@ __global__ void __launch_bounds__(kBwdThreads)
     const int cnt = int(st.count(b));
     // this warp only needs entries below its largest n_contrib
     const int jmax = int(min(uint32_t(cnt), warp_max > pos0 ? warp_max - pos0 : 0u));
-    // 32 entries at a time, from the top: cull against the warp's block with one
-    // ballot, then walk the set bits from the highest down.
+    // 32 entries at a time, from the top: the warp walks, from the highest down, the
+    // entries that at least one of its pixels composited in the forward (the union of
+    // the pixels' masks for this chunk); a pixel takes part in an entry its own mask has
     for (int j0 = ((jmax - 1) >> 5) << 5; j0 >= 0 && jmax > 0; j0 -= 32) {
-      uint32_t mask = warp_cull_ellipse(R, j0, jmax, bx0, bx1, by0, by1);
-      while (mask) {
-        const int hb = 31 - __clz(mask);
-        mask &= ~(1u << hb);
+      const uint32_t mine = cmask[cmask_index(start, tile, pos0 + uint32_t(j0), block, lane)];
+      uint32_t any = __reduce_or_sync(0xffffffffu, mine);
+      while (any) {
+        const int hb = 31 - __clz(any);
+        any &= ~(1u << hb);
         const int j = j0 + hb;
-        const uint32_t pos = pos0 + uint32_t(j);
-        // Every lane evaluates the entry; skip and clamp decisions become predicates
-        // and a non-contributing lane carries alpha = 0, which leaves its state
-        // unchanged and its partials zero (the warp stays converged).
+        const bool contrib = (mine >> hb) & 1u;
         const float4 ra = R[j].a;
         const float4 rb = R[j].b;
         const float4 rc = R[j].c;
         const float dx = __fsub_rn(px, ra.x), dy = __fsub_rn(py, ra.y);
         const float power = conic_power(dx, dy, ra.z, ra.w, rb.x);
-        const bool in_range = (pos < nc) && !(power > 0.0f) && !(power < kPowerSkip);
-        const float e = gs_expf_core(in_range ? power : 0.0f);
+        // the forward's decisions, recomputed for a composited entry in the same fp32
+        // sequence: alpha and whether it sits at the 0.99 clamp.  Every lane evaluates
+        // the entry; a lane that did not composite it carries alpha = 0, which leaves its
+        // state unchanged and its partials zero (the warp stays converged).
+        const float e = gs_expf_core(contrib ? power : 0.0f);
         const float vv = __fmul_rn(rb.y, e);
         const bool clamped = !(vv < kAlphaMax);
-        const float alpha_raw = clamped ? kAlphaMax : vv;
-        const bool contrib = in_range && !(alpha_raw < kAlphaMin);
-        const float alpha = contrib ? alpha_raw : 0.0f;
+        const float alpha = contrib ? (clamped ? kAlphaMax : vv) : 0.0f;
         const float Ti = __fdividef(T, 1.0f - alpha);
         const float wgt = alpha * Ti;
         float v[9];
@@ -194,26 +194,23 @@ __global__ void __launch_bounds__(kBwdThreads)
         v[3] = v[0] * dy;
         v[4] = v[1] * dy;
         const uint32_t cm = __ballot_sync(0xffffffffu, contrib);
-        if (cm) {
-          const uint32_t gid = __float_as_uint(rc.y);
-          float* slot = grad2d + int64_t(gid) * GS_GRAD2D_STRIDE;
-          if (__popc(cm) <= kDirectLanes) {
-            // few contributing lanes: each adds its own partials with two vector
-            // atomics and one scalar (no more L2 operations than the reduction's
-            // nine, without its shuffles)
-            if (contrib) {
-              atomicAdd(reinterpret_cast<float4*>(slot), make_float4(v[0], v[1], v[2], v[3]));
-              atomicAdd(reinterpret_cast<float4*>(slot) + 1, make_float4(v[4], v[5], v[6], v[7]));
-              atomicAdd(slot + 8, v[8]);
-            }
-          } else {
-            float s8, s9;
-            warp_reduce9(v, &s8, &s9);
-            // one atomic instruction: lanes 0, 4, ..., 28 add partials 0..7, lane 1
-            // partial 8, all into the Gaussian's 12-float slot
-            const bool nine = lane == 1;
-            if (((lane & 3) == 0) || nine) atomicAdd(slot + (nine ? 8 : (lane >> 2)), nine ? s9 : s8);
+        float* slot_p = grad2d + int64_t(__float_as_uint(rc.y)) * GS_GRAD2D_STRIDE;
+        if (__popc(cm) <= kDirectLanes) {
+          // few contributing lanes: each adds its own partials with two vector atomics
+          // and one scalar (no more L2 operations than the reduction's nine, without
+          // its shuffles)
+          if (contrib) {
+            atomicAdd(reinterpret_cast<float4*>(slot_p), make_float4(v[0], v[1], v[2], v[3]));
+            atomicAdd(reinterpret_cast<float4*>(slot_p) + 1, make_float4(v[4], v[5], v[6], v[7]));
+            atomicAdd(slot_p + 8, v[8]);
           }
+        } else {
+          float s8, s9;
+          warp_reduce9(v, &s8, &s9);
+          // one atomic instruction: lanes 0, 4, ..., 28 add partials 0..7, lane 1
+          // partial 8, all into the Gaussian's 12-float slot
+          const bool nine = lane == 1;
+          if (((lane & 3) == 0) || nine) atomicAdd(slot_p + (nine ? 8 : (lane >> 2)), nine ? s9 : s8);
         }
       }
     }
@@ -235,14 +232,17 @@ __global__ void k_zero4(float4* __restrict__ p, int64_t n4, float* __restrict__ 
 
 extern "C" gs_status gs_render_bwd(gs_dims dims, const gs_camera* cam, const gs_bins* bins, uint32_t capacity_K,
                                    const float bg[3], const float* image, const float* target, const float* T_final,
-                                   const uint32_t* n_contrib, float l1_weight, const float* dLdC_extra, float* grad2d,
-                                   float* loss_out, uint32_t* dev_status, cudaStream_t stream) {
+                                   const uint32_t* n_contrib, const uint32_t* cmask, size_t cmask_bytes,
+                                   float l1_weight, const float* dLdC_extra, float* grad2d, float* loss_out,
+                                   uint32_t* dev_status, cudaStream_t stream) {
   using namespace gs;
-  if (!dims_ok(dims) || !camera_ok(cam) || !bins || !bg || !image || !target || !T_final || !n_contrib || !grad2d ||
-      !loss_out || !dev_status)
+  if (!dims_ok(dims) || !camera_ok(cam) || !bins || !bg || !image || !target || !T_final || !n_contrib || !cmask ||
+      !grad2d || !loss_out || !dev_status)
     return GS_ERR_INVALID_ARG;
   if (!bins->rec || !bins->ranges || !bins->n_isect || capacity_K == 0) return GS_ERR_INVALID_ARG;
-  if (!aligned(bins->rec, 16) || !aligned(bins->ranges, 8) || !aligned(grad2d, 16)) return GS_ERR_INVALID_ARG;
+  if (!aligned(bins->rec, 16) || !aligned(bins->ranges, 8) || !aligned(grad2d, 16) || !aligned(cmask, 4))
+    return GS_ERR_INVALID_ARG;
+  if (cmask_bytes < gs_render_cmask_bytes(capacity_K, cam->width, cam->height)) return GS_ERR_INVALID_ARG;
   if (!(l1_weight >= 0.0f) || !std::isfinite(l1_weight)) return GS_ERR_INVALID_ARG;
   const int64_t n4 = int64_t(GS_GRAD2D_STRIDE) * dims.n_pad / 4;
   k_zero4<<<grid_for(n4, 256, sm_count() * 8), 256, 0, stream>>>(reinterpret_cast<float4*>(grad2d), n4, loss_out);
@@ -251,7 +251,7 @@ extern "C" gs_status gs_render_bwd(gs_dims dims, const gs_camera* cam, const gs_
   const float inv3P = float(1.0 / (3.0 * double(cam->width) * double(cam->height)));
   k_render_bwd<<<int(tiles * kBwdCtasPerTile), kBwdThreads, 0, stream>>>(
       reinterpret_cast<const Rec*>(bins->rec), reinterpret_cast<const uint2*>(bins->ranges), bins->n_isect,
-      capacity_K, cam->width, cam->height, TX, bg[0], bg[1], bg[2], image, target, T_final, n_contrib, grad2d,
+      capacity_K, cam->width, cam->height, TX, bg[0], bg[1], bg[2], image, target, T_final, n_contrib, cmask, grad2d,
       dims.n_pad, loss_out, inv3P, l1_weight, dLdC_extra, dev_status);
   return launch_status();
 }

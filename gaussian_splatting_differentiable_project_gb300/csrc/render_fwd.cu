@@ -5,7 +5,9 @@
 // cp.async.bulk with two mbarrier-tracked buffers, so the next batch streams in
 // while the current one is composited; every thread reads the same record
 // (shared-memory broadcast).  A pixel stops at its transmittance threshold; the
-// CTA stops loading once __syncthreads_count reports no live pixel.  The counting
+// CTA stops loading once __syncthreads_count reports no live pixel.  For every
+// 32-entry chunk a warp walks it stores each pixel's mask of composited entries, which
+// the backward walks instead of re-evaluating the whole list.  The counting
 // instantiation (gs_render_fwd_counted) also writes each pixel's number of
 // composited entries; the training step runs the one without.
 #include "api_util.h"
@@ -14,11 +16,11 @@
 namespace gs {
 
 template <bool kCount>
-__global__ void __launch_bounds__(kRasterThreads)
+__global__ void __launch_bounds__(kRasterThreads, 20)
     k_render_fwd(const Rec* __restrict__ srec, const uint2* __restrict__ ranges, const uint32_t* __restrict__ n_isect,
                  uint32_t cap, int W, int H, int TX, float bg0, float bg1, float bg2, float* __restrict__ image,
                  float* __restrict__ T_final, uint32_t* __restrict__ n_contrib, uint32_t* __restrict__ n_used,
-                 uint32_t* __restrict__ dev_status) {
+                 uint32_t* __restrict__ cmask, uint32_t* __restrict__ dev_status) {
   __shared__ __align__(128) Rec s_rec[2][kBatchFwd];
   __shared__ __align__(8) uint64_t s_bar[2];
 
@@ -29,6 +31,10 @@ __global__ void __launch_bounds__(kRasterThreads)
   const float px = float(pxi) + 0.5f, py = float(pyi) + 0.5f;
   float bx0, bx1, by0, by1;
   warp_block_bounds(TX, bx0, bx1, by0, by1);
+  const int lane = threadIdx.x & 31;
+  // this warp's 8x4 block within the tile: row block (q >> 1) * 2 + warp, column q & 1
+  const int q = int(blockIdx.x) % kCtasPerTile;
+  const int block = (((q >> 1) * 2 + (threadIdx.x >> 5)) << 1) + (q & 1);
 
   const uint32_t K = min(*n_isect, cap);
   const uint2 rg = ranges[tile];
@@ -66,9 +72,11 @@ __global__ void __launch_bounds__(kRasterThreads)
       if (!__all_sync(0xffffffffu, done)) {
         for (int j0 = 0; j0 < cnt; j0 += 32) {
           uint32_t mask = warp_cull(R, j0, cnt, bx0, bx1, by0, by1);
+          uint32_t cm = 0;  // this pixel's composited entries of the chunk
           while (mask) {
-            const int j = j0 + __ffs(mask) - 1;
-            mask &= mask - 1u;
+            const uint32_t low = mask & (0u - mask);  // the entry's bit
+            mask ^= low;
+            const int j = j0 + __ffs(low) - 1;
             const float4 ra = R[j].a;  // mx, my, ca, cb
             const float4 rb = R[j].b;  // cc, o, r, g
             const float dx = __fsub_rn(px, ra.x), dy = __fsub_rn(py, ra.y);
@@ -86,12 +94,15 @@ __global__ void __launch_bounds__(kRasterThreads)
                   C1 = __fmaf_rn(rb.w, w, C1);
                   C2 = __fmaf_rn(R[j].c.x, w, C2);
                   T = Tn;
-                  last = pos0 + uint32_t(j) + 1u;
+                  cm |= low;
                   if (kCount) ++used;
                 }
               }
             }
           }
+          cmask[cmask_index(start, tile, pos0 + uint32_t(j0), block, lane)] = cm;
+          // the last composited entry so far: the highest bit of this chunk's mask
+          if (cm) last = pos0 + uint32_t(j0) + 32u - uint32_t(__clz(cm));
           if (__all_sync(0xffffffffu, done)) break;
         }
       }
@@ -123,12 +134,14 @@ __global__ void __launch_bounds__(kRasterThreads)
 
 namespace {
 gs_status render_fwd_launch(const gs_camera* cam, const gs_bins* bins, uint32_t capacity_K, const float bg[3],
-                            float* image, float* T_final, uint32_t* n_contrib, uint32_t* n_used, uint32_t* dev_status,
-                            cudaStream_t stream) {
+                            float* image, float* T_final, uint32_t* n_contrib, uint32_t* n_used, uint32_t* cmask,
+                            size_t cmask_bytes, uint32_t* dev_status, cudaStream_t stream) {
   using namespace gs;
-  if (!camera_ok(cam) || !bins || !bg || !image || !T_final || !n_contrib || !dev_status) return GS_ERR_INVALID_ARG;
+  if (!camera_ok(cam) || !bins || !bg || !image || !T_final || !n_contrib || !cmask || !dev_status)
+    return GS_ERR_INVALID_ARG;
   if (!bins->rec || !bins->ranges || !bins->n_isect || capacity_K == 0) return GS_ERR_INVALID_ARG;
-  if (!aligned(bins->rec, 16) || !aligned(bins->ranges, 8)) return GS_ERR_INVALID_ARG;
+  if (!aligned(bins->rec, 16) || !aligned(bins->ranges, 8) || !aligned(cmask, 4)) return GS_ERR_INVALID_ARG;
+  if (cmask_bytes < gs_render_cmask_bytes(capacity_K, cam->width, cam->height)) return GS_ERR_INVALID_ARG;
   const int TX = (cam->width + kTile - 1) / kTile;
   const int64_t tiles = n_tiles(cam);
   const Rec* rec = reinterpret_cast<const Rec*>(bins->rec);
@@ -136,26 +149,36 @@ gs_status render_fwd_launch(const gs_camera* cam, const gs_bins* bins, uint32_t 
   if (n_used)
     k_render_fwd<true><<<int(tiles * kCtasPerTile), kRasterThreads, 0, stream>>>(
         rec, ranges, bins->n_isect, capacity_K, cam->width, cam->height, TX, bg[0], bg[1], bg[2], image, T_final,
-        n_contrib, n_used, dev_status);
+        n_contrib, n_used, cmask, dev_status);
   else
     k_render_fwd<false><<<int(tiles * kCtasPerTile), kRasterThreads, 0, stream>>>(
         rec, ranges, bins->n_isect, capacity_K, cam->width, cam->height, TX, bg[0], bg[1], bg[2], image, T_final,
-        n_contrib, nullptr, dev_status);
+        n_contrib, nullptr, cmask, dev_status);
   return launch_status();
 }
 }  // namespace
 
+extern "C" size_t gs_render_cmask_bytes(uint32_t capacity_K, int32_t width, int32_t height) {
+  if (width <= 0 || height <= 0) return 0;
+  const uint64_t tiles = uint64_t((width + GS_TILE - 1) / GS_TILE) * uint64_t((height + GS_TILE - 1) / GS_TILE);
+  const uint64_t slots = uint64_t(capacity_K) / 32 + tiles + 1;
+  return size_t(slots * gs::kBlocksPerTile * 32 * sizeof(uint32_t));
+}
+
 extern "C" gs_status gs_render_fwd(const gs_camera* cam, const gs_bins* bins, uint32_t capacity_K, const float bg[3],
-                                   float* image, float* T_final, uint32_t* n_contrib, uint32_t* dev_status,
-                                   cudaStream_t stream) {
-  return render_fwd_launch(cam, bins, capacity_K, bg, image, T_final, n_contrib, nullptr, dev_status, stream);
+                                   float* image, float* T_final, uint32_t* n_contrib, uint32_t* cmask,
+                                   size_t cmask_bytes, uint32_t* dev_status, cudaStream_t stream) {
+  return render_fwd_launch(cam, bins, capacity_K, bg, image, T_final, n_contrib, nullptr, cmask, cmask_bytes,
+                           dev_status, stream);
 }
 
 extern "C" gs_status gs_render_fwd_counted(const gs_camera* cam, const gs_bins* bins, uint32_t capacity_K,
                                            const float bg[3], float* image, float* T_final, uint32_t* n_contrib,
-                                           uint32_t* n_used, uint32_t* dev_status, cudaStream_t stream) {
+                                           uint32_t* n_used, uint32_t* cmask, size_t cmask_bytes,
+                                           uint32_t* dev_status, cudaStream_t stream) {
   if (!n_used) return GS_ERR_INVALID_ARG;
-  return render_fwd_launch(cam, bins, capacity_K, bg, image, T_final, n_contrib, n_used, dev_status, stream);
+  return render_fwd_launch(cam, bins, capacity_K, bg, image, T_final, n_contrib, n_used, cmask, cmask_bytes,
+                           dev_status, stream);
 }
 
 // ------------------------------------------------------------------ wait probe

@@ -191,21 +191,29 @@ gs_status gs_bin_sort(gs_dims dims, const gs_proj* proj, const gs_camera* cam, u
  *   bins       from gs_bin_sort (read).   bg: 3 floats (host).
  *   image      3 x H x W fp32 (channel planes), T_final H x W fp32,
  *   n_contrib  H x W uint32: entries iterated up to the last composited (write).
- * Errors: GS_ERR_INVALID_ARG for null/misaligned pointers or bad sizes. */
+ *   cmask      composited-entry masks for gs_render_bwd (write, 4-byte aligned,
+ *              cmask_bytes >= gs_render_cmask_bytes(capacity_K, width, height)):
+ *              for every 8x4 pixel block of a tile and every 32-entry chunk of the
+ *              tile's list that the block walks, each pixel's 32-bit mask of the
+ *              entries it composited.  Chunks past a block's last composited entry
+ *              are not written.  Treat the layout as opaque: gs_render_bwd reads it.
+ * Errors: GS_ERR_INVALID_ARG for null/misaligned pointers, bad sizes or a short
+ * cmask. */
+size_t gs_render_cmask_bytes(uint32_t capacity_K, int32_t width, int32_t height);
 gs_status gs_render_fwd(const gs_camera* cam, const gs_bins* bins, uint32_t capacity_K, const float bg[3],
-                        float* image, float* T_final, uint32_t* n_contrib, uint32_t* dev_status,
-                        cudaStream_t stream);
+                        float* image, float* T_final, uint32_t* n_contrib, uint32_t* cmask, size_t cmask_bytes,
+                        uint32_t* dev_status, cudaStream_t stream);
 
 /* gs_render_fwd_counted -- gs_render_fwd that also writes, per pixel, the number of
  * entries it composited (alpha >= 1/255 and not stopped by the transmittance test):
  *   n_used  H x W uint32 (write).
- * The image, T_final and n_contrib are those of gs_render_fwd, bit for bit.  Not part
- * of the training step: it measures how much of the iterated work composites (the
- * mean number of Gaussians composited per pixel of a view).
+ * The image, T_final, n_contrib and cmask are those of gs_render_fwd, bit for bit.
+ * Not part of the training step: it measures how much of the iterated work
+ * composites (the mean number of Gaussians composited per pixel of a view).
  * Errors: as gs_render_fwd, plus a null n_used. */
 gs_status gs_render_fwd_counted(const gs_camera* cam, const gs_bins* bins, uint32_t capacity_K, const float bg[3],
                                 float* image, float* T_final, uint32_t* n_contrib, uint32_t* n_used,
-                                uint32_t* dev_status, cudaStream_t stream);
+                                uint32_t* cmask, size_t cmask_bytes, uint32_t* dev_status, cudaStream_t stream);
 
 /* ---------------------------------------------------------------------------
  * gs_render_bwd -- loss gradient and the compositing backward.  "Scaling 3D
@@ -215,18 +223,19 @@ gs_status gs_render_fwd_counted(const gs_camera* cam, const gs_bins* bins, uint3
  * (loss computed locally, gradients back through the same stages).
  * dL/dC = l1_weight sign(C - C*) / (3 H W) + dLdC_extra (if non-null, e.g. the D-SSIM
  * term's gradient from gs_ssim_bwd); loss_out = l1_weight mean |C - C*| over the
- * 3 H W values.  Each pixel walks its composited entries in reverse, recovering T
- * by division by (1 - alpha), and produces per entry the partials of the loss with
+ * 3 H W values.  Each pixel walks the entries it composited (the forward's cmask) in
+ * reverse, recomputing alpha in the forward's fp32 sequence and recovering T by
+ * division by (1 - alpha), and produces per entry the partials of the loss with
  * respect to opacity and colour (r, g, b) and, for mean2d and the conic, the five
- * moments of q = dL/dpower over the pixel offset (dx, dy) = (px - mx, py - my);
- * a warp's partials for one entry are added to grad2d with global atomics, lane by
- * lane when few lanes contribute and after a shuffle reduction otherwise (summation
- * order is not fixed).  The conic is the Gaussian's own, so its
+ * moments of q = dL/dpower over the pixel offset (dx, dy) = (px - mx, py - my); each
+ * pixel adds its partials to grad2d with global atomics (summation order is not
+ * fixed).  The conic is the Gaussian's own, so its
  * products are applied once to the sums, by the consumers: with power =
  * -(A dx^2 + C dy^2)/2 - B dx dy and S1..S5 the sums of q dx, q dy, q dx^2, q dx dy,
  * q dy^2,  dL/dmx = A S1 + B S2,  dL/dmy = B S1 + C S2,  dL/dA = -S3/2,
  * dL/dB = -S4,  dL/dC = -S5/2.
- *   image, T_final, n_contrib: outputs of gs_render_fwd (read).
+ *   image, T_final, n_contrib, cmask: outputs of gs_render_fwd for the same bins (read;
+ *   cmask_bytes as there).
  *   target      3 x H x W fp32 (read).
  *   l1_weight   weight of the L1 term (1 for the L1 objective, 1 - lambda with D-SSIM).
  *   dLdC_extra  3 x H x W fp32 added to the loss gradient, or null.
@@ -240,8 +249,9 @@ gs_status gs_render_fwd_counted(const gs_camera* cam, const gs_bins* bins, uint3
  * Errors: as gs_render_fwd, plus a negative or non-finite l1_weight. */
 gs_status gs_render_bwd(gs_dims dims, const gs_camera* cam, const gs_bins* bins, uint32_t capacity_K,
                         const float bg[3], const float* image, const float* target, const float* T_final,
-                        const uint32_t* n_contrib, float l1_weight, const float* dLdC_extra, float* grad2d,
-                        float* loss_out, uint32_t* dev_status, cudaStream_t stream);
+                        const uint32_t* n_contrib, const uint32_t* cmask, size_t cmask_bytes, float l1_weight,
+                        const float* dLdC_extra, float* grad2d, float* loss_out, uint32_t* dev_status,
+                        cudaStream_t stream);
 
 /* ---------------------------------------------------------------------------
  * gs_ssim_fwd / gs_ssim_bwd -- the D-SSIM term.  "Scaling 3D Gaussian Splatting

@@ -86,10 +86,19 @@ def test_argument_errors_are_returned_without_a_gpu():
     # render backward: negative or non-finite L1 weight
     bins = gs.GsBins(16, 16, 16, 16, 16)
     bg = (ctypes.c_float * 3)(0, 0, 0)
+    cmb = lib.gs_render_cmask_bytes(1000, 128, 128)
+    # (1000 / 32 + 64 tiles + 1) chunk slots x 8 blocks x 32 pixels x 4 bytes
+    assert cmb == (1000 // 32 + 64 + 1) * 8 * 32 * 4
     for w in (-1.0, float("nan"), float("inf")):
-        r = lib.gs_render_bwd(gs.dims(10, 256), ctypes.byref(cam), ctypes.byref(bins), 1000, bg, p, p, p, p, w, None,
-                              p, p, p, None)
+        r = lib.gs_render_bwd(gs.dims(10, 256), ctypes.byref(cam), ctypes.byref(bins), 1000, bg, p, p, p, p, p, cmb,
+                              w, None, p, p, p, None)
         assert r == gs.GS_ERR_INVALID_ARG, w
+    # render forward and backward: a composited-entry mask buffer too short for the view
+    r = lib.gs_render_bwd(gs.dims(10, 256), ctypes.byref(cam), ctypes.byref(bins), 1000, bg, p, p, p, p, p, cmb - 4,
+                          1.0, None, p, p, p, None)
+    assert r == gs.GS_ERR_INVALID_ARG
+    assert lib.gs_render_fwd(ctypes.byref(cam), ctypes.byref(bins), 1000, bg, p, p, p, p, cmb - 4, p, None) == \
+        gs.GS_ERR_INVALID_ARG
     # spatial order: null perm, short or misaligned workspace; permutation: no planes,
     # aliasing buffers
     need = lib.gs_spatial_order_workspace_bytes(gs.dims(1000, 1024))
@@ -201,10 +210,10 @@ def test_binding_checks_buffer_types_and_sizes(monkeypatch):
     monkeypatch.setattr(gs, "load", lambda *a, **k: _StubLib())
 
     def refused(match, fn, *a, **k):
-        before = len(calls)
+        before = len([c for c in calls if not c.endswith("_bytes")])
         with pytest.raises(gs.GsError, match=match):
             fn(*a, **k)
-        assert len(calls) == before
+        assert len([c for c in calls if not c.endswith("_bytes")]) == before
 
     params = torch.zeros((gs.N_PLANES, n_pad))
     img, T, nc = torch.zeros((3, H, W)), torch.zeros((H, W)), torch.zeros((H, W), dtype=torch.int32)
@@ -218,7 +227,9 @@ def test_binding_checks_buffer_types_and_sizes(monkeypatch):
     gs.render_bwd(n, n_pad, cam, bins, (0, 0, 0), img, img, T, nc, g2, torch.zeros(1), st, dLdC_extra=img)
     gs.adam_step(n, params, params, params, params, lr, 0.9, 0.999, 1e-15, 1)
     gs.permute_planes(n, i32(n), params, params)
-    assert calls == ["gs_project", "gs_render_fwd", "gs_render_bwd", "gs_adam_step", "gs_permute_planes"]
+    # (size queries such as gs_render_cmask_bytes are host calls, left out of the count)
+    assert [c for c in calls if not c.endswith("_bytes")] == ["gs_project", "gs_render_fwd", "gs_render_bwd",
+                                                             "gs_adam_step", "gs_permute_planes"]
     u8 = torch.zeros(n, dtype=torch.uint8)
     i64 = torch.zeros(1, dtype=torch.int64)
     cfg = gs.densify_thresholds(3.0)[0]
@@ -241,7 +252,8 @@ def test_binding_checks_buffer_types_and_sizes(monkeypatch):
     gs.render_fwd_counted(cam, bins, (0, 0, 0), img, T, nc, i32(W * H), st)
     gs.batch_hyper(3, lr, 0.9, 0.999, 1e-15)
     # the calls above plus the one inside densify_thresholds
-    assert len(calls) == 23 and calls.count("gs_densify_thresholds") == 1
+    work = [c for c in calls if not c.endswith("_bytes")]
+    assert len(work) == 23 and work.count("gs_densify_thresholds") == 1
 
     refused("params: expected fp32", gs.project, n, params.double(), cam, proj, st)
     refused("params: needs", gs.project, n, params[:58].contiguous(), cam, proj, st)
@@ -331,8 +343,10 @@ def test_size_and_camera_limits_are_refused_on_the_host():
     assert lib.gs_project(gs.dims(10, 256), p, ctypes.byref(cam(near_z=float("inf"))), pc, p, None) == bad
     bg = (ctypes.c_float * 3)(0, 0, 0)
     bins = gs.GsBins(16, 16, 16, 16, 16)
-    assert lib.gs_render_fwd(ctypes.byref(c), ctypes.byref(bins), 1000, bg, None, p, p, p, None) == bad
+    cmb = lib.gs_render_cmask_bytes(1000, 128, 128)
+    assert lib.gs_render_fwd(ctypes.byref(c), ctypes.byref(bins), 1000, bg, None, p, p, p, cmb, p, None) == bad
     misaligned = gs.GsBins(16, 16, 20, 16, 16)
-    assert lib.gs_render_fwd(ctypes.byref(c), ctypes.byref(misaligned), 1000, bg, p, p, p, p, None) == bad
+    assert lib.gs_render_fwd(ctypes.byref(c), ctypes.byref(misaligned), 1000, bg, p, p, p, p, cmb, p, None) == bad
+    assert lib.gs_render_fwd(ctypes.byref(c), ctypes.byref(bins), 1000, bg, p, p, p, None, cmb, p, None) == bad
     assert lib.gs_densify_apply(gs.dims(10, 256), 100, p, p, p, p, p, p, p, 0.47, p, p, p, p, None) == bad
     assert lib.gs_opacity_reset(gs.dims(10, 256), p, None, p, -4.0, None) == bad
