@@ -188,9 +188,11 @@ def passes_for(width, height):
     return (b + 7) // 8
 
 
-def stage_bytes(N, n_pad, V, K, P, passes, dssim=False):
+def stage_bytes(N, n_pad, V, K, P, passes, dssim=False, E=0.0):
     """Algorithmic DRAM bytes of each stage per step (the traffic the method needs
-    with the data layout used: SoA planes, 48-byte records, 8+4-byte keys)."""
+    with the data layout used: SoA planes, 48-byte records, 8+4-byte keys).  E is the
+    number of iterated (pixel, entry) pairs: the composited-entry masks hold 4 bytes
+    per pixel and 32-entry chunk, E / 8 bytes in all."""
     return {
         # all N: 11 geometric planes + depth/radius/rect/count; visible: 48 SH + record
         "project": 64 * N + 240 * V,
@@ -199,11 +201,13 @@ def stage_bytes(N, n_pad, V, K, P, passes, dssim=False):
         # (tile, index) emitted, each tile pass reads and writes 16 bytes, then tile
         # key + index read, 48-byte record gathered and written, 64-bit key written
         "bin_sort": 8 * N + 100 * V + (8 + 16 * passes + 112) * K,
-        # records once per tile, image + T + n_contrib written
-        "render_fwd": 48 * K + 20 * P,
+        # records once per tile, image + T + n_contrib written, the composited-entry
+        # masks written
+        "render_fwd": 48 * K + 20 * P + E / 8,
         # grad2d (12 floats per Gaussian) cleared, records once per tile,
-        # image/target/T/n_contrib read (and the D-SSIM image gradient when that term is on)
-        "render_bwd": 48 * n_pad + 48 * K + (44 if dssim else 32) * P,
+        # image/target/T/n_contrib read (and the D-SSIM image gradient when that term is
+        # on), the masks read
+        "render_bwd": 48 * n_pad + 48 * K + (44 if dssim else 32) * P + E / 8,
         # D-SSIM: image + target read, 15 maps (3 partials, 2 means per channel)
         # written; the maps, image and target read again, the image gradient written
         "ssim": 180 * P,
@@ -575,7 +579,7 @@ def run_gb300(args, cfg, ws, rank, local):
     Emean = float(np.mean([E[v] for v in views]))
     Eused = float(np.mean([E_used[v] for v in views]))
     Pix = W * H
-    byt = stage_bytes(n, n_pad, Vmean, Kmean, Pix, passes, dssim=args.dssim > 0)
+    byt = stage_bytes(n, n_pad, Vmean, Kmean, Pix, passes, dssim=args.dssim > 0, E=Emean)
     peak_bw = _peak("hbm_gbs", 6800.0)
     sm_mhz = clk.get("sm_max_mhz") or 2070.0
     sms = gs.sm_count()

@@ -137,6 +137,10 @@ __global__ void __launch_bounds__(kBwdThreads)
     if (nb > 1) st.issue(nb - 2, 1);
   }
   float acc0 = bg0, acc1 = bg1, acc2 = bg2;
+  // The chunks are walked from the one holding entry n_max - 1 down to chunk 0; each
+  // chunk's masks are loaded one chunk ahead, so the load overlaps the walk before it.
+  int chunk = int((n_max - 1) >> 5);
+  uint32_t next_mask = cmask[cmask_index(start, tile, uint32_t(chunk) << 5, block, lane)];
   for (int u = 0; u < nb; ++u) {
     const int b = nb - 1 - u;
     const int slot = u & 1;
@@ -150,7 +154,9 @@ __global__ void __launch_bounds__(kBwdThreads)
     // entries that at least one of its pixels composited in the forward (the union of
     // the pixels' masks for this chunk); a pixel takes part in an entry its own mask has
     for (int j0 = ((jmax - 1) >> 5) << 5; j0 >= 0 && jmax > 0; j0 -= 32) {
-      const uint32_t mine = cmask[cmask_index(start, tile, pos0 + uint32_t(j0), block, lane)];
+      const uint32_t mine = next_mask;  // chunk (pos0 + j0) / 32
+      --chunk;
+      if (chunk >= 0) next_mask = cmask[cmask_index(start, tile, uint32_t(chunk) << 5, block, lane)];
       uint32_t any = __reduce_or_sync(0xffffffffu, mine);
       while (any) {
         const int hb = 31 - __clz(any);

@@ -22,7 +22,7 @@ GRAD2D = 12 * F            # interleaved 2D-gradient slot
 
 def _coef(fn, unit, **kw):
     """The coefficient of one unit count in a linear byte model."""
-    args = dict(N=0, n_pad=0, V=0, K=0, P=0)
+    args = dict(N=0, n_pad=0, V=0, K=0, P=0, E=0)
     args.update(kw)
     base = fn(**args)
     args[unit] = 1
@@ -32,7 +32,7 @@ def _coef(fn, unit, **kw):
 
 def _stage(**kw):
     return bench.stage_bytes(kw["N"], kw["n_pad"], kw["V"], kw["K"], kw["P"], kw.get("passes", 2),
-                             dssim=kw.get("dssim", False))
+                             dssim=kw.get("dssim", False), E=kw.get("E", 0))
 
 
 def test_layout_constants_match_the_binding():
@@ -51,11 +51,13 @@ def test_render_bytes():
     n = _coef(_stage, "n_pad")
     k = _coef(_stage, "K")
     p = _coef(_stage, "P")
-    # forward: each intersection's record read once; image (3), T and n_contrib written
-    assert k["render_fwd"] == REC and p["render_fwd"] == (3 + 1 + 1) * F
+    e = _coef(_stage, "E")
+    # forward: each intersection's record read once; image (3), T and n_contrib
+    # written; a 4-byte mask per pixel and 32 iterated entries written
+    assert k["render_fwd"] == REC and p["render_fwd"] == (3 + 1 + 1) * F and e["render_fwd"] == F / 32
     # backward: the grad2d slots cleared, records read once; image and target (3 each),
-    # T and n_contrib read
-    assert n["render_bwd"] == GRAD2D and k["render_bwd"] == REC
+    # T and n_contrib read; the masks read
+    assert n["render_bwd"] == GRAD2D and k["render_bwd"] == REC and e["render_bwd"] == F / 32
     assert p["render_bwd"] == (3 + 3 + 1 + 1) * F
     # with D-SSIM the backward also reads its 3-plane image gradient
     assert _coef(lambda **a: _stage(dssim=True, **a), "P")["render_bwd"] == (3 + 3 + 1 + 1 + 3) * F
