@@ -85,7 +85,8 @@ __global__ void __launch_bounds__(kRasterThreads, 20)
               const float v = __fmul_rn(rb.y, gs_expf_core(power));
               const float alpha = (v < kAlphaMax) ? v : kAlphaMax;
               if (!(alpha < kAlphaMin)) {
-                const float Tn = __fmul_rn(T, __fsub_rn(1.0f, alpha));
+                // T (1 - alpha) as T - alpha T, one rounding (the frozen sequence)
+                const float Tn = __fmaf_rn(-alpha, T, T);
                 if (Tn < kTMin) {
                   done = true;
                 } else {

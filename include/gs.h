@@ -187,7 +187,8 @@ gs_status gs_bin_sort(gs_dims dims, const gs_proj* proj, const gs_camera* cam, u
  * power = ca dx^2 + cb dx dy + cc dy^2 with d = pixel centre - mean2d; skip if
  * power > 0; alpha = min(0.99, o exp(power)); skip if alpha < 1/255; stop,
  * without compositing, if T (1 - alpha) < 1e-4; else C += rgb alpha T and
- * T *= 1 - alpha.  Output C + T bg.
+ * T <- T (1 - alpha).  Output C + T bg.  T (1 - alpha) is formed as the fused
+ * T - alpha T (one rounding), part of the frozen fp32 sequence.
  *   bins       from gs_bin_sort (read).   bg: 3 floats (host).
  *   image      3 x H x W fp32 (channel planes), T_final H x W fp32,
  *   n_contrib  H x W uint32: entries iterated up to the last composited (write).

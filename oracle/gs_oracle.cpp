@@ -499,7 +499,8 @@ void render_pixel_fwd(const std::vector<Splat<S>>& sp, const std::vector<int32_t
     const bool clamped = !(v < S(0.99));
     const S alpha = clamped ? S(0.99) : v;
     if (alpha < one_255) continue;
-    const S Tn = T * (S(1) - alpha);
+    // T (1 - alpha), evaluated as T - alpha T with one rounding
+    const S Tn = fma_(-alpha, T, T);
     if (Tn < S(1e-4)) break;
     const S wgt = alpha * T;
     for (int ch = 0; ch < 3; ++ch) Cc[ch] = fma_(g.rgb[ch], wgt, Cc[ch]);
