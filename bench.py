@@ -548,13 +548,16 @@ def run_gb300(args, cfg, ws, rank, local):
             slots = [staged.put(host_t[v]) for v in views_of(args.warmup)]
             for s in range(K):
                 vs = views_of(args.warmup + s)
-                nxt = [staged.put(host_t[v]) for v in views_of(args.warmup + s + 1)] if s + 1 < K else None
                 if B == 1:
                     tr.step_staged(cams[vs[0]], staged, slots[0])
+                    # the next target's upload starts once this step's rasterisers are done
+                    nxt = ([staged.put(host_t[v], after=tr.after_backward) for v in views_of(args.warmup + s + 1)]
+                           if s + 1 < K else None)
                     loss_host[s, 0:1].copy_(tr.loss, non_blocking=True)
                     if args.dssim > 0:
                         loss_host[s, 1:2].copy_(tr.ssim_val, non_blocking=True)
                 else:
+                    nxt = [staged.put(host_t[v]) for v in views_of(args.warmup + s + 1)] if s + 1 < K else None
                     tr.step_batch([cams[v] for v in vs], [staged.get(sl) for sl in slots])
                     for sl in slots:
                         staged.release(sl)

@@ -26,7 +26,10 @@ class HostTargets:
     stream of its own and returns the slot; ``get`` orders a compute stream after that
     upload; ``release`` marks the slot free once the work enqueued so far on the
     compute stream is done.  The upload for the next step thus runs while the current
-    step computes."""
+    step computes.  With ``after`` (an event on the compute stream) the upload waits for
+    it: ``Trainer.step_staged`` records one after its backward, so that the upload's
+    writes pass through L2 during the streaming projection-backward and Adam pass
+    rather than while the rasterisers' working set is there."""
 
     def __init__(self, shape, device="cuda", slots: int = 2):
         import torch
@@ -37,13 +40,15 @@ class HostTargets:
         self.stream = torch.cuda.Stream(device=device)
         self.next = 0
 
-    def put(self, host) -> int:
+    def put(self, host, after=None) -> int:
         import torch
         k = self.next
         self.next = (k + 1) % len(self.bufs)
         with torch.cuda.stream(self.stream):
             if self.used[k]:
                 self.stream.wait_event(self.consumed[k])
+            if after is not None:
+                self.stream.wait_event(after)
             self.bufs[k].copy_(host, non_blocking=True)
             self.copied[k].record(self.stream)
         self.used[k] = True
@@ -296,9 +301,28 @@ class Trainer:
     _t_dev_synced = -1
 
     def step_staged(self, cam: dict, targets: HostTargets, slot: int, stream=None) -> None:
-        """``step`` against the target uploaded into ``slot`` of ``targets``."""
-        self.step(cam, targets.get(slot, stream), stream)
-        targets.release(slot, stream)
+        """``step`` against the target uploaded into ``slot`` of ``targets``.  The step
+        waits for that upload only before its loss backward (projection, binning and
+        the forward do not read the target), and records ``after_backward`` once the
+        rasterisers are done: pass it to ``targets.put`` for the next step's upload."""
+        import torch
+        s = stream or torch.cuda.current_stream()
+        if getattr(self, "after_backward", None) is None:
+            self.after_backward = torch.cuda.Event()
+        self.forward(cam, stream)
+        target = targets.get(slot, s)
+        if not self.fused:
+            self.backward(cam, target, stream)
+            self.after_backward.record(s)
+            self.optimizer_step(stream)
+        else:
+            self.loss_backward(cam, target, stream)
+            self.accumulate_density(cam, stream)
+            self.after_backward.record(s)
+            self.t += 1
+            project_bwd_adam(self.n, self.params, cam, self.proj, self.grad2d, self.m, self.v, self.lr_plane,
+                             self.beta1, self.beta2, self.eps, self.t, self.status, stream)
+        targets.release(slot, s)
 
     # checkpoint ----------------------------------------------------------------------
     def save(self, path) -> None:

@@ -486,11 +486,14 @@ def test_render_bwd_extra_image_gradient(case):
     _grad_close(_partials(tr, n, ref["conic"]), rd["grad2d"], what="grad2d")
 
 
-def test_staged_host_targets_feed_the_right_step(case):
+@pytest.mark.parametrize("order", ["before", "after_backward"])
+def test_staged_host_targets_feed_the_right_step(case, order):
     """Targets uploaded from pinned host memory through HostTargets (copy stream,
     two slots, the next upload overlapping the current step) drive the same steps as
     targets already on the device: per-step losses agree over four steps with four
-    different targets, so every step read its own upload."""
+    different targets, so every step read its own upload.  The next upload is enqueued
+    before the current step, or after it and waiting on the step's after_backward event
+    (the bench's end-to-end order)."""
     P, cam, n = case["P"], case["cam"], case["n"]
     W, H = cam["width"], cam["height"]
     base = _target_for(case)
@@ -506,8 +509,12 @@ def test_staged_host_targets_feed_the_right_step(case):
     slot = staged.put(host[0])
     loss_b = torch.empty((4,), dtype=torch.float32).pin_memory()
     for k in range(4):
-        nxt = staged.put(host[k + 1]) if k + 1 < 4 else None
-        b.step_staged(cam, staged, slot)
+        if order == "before":
+            nxt = staged.put(host[k + 1]) if k + 1 < 4 else None
+            b.step_staged(cam, staged, slot)
+        else:
+            b.step_staged(cam, staged, slot)
+            nxt = staged.put(host[k + 1], after=b.after_backward) if k + 1 < 4 else None
         loss_b[k:k + 1].copy_(b.loss, non_blocking=True)
         slot = nxt
     torch.cuda.synchronize()
