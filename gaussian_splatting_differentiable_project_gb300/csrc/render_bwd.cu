@@ -25,11 +25,13 @@ namespace gs {
 // A warp with at most this many contributing lanes skips the reduction: each
 // contributing lane adds its own nine partials with three atomics (two float4, one
 // scalar) to the Gaussian's slot.  That trades the reduction's 14 shuffles, 14 adds
-// and 14 selects for more L2 atomic traffic into one slot, which pays until nearly
-// every lane of the warp hits the same address.  Measured on the 4M-Gaussian
-// isosurface at 2048^2 (relative time of the backward): thresholds 0 / 4 / 12 / 24 /
-// 28 / 32 give 1.00 / 0.97 / 0.90 / 0.86 / 0.90 / 1.22.
-constexpr int kDirectLanes = 24;
+// and 14 selects for 3 k L2 reductions into one slot (the reduction's one atomic
+// instruction reaches L2 as about two requests, its nine addresses lying in two
+// sectors).  Those L2 reductions are what limits the walk once k grows.  Measured on the
+// 4M-Gaussian isosurface at 2048^2 (backward ms, walking the composited-entry masks):
+// thresholds 0 / 4 / 8 / 12 / 14 / 16 / 20 / 24 / 28 give 1.87 / 1.72 / 1.64 / 1.58 /
+// 1.56 / 1.55 / 1.61 / 1.85 / 2.15.
+constexpr int kDirectLanes = 16;
 
 // Reduce-scatter of nine per-lane values over the warp.  On return lane l with
 // (l & 3) == 0 holds the warp sum of value l >> 2 (values 0..7) in *out8 and every
