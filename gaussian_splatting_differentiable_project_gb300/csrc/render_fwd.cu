@@ -3,25 +3,98 @@
 // One CTA per 8x8 quarter of a 16x16 tile, one thread per pixel.  The tile's
 // sorted records are staged into shared memory in batches of 96 (4.5 KB) by
 // cp.async.bulk with two mbarrier-tracked buffers, so the next batch streams in
-// while the current one is composited; every thread reads the same record
-// (shared-memory broadcast).  A pixel stops at its transmittance threshold; the
-// CTA stops loading once __syncthreads_count reports no live pixel.  For every
-// 32-entry chunk a warp walks it stores each pixel's mask of composited entries, which
-// the backward walks instead of re-evaluating the whole list.  The counting
-// instantiation (gs_render_fwd_counted) also writes each pixel's number of
-// composited entries; the training step runs the one without.
+// while the current one is composited.  A pixel stops at its transmittance
+// threshold; the CTA stops loading once __syncthreads_count reports no live pixel.
+//
+// Each warp (an 8x4 block) takes a batch 32 entries at a time: one lane per entry
+// culls it against the block, and the entries that survive are packed, in order, into
+// pairs in the warp's shared memory.  The walk then takes two entries per step: their
+// offsets, powers, exponentials and opacity products are formed with the two-wide fp32
+// instructions (fma.rn.f32x2 and kin, each half rounded exactly as the scalar
+// instruction), and the pair is composited in list order, one entry after the other.
+// Every lane reads the same pair (shared-memory broadcast).  For every 32-entry chunk
+// a warp walks it stores each pixel's mask of composited entries, which the backward
+// walks instead of re-evaluating the whole list.  The counting instantiation
+// (gs_render_fwd_counted) also writes each pixel's number of composited entries; the
+// training step runs the one without.
 #include "api_util.h"
 #include "raster_common.cuh"
 
 namespace gs {
 
+// gs_expf_core on two arguments at once with the two-wide fp32 instructions: each
+// half takes exactly the scalar sequence's roundings (the fused multiply-add, add and
+// multiply of a pair round each half as their scalar forms do), and the integer steps
+// stay per half.  s - 1.5 * 2^23 is formed as s + (-1.5 * 2^23) and -k ln2 r as
+// k (-ln2) r, which round identically.
+__device__ __forceinline__ float2 gs_expf2_core(float2 x) {
+  const float kRound = 12582912.0f;
+  const float2 s = __ffma2_rn(x, make_float2(1.44269504088896341f, 1.44269504088896341f), make_float2(kRound, kRound));
+  const float2 kf = __fadd2_rn(s, make_float2(-kRound, -kRound));
+  float2 r = __ffma2_rn(kf, make_float2(-0.693145751953125f, -0.693145751953125f), x);
+  r = __ffma2_rn(kf, make_float2(-1.4286068203094173e-06f, -1.4286068203094173e-06f), r);
+  float2 p = __ffma2_rn(make_float2(1.0f / 5040.0f, 1.0f / 5040.0f), r, make_float2(1.0f / 720.0f, 1.0f / 720.0f));
+  p = __ffma2_rn(p, r, make_float2(1.0f / 120.0f, 1.0f / 120.0f));
+  p = __ffma2_rn(p, r, make_float2(1.0f / 24.0f, 1.0f / 24.0f));
+  p = __ffma2_rn(p, r, make_float2(1.0f / 6.0f, 1.0f / 6.0f));
+  p = __ffma2_rn(p, r, make_float2(0.5f, 0.5f));
+  p = __ffma2_rn(p, r, make_float2(1.0f, 1.0f));
+  p = __ffma2_rn(p, r, make_float2(1.0f, 1.0f));
+  return make_float2(__uint_as_float(__float_as_uint(p.x) + (__float_as_uint(s.x) << 23)),
+                     __uint_as_float(__float_as_uint(p.y) + (__float_as_uint(s.y) << 23)));
+}
+
+// conic_power on two entries at once (two-wide instructions, the same roundings).
+__device__ __forceinline__ float2 conic_power2(float2 dx, float2 dy, float2 ca, float2 cb, float2 cc) {
+  return __ffma2_rn(dx, __ffma2_rn(ca, dx, __fmul2_rn(cb, dy)), __fmul2_rn(__fmul2_rn(cc, dy), dy));
+}
+
+// Culled entries of one chunk, packed in pairs: pair p holds the warp's compacted
+// entries 2p (.x) and 2p + 1 (.y).  The mean is stored negated, so px + (-mx) gives
+// px - mx's bits.
+struct __align__(16) EntryPair {
+  float2 nmx, nmy;
+  float2 ca, cb;
+  float2 cc, o;
+};
+
+// One entry of the walk, in list order: the next bit of `rem` is its list position.
+// The frozen compositing decisions of the scalar walk, given its power and o e^power.
 template <bool kCount>
-__global__ void __launch_bounds__(kRasterThreads, 20)
+__device__ __forceinline__ void composite_one(float power, float v, const float4& col, uint32_t& rem, bool& done,
+                                              float& T, float& C0, float& C1, float& C2, uint32_t& cm,
+                                              uint32_t& used) {
+  const uint32_t low = rem & (0u - rem);  // the entry's bit
+  rem ^= low;
+  if (!done && !(power > 0.0f) && !(power < kPowerSkip)) {
+    const float alpha = (v < kAlphaMax) ? v : kAlphaMax;
+    if (!(alpha < kAlphaMin)) {
+      // T (1 - alpha) as T - alpha T, one rounding (the frozen sequence)
+      const float Tn = __fmaf_rn(-alpha, T, T);
+      if (Tn < kTMin) {
+        done = true;
+      } else {
+        const float w = __fmul_rn(alpha, T);
+        C0 = __fmaf_rn(col.x, w, C0);
+        C1 = __fmaf_rn(col.y, w, C1);
+        C2 = __fmaf_rn(col.z, w, C2);
+        T = Tn;
+        cm |= low;
+        if (kCount) ++used;
+      }
+    }
+  }
+}
+
+template <bool kCount>
+__global__ void __launch_bounds__(kRasterThreads, 16)
     k_render_fwd(const Rec* __restrict__ srec, const uint2* __restrict__ ranges, const uint32_t* __restrict__ n_isect,
                  uint32_t cap, int W, int H, int TX, float bg0, float bg1, float bg2, float* __restrict__ image,
                  float* __restrict__ T_final, uint32_t* __restrict__ n_contrib, uint32_t* __restrict__ n_used,
                  uint32_t* __restrict__ cmask, uint32_t* __restrict__ dev_status) {
   __shared__ __align__(128) Rec s_rec[2][kBatchFwd];
+  __shared__ EntryPair s_pair[kRasterThreads / 32][16];
+  __shared__ float4 s_col[kRasterThreads / 32][32];  // r, g, b of compacted entry k
   __shared__ __align__(8) uint64_t s_bar[2];
 
   const int tile = tile_of_block();
@@ -31,7 +104,10 @@ __global__ void __launch_bounds__(kRasterThreads, 20)
   const float px = float(pxi) + 0.5f, py = float(pyi) + 0.5f;
   float bx0, bx1, by0, by1;
   warp_block_bounds(TX, bx0, bx1, by0, by1);
-  const int lane = threadIdx.x & 31;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const float2 px2 = make_float2(px, px), py2 = make_float2(py, py);
+  EntryPair* const my_pair = s_pair[warp];
+  float4* const my_col = s_col[warp];
   // this warp's 8x4 block within the tile: row block (q >> 1) * 2 + warp, column q & 1
   const int q = int(blockIdx.x) % kCtasPerTile;
   const int block = (((q >> 1) * 2 + (threadIdx.x >> 5)) << 1) + (q & 1);
@@ -65,41 +141,49 @@ __global__ void __launch_bounds__(kRasterThreads, 20)
       const Rec* R = st.buffer(slot);
       const int cnt = int(st.count(b));
       const uint32_t pos0 = uint32_t(b) * kBatchFwd;
-      // Warp-uniform walk over the batch: 32 entries at a time are culled against
-      // the warp's 8x4 block by one ballot, then the warp steps through the set
-      // bits in order; every lane takes its skip / stop decisions as predicates,
-      // so the warp stays converged.
+      // Warp-uniform walk over the batch, 32 entries at a time: each lane culls one
+      // entry against the warp's 8x4 block and, if it survives, writes it to its
+      // compacted slot; the warp then steps through the compacted entries two at a
+      // time.  Every lane takes its skip / stop decisions as predicates, so the warp
+      // stays converged.
       if (!__all_sync(0xffffffffu, done)) {
         for (int j0 = 0; j0 < cnt; j0 += 32) {
-          uint32_t mask = warp_cull(R, j0, cnt, bx0, bx1, by0, by1);
+          const int jl = j0 + lane;
+          bool near = false;
+          Rec e;
+          if (jl < cnt) {
+            e = R[jl];
+            const float ex = fmaxf(fmaxf(bx0 - e.a.x, e.a.x - bx1), 0.0f);
+            const float ey = fmaxf(fmaxf(by0 - e.a.y, e.a.y - by1), 0.0f);
+            const float r = e.c.z;
+            near = (r >= 0.0f) && (ex * ex + ey * ey <= r * r);
+          }
+          const uint32_t mask = __ballot_sync(0xffffffffu, near);
+          __syncwarp();  // the previous chunk's pairs have been read
+          if (near) {
+            const int k = __popc(mask & ((1u << lane) - 1u));
+            float* f = reinterpret_cast<float*>(&my_pair[k >> 1]) + (k & 1);
+            f[0] = -e.a.x;
+            f[2] = -e.a.y;
+            f[4] = e.a.z;
+            f[6] = e.a.w;
+            f[8] = e.b.x;
+            f[10] = e.b.y;
+            my_col[k] = make_float4(e.b.z, e.b.w, e.c.x, 0.0f);
+          }
+          __syncwarp();
+          const int m = __popc(mask);
+          uint32_t rem = mask;
           uint32_t cm = 0;  // this pixel's composited entries of the chunk
-          while (mask) {
-            const uint32_t low = mask & (0u - mask);  // the entry's bit
-            mask ^= low;
-            const int j = j0 + __ffs(low) - 1;
-            const float4 ra = R[j].a;  // mx, my, ca, cb
-            const float4 rb = R[j].b;  // cc, o, r, g
-            const float dx = __fsub_rn(px, ra.x), dy = __fsub_rn(py, ra.y);
-            const float power = conic_power(dx, dy, ra.z, ra.w, rb.x);
-            if (!done && !(power > 0.0f) && !(power < kPowerSkip)) {
-              const float v = __fmul_rn(rb.y, gs_expf_core(power));
-              const float alpha = (v < kAlphaMax) ? v : kAlphaMax;
-              if (!(alpha < kAlphaMin)) {
-                // T (1 - alpha) as T - alpha T, one rounding (the frozen sequence)
-                const float Tn = __fmaf_rn(-alpha, T, T);
-                if (Tn < kTMin) {
-                  done = true;
-                } else {
-                  const float w = __fmul_rn(alpha, T);
-                  C0 = __fmaf_rn(rb.z, w, C0);
-                  C1 = __fmaf_rn(rb.w, w, C1);
-                  C2 = __fmaf_rn(R[j].c.x, w, C2);
-                  T = Tn;
-                  cm |= low;
-                  if (kCount) ++used;
-                }
-              }
-            }
+          for (int k = 0; k < m; k += 2) {
+            const EntryPair P = my_pair[k >> 1];
+            const float2 dx = __fadd2_rn(px2, P.nmx), dy = __fadd2_rn(py2, P.nmy);
+            const float2 power = conic_power2(dx, dy, P.ca, P.cb, P.cc);
+            // o e^power for both entries; an entry that the range test skips (or the
+            // missing second entry of an odd count) discards its value unused
+            const float2 v = __fmul2_rn(P.o, gs_expf2_core(power));
+            composite_one<kCount>(power.x, v.x, my_col[k], rem, done, T, C0, C1, C2, cm, used);
+            if (k + 1 < m) composite_one<kCount>(power.y, v.y, my_col[k + 1], rem, done, T, C0, C1, C2, cm, used);
           }
           cmask[cmask_index(start, tile, pos0 + uint32_t(j0), block, lane)] = cm;
           // the last composited entry so far: the highest bit of this chunk's mask
