@@ -30,7 +30,7 @@
 //   k_bs_ranges_gather per intersection: tile [start, end), the 64-bit key (the depth
 //                      is in the record's last slot) and the 48-byte record gathered
 // A onesweep pass: CTAs take 4096-key partitions in ticket order, rank their keys
-// stably by digit (nine ballots per warp, per-warp histograms), publish per-digit
+// stably by digit (per-warp digit-class tables, per-warp histograms), publish per-digit
 // aggregates and look back over earlier partitions (bounded wait), then scatter
 // through shared memory so each digit's run leaves contiguously.  A pass whose
 // histogram puts every key at digit 0 is the identity and only copies.
@@ -303,6 +303,11 @@ __global__ void __launch_bounds__(kScanThreads, 8)
   }
 }
 
+// Words of one per-warp digit-class table of the onesweep ranking: 256 digits and the
+// out-of-range marker, padded.
+constexpr int kMatchWords = 264;
+static_assert(kSortWarps * 2 * kMatchWords <= 2 * kPart, "the class tables fit in the key and value staging area");
+
 // One stable 8-bit LSD pass over 32-bit keys with 32-bit values: keys
 // [0, min(*n_ptr, cap)) of kin/vin -> kout/vout by digit (key >> shift) & 255.
 __global__ void __launch_bounds__(kSortThreads)
@@ -350,32 +355,34 @@ __global__ void __launch_bounds__(kSortThreads)
       val[it] = 0u;
     }
   }
-  // stable warp-level ranking: item order is (it, lane)
+  // stable warp-level ranking: item order is (it, lane).  A lane finds the lanes holding
+  // its digit by OR-ing its bit into its digit's word of a per-warp table in shared
+  // memory (the out-of-range marker 256 has its own word) and reading the word back;
+  // the class's lowest lane clears the word and advances the digit's count.  Items
+  // alternate between two tables, so a clear of one item's words is ordered before
+  // the next use of that table by the next item's warp barrier.  The tables live in
+  // the key and value staging area, which the scatter below reuses only after a block
+  // barrier.
   uint32_t* wh = s_whist + warp * 256;
+  uint32_t* const wm0 = s_keys + warp * (2 * kMatchWords);
+  for (int k = lane; k < 2 * kMatchWords; k += 32) wm0[k] = 0u;
+  __syncwarp();
   const uint32_t lt = (1u << lane) - 1u;
 #pragma unroll
   for (int it = 0; it < kSortItems; ++it) {
     const uint32_t idx = wbase + uint32_t(it) * 32 + uint32_t(lane);
     const uint32_t d = (idx < K) ? (key[it] >> shift) & 0xFFu : 256u;
-    // lanes holding the same digit: eight ballots, one per digit bit, narrow the
-    // warp to this lane's digit class (the out-of-range marker 256 forms its own
-    // class through the ninth bit)
-    uint32_t peers = __ballot_sync(0xffffffffu, d >> 8);
-    peers = (d >> 8) ? peers : ~peers;
-#pragma unroll
-    for (int bit = 0; bit < 8; ++bit) {
-      const uint32_t b = __ballot_sync(0xffffffffu, (d >> bit) & 1u);
-      peers &= ((d >> bit) & 1u) ? b : ~b;
-    }
-    const int leader = __ffs(peers) - 1;
-    uint32_t old = 0;
-    if (d < 256u && lane == leader) {
-      old = wh[d];
-      wh[d] = old + __popc(peers);
-    }
-    old = __shfl_sync(0xffffffffu, old, leader);
-    rank[it] = old + __popc(peers & lt);
+    uint32_t* const wm = wm0 + (it & 1) * kMatchWords;
+    atomicOr(&wm[d], 1u << lane);
     __syncwarp();
+    const uint32_t peers = wm[d];
+    const uint32_t old = (d < 256u) ? wh[d] : 0u;
+    __syncwarp();
+    if (lane == __ffs(peers) - 1) {
+      wm[d] = 0u;
+      if (d < 256u) wh[d] = old + __popc(peers);
+    }
+    rank[it] = old + __popc(peers & lt);
   }
   __syncthreads();
 
