@@ -190,12 +190,22 @@ __global__ void __launch_bounds__(kScanThreads)
   }
 }
 
+// The depth-sorted ids: the last depth pass leaves them in sorted_a, except when its
+// digits are all 0 (depths within a factor of about four), in which case it skips its
+// copy and they stay in the third pass's output sorted_b.
+__device__ __forceinline__ const uint32_t* depth_sorted_ids(const uint32_t* sorted_a, const uint32_t* sorted_b,
+                                                            const uint32_t* last_hist, uint32_t V) {
+  return last_hist[0] == V ? sorted_b : sorted_a;
+}
+
 // Per 4096 depth-sorted Gaussians: the sum of their tile counts.
 __global__ void __launch_bounds__(kScanThreads)
-    k_bs_sorted_sums(const uint32_t* __restrict__ sorted_ids, const uint32_t* __restrict__ vcount,
+    k_bs_sorted_sums(const uint32_t* __restrict__ sorted_a, const uint32_t* __restrict__ sorted_b,
+                     const uint32_t* __restrict__ last_hist, const uint32_t* __restrict__ vcount,
                      const uint32_t* __restrict__ count, uint64_t* __restrict__ block_sums) {
   __shared__ uint64_t s_w[8];
   const uint32_t V = *vcount;
+  const uint32_t* const sorted_ids = depth_sorted_ids(sorted_a, sorted_b, last_hist, V);
   const int64_t base = int64_t(blockIdx.x) * kScanBlock;
   uint64_t s = 0;
 #pragma unroll 4
@@ -220,7 +230,8 @@ constexpr int kEmitStage = 2048;
 // shared memory so that they leave in contiguous, coalesced runs.  The digit
 // histograms of every tile pass are accumulated on the way out.
 __global__ void __launch_bounds__(kScanThreads, 8)
-    k_bs_emit(const uint32_t* __restrict__ sorted_ids, const uint32_t* __restrict__ vcount,
+    k_bs_emit(const uint32_t* __restrict__ sorted_a, const uint32_t* __restrict__ sorted_b,
+              const uint32_t* __restrict__ last_hist, const uint32_t* __restrict__ vcount,
               const uint32_t* __restrict__ count, const uint2* __restrict__ rect,
               const uint64_t* __restrict__ block_prefix, uint32_t* __restrict__ tk, uint32_t* __restrict__ tv,
               uint32_t cap, int TX, int passes, uint32_t* __restrict__ hist) {
@@ -230,6 +241,7 @@ __global__ void __launch_bounds__(kScanThreads, 8)
   __shared__ uint32_t s_id[kEmitStage];
   for (int k = threadIdx.x; k < passes * 256; k += kScanThreads) s_hist[k] = 0;
   const uint32_t V = *vcount;
+  const uint32_t* const sorted_ids = depth_sorted_ids(sorted_a, sorted_b, last_hist, V);
   uint64_t round_base = block_prefix[blockIdx.x];
   const int64_t base = int64_t(blockIdx.x) * kScanBlock;
   // the gathers of round r + 1 (index, then that Gaussian's count and rect) are in
@@ -314,7 +326,7 @@ __global__ void __launch_bounds__(kSortThreads)
     k_bs_onesweep(const uint32_t* __restrict__ kin, const uint32_t* __restrict__ vin, uint32_t* __restrict__ kout,
                   uint32_t* __restrict__ vout, const uint32_t* __restrict__ n_ptr, uint32_t cap, int shift,
                   const uint32_t* __restrict__ hist, uint32_t* __restrict__ look, uint32_t* __restrict__ ticket,
-                  uint32_t* __restrict__ dev_status, int spin_limit = kSpinLimit) {
+                  uint32_t* __restrict__ dev_status, int spin_limit = kSpinLimit, bool skip_identity = false) {
   extern __shared__ __align__(16) unsigned char smem[];
   uint32_t* s_keys = reinterpret_cast<uint32_t*>(smem);
   uint32_t* s_vals = s_keys + kPart;
@@ -324,7 +336,9 @@ __global__ void __launch_bounds__(kSortThreads)
 
   const uint32_t K = min(*n_ptr, cap);
   if (hist[0] == K) {
-    // every key has digit 0 here: the stable pass is the identity, so copy
+    // every key has digit 0 here: the stable pass is the identity, so copy (or, when the
+    // caller reads the input in that case, do nothing)
+    if (skip_identity) return;
     const uint32_t lo = blockIdx.x * uint32_t(kPart), hi = min(K, lo + uint32_t(kPart));
     for (uint32_t i = lo + threadIdx.x; i < hi; i += kSortThreads) {
       kout[i] = kin[i];
@@ -641,11 +655,12 @@ extern "C" gs_status gs_bin_sort(gs_dims dims, const gs_proj* proj, const gs_cam
   // 2. V (and the compaction offsets), the smallest visible depth bits; K (capacity check)
   k_bs_scan_sums<<<1, 1024, 0, stream>>>(block_vis, L.n_blocks, vcount, ~0ull, dev_status, block_sums, vcount + 1);
   k_bs_scan_sums<<<1, 1024, 0, stream>>>(block_cnt, L.n_blocks, bins.n_isect, capacity_K, dev_status);
-  // 3. compaction + depth digit histograms, 4. depth passes (even: ends in A)
+  // 3. compaction + depth digit histograms, 4. depth passes (even: ends in A; in B when
+  //    the last pass is the identity, which then skips its copy)
   uint32_t* dkA = reinterpret_cast<uint32_t*>(ws + L.dkA());
   uint32_t* dvA = reinterpret_cast<uint32_t*>(ws + L.dvA);
-  uint32_t* dkB = reinterpret_cast<uint32_t*>(ws + L.dkB(dims.n));
-  uint32_t* dvB = reinterpret_cast<uint32_t*>(ws + L.dvB(dims.n));
+  uint32_t* dkB = reinterpret_cast<uint32_t*>(ws + L.dkB());
+  uint32_t* dvB = reinterpret_cast<uint32_t*>(ws + L.dvB());
   k_bs_compact<<<int(L.n_blocks), kScanThreads, 0, stream>>>(proj->count, proj->depth, dims.n, block_vis,
                                                              vcount + 1, dkA, dvA, hist);
   {
@@ -653,7 +668,7 @@ extern "C" gs_status gs_bin_sort(gs_dims dims, const gs_proj* proj, const gs_cam
     for (int p = 0; p < kDepthPasses; ++p) {
       k_bs_onesweep<<<int(L.n_parts_n), kSortThreads, kSortSmem, stream>>>(
           ka, va, kb, vb, vcount, uint32_t(dims.n), 8 * p, hist + 256 * p, look_d + size_t(p) * L.n_parts_n * 256,
-          tickets + p, dev_status);
+          tickets + p, dev_status, kSpinLimit, p == kDepthPasses - 1);
       uint32_t* t = ka;
       ka = kb;
       kb = t;
@@ -663,18 +678,20 @@ extern "C" gs_status gs_bin_sort(gs_dims dims, const gs_proj* proj, const gs_cam
     }
   }
   // 5. offsets of the depth-sorted Gaussians' pairs
-  k_bs_sorted_sums<<<int(L.n_blocks), kScanThreads, 0, stream>>>(dvA, vcount, proj->count, block_sums);
+  const uint32_t* last_hist = hist + 256 * (kDepthPasses - 1);
+  k_bs_sorted_sums<<<int(L.n_blocks), kScanThreads, 0, stream>>>(dvA, dvB, last_hist, vcount, proj->count,
+                                                                  block_sums);
   k_bs_scan_sums<<<1, 1024, 0, stream>>>(block_sums, L.n_blocks, nullptr, 0, dev_status);
   // 6. emit (tile, index) pairs into the buffers that make the last tile pass land in
   //    bins.ids
   uint32_t* tkA = reinterpret_cast<uint32_t*>(ws + L.tkA());
-  uint32_t* tkB = reinterpret_cast<uint32_t*>(ws + L.tkB(capacity_K));
-  uint32_t* tvAlt = reinterpret_cast<uint32_t*>(ws + L.tvAlt(capacity_K));
+  uint32_t* tkB = reinterpret_cast<uint32_t*>(ws + L.tkB());
+  uint32_t* tvAlt = reinterpret_cast<uint32_t*>(ws + L.tvAlt());
   const bool even = (L.passes_t % 2) == 0;
   uint32_t *ka = tkA, *kb = tkB;
   uint32_t* va = even ? bins.ids : tvAlt;
   uint32_t* vb = even ? tvAlt : bins.ids;
-  k_bs_emit<<<int(L.n_blocks), kScanThreads, 0, stream>>>(dvA, vcount, proj->count,
+  k_bs_emit<<<int(L.n_blocks), kScanThreads, 0, stream>>>(dvA, dvB, last_hist, vcount, proj->count,
                                                           reinterpret_cast<const uint2*>(proj->rect), block_sums, ka,
                                                           va, capacity_K, cd.TX, L.passes_t, hist + 256 * kDepthPasses);
   // 7. tile passes

@@ -36,21 +36,26 @@ constexpr int tile_bits(int64_t tiles) {
 constexpr int tile_passes(int64_t tiles) { return (tile_bits(tiles) + 7) / 8; }
 
 // Workspace layout.  The depth sort's scratch (keys A and B, values B) and the tile
-// sort's (keys A and B, the values buffer that is not bins.ids) are never live at the
-// same time and share one region; the depth-sorted indices (values A) stay live
-// through the emission.
+// sort's (keys A and B, the values buffer that is not bins.ids) share one region of
+// three slots, each large enough for either sort's buffers.  The depth-sorted indices
+// end in values A (outside the region) or, when the last depth pass is the identity
+// and skips its copy, in values B, which the emission reads while it writes the tile
+// keys A and values: so values B takes the slot of tile keys B, which nothing writes
+// before the first tile pass.
+//   slot 0: depth keys A, tile keys A;  slot 1: depth values B, tile keys B;
+//   slot 2: depth keys B, the tile sort's other values buffer
 struct SortLayout {
-  size_t block_vis, block_cnt, block_sums, vcount, dvA, shared, hist, tickets, look_d, look_t, total;
+  size_t block_vis, block_cnt, block_sums, vcount, dvA, shared, slot, hist, tickets, look_d, look_t, total;
   size_t zero_begin, zero_bytes;
   int64_t n_blocks, n_parts_n, n_parts_k;
   int passes_t;
   // offsets inside the shared region
   size_t dkA() const { return shared; }
-  size_t dkB(int64_t n) const { return shared + align256(size_t(n) * 4); }
-  size_t dvB(int64_t n) const { return shared + 2 * align256(size_t(n) * 4); }
+  size_t dvB() const { return shared + slot; }
+  size_t dkB() const { return shared + 2 * slot; }
   size_t tkA() const { return shared; }
-  size_t tkB(uint32_t cap) const { return shared + align256(size_t(cap) * 4); }
-  size_t tvAlt(uint32_t cap) const { return shared + 2 * align256(size_t(cap) * 4); }
+  size_t tkB() const { return shared + slot; }
+  size_t tvAlt() const { return shared + 2 * slot; }
 };
 
 constexpr SortLayout sort_layout(int64_t n, uint32_t cap, int64_t tiles) {
@@ -74,7 +79,8 @@ constexpr SortLayout sort_layout(int64_t n, uint32_t cap, int64_t tiles) {
   L.dvA = off;
   off += align256(size_t(n) * 4);
   L.shared = off;
-  off += 3 * max_sz(align256(size_t(n) * 4), align256(size_t(cap) * 4));
+  L.slot = max_sz(align256(size_t(n) * 4), align256(size_t(cap) * 4));
+  off += 3 * L.slot;
   L.hist = off;
   off += align256(size_t(kMaxPasses) * 256 * 4);
   L.tickets = off;
