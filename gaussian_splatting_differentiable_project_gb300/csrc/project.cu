@@ -27,33 +27,46 @@ __device__ __forceinline__ float skip_radius(float lam, float o) {
   return r <= 128.0f ? r : __int_as_float(0x7f7fffff);
 }
 
-constexpr int kProjGroup = 256;                                        // Gaussians per CTA group
-constexpr size_t kProjSmem = size_t(kPlanes) * kProjGroup * sizeof(float);  // 59 planes: 60416 bytes
+constexpr int kProjGroup = 128;                                        // Gaussians per CTA group
+constexpr size_t kProjSmem = 2 * size_t(kPlanes) * kProjGroup * sizeof(float);  // two groups of 59 planes: 60416 bytes
 
 __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
   const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst));
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(src) : "memory");
 }
 
-// One CTA takes groups of 256 consecutive Gaussians.  The group's 59 parameter
-// planes (60 KB) are first copied into shared memory with cp.async, all of them in
-// flight at once, so one thread per Gaussian then projects from shared memory
-// without the two dependent rounds of global loads (geometry, then SH for the
-// visible) that bound it before.  The frozen operation sequence is unchanged.
-__global__ void __launch_bounds__(kProjGroup, 2)
+// One CTA takes groups of 128 consecutive Gaussians.  A group's 59 parameter planes
+// (30 KB) are copied into shared memory with cp.async, all of them in flight at once,
+// so one thread per Gaussian then projects from shared memory without the two
+// dependent rounds of global loads (geometry, then SH for the visible) that bound it
+// before.  The copies are double-buffered: the next group's planes are in flight while
+// this group is projected, three CTAs to an SM.  The frozen operation sequence is
+// unchanged.
+__global__ void __launch_bounds__(kProjGroup, 3)
     k_project(const float* __restrict__ P, int64_t n, int64_t n_pad, CamDev cam, float4* __restrict__ rec,
               float* __restrict__ depth, int32_t* __restrict__ radius, uint2* __restrict__ rect,
               uint32_t* __restrict__ count, uint32_t* __restrict__ dev_status) {
-  extern __shared__ __align__(16) float s_p[];  // [kPlanes][kProjGroup]
+  extern __shared__ __align__(16) float s_buf[];  // [2][kPlanes][kProjGroup]
   const int tid = threadIdx.x;
-  for (int64_t b0 = int64_t(blockIdx.x) * kProjGroup; b0 < n_pad; b0 += int64_t(gridDim.x) * kProjGroup) {
-    constexpr int kRow4 = kProjGroup / 4;
+  constexpr int kRow4 = kProjGroup / 4;
+  const int64_t gstride = int64_t(gridDim.x) * kProjGroup;
+  auto stage = [&](int64_t g0, float* dst) {
     for (int e = tid; e < kPlanes * kRow4; e += kProjGroup) {
       const int pl = e / kRow4, q = (e % kRow4) * 4;
-      cp_async16(s_p + pl * kProjGroup + q, P + int64_t(pl) * n_pad + b0 + q);
+      cp_async16(dst + pl * kProjGroup + q, P + int64_t(pl) * n_pad + g0 + q);
     }
     asm volatile("cp.async.commit_group;" ::: "memory");
-    asm volatile("cp.async.wait_group 0;" ::: "memory");
+  };
+  int buf = 0;
+  if (int64_t(blockIdx.x) * kProjGroup < n_pad) stage(int64_t(blockIdx.x) * kProjGroup, s_buf);
+  for (int64_t b0 = int64_t(blockIdx.x) * kProjGroup; b0 < n_pad; b0 += gstride) {
+    float* s_p = s_buf + buf * (kPlanes * kProjGroup);
+    if (b0 + gstride < n_pad) {
+      stage(b0 + gstride, s_buf + (buf ^ 1) * (kPlanes * kProjGroup));
+      asm volatile("cp.async.wait_group 1;" ::: "memory");
+    } else {
+      asm volatile("cp.async.wait_group 0;" ::: "memory");
+    }
     __syncthreads();
     const int64_t i = b0 + tid;
     Geo g;
@@ -88,7 +101,8 @@ __global__ void __launch_bounds__(kProjGroup, 2)
       rect[i] = make_uint2(0u, 0u);
       count[i] = 0u;
     }
-    __syncthreads();  // the group's planes are read before the next group is staged
+    __syncthreads();  // the group's planes are read before this buffer is staged again
+    buf ^= 1;
   }
 }
 
@@ -107,7 +121,7 @@ extern "C" gs_status gs_project(gs_dims dims, const float* params, const gs_came
       return GS_ERR_CUDA;
     attr_set = true;
   }
-  const int blocks = grid_for(dims.n_pad / kProjGroup, 1, sm_count() * 2);
+  const int blocks = grid_for(dims.n_pad / kProjGroup, 1, sm_count() * 3);
   k_project<<<blocks, kProjGroup, kProjSmem, stream>>>(params, dims.n, dims.n_pad, cam_dev(*cam),
                                                       reinterpret_cast<float4*>(proj.rec), proj.depth, proj.radius,
                                                       reinterpret_cast<uint2*>(proj.rect), proj.count, dev_status);
