@@ -476,22 +476,49 @@ __global__ void __launch_bounds__(kSortThreads)
 
 // Per intersection i: the tile's [start, end) from the neighbouring tile keys, the
 // 64-bit key (tile << 32 | depth bits from the record's last slot) and the record.
+// A thread takes four intersections per pass and issues all their loads before its
+// stores, so each thread keeps four dependent id -> record loads in flight.
 __global__ void __launch_bounds__(256)
     k_bs_ranges_gather(const uint32_t* __restrict__ tk, const uint32_t* __restrict__ ids,
                        const uint32_t* __restrict__ n_isect, uint32_t cap, const float4* __restrict__ rec_in,
                        float4* __restrict__ rec_out, uint64_t* __restrict__ keys, uint2* __restrict__ ranges) {
+  constexpr int kU = 4;  // intersections per thread per pass, their loads issued together
   const uint32_t K = min(*n_isect, cap);
   const uint32_t stride = gridDim.x * blockDim.x;
-  for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < K; i += stride) {
-    const uint32_t t = tk[i];
-    if (i == 0 || tk[i - 1] != t) ranges[t].x = i;
-    if (i + 1 == K || tk[i + 1] != t) ranges[t].y = i + 1;
-    const uint32_t g = ids[i];
-    const float4 a = rec_in[3 * size_t(g)], b = rec_in[3 * size_t(g) + 1], c = rec_in[3 * size_t(g) + 2];
-    rec_out[3 * size_t(i)] = a;
-    rec_out[3 * size_t(i) + 1] = b;
-    rec_out[3 * size_t(i) + 2] = c;
-    keys[i] = (uint64_t(t) << 32) | __float_as_uint(c.w);
+  for (uint32_t i0 = blockIdx.x * blockDim.x + threadIdx.x; i0 < K; i0 += kU * stride) {
+    uint32_t t[kU], gid[kU];
+    float4 a[kU], b[kU], c[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const uint32_t i = i0 + uint32_t(u) * stride;
+      t[u] = 0u;
+      gid[u] = 0u;
+      if (i < K) {
+        t[u] = tk[i];
+        gid[u] = ids[i];
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const uint32_t i = i0 + uint32_t(u) * stride;
+      if (i < K) {
+        a[u] = rec_in[3 * size_t(gid[u])];
+        b[u] = rec_in[3 * size_t(gid[u]) + 1];
+        c[u] = rec_in[3 * size_t(gid[u]) + 2];
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const uint32_t i = i0 + uint32_t(u) * stride;
+      if (i < K) {
+        if (i == 0 || tk[i - 1] != t[u]) ranges[t[u]].x = i;
+        if (i + 1 == K || tk[i + 1] != t[u]) ranges[t[u]].y = i + 1;
+        rec_out[3 * size_t(i)] = a[u];
+        rec_out[3 * size_t(i) + 1] = b[u];
+        rec_out[3 * size_t(i) + 2] = c[u];
+        keys[i] = (uint64_t(t[u]) << 32) | __float_as_uint(c[u].w);
+      }
+    }
   }
 }
 
@@ -707,7 +734,7 @@ extern "C" gs_status gs_bin_sort(gs_dims dims, const gs_proj* proj, const gs_cam
     vb = t;
   }
   // 8. ranges, 64-bit keys and the record gather
-  const int g = grid_for(capacity_K, 256, sm_count() * 16);
+  const int g = grid_for(capacity_K, 256, sm_count() * 4);
   k_bs_ranges_gather<<<g, 256, 0, stream>>>(ka, bins.ids, bins.n_isect, capacity_K,
                                             reinterpret_cast<const float4*>(proj->rec),
                                             reinterpret_cast<float4*>(bins.rec), bins.keys,
