@@ -63,16 +63,16 @@ struct __align__(16) EntryPair {
 // taken as selects rather than branches: every value is formed and kept only where the
 // pixel composites the entry (a branch per decision cost 0.11 ms of 1.13).
 template <bool kCount>
-__device__ __forceinline__ void composite_one(float power, float v, const float4& col, bool& done,
+__device__ __forceinline__ void composite_one(float power, float v, const float4& col, float& amin,
                                               float& T, float& C0, float& C1, float& C2, uint32_t& cm,
                                               uint32_t& used) {
   const uint32_t low = __float_as_uint(col.w);  // the entry's bit
   const float alpha = (v < kAlphaMax) ? v : kAlphaMax;
   const float Tn = __fmaf_rn(-alpha, T, T);
-  const bool pass = !done && !(power > 0.0f) && !(power < kPowerSkip) && !(alpha < kAlphaMin);
+  const bool pass = !(power > 0.0f) && !(power < kPowerSkip) && !(alpha < amin);
   const bool stop = Tn < kTMin;
   const bool take = pass && !stop;
-  done = done || (pass && stop);
+  amin = (pass && stop) ? __int_as_float(0x7f800000) : amin;
   const float w = __fmul_rn(alpha, T);
   const float n0 = __fmaf_rn(col.x, w, C0), n1 = __fmaf_rn(col.y, w, C1), n2 = __fmaf_rn(col.z, w, C2);
   C0 = take ? n0 : C0;
@@ -116,7 +116,8 @@ __global__ void __launch_bounds__(kRasterThreads, 16)
 
   float T = 1.0f, C0 = 0.0f, C1 = 0.0f, C2 = 0.0f;
   uint32_t last = 0, used = 0;
-  bool done = !inside;
+  // the alpha threshold of the compositing rule; +inf once the pixel has stopped
+  float amin = inside ? kAlphaMin : __int_as_float(0x7f800000);
 
   if (n > 0) {
     BatchStager<kBatchFwd> st{srec + start, n, &s_rec[0][0], s_bar};
@@ -143,7 +144,7 @@ __global__ void __launch_bounds__(kRasterThreads, 16)
       // compacted slot; the warp then steps through the compacted entries two at a
       // time.  Every lane takes its skip / stop decisions as predicates, so the warp
       // stays converged.
-      if (!__all_sync(0xffffffffu, done)) {
+      if (!__all_sync(0xffffffffu, amin > 1.0f)) {
         for (int j0 = 0; j0 < cnt; j0 += 32) {
           const int jl = j0 + lane;
           bool near = false;
@@ -178,16 +179,16 @@ __global__ void __launch_bounds__(kRasterThreads, 16)
             // o e^power for both entries; an entry that the range test skips (or the
             // missing second entry of an odd count) discards its value unused
             const float2 v = __fmul2_rn(P.o, gs_expf2_core(power));
-            composite_one<kCount>(power.x, v.x, my_col[k], done, T, C0, C1, C2, cm, used);
-            if (k + 1 < m) composite_one<kCount>(power.y, v.y, my_col[k + 1], done, T, C0, C1, C2, cm, used);
+            composite_one<kCount>(power.x, v.x, my_col[k], amin, T, C0, C1, C2, cm, used);
+            if (k + 1 < m) composite_one<kCount>(power.y, v.y, my_col[k + 1], amin, T, C0, C1, C2, cm, used);
           }
           cmask[cmask_index(start, tile, pos0 + uint32_t(j0), block, lane)] = cm;
           // the last composited entry so far: the highest bit of this chunk's mask
           if (cm) last = pos0 + uint32_t(j0) + 32u - uint32_t(__clz(cm));
-          if (__all_sync(0xffffffffu, done)) break;
+          if (__all_sync(0xffffffffu, amin > 1.0f)) break;
         }
       }
-      const int alive = __syncthreads_count(!done);
+      const int alive = __syncthreads_count(!(amin > 1.0f));
       if (alive == 0) {
         // no pixel needs more: drain copies still in flight before the CTA exits
         for (int q = b + 1; q < issued; ++q) mbar_wait(&s_bar[q & 1], uint32_t((q >> 1) & 1), dev_status);
