@@ -59,9 +59,10 @@ struct __align__(16) EntryPair {
 };
 
 // One entry of the walk, in list order: col holds its colour and, in .w, the bits of
-// its position's bit in the chunk.  The frozen compositing decisions of the scalar walk, given its power and o e^power,
-// taken as selects rather than branches: every value is formed and kept only where the
-// pixel composites the entry (a branch per decision cost 0.11 ms of 1.13).
+// its position's bit in the chunk.  The frozen compositing decisions of the scalar
+// walk, given its power and o e^power, taken as selects rather than branches: every
+// value is formed and kept only where the pixel composites the entry (a branch per
+// decision cost 0.11 ms of 1.13).
 template <bool kCount>
 __device__ __forceinline__ void composite_one(float power, float v, const float4& col, float& amin,
                                               float& T, float& C0, float& C1, float& C2, uint32_t& cm,
