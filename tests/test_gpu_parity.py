@@ -240,6 +240,34 @@ def test_render_fwd_counted_parity(case):
     assert (rd["n_used"] <= rd["n_contrib"]).all() and rd["n_used"].sum() > 0
 
 
+def test_render_fwd_overflowing_colour():
+    """A Gaussian whose SH coefficients are finite but whose colour sum overflows to
+    +inf (every coefficient of the red channel 3e38 with the sign of its basis value):
+    the projection flags nothing, the pixels that composite it turn to inf, and every
+    other pixel, the entry's neighbours in the same walk included, is untouched, bit
+    for bit as the oracle renders it."""
+    cfg = gi.CONFIGS["tiny"]
+    n = 300
+    P = gi.scene_for(cfg, n=n, seed=3).copy()
+    cam = gi.camera((0.0, 0.0, 3.0), 128, 128)
+    P[0:3, 0] = [0.02, -0.01, 0.0]
+    P[3:6, 0] = np.log(0.05)
+    P[10, 0] = 3.0
+    d = P[0:3, 0].astype(np.float64) - cam["campos"].astype(np.float64)
+    Y = oracle.sh_basis((d / np.linalg.norm(d))[None, :].astype(np.float32))[0]
+    for k in range(16):
+        P[11 + 3 * k, 0] = np.float32(3.0e38) * (1.0 if Y[k] >= 0 else -1.0) if abs(Y[k]) > 1e-3 else 0.0
+    ref = oracle.project(P, n, cam, 32)
+    assert np.isinf(ref["rgb"][0, 0]) and ref["visible"][0]
+    rd = oracle.render(ref, 128, 128)
+    assert np.isinf(rd["image"]).sum() > 50 and np.isfinite(rd["image"]).sum() > 40000
+    tr = _gpu_forward(P, n, cam)
+    assert tr.check_status() == 0
+    np.testing.assert_array_equal(_u32(tr.image), rd["image"].view(np.uint32))
+    np.testing.assert_array_equal(_u32(tr.T_final), rd["T_final"].view(np.uint32))
+    np.testing.assert_array_equal(_u32(tr.n_contrib), rd["n_contrib"])
+
+
 # ----------------------------------------------------------------------------- backward
 
 def _target_for(case):
