@@ -104,6 +104,17 @@ __device__ __forceinline__ void ssim_tap4(float (&out)[kSsimGroup], const float 
       if (k - j >= 0 && k - j < 11) out[j] = fmaf(w.g[k - j], v[k], out[j]);
 }
 
+// ssim_tap4 on two maps at once: out[j] (a pair of maps) += g v[k] (a pair) with the
+// two-wide fused multiply-add, each half rounded as fmaf, in the same order.
+__device__ __forceinline__ void ssim_tap4x2(float2 (&out)[kSsimGroup], const float2 (&v)[kSsimWin],
+                                            const SsimWindow& w) {
+#pragma unroll
+  for (int k = 0; k < kSsimWin; ++k)
+#pragma unroll
+    for (int j = 0; j < kSsimGroup; ++j)
+      if (k - j >= 0 && k - j < 11) out[j] = __ffma2_rn(make_float2(w.g[k - j], w.g[k - j]), v[k], out[j]);
+}
+
 // Four CTAs per SM (at most 64 registers a thread; it needs 51 so, 73 unbounded).
 __global__ void __launch_bounds__(kSsimThreads, 4)
     k_ssim_fwd(const float* __restrict__ x, const float* __restrict__ y, int W, int H, SsimWindow w, float dLdS,
@@ -126,36 +137,57 @@ __global__ void __launch_bounds__(kSsimThreads, 4)
     // shift is taken here (outside the image: 0 - shift)
     for (int i = threadIdx.x; i < kSsimHItems; i += kSsimThreads) {
       const int r = i % kSsimIn, c0 = (i / kSsimIn) * kSsimGroup;
-      float a[kSsimWin], b[kSsimWin], aa[kSsimWin], bb[kSsimWin], ab[kSsimWin];
+      // (x, y) and (x^2, y^2) as pairs for the two-wide taps, x y alone
+      float2 ab[kSsimWin], sq[kSsimWin];
+      float xy[kSsimWin];
 #pragma unroll
       for (int k = 0; k < kSsimWin; ++k) {
-        a[k] = s_in[0][r][c0 + k] - shift[0];
-        b[k] = s_in[1][r][c0 + k] - shift[1];
-        aa[k] = a[k] * a[k];
-        bb[k] = b[k] * b[k];
-        ab[k] = a[k] * b[k];
+        ab[k] = make_float2(s_in[0][r][c0 + k] - shift[0], s_in[1][r][c0 + k] - shift[1]);
+        sq[k] = make_float2(ab[k].x * ab[k].x, ab[k].y * ab[k].y);
+        xy[k] = ab[k].x * ab[k].y;
       }
-      float m[5][kSsimGroup] = {};
-      ssim_tap4(m[0], a, w);
-      ssim_tap4(m[1], b, w);
-      ssim_tap4(m[2], aa, w);
-      ssim_tap4(m[3], bb, w);
-      ssim_tap4(m[4], ab, w);
+      float2 m01[kSsimGroup], m23[kSsimGroup];
+      float m4[kSsimGroup] = {};
 #pragma unroll
-      for (int q = 0; q < 5; ++q)
+      for (int j = 0; j < kSsimGroup; ++j) m01[j] = m23[j] = make_float2(0.0f, 0.0f);
+      ssim_tap4x2(m01, ab, w);
+      ssim_tap4x2(m23, sq, w);
+      ssim_tap4(m4, xy, w);
 #pragma unroll
-        for (int j = 0; j < kSsimGroup; ++j) s_h[q][r][c0 + j] = m[q][j];
+      for (int j = 0; j < kSsimGroup; ++j) {
+        s_h[0][r][c0 + j] = m01[j].x;
+        s_h[1][r][c0 + j] = m01[j].y;
+        s_h[2][r][c0 + j] = m23[j].x;
+        s_h[3][r][c0 + j] = m23[j].y;
+        s_h[4][r][c0 + j] = m4[j];
+      }
     }
     __syncthreads();  // s_in read by every thread: the next channel may land there
     if (c + 1 < 3) ssim_stage<2>(s_in, planes, W, H, P, c + 1, ox, oy);
     // vertical: 4 rows of one column per thread
     float m[5][kSsimGroup] = {};
+    {
+      float2 m01[kSsimGroup], m23[kSsimGroup];
 #pragma unroll
-    for (int q = 0; q < 5; ++q) {
-      float v[kSsimWin];
+      for (int j = 0; j < kSsimGroup; ++j) m01[j] = m23[j] = make_float2(0.0f, 0.0f);
 #pragma unroll
-      for (int k = 0; k < kSsimWin; ++k) v[k] = s_h[q][vrow + k][vcol];
-      ssim_tap4(m[q], v, w);
+      for (int q = 0; q < 4; q += 2) {
+        float2 v[kSsimWin];
+#pragma unroll
+        for (int k = 0; k < kSsimWin; ++k) v[k] = make_float2(s_h[q][vrow + k][vcol], s_h[q + 1][vrow + k][vcol]);
+        ssim_tap4x2(q == 0 ? m01 : m23, v, w);
+      }
+      float v4[kSsimWin];
+#pragma unroll
+      for (int k = 0; k < kSsimWin; ++k) v4[k] = s_h[4][vrow + k][vcol];
+      ssim_tap4(m[4], v4, w);
+#pragma unroll
+      for (int j = 0; j < kSsimGroup; ++j) {
+        m[0][j] = m01[j].x;
+        m[1][j] = m01[j].y;
+        m[2][j] = m23[j].x;
+        m[3][j] = m23[j].y;
+      }
     }
 #pragma unroll
     for (int j = 0; j < kSsimGroup; ++j) {
@@ -212,32 +244,50 @@ __global__ void __launch_bounds__(kSsimThreads)
     __syncthreads();  // channel c staged for every thread; the previous vertical pass done with s_h
     for (int i = threadIdx.x; i < kSsimHItems; i += kSsimThreads) {
       const int r = i % kSsimIn, c0 = (i / kSsimIn) * kSsimGroup;
-      float va[kSsimWin], vb[kSsimWin], vc[kSsimWin];
+      float2 vab[kSsimWin];
+      float vc[kSsimWin];
 #pragma unroll
       for (int k = 0; k < kSsimWin; ++k) {
-        vb[k] = s_in[1][r][c0 + k];
+        const float vb = s_in[1][r][c0 + k];
         vc[k] = s_in[2][r][c0 + k];
-        // A about the shift
-        va[k] = s_in[0][r][c0 + k] - 2.f * (s_in[3][r][c0 + k] - sx) * vb[k] - (s_in[4][r][c0 + k] - sy) * vc[k];
+        // A about the shift, paired with b for the two-wide taps
+        vab[k] = make_float2(s_in[0][r][c0 + k] - 2.f * (s_in[3][r][c0 + k] - sx) * vb - (s_in[4][r][c0 + k] - sy) * vc[k],
+                             vb);
       }
-      float o[3][kSsimGroup] = {};
-      ssim_tap4(o[0], va, w);
-      ssim_tap4(o[1], vb, w);
-      ssim_tap4(o[2], vc, w);
+      float2 o01[kSsimGroup];
+      float o2[kSsimGroup] = {};
 #pragma unroll
-      for (int q = 0; q < 3; ++q)
+      for (int j = 0; j < kSsimGroup; ++j) o01[j] = make_float2(0.0f, 0.0f);
+      ssim_tap4x2(o01, vab, w);
+      ssim_tap4(o2, vc, w);
 #pragma unroll
-        for (int j = 0; j < kSsimGroup; ++j) s_h[q][r][c0 + j] = o[q][j];
+      for (int j = 0; j < kSsimGroup; ++j) {
+        s_h[0][r][c0 + j] = o01[j].x;
+        s_h[1][r][c0 + j] = o01[j].y;
+        s_h[2][r][c0 + j] = o2[j];
+      }
     }
     __syncthreads();  // s_in read by every thread: the next channel may land there
     if (c + 1 < 3) ssim_stage<5>(s_in, planes, W, H, P, c + 1, ox, oy);
     float g[3][kSsimGroup] = {};
+    {
+      float2 g01[kSsimGroup];
 #pragma unroll
-    for (int q = 0; q < 3; ++q) {
-      float v[kSsimWin];
+      for (int j = 0; j < kSsimGroup; ++j) g01[j] = make_float2(0.0f, 0.0f);
+      float2 v[kSsimWin];
+      float v2[kSsimWin];
 #pragma unroll
-      for (int k = 0; k < kSsimWin; ++k) v[k] = s_h[q][vrow + k][vcol];
-      ssim_tap4(g[q], v, w);
+      for (int k = 0; k < kSsimWin; ++k) {
+        v[k] = make_float2(s_h[0][vrow + k][vcol], s_h[1][vrow + k][vcol]);
+        v2[k] = s_h[2][vrow + k][vcol];
+      }
+      ssim_tap4x2(g01, v, w);
+      ssim_tap4(g[2], v2, w);
+#pragma unroll
+      for (int j = 0; j < kSsimGroup; ++j) {
+        g[0][j] = g01[j].x;
+        g[1][j] = g01[j].y;
+      }
     }
 #pragma unroll
     for (int j = 0; j < kSsimGroup; ++j) {
