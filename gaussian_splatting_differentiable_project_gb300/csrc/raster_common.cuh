@@ -74,64 +74,6 @@ __device__ __forceinline__ void warp_block_bounds(int TX, float& x0, float& x1, 
   y1 = by + 3.5f;
 }
 
-// Lane-parallel culling of 32 entries [j0, j0 + 32) of a staged batch against the
-// warp's block: bit l set if entry j0 + l may reach one of the warp's pixels, i.e.
-// the block is within the entry's skip radius of its mean.  A cleared
-// bit is an entry every lane of the warp would skip (power below the skip
-// threshold), so walking only the set bits changes no decision.
-__device__ __forceinline__ uint32_t warp_cull(const Rec* R, int j0, int cnt, float x0, float x1, float y0,
-                                              float y1) {
-  const int j = j0 + (threadIdx.x & 31);
-  bool near = false;
-  if (j < cnt) {
-    const float2 m = *reinterpret_cast<const float2*>(&R[j].a);
-    const float r = R[j].c.z;
-    // Euclidean distance from the mean to the block of pixel centres
-    const float ex = fmaxf(fmaxf(x0 - m.x, m.x - x1), 0.0f);
-    const float ey = fmaxf(fmaxf(y0 - m.y, m.y - y1), 0.0f);
-    near = (r >= 0.0f) && (ex * ex + ey * ey <= r * r);
-  }
-  return __ballot_sync(0xffffffffu, near);
-}
-
-// warp_cull tightened by each entry's ellipse, for the backward (whose walk costs
-// about 115 instructions per entry, so the extra test pays; in the forward, at about
-// 45, it does not).  An entry that passes the circle is kept only if the largest
-// power over the block of pixel centres reaches -(ln(255 o) + 0.05): the power is a
-// concave quadratic, so its largest value over the box lies at the mean when the
-// mean is inside, else on one of the four edges, each a 1D quadratic maximised at a
-// clamped stationary point.  The 0.05 margin below alpha's 1/255 threshold matches
-// the skip radius's and covers the fp32 rounding of the quadratic's terms (below
-// 0.02 for entries whose skip radius is finite, at most 128 px).  A culled entry has
-// alpha below 1/255 at every pixel of the block, so no decision changes.
-__device__ __forceinline__ uint32_t warp_cull_ellipse(const Rec* R, int j0, int cnt, float x0, float x1, float y0,
-                                                      float y1) {
-  const int j = j0 + (threadIdx.x & 31);
-  bool near = false;
-  if (j < cnt) {
-    const float4 a = R[j].a;                                        // mx, my, ca, cb
-    const float2 b = *reinterpret_cast<const float2*>(&R[j].b);     // cc, o
-    const float r = R[j].c.z;
-    const float ex = fmaxf(fmaxf(x0 - a.x, a.x - x1), 0.0f);
-    const float ey = fmaxf(fmaxf(y0 - a.y, a.y - y1), 0.0f);
-    near = (r >= 0.0f) && (ex * ex + ey * ey <= r * r);
-    if (near && r <= 128.0f && (ex > 0.0f || ey > 0.0f)) {
-      const float ca = a.z, cb = a.w, cc = b.x;  // power = ca dx^2 + cb dx dy + cc dy^2, ca, cc < 0
-      const float ia = __fdividef(-0.5f, ca), ic = __fdividef(-0.5f, cc);
-      const float lx = x0 - a.x, hx = x1 - a.x, ly = y0 - a.y, hy = y1 - a.y;
-      // edges dx = lx, hx: best dy = cb dx / (-2 cc); edges dy = ly, hy: best dx = cb dy / (-2 ca)
-      const float dy0 = fminf(fmaxf(cb * lx * ic, ly), hy), dy1 = fminf(fmaxf(cb * hx * ic, ly), hy);
-      const float dx0 = fminf(fmaxf(cb * ly * ia, lx), hx), dx1 = fminf(fmaxf(cb * hy * ia, lx), hx);
-      const float p0 = ca * lx * lx + cb * lx * dy0 + cc * dy0 * dy0;
-      const float p1 = ca * hx * hx + cb * hx * dy1 + cc * dy1 * dy1;
-      const float p2 = ca * dx0 * dx0 + cb * dx0 * ly + cc * ly * ly;
-      const float p3 = ca * dx1 * dx1 + cb * dx1 * hy + cc * hy * hy;
-      near = fmaxf(fmaxf(p0, p1), fmaxf(p2, p3)) >= -(__logf(255.0f * b.y) + 0.05f);
-    }
-  }
-  return __ballot_sync(0xffffffffu, near);
-}
-
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

@@ -12,9 +12,10 @@
 // offsets, powers, exponentials and opacity products are formed with the two-wide fp32
 // instructions (fma.rn.f32x2 and kin, each half rounded exactly as the scalar
 // instruction), and the pair is composited in list order, one entry after the other.
-// Every lane reads the same pair (shared-memory broadcast).  For every 32-entry chunk
-// a warp walks it stores each pixel's mask of composited entries, which the backward
-// walks instead of re-evaluating the whole list.  The counting instantiation
+// Every lane reads the same pair (shared-memory broadcast).  A pixel that stops raises
+// its alpha threshold to +inf, so it fails every later alpha test.  For every 32-entry
+// chunk a warp walks it stores each pixel's mask of composited entries, which the
+// backward walks instead of re-evaluating the whole list.  The counting instantiation
 // (gs_render_fwd_counted) also writes each pixel's number of composited entries; the
 // training step runs the one without.
 #include "api_util.h"
@@ -25,8 +26,8 @@ namespace gs {
 // gs_expf_core on two arguments at once with the two-wide fp32 instructions: each
 // half takes exactly the scalar sequence's roundings (the fused multiply-add, add and
 // multiply of a pair round each half as their scalar forms do), and the integer steps
-// stay per half.  s - 1.5 * 2^23 is formed as s + (-1.5 * 2^23) and -k ln2 r as
-// k (-ln2) r, which round identically.
+// stay per half.  s - 1.5 * 2^23 is formed as s + (-1.5 * 2^23) and -k ln2 + r as
+// k (-ln2) + r, which round identically.
 __device__ __forceinline__ float2 gs_expf2_core(float2 x) {
   const float kRound = 12582912.0f;
   const float2 s = __ffma2_rn(x, make_float2(1.44269504088896341f, 1.44269504088896341f), make_float2(kRound, kRound));
@@ -151,6 +152,10 @@ __global__ void __launch_bounds__(kRasterThreads, 16)
           bool near = false;
           Rec e;
           if (jl < cnt) {
+            // the entry may reach one of the warp's pixels when the block of pixel
+            // centres lies within its skip radius of its mean (Euclidean distance from
+            // the mean to the block); an entry outside it would be skipped by every
+            // lane, so culling it changes no decision
             e = R[jl];
             const float ex = fmaxf(fmaxf(bx0 - e.a.x, e.a.x - bx1), 0.0f);
             const float ey = fmaxf(fmaxf(by0 - e.a.y, e.a.y - by1), 0.0f);
