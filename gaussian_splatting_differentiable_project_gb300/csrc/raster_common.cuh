@@ -19,6 +19,9 @@ constexpr int kCtasPerTile = 4;
 // and not in the backward (1.0x).
 constexpr int kBatch = 64;
 constexpr int kBatchFwd = 96;
+// Both walks index the composited-entry masks by 32-entry chunks of the tile's list, so
+// every batch must start on a chunk: a 48-record backward batch broke that and faulted.
+static_assert(kBatch % 32 == 0 && kBatchFwd % 32 == 0, "batches start on 32-entry mask chunks");
 constexpr int kWaitLimit = 1 << 24;                  // bounded mbarrier wait (iterations)
 
 __device__ __forceinline__ int tile_of_block() { return int(blockIdx.x) / kCtasPerTile; }
@@ -46,21 +49,15 @@ __device__ __forceinline__ size_t cmask_index(uint32_t start, int tile, uint32_t
   return (slot * kBlocksPerTile + size_t(block)) * 32 + size_t(lane);
 }
 
-// The backward runs one warp (one 8x4 block) per CTA, eight CTAs per tile: a warp whose
-// pixels need fewer entries than its neighbour's then finishes and frees its slot,
-// instead of waiting at every batch barrier for the other warp of a two-warp CTA
-// (0.987x of the backward's time against two-warp CTAs).
-constexpr int kBwdThreads = 32;
-constexpr int kBwdCtasPerTile = 8;
-
-__device__ __forceinline__ int bwd_tile_of_block() { return int(blockIdx.x) / kBwdCtasPerTile; }
-
-// Origin (top-left pixel) of the backward CTA's 8x4 block.
-__device__ __forceinline__ void bwd_block_origin(int TX, int& bx, int& by) {
-  const int tile = bwd_tile_of_block(), q = int(blockIdx.x) % kBwdCtasPerTile;
-  bx = (tile % TX) * kTile + (q & 1) * 8;
-  by = (tile / TX) * kTile + (q >> 1) * 4;
-}
+// The backward runs one warp per 8x4 block (eight per tile), each warp on its own: its
+// own staging buffers and barriers, no barrier with any other warp, so a warp whose
+// pixels need fewer entries than its neighbour's finishes and frees its slot (against
+// two warps sharing a tile's batches: 0.987x of the backward's time).  Four such warps
+// share a CTA, which only pools their shared memory and scheduling (1.51 against
+// 1.55 ms for one warp per CTA).
+constexpr int kBwdBlocksPerTile = 8;
+constexpr int kBwdWarpsPerCta = 4;
+static_assert(kBwdBlocksPerTile % kBwdWarpsPerCta == 0, "a tile's blocks fill whole CTAs");
 
 // Pixel-centre bounds of this warp's 8x4 block.
 __device__ __forceinline__ void warp_block_bounds(int TX, float& x0, float& x1, float& y0, float& y1) {

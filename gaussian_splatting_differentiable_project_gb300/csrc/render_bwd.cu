@@ -1,8 +1,8 @@
 // gs_render_bwd: L1 loss gradient and the compositing backward.
 //
-// One warp per CTA, one 8x4 block of a 16x16 tile (eight CTAs per tile), one thread per
-// pixel, the tile's records staged in reverse batches by cp.async.bulk (as in the
-// forward).  The warp walks back to front only the entries that at least one of its
+// One warp per 8x4 block of a 16x16 tile, one thread per pixel, four independent warps
+// to a CTA; each warp stages its tile's records in reverse batches by cp.async.bulk into
+// buffers of its own (as the forward does per CTA).  The warp walks back to front only the entries that at least one of its
 // pixels composited, as the forward's per-chunk masks record them (the union of the
 // block's masks), so entries that every pixel skipped cost nothing and no pixel tests
 // whether an entry is in range.  At each entry a pixel that composited it recomputes
@@ -67,21 +67,25 @@ __device__ __forceinline__ void warp_reduce9(const float v[9], float* out8, floa
   *out9 = z;
 }
 
-__global__ void __launch_bounds__(kBwdThreads)
+__global__ void __launch_bounds__(32 * kBwdWarpsPerCta)
     k_render_bwd(const Rec* __restrict__ srec, const uint2* __restrict__ ranges, const uint32_t* __restrict__ n_isect,
                  uint32_t cap, int W, int H, int TX, float bg0, float bg1, float bg2, const float* __restrict__ image,
                  const float* __restrict__ target, const float* __restrict__ T_final,
                  const uint32_t* __restrict__ n_contrib, const uint32_t* __restrict__ cmask,
                  float* __restrict__ grad2d, int64_t n_pad, float* __restrict__ loss, float inv3P, float l1w,
                  const float* __restrict__ dLdC_extra, uint32_t* __restrict__ dev_status) {
-  __shared__ __align__(128) Rec s_rec[2][kBatch];
-  __shared__ __align__(8) uint64_t s_bar[2];
+  __shared__ __align__(128) Rec s_rec_all[kBwdWarpsPerCta][2][kBatch];
+  __shared__ __align__(8) uint64_t s_bar_all[kBwdWarpsPerCta][2];
 
-  const int tile = bwd_tile_of_block();
-  const int block = int(blockIdx.x) % kBwdCtasPerTile;  // the 8x4 block within the tile
+  const int warp = threadIdx.x >> 5;
+  const int vb = int(blockIdx.x) * kBwdWarpsPerCta + warp;  // this warp's 8x4 block, over all tiles
+  const int tile = vb / kBwdBlocksPerTile;
+  const int block = vb % kBwdBlocksPerTile;  // the 8x4 block within the tile
   const int lane = threadIdx.x & 31;
-  int obx, oby;
-  bwd_block_origin(TX, obx, oby);
+  Rec (*s_rec)[kBatch] = s_rec_all[warp];
+  uint64_t* s_bar = s_bar_all[warp];
+  const int obx = (tile % TX) * kTile + (block & 1) * 8;
+  const int oby = (tile / TX) * kTile + (block >> 1) * 4;
   const int pxi = obx + (lane & 7), pyi = oby + (lane >> 3);
   const bool inside = pxi < W && pyi < H;
   const float px = float(pxi) + 0.5f, py = float(pyi) + 0.5f;
@@ -127,14 +131,14 @@ __global__ void __launch_bounds__(kBwdThreads)
 
   BatchStager<kBatch> st{srec + start, n_max, &s_rec[0][0], s_bar};
   const int nb = int((n_max + kBatch - 1) / kBatch);
-  if (threadIdx.x == 0) {
+  if (lane == 0) {
     mbar_init(&s_bar[0], 1);
     mbar_init(&s_bar[1], 1);
     fence_mbar_init();
   }
-  __syncthreads();
+  __syncwarp();
   // batches are consumed last to first; u counts consumption order
-  if (threadIdx.x == 0) {
+  if (lane == 0) {
     st.issue(nb - 1, 0);
     if (nb > 1) st.issue(nb - 2, 1);
   }
@@ -222,9 +226,9 @@ __global__ void __launch_bounds__(kBwdThreads)
         }
       }
     }
-    __syncthreads();
+    __syncwarp();
     if (u + 2 < nb) {
-      if (threadIdx.x == 0) st.issue(nb - 1 - (u + 2), slot);
+      if (lane == 0) st.issue(nb - 1 - (u + 2), slot);
     }
   }
 }
@@ -257,7 +261,7 @@ extern "C" gs_status gs_render_bwd(gs_dims dims, const gs_camera* cam, const gs_
   const int TX = (cam->width + kTile - 1) / kTile;
   const int64_t tiles = n_tiles(cam);
   const float inv3P = float(1.0 / (3.0 * double(cam->width) * double(cam->height)));
-  k_render_bwd<<<int(tiles * kBwdCtasPerTile), kBwdThreads, 0, stream>>>(
+  k_render_bwd<<<int(tiles * kBwdBlocksPerTile / kBwdWarpsPerCta), 32 * kBwdWarpsPerCta, 0, stream>>>(
       reinterpret_cast<const Rec*>(bins->rec), reinterpret_cast<const uint2*>(bins->ranges), bins->n_isect,
       capacity_K, cam->width, cam->height, TX, bg[0], bg[1], bg[2], image, target, T_final, n_contrib, cmask, grad2d,
       dims.n_pad, loss_out, inv3P, l1_weight, dLdC_extra, dev_status);
