@@ -550,8 +550,9 @@ def run_gb300(args, cfg, ws, rank, local):
                 vs = views_of(args.warmup + s)
                 if B == 1:
                     tr.step_staged(cams[vs[0]], staged, slots[0])
-                    # the next target's upload starts once this step's rasterisers are done
-                    nxt = ([staged.put(host_t[v], after=tr.after_backward) for v in views_of(args.warmup + s + 1)]
+                    # the next target's upload starts as soon as its slot is free (the step
+                    # before this one has released it), so it has a whole step to land
+                    nxt = ([staged.put(host_t[v]) for v in views_of(args.warmup + s + 1)]
                            if s + 1 < K else None)
                     loss_host[s, 0:1].copy_(tr.loss, non_blocking=True)
                     if args.dssim > 0:
