@@ -37,35 +37,51 @@ constexpr int kDirectLanes = 16;
 // (l & 3) == 0 holds the warp sum of value l >> 2 (values 0..7) in *out8 and every
 // lane holds the warp sum of value 8 in *out9.
 __device__ __forceinline__ void warp_reduce9(const float v[9], float* out8, float* out9) {
+  // the adds of each level taken two at a time (two-wide fp32 add, each half rounded
+  // as the scalar add, in the same order): value 8 rides along with a pair or with the
+  // last single value of every level
   const int lane = threadIdx.x & 31;
   const bool b16 = lane & 16, b8 = lane & 8, b4 = lane & 4;
-  float w[4];
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const float send = b16 ? v[k] : v[k + 4];
-    const float keep = b16 ? v[k + 4] : v[k];
-    w[k] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
-  }
-  float x[2];
-#pragma unroll
-  for (int k = 0; k < 2; ++k) {
-    const float send = b8 ? w[k] : w[k + 2];
-    const float keep = b8 ? w[k + 2] : w[k];
-    x[k] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
-  }
+  float2 w01, w23;
+  float z;
   {
-    const float send = b4 ? x[0] : x[1];
-    const float keep = b4 ? x[1] : x[0];
-    float y = keep + __shfl_xor_sync(0xffffffffu, send, 4);
-    y += __shfl_xor_sync(0xffffffffu, y, 2);
-    y += __shfl_xor_sync(0xffffffffu, y, 1);
-    *out8 = y;
+    const float s0 = b16 ? v[0] : v[4], k0 = b16 ? v[4] : v[0];
+    const float s1 = b16 ? v[1] : v[5], k1 = b16 ? v[5] : v[1];
+    const float s2 = b16 ? v[2] : v[6], k2 = b16 ? v[6] : v[2];
+    const float s3 = b16 ? v[3] : v[7], k3 = b16 ? v[7] : v[3];
+    const float r0 = __shfl_xor_sync(0xffffffffu, s0, 16), r1 = __shfl_xor_sync(0xffffffffu, s1, 16);
+    const float r2 = __shfl_xor_sync(0xffffffffu, s2, 16), r3 = __shfl_xor_sync(0xffffffffu, s3, 16);
+    const float r8 = __shfl_xor_sync(0xffffffffu, v[8], 16);
+    w01 = __fadd2_rn(make_float2(k0, k1), make_float2(r0, r1));
+    w23 = __fadd2_rn(make_float2(k2, k3), make_float2(r2, r3));
+    z = v[8] + r8;
   }
-  float z = v[8];
+  float2 xz;  // (x, z) after the next level; x the kept sum of this lane's half
+  float x1;
+  {
+    const float s0 = b8 ? w01.x : w23.x, k0 = b8 ? w23.x : w01.x;
+    const float s1 = b8 ? w01.y : w23.y, k1 = b8 ? w23.y : w01.y;
+    const float r0 = __shfl_xor_sync(0xffffffffu, s0, 8), r1 = __shfl_xor_sync(0xffffffffu, s1, 8);
+    const float r8 = __shfl_xor_sync(0xffffffffu, z, 8);
+    const float2 x = __fadd2_rn(make_float2(k0, k1), make_float2(r0, r1));
+    xz = make_float2(x.x, z + r8);
+    x1 = x.y;
+  }
+  float2 yz;
+  {
+    const float send = b4 ? xz.x : x1;
+    const float keep = b4 ? x1 : xz.x;
+    const float r = __shfl_xor_sync(0xffffffffu, send, 4);
+    const float r8 = __shfl_xor_sync(0xffffffffu, xz.y, 4);
+    yz = __fadd2_rn(make_float2(keep, xz.y), make_float2(r, r8));
+  }
 #pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
-  *out9 = z;
+  for (int o = 2; o >= 1; o >>= 1)
+    yz = __fadd2_rn(yz, make_float2(__shfl_xor_sync(0xffffffffu, yz.x, o), __shfl_xor_sync(0xffffffffu, yz.y, o)));
+  *out8 = yz.x;
+  *out9 = yz.y;
 }
+
 
 __global__ void __launch_bounds__(32 * kBwdWarpsPerCta)
     k_render_bwd(const Rec* __restrict__ srec, const uint2* __restrict__ ranges, const uint32_t* __restrict__ n_isect,
